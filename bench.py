@@ -1,0 +1,481 @@
+"""Benchmark of the NVFP4 paged-KV decode step on GB300.
+
+A step is one pass of the hot path over one batch: quantize_append of the
+newest token of every sequence into the NVFP4 cache, then the paged decode
+(split-KV attention + merge) of one query token per sequence over the whole
+cache.  value = KV-tokens attended per second per layer (sum of sequence
+lengths / step time), summed over ranks.  The same step over the FP8-E4M3
+comparison cache is timed beside it, and the dominant kernel's achieved HBM
+bandwidth is reported against the measured copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own copy of the workload (its own
+sequences; no collective on the data path) and rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "NVFP4 paged decode KV-tokens/s per layer and achieved HBM GB/s vs GB300 peak"
+UNIT = "KV-tokens/s"
+WORKLOADS = {
+    "llama70b_b12": ("llama70b", 12),
+    "llama70b_b21": ("llama70b", 21),
+    "ctx32k_b44": ("ctx32k", 44),
+    "ctx32k_b70": ("ctx32k", 70),
+    "ctx160k_b10": ("ctx160k", 10),
+    "ctx160k_b15": ("ctx160k", 15),
+    "ctx1m_b1": ("ctx1m", 1),
+    "ctx1m_b2": ("ctx1m", 2),
+}
+NVFP4_BYTES_PER_TOKEN_HEAD = 2 * (64 + 8)        # K and V: packed data + scales
+FP8_BYTES_PER_TOKEN_HEAD = 2 * 128
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="llama70b_b12", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--num-workers", type=int, default=0)
+    a = ap.parse_args()
+    a.warmup = max(3, a.warmup)
+    a.steps = max(1, a.steps)
+    return a
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return None
+
+
+def profiled_traffic(kernel_tag: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (the summary records their hash)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.startswith("- "):
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    csrc = os.path.join(ROOT, "nvfp4_quantized_paged_nvfp4kv_gb300", "csrc")
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, fn), "rb").read())
+    if fields.get("kernel_sources_sha256") != h.hexdigest()[:16]:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU is loaded."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+class DecodeSetup:
+    """Cache replicas (rotated to defeat L2), tables, queries and the new token."""
+
+    def __init__(self, w, fmt: str, dev, replicas: int, num_workers: int):
+        import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+        self.nv, self.w, self.fmt, self.dev = nv, w, fmt, dev
+        bt, num_pages = workloads.block_table(w)
+        self.num_pages = num_pages
+        self.bt = torch.from_numpy(bt).to(dev)
+        self.sl = torch.tensor(w.seq_lens, dtype=torch.int32, device=dev)
+        first = self._fill(bt)
+        self.caches = [first] + [self._clone(first) for _ in range(replicas - 1)]
+        self.q = workloads.query(w, device=dev)
+        self.out = torch.empty((w.batch, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+        self.num_workers = num_workers
+        self.ws = nv.new_workspace(num_workers, device=dev)
+        # newest token of every sequence: its slot and fresh K/V rows
+        last = np.array([workloads.slot_mapping(w, bt, b, L - 1, L)[0] for b, L in enumerate(w.seq_lens)],
+                        np.int32)
+        self.new_slots = torch.from_numpy(last).to(dev)
+        self.k_new, self.v_new = workloads.new_tokens(w, w.batch, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def _fill(self, bt):
+        nv, w = self.nv, self.w
+        if self.fmt == "nvfp4":
+            c = nv.NVFP4Cache.allocate(self.num_pages, w.num_kv_heads, device=self.dev, zero=False)
+            app = nv.nvfp4kv_quantize_append
+        else:
+            c = nv.FP8Cache.allocate(self.num_pages, w.num_kv_heads, device=self.dev, zero=False)
+            app = nv.fp8kv_quantize_append
+        for b, L in enumerate(w.seq_lens):
+            for t0 in range(0, L, workloads.CHUNK):
+                t1 = min(L, t0 + workloads.CHUNK)
+                sm = torch.from_numpy(workloads.slot_mapping(w, bt, b, t0, t1)).to(self.dev)
+                k = workloads.kv_rows(w, "k", b, t0, t1, device=self.dev).to(torch.bfloat16)
+                v = workloads.kv_rows(w, "v", b, t0, t1, device=self.dev).to(torch.bfloat16)
+                app(c, k, v, sm)
+        return c
+
+    def _clone(self, c):
+        nv = self.nv
+        if self.fmt == "nvfp4":
+            return nv.NVFP4Cache(c.k_data.clone(), c.k_scale.clone(), c.v_data.clone(), c.v_scale.clone())
+        return nv.FP8Cache(c.k.clone(), c.v.clone())
+
+    def cache_bytes(self):
+        return self.caches[0].nbytes()
+
+    def append(self, i, k=None, v=None, slots=None):
+        nv = self.nv
+        c = self.caches[i % len(self.caches)]
+        fn = nv.nvfp4kv_quantize_append if self.fmt == "nvfp4" else nv.fp8kv_quantize_append
+        fn(c, self.k_new if k is None else k, self.v_new if v is None else v,
+           self.new_slots if slots is None else slots, self.status)
+
+    def decode(self, i, q=None, sl=None):
+        nv = self.nv
+        c = self.caches[i % len(self.caches)]
+        fn = nv.nvfp4kv_paged_decode if self.fmt == "nvfp4" else nv.fp8kv_paged_decode
+        fn(c, self.q if q is None else q, self.bt, self.sl if sl is None else sl, self.out, self.ws,
+           num_workers=self.num_workers, dev_status=self.status)
+
+    def step(self, i):
+        self.append(i)
+        self.decode(i)
+
+
+def time_steps(setup: DecodeSetup, steps: int, warmup: int, world: int):
+    """Device time of `steps` steps (barrier + synchronize on both sides) and the
+    mean device time of the decode call inside them, on the launching stream."""
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        setup.step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(steps):
+        setup.append(i)
+        ev[i][0].record(stream)
+        setup.decode(i)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = t0.elapsed_time(t1)
+    decode_ms = [a.elapsed_time(b) for a, b in ev]
+    return total_ms, statistics.mean(decode_ms)
+
+
+def time_e2e(setup: DecodeSetup, steps: int, world: int):
+    """Same step through the public API with the step's inputs in pinned host
+    memory: H2D of queries, new K/V rows, slots and lengths; D2H of the output."""
+    dev = setup.dev
+    hq = setup.q.cpu().pin_memory()
+    hk = setup.k_new.cpu().pin_memory()
+    hv = setup.v_new.cpu().pin_memory()
+    hs = setup.new_slots.cpu().pin_memory()
+    hl = setup.sl.cpu().pin_memory()
+    hout = torch.empty(setup.out.shape, dtype=setup.out.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(setup.q), torch.empty_like(setup.k_new), torch.empty_like(setup.v_new)
+    ds, dl = torch.empty_like(setup.new_slots), torch.empty_like(setup.sl)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hl))
+    d2h = hout.numel() * hout.element_size()
+    stream = torch.cuda.current_stream()
+    for i in range(3):
+        setup.append(i)
+        setup.decode(i)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(steps):
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        ds.copy_(hs, non_blocking=True)
+        dl.copy_(hl, non_blocking=True)
+        setup.append(i, dk, dv, ds)
+        setup.decode(i, dq, dl)
+        hout.copy_(setup.out, non_blocking=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    del dev
+    return t0.elapsed_time(t1), h2d, d2h
+
+
+def run_ours(args, world, rank, local):
+    import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+    nv.load()
+    dev = torch.device("cuda", local)
+    name, batch = WORKLOADS[args.workload]
+    w = workloads.make(name, batch=batch)
+    tokens = w.total_tokens
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nv_bytes_est = tokens * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
+    replicas = max(2, math.ceil(3 * l2 / max(1, nv_bytes_est)) + 1) if nv_bytes_est < 4 * l2 else 1
+    setup = DecodeSetup(w, "nvfp4", dev, replicas, args.num_workers)
+    sampler = ClockSampler(local)
+    sampler.start()
+    # soak: keep the GPU loaded for ~1 s so the clock samples see load clocks
+    t_end = time.time() + 1.0
+    i = 0
+    while time.time() < t_end:
+        setup.step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    total_ms, dec_ms = time_steps(setup, args.steps, args.warmup, world)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = tokens * world / (ms_per_step / 1e3)
+    e2e_ms, h2d, d2h = time_e2e(setup, args.steps, world)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e_value = tokens * world / (e2e_ms / args.steps / 1e3)
+    st = int(setup.status.item())
+    hbm = (measured_peaks() or {}).get("hbm_gbs")
+    peak_src = "measured"
+    if hbm is None:
+        hbm, peak_src = 6800.0, "fallback"
+    alg_bytes = (tokens * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
+                 + 2 * w.batch * w.num_q_heads * w.head_dim * 2
+                 + w.batch * w.max_pages * 4 + w.batch * 4)
+    achieved = alg_bytes / (dec_ms / 1e3) / 1e9
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1 + e4m3 scales) cache; f16 mma, f32 accumulate",
+        "data": "synthetic (seeded generators; shapes and distributions of the workload, no real weights)",
+        "config": {"workload": args.workload, "batch": w.batch, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+                   "seq_len": (w.seq_lens[0] if len(set(w.seq_lens)) == 1 else "ragged"),
+                   "kv_tokens_per_step": tokens,
+                   "l2": (f"{replicas} rotating cache replicas of {setup.cache_bytes() / 1e6:.1f} MB "
+                          f"(L2 {l2 / 1e6:.0f} MB)") if replicas > 1 else
+                         f"cache {setup.cache_bytes() / 1e6:.1f} MB > 4x L2",
+                   "parallelism": f"replicas x{world} (each rank its own sequences)",
+                   "step": "quantize_append(newest token per sequence) + paged_decode"},
+        "roofline": {"bound": "hbm", "kernel": "nvfp4 paged decode (split-KV attention + merge)",
+                     "achieved": achieved, "peak": hbm, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": achieved / hbm, "frac_of_8tbs_nominal": achieved / 8000.0,
+                     "alg_bytes_per_launch": alg_bytes, "decode_ms": dec_ms,
+                     "traffic": profiled_traffic("decode_nvfp4", args.workload)},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "device_status": st,
+    }
+    if not args.no_fp8:
+        del setup
+        torch.cuda.empty_cache()
+        fs = DecodeSetup(w, "fp8", dev, max(1, replicas if tokens * w.num_kv_heads * FP8_BYTES_PER_TOKEN_HEAD
+                                                < 4 * l2 else 1), args.num_workers)
+        f_total, f_dec = time_steps(fs, args.steps, args.warmup, world)
+        f_total = max_over_ranks(f_total, world)
+        f_value = tokens * world / (f_total / args.steps / 1e3)
+        f_bytes = tokens * w.num_kv_heads * FP8_BYTES_PER_TOKEN_HEAD + (alg_bytes - tokens * w.num_kv_heads *
+                                                                        NVFP4_BYTES_PER_TOKEN_HEAD)
+        result["fp8_comparison"] = {
+            "value": f_value, "unit": UNIT, "ms_per_step": f_total / args.steps, "decode_ms": f_dec,
+            "achieved_gbs": f_bytes / (f_dec / 1e3) / 1e9,
+            "nvfp4_over_fp8_step": value / f_value, "nvfp4_over_fp8_decode": f_dec / dec_ms}
+    cpu = cpu_baseline(w, budget_s=10.0) if rank == 0 and world == 1 else None
+    if cpu is not None:
+        result["cpu_baseline"] = cpu
+    return result
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle: the baseline line and the reference arm
+
+def _cpu_sample(w, n_heads: int):
+    """CPU cache of sequence 0 restricted to its first n_heads kv heads."""
+    import oracle
+    L = w.seq_lens[0]
+    npg = (L + 15) // 16
+    bt = np.arange(npg, dtype=np.int32)[None, :]
+    sm = np.arange(L, dtype=np.int32)
+    pools = [np.zeros((npg, n_heads, 16, s), np.uint8) for s in (64, 8, 64, 8)]
+    for t0 in range(0, L, workloads.CHUNK):
+        t1 = min(L, t0 + workloads.CHUNK)
+        k = workloads.kv_rows(w, "k", 0, t0, t1)[:, :n_heads].contiguous().numpy()
+        v = workloads.kv_rows(w, "v", 0, t0, t1)[:, :n_heads].contiguous().numpy()
+        oracle.quantize_append(k, sm[t0:t1], pools[0], pools[1])
+        oracle.quantize_append(v, sm[t0:t1], pools[2], pools[3])
+    q = workloads.query(w)[:1, :n_heads * w.group].float().numpy()
+    return pools, bt, q, L
+
+
+def cpu_baseline(w, budget_s: float = 10.0):
+    """The oracle decode timed on this host's cores on a bounded sample: sequence
+    0, as many kv heads as fit the time budget (one first)."""
+    import oracle
+    pools, bt, q, L = _cpu_sample(w, 1)
+    t = time.perf_counter()
+    oracle.paged_decode(*pools, q, bt, np.int32([L]))
+    one = time.perf_counter() - t
+    heads = 1
+    if one < budget_s / 3:
+        heads = int(min(w.num_kv_heads, max(1, budget_s / max(one, 1e-6) / 2)))
+        pools, bt, q, L = _cpu_sample(w, heads)
+        t = time.perf_counter()
+        oracle.paged_decode(*pools, q, bt, np.int32([L]))
+        one = time.perf_counter() - t
+    kv_tokens = L * heads / w.num_kv_heads
+    return {"value": kv_tokens / one, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"sequence 0 ({L} tokens), {heads} of {w.num_kv_heads} kv heads "
+                      f"({heads * w.group} query heads), fp64 oracle decode, {one:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: each step is a bounded sample (one kv
+    head of sequence 0) of the workload, timed on the host cores."""
+    import oracle
+    name, batch = WORKLOADS[args.workload]
+    w = workloads.make(name, batch=batch)
+    pools, bt, q, L = _cpu_sample(w, 1)
+    for _ in range(args.warmup if L * w.group <= 65536 else 1):
+        oracle.paged_decode(*pools, q, bt, np.int32([L]))
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.paged_decode(*pools, q, bt, np.int32([L]))
+    el = time.perf_counter() - t
+    kv_tokens = L / w.num_kv_heads
+    value = kv_tokens * args.steps / el
+    sample = (f"per step: sequence 0 ({L} tokens), kv head 0 of {w.num_kv_heads} "
+              f"({w.group} query heads), fp64 oracle decode")
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": w.batch, "num_q_heads": w.num_q_heads,
+                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, world, rank)))
+        return 0
+    world, rank, local = dist_init(args)
+    res = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,211 @@
+/*
+ * nvfp4kv -- NVFP4 paged KV cache for GQA decode on one GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only.  Every device pointer is a CUDA
+ * device address owned by the caller; the library allocates no device memory
+ * and keeps no state between calls except a per-device cache of the SM count.
+ * Every launching call is asynchronous on the given stream: it validates its
+ * arguments on the host first (returning an error and launching nothing when
+ * they are bad), then enqueues its kernels and returns.  A NULL stream is the
+ * legacy default stream.
+ *
+ * The method (from the pages this library implements; cited by title and
+ * section):
+ *   "SGLang stores KV cache in 4 bits: long-context decode throughput rises
+ *   26-30%, ..." (summary of the LMSYS post "Accelerating Long-Context and
+ *   Agentic Inference with NVFP4 KV Cache"), Interpretation: the KV cache is
+ *   paged; each block of 16 values is 8 bytes of packed 4-bit data plus one
+ *   byte of block scale; decode dequantises inside the attention kernel; the
+ *   extend path dequantises the cached prefix into an FP8 workspace; prefill
+ *   quantises the new K/V into the cache.  Perspective: the per-tensor FP32
+ *   global scale is left at 1.0.
+ *   "NVFP4-KV-Cache auf der NVIDIA RTX PRO 6000 Blackwell Server Edition",
+ *   "Bytes pro Token": E2M1 elements (1 sign, 2 exponent, 1 mantissa bit),
+ *   one FP8-E4M3 scale per 16 values, an FP32 tensor scale above them;
+ *   "Unterstuetzung in den Engines": the FP8-E4M3 cache is the baseline.
+ *
+ * Formats (readings where the pages are silent):
+ *   E2M1 code: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa;
+ *     magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ *   E4M3 (OCP "FN"): bias 7, subnormals m/8 * 2^-6, max 448, 0x7F = NaN.
+ *   Block of 16 consecutive channels of one token-head:
+ *     S = E4M3_rn_satfinite(fl32(amax / 6)), s = value(S) (x global 1.0),
+ *     q_i = E2M1_rn_satfinite(fl32(x_i / s)), or 0 for all i if s == 0.
+ *     Packed byte j = q_{2j} | q_{2j+1} << 4 (low nibble = even channel).
+ *
+ * NVFP4 cache layout (HND, per K and per V):
+ *   data [num_pages][num_kv_heads][page_size][head_dim/2]  uint8
+ *   scale[num_pages][num_kv_heads][page_size][head_dim/16] uint8 (E4M3)
+ *   A token's slot is physical_page * page_size + offset_in_page.
+ * FP8 cache layout: k, v [num_pages][num_kv_heads][page_size][head_dim] E4M3.
+ *
+ * Supported geometry: head_dim 128, page_size 16, num_q_heads a multiple of
+ * num_kv_heads with group g = num_q_heads / num_kv_heads in 1..8,
+ * global_scale 1.0.  Anything else returns NVFP4KV_ERR_UNSUPPORTED.
+ *
+ * Device-side checks: kernels that read page ids, slots or lengths from
+ * device memory check them and, instead of faulting, OR a bit into the
+ * optional caller-owned device word *dev_status (int32, may be NULL) and
+ * treat the item as described per call.  Read it after synchronising.
+ */
+#ifndef NVFP4KV_H
+#define NVFP4KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle (the same object as cudaStream_t). */
+typedef struct CUstream_st *nvfp4kv_stream_t;
+
+typedef enum {
+    NVFP4KV_OK = 0,
+    NVFP4KV_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size ... */
+    NVFP4KV_ERR_UNSUPPORTED = 2,  /* valid but outside the supported geometry   */
+    NVFP4KV_ERR_WORKSPACE = 3,    /* decode workspace smaller than required     */
+    NVFP4KV_ERR_CUDA = 4          /* a CUDA runtime call or launch failed       */
+} nvfp4kv_status;
+
+/* Bits ORed into *dev_status by the kernels. */
+#define NVFP4KV_DEV_BAD_PAGE 0x1  /* block-table entry outside [0, num_pages)     */
+#define NVFP4KV_DEV_BAD_SLOT 0x2  /* slot outside [0, num_pages * page_size)      */
+#define NVFP4KV_DEV_BAD_LEN 0x4   /* length < 0 or > max_pages_per_seq*page_size  */
+#define NVFP4KV_DEV_TIMEOUT 0x8   /* a bounded wait for staged data gave up        */
+
+typedef enum { NVFP4KV_F32 = 0, NVFP4KV_BF16 = 1 } nvfp4kv_dtype;
+
+/* NVFP4 cache: four pools laid out as above.  Every pool pointer must be
+ * 16-byte aligned.  global_scale must be 1.0f. */
+typedef struct {
+    void *k_data;
+    void *k_scale;
+    void *v_data;
+    void *v_scale;
+    int32_t num_pages;
+    int32_t num_kv_heads;
+    int32_t page_size;
+    int32_t head_dim;
+    float global_scale;
+} nvfp4kv_cache;
+
+/* FP8-E4M3 comparison cache (scale 1.0).  Pointers 16-byte aligned. */
+typedef struct {
+    void *k;
+    void *v;
+    int32_t num_pages;
+    int32_t num_kv_heads;
+    int32_t page_size;
+    int32_t head_dim;
+} fp8kv_cache;
+
+/* Write side ("SGLang stores KV cache in 4 bits", Interpretation ¶2: prefill
+ * quantises the new K/V into the NVFP4 cache).
+ * k_new, v_new: [num_tokens][num_kv_heads][head_dim] contiguous, fp32 or bf16
+ *   (in_dtype), 16-byte aligned; read only.
+ * slot_mapping: int32[num_tokens] device array; slot < 0 skips the token; a
+ *   slot >= num_pages * page_size is skipped and sets NVFP4KV_DEV_BAD_SLOT.
+ *   Slots must be distinct (two tokens writing one slot is a data race).
+ * Writes the data and scale bytes of every (token, kv head) row of K and V.
+ * Inputs must be finite (non-finite values give unspecified codes). */
+nvfp4kv_status nvfp4kv_quantize_append(const nvfp4kv_cache *cache, const void *k_new,
+                                       const void *v_new, nvfp4kv_dtype in_dtype,
+                                       int32_t num_tokens, const int32_t *slot_mapping,
+                                       int32_t *dev_status, nvfp4kv_stream_t stream);
+
+/* Bytes of decode workspace needed by nvfp4kv_paged_decode / fp8kv_paged_decode
+ * when called with the same num_workers on the current device (num_workers 0 =
+ * the automatic choice, whose need is bounded by this value).  Host only; the
+ * result depends on the current device's SM count. */
+size_t nvfp4kv_decode_workspace_size(int32_t num_workers);
+
+/* Decode attention over the NVFP4 cache ("SGLang stores KV cache in 4 bits",
+ * Interpretation ¶2: the decode path dequantises inside the attention kernel;
+ * "NVFP4-KV-Cache auf der ...", "Geschwindigkeit": bf16 queries against
+ * NVFP4 keys and values).
+ * For sequence b and query head i (kv head h = i / g):
+ *   o[b][i] = sum_j softmax_j(sm_scale * q[b][i] . k_j) v_j over the
+ *   seq_lens[b] tokens j of sequence b, token j in page block_table[b][j/16]
+ *   at offset j%16; no causal mask (the query sees all cached tokens).
+ * q: bf16 [batch][num_q_heads][128], 16-byte aligned.  Computation: q is
+ *   multiplied by sm_scale*log2(e) and rounded to fp16 (|q * sm_scale| must
+ *   stay below 4.5e4); K and V are dequantised exactly to fp16; QK^T and PV run
+ *   on tensor cores with fp32 accumulation; softmax in fp32.
+ * block_table: int32 [batch][max_pages_per_seq]; only the first
+ *   ceil(seq_lens[b]/16) entries of row b are read; an entry outside
+ *   [0, num_pages) reads page 0 instead and sets NVFP4KV_DEV_BAD_PAGE.
+ * seq_lens: int32[batch]; a length outside [0, max_pages_per_seq*16] is
+ *   clamped into it and sets NVFP4KV_DEV_BAD_LEN.  Length 0 gives zeros.
+ * out: [batch][num_q_heads][128] in out_dtype, 16-byte aligned.
+ * workspace: device scratch of workspace_bytes >= the size above, 256-byte
+ *   aligned; its contents need no initialisation and are overwritten.  Two
+ *   calls in flight at once must not share a workspace.
+ * num_workers: 0 = automatic; otherwise the number of warp workers the
+ *   page-heads are balanced over (results agree to fp32 rounding for any
+ *   value).
+ * Launches two kernels (split-KV attention, then the split merge). */
+nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q,
+                                    int32_t batch, int32_t num_q_heads,
+                                    const int32_t *block_table, int32_t max_pages_per_seq,
+                                    const int32_t *seq_lens, float sm_scale, void *out,
+                                    nvfp4kv_dtype out_dtype, void *workspace,
+                                    size_t workspace_bytes, int32_t num_workers,
+                                    int32_t *dev_status, nvfp4kv_stream_t stream);
+
+/* Extend path ("SGLang stores KV cache in 4 bits", Interpretation ¶2: the
+ * cached prefix is dequantised into one FP8 workspace shared across layers).
+ * For sequence b, token j < prefix_lens[b], kv head h, channel c:
+ *   out[kv_indptr[b] + j][h][c] = E4M3_rn_satfinite(E2M1 x scale x 1.0)
+ * for K into k_fp8_out and V into v_fp8_out (each [rows][num_kv_heads][128]
+ * uint8, 16-byte aligned; the caller sizes it to cover every row written).
+ * kv_indptr: int32[batch] row offsets; prefix_lens: int32[batch].
+ * Page-id and length checks as in nvfp4kv_paged_decode. */
+nvfp4kv_status nvfp4kv_dequant_prefix_fp8(const nvfp4kv_cache *cache,
+                                          const int32_t *block_table,
+                                          int32_t max_pages_per_seq,
+                                          const int32_t *prefix_lens,
+                                          const int32_t *kv_indptr, int32_t batch,
+                                          void *k_fp8_out, void *v_fp8_out,
+                                          int32_t *dev_status, nvfp4kv_stream_t stream);
+
+/* FP8-E4M3 comparison cache, written and read the same way ("NVFP4-KV-Cache
+ * auf der ...", "Unterstuetzung in den Engines": the FP8 baseline runs with
+ * --kv-cache-dtype fp8_e4m3; "Bytes pro Token": scales 1.0 uncalibrated).
+ * Each value is E4M3_rn_satfinite(x).  Arguments as for the NVFP4 calls. */
+nvfp4kv_status fp8kv_quantize_append(const fp8kv_cache *cache, const void *k_new,
+                                     const void *v_new, nvfp4kv_dtype in_dtype,
+                                     int32_t num_tokens, const int32_t *slot_mapping,
+                                     int32_t *dev_status, nvfp4kv_stream_t stream);
+
+nvfp4kv_status fp8kv_paged_decode(const fp8kv_cache *cache, const void *q, int32_t batch,
+                                  int32_t num_q_heads, const int32_t *block_table,
+                                  int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                  float sm_scale, void *out, nvfp4kv_dtype out_dtype,
+                                  void *workspace, size_t workspace_bytes,
+                                  int32_t num_workers, int32_t *dev_status,
+                                  nvfp4kv_stream_t stream);
+
+/* Bytes of all four NVFP4 pools (K and V data and scales) for a geometry:
+ * num_pages * num_kv_heads * page_size * 2 * (head_dim/2 + head_dim/16),
+ * i.e. 9 bytes per 16 values ("SGLang stores KV cache in 4 bits",
+ * Interpretation).  Returns -1 for invalid arguments.  Host only. */
+int64_t nvfp4kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
+                            int32_t head_dim);
+
+/* Bytes of both FP8 pools: num_pages * num_kv_heads * page_size * 2 * head_dim. */
+int64_t fp8kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
+                          int32_t head_dim);
+
+/* Static description of a status code. */
+const char *nvfp4kv_status_string(nvfp4kv_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t nvfp4kv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4KV_H */

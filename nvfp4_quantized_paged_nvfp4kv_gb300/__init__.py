@@ -1,0 +1,264 @@
+"""Python binding of libnvfp4kv (the C ABI in include/nvfp4kv.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  There is no fallback:
+if the shared library is missing or fails to load, importing the binding's
+functions raises.
+
+Functions carry the C names and take torch tensors:
+
+  nvfp4kv_quantize_append(cache, k_new, v_new, slot_mapping, dev_status=None)
+  nvfp4kv_paged_decode(cache, q, block_table, seq_lens, out, workspace, ...)
+  nvfp4kv_dequant_prefix_fp8(cache, block_table, prefix_lens, kv_indptr, k_out, v_out)
+  fp8kv_quantize_append(cache, k_new, v_new, slot_mapping, dev_status=None)
+  fp8kv_paged_decode(cache, q, block_table, seq_lens, out, workspace, ...)
+  nvfp4kv_decode_workspace_size(num_workers=0)
+  nvfp4kv_cache_bytes / fp8kv_cache_bytes / nvfp4kv_status_string / nvfp4kv_version
+
+``NVFP4Cache`` and ``FP8Cache`` hold the pool tensors and build the C structs.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import _build
+
+PAGE_SIZE = 16
+HEAD_DIM = 128
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = 0, 1, 2, 3, 4
+DEV_BAD_PAGE, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+F32, BF16 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Nvfp4kvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+
+
+class _Nvfp4Cache(ctypes.Structure):
+    _fields_ = [("k_data", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_data", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("global_scale", ctypes.c_float)]
+
+
+class _Fp8Cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_st = ctypes.c_int
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libnvfp4kv.so (building it in-tree first if it is absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            if not build_if_missing:
+                raise OSError(f"libnvfp4kv.so not built at {_build.LIB}")
+            _build.build()
+        try:
+            import torch  # noqa: F401  (loads the CUDA runtime torch uses first)
+        except ImportError:
+            pass
+        lib = ctypes.CDLL(_build.LIB)
+        sig = {
+            "nvfp4kv_quantize_append": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _vp, _st, _i32, _vp, _vp, _vp]),
+            "nvfp4kv_decode_workspace_size": (ctypes.c_size_t, [_i32]),
+            "nvfp4kv_paged_decode": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _i32, _i32, _vp, _i32, _vp,
+                                           ctypes.c_float, _vp, _st, _vp, ctypes.c_size_t, _i32, _vp, _vp]),
+            "nvfp4kv_dequant_prefix_fp8": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _i32, _vp, _vp, _i32,
+                                                 _vp, _vp, _vp, _vp]),
+            "fp8kv_quantize_append": (_st, [ctypes.POINTER(_Fp8Cache), _vp, _vp, _st, _i32, _vp, _vp, _vp]),
+            "fp8kv_paged_decode": (_st, [ctypes.POINTER(_Fp8Cache), _vp, _i32, _i32, _vp, _i32, _vp,
+                                         ctypes.c_float, _vp, _st, _vp, ctypes.c_size_t, _i32, _vp, _vp]),
+            "nvfp4kv_cache_bytes": (ctypes.c_int64, [_i32, _i32, _i32, _i32]),
+            "fp8kv_cache_bytes": (ctypes.c_int64, [_i32, _i32, _i32, _i32]),
+            "nvfp4kv_status_string": (ctypes.c_char_p, [_st]),
+            "nvfp4kv_version": (_i32, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise Nvfp4kvError(status, what)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+# --- caches -----------------------------------------------------------------
+
+class NVFP4Cache:
+    """The four NVFP4 pools: data [pages][Hkv][16][64] and scale [pages][Hkv][16][8]."""
+
+    def __init__(self, k_data, k_scale, v_data, v_scale):
+        self.k_data, self.k_scale, self.v_data, self.v_scale = k_data, k_scale, v_data, v_scale
+        self.num_pages, self.num_kv_heads, self.page_size, half = k_data.shape
+        self.head_dim = half * 2
+        self._c = _Nvfp4Cache(k_data.data_ptr(), k_scale.data_ptr(), v_data.data_ptr(),
+                              v_scale.data_ptr(), self.num_pages, self.num_kv_heads, self.page_size,
+                              self.head_dim, 1.0)
+
+    @classmethod
+    def allocate(cls, num_pages, num_kv_heads, device="cuda", zero=True):
+        import torch
+        f = torch.zeros if zero else torch.empty
+        d = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM // 2)
+        s = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM // 16)
+        return cls(f(d, dtype=torch.uint8, device=device), f(s, dtype=torch.uint8, device=device),
+                   f(d, dtype=torch.uint8, device=device), f(s, dtype=torch.uint8, device=device))
+
+    @property
+    def c(self):
+        return ctypes.byref(self._c)
+
+    def nbytes(self) -> int:
+        return sum(t.numel() for t in (self.k_data, self.k_scale, self.v_data, self.v_scale))
+
+
+class FP8Cache:
+    """The two FP8-E4M3 pools [pages][Hkv][16][128]."""
+
+    def __init__(self, k, v):
+        self.k, self.v = k, v
+        self.num_pages, self.num_kv_heads, self.page_size, self.head_dim = k.shape
+        self._c = _Fp8Cache(k.data_ptr(), v.data_ptr(), self.num_pages, self.num_kv_heads,
+                            self.page_size, self.head_dim)
+
+    @classmethod
+    def allocate(cls, num_pages, num_kv_heads, device="cuda", zero=True):
+        import torch
+        f = torch.zeros if zero else torch.empty
+        shape = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM)
+        return cls(f(shape, dtype=torch.uint8, device=device), f(shape, dtype=torch.uint8, device=device))
+
+    @property
+    def c(self):
+        return ctypes.byref(self._c)
+
+    def nbytes(self) -> int:
+        return self.k.numel() + self.v.numel()
+
+
+# --- entry points -------------------------------------------------------------
+
+def nvfp4kv_quantize_append(cache: NVFP4Cache, k_new, v_new, slot_mapping, dev_status=None,
+                            stream=None) -> None:
+    st = load().nvfp4kv_quantize_append(cache.c, _ptr(k_new), _ptr(v_new), _dtype_code(k_new),
+                                        k_new.shape[0], _ptr(slot_mapping), _ptr(dev_status),
+                                        _stream(stream))
+    _check(st, "nvfp4kv_quantize_append")
+
+
+def fp8kv_quantize_append(cache: FP8Cache, k_new, v_new, slot_mapping, dev_status=None,
+                          stream=None) -> None:
+    st = load().fp8kv_quantize_append(cache.c, _ptr(k_new), _ptr(v_new), _dtype_code(k_new),
+                                      k_new.shape[0], _ptr(slot_mapping), _ptr(dev_status),
+                                      _stream(stream))
+    _check(st, "fp8kv_quantize_append")
+
+
+def nvfp4kv_decode_workspace_size(num_workers: int = 0) -> int:
+    return int(load().nvfp4kv_decode_workspace_size(int(num_workers)))
+
+
+def _decode(fn, name, cache, q, block_table, seq_lens, out, workspace, sm_scale, num_workers,
+            dev_status, stream):
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    B, Hq, _ = q.shape
+    st = fn(cache.c, _ptr(q), B, Hq, _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+            float(sm_scale), _ptr(out), _dtype_code(out), _ptr(workspace),
+            0 if workspace is None else workspace.numel() * workspace.element_size(),
+            int(num_workers), _ptr(dev_status), _stream(stream))
+    _check(st, name)
+
+
+def nvfp4kv_paged_decode(cache: NVFP4Cache, q, block_table, seq_lens, out, workspace,
+                         sm_scale=None, num_workers=0, dev_status=None, stream=None) -> None:
+    _decode(load().nvfp4kv_paged_decode, "nvfp4kv_paged_decode", cache, q, block_table, seq_lens,
+            out, workspace, sm_scale, num_workers, dev_status, stream)
+
+
+def fp8kv_paged_decode(cache: FP8Cache, q, block_table, seq_lens, out, workspace,
+                       sm_scale=None, num_workers=0, dev_status=None, stream=None) -> None:
+    _decode(load().fp8kv_paged_decode, "fp8kv_paged_decode", cache, q, block_table, seq_lens,
+            out, workspace, sm_scale, num_workers, dev_status, stream)
+
+
+def nvfp4kv_dequant_prefix_fp8(cache: NVFP4Cache, block_table, prefix_lens, kv_indptr, k_out, v_out,
+                               dev_status=None, stream=None) -> None:
+    st = load().nvfp4kv_dequant_prefix_fp8(cache.c, _ptr(block_table), block_table.shape[1],
+                                           _ptr(prefix_lens), _ptr(kv_indptr), prefix_lens.shape[0],
+                                           _ptr(k_out), _ptr(v_out), _ptr(dev_status),
+                                           _stream(stream))
+    _check(st, "nvfp4kv_dequant_prefix_fp8")
+
+
+def nvfp4kv_cache_bytes(num_pages, num_kv_heads, page_size=PAGE_SIZE, head_dim=HEAD_DIM) -> int:
+    return int(load().nvfp4kv_cache_bytes(num_pages, num_kv_heads, page_size, head_dim))
+
+
+def fp8kv_cache_bytes(num_pages, num_kv_heads, page_size=PAGE_SIZE, head_dim=HEAD_DIM) -> int:
+    return int(load().fp8kv_cache_bytes(num_pages, num_kv_heads, page_size, head_dim))
+
+
+def status_string(status: int) -> str:
+    return load().nvfp4kv_status_string(int(status)).decode()
+
+
+nvfp4kv_status_string = status_string
+
+
+def nvfp4kv_version() -> int:
+    return int(load().nvfp4kv_version())
+
+
+def new_workspace(num_workers: int = 0, device="cuda"):
+    """A decode workspace tensor of the size the library asks for."""
+    import torch
+    n = nvfp4kv_decode_workspace_size(num_workers)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)

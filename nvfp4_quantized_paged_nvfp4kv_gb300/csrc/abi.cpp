@@ -1,0 +1,378 @@
+// C ABI of the library: argument validation, tensor-map set-up and launches.
+// The contract of every entry point is documented in include/nvfp4kv.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "nvfp4kv.h"
+#include "nvfp4kv_internal.h"
+
+using namespace nvfp4kv;
+
+namespace {
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+cudaStream_t to_cuda(nvfp4kv_stream_t s)
+{
+    return reinterpret_cast<cudaStream_t>(s);
+}
+
+nvfp4kv_status from_cuda(cudaError_t e)
+{
+    return e == cudaSuccess ? NVFP4KV_OK : NVFP4KV_ERR_CUDA;
+}
+
+// Shared geometry checks for both cache kinds.
+nvfp4kv_status check_geometry(int32_t num_pages, int32_t hkv, int32_t page_size, int32_t head_dim)
+{
+    if (num_pages <= 0 || hkv <= 0 || page_size <= 0 || head_dim <= 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (page_size != kPageSize || head_dim != kHeadDim)
+        return NVFP4KV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(num_pages) * hkv > (int64_t{1} << 31) - 1)
+        return NVFP4KV_ERR_UNSUPPORTED;
+    return NVFP4KV_OK;
+}
+
+nvfp4kv_status check_nvfp4(const nvfp4kv_cache *c)
+{
+    if (c == nullptr)
+        return NVFP4KV_ERR_INVALID_ARG;
+    nvfp4kv_status st = check_geometry(c->num_pages, c->num_kv_heads, c->page_size, c->head_dim);
+    if (st != NVFP4KV_OK)
+        return st;
+    if (!(c->global_scale == 1.0f))
+        return NVFP4KV_ERR_UNSUPPORTED;
+    const void *ptrs[4] = {c->k_data, c->k_scale, c->v_data, c->v_scale};
+    for (const void *p : ptrs)
+        if (p == nullptr || !aligned16(p))
+            return NVFP4KV_ERR_INVALID_ARG;
+    return NVFP4KV_OK;
+}
+
+nvfp4kv_status check_fp8(const fp8kv_cache *c)
+{
+    if (c == nullptr)
+        return NVFP4KV_ERR_INVALID_ARG;
+    nvfp4kv_status st = check_geometry(c->num_pages, c->num_kv_heads, c->page_size, c->head_dim);
+    if (st != NVFP4KV_OK)
+        return st;
+    if (c->k == nullptr || c->v == nullptr || !aligned16(c->k) || !aligned16(c->v))
+        return NVFP4KV_ERR_INVALID_ARG;
+    return NVFP4KV_OK;
+}
+
+nvfp4kv_status check_append(const void *k_new, const void *v_new, nvfp4kv_dtype in_dtype, int32_t num_tokens,
+                            const int32_t *slot_mapping)
+{
+    if (num_tokens < 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (in_dtype != NVFP4KV_F32 && in_dtype != NVFP4KV_BF16)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return NVFP4KV_OK;
+    if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 3u))
+        return NVFP4KV_ERR_INVALID_ARG;
+    return NVFP4KV_OK;
+}
+
+// Decode arguments common to both cache kinds.  Fills p (except the cache
+// pointers) on success.
+nvfp4kv_status check_decode(int32_t hkv, int32_t num_pages, const void *q, int32_t batch, int32_t num_q_heads,
+                            const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+                            float sm_scale, void *out, nvfp4kv_dtype out_dtype, void *workspace,
+                            size_t workspace_bytes, int32_t num_workers, int32_t *dev_status, DecodeParams &p)
+{
+    if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0 || num_workers < 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4KV_F32 && out_dtype != NVFP4KV_BF16)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale))
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (num_q_heads % hkv != 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    const int group = num_q_heads / hkv;
+    if (group > kMaxGroup)
+        return NVFP4KV_ERR_UNSUPPORTED;
+    if (batch > kMaxBatch)
+        return NVFP4KV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(batch) * hkv * max_pages_per_seq > (int64_t{1} << 31) - 1)
+        return NVFP4KV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(max_pages_per_seq) * kPageSize > (int64_t{1} << 30))
+        return NVFP4KV_ERR_UNSUPPORTED;
+    if (batch > 0) {
+        if (q == nullptr || out == nullptr || block_table == nullptr || seq_lens == nullptr)
+            return NVFP4KV_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+            (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+            return NVFP4KV_ERR_INVALID_ARG;
+    }
+    int nw = num_workers;
+    if (nw == 0) {
+        // automatic: the device default, but no more than one worker per four
+        // page-heads of the largest possible batch
+        const int64_t upper = static_cast<int64_t>(batch) * hkv * max_pages_per_seq;
+        int64_t cap = upper / 4;
+        if (cap < 1)
+            cap = 1;
+        nw = default_num_workers();
+        if (nw > cap)
+            nw = static_cast<int>(cap);
+    }
+    if (batch > 0) {
+        if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return NVFP4KV_ERR_WORKSPACE;
+        if (workspace_bytes < decode_workspace_bytes(nw))
+            return NVFP4KV_ERR_WORKSPACE;
+    }
+    p = DecodeParams{};
+    p.q = static_cast<const uint16_t *>(q);
+    p.out = out;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.dev_status = dev_status;
+    p.partials = static_cast<float *>(workspace);
+    p.batch = batch;
+    p.hq = num_q_heads;
+    p.hkv = hkv;
+    p.group = group;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.out_bf16 = out_dtype == NVFP4KV_BF16;
+    p.num_workers = nw;
+    p.qscale = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+    return NVFP4KV_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Tensor map over one data pool viewed as [page-heads][16 rows][row_bytes]
+// bytes, box = one page-head, swizzle span = row width (64 or 128 bytes).
+bool make_page_map(CUtensorMap *map, const void *pool, int64_t page_heads, uint32_t row_bytes)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    cuuint64_t dims[3] = {row_bytes, static_cast<cuuint64_t>(kPageSize), static_cast<cuuint64_t>(page_heads)};
+    cuuint64_t strides[2] = {row_bytes, static_cast<cuuint64_t>(row_bytes) * kPageSize};
+    cuuint32_t box[3] = {row_bytes, static_cast<cuuint32_t>(kPageSize), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(pool), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+} // namespace
+
+extern "C" {
+
+nvfp4kv_status nvfp4kv_quantize_append(const nvfp4kv_cache *cache, const void *k_new, const void *v_new,
+                                       nvfp4kv_dtype in_dtype, int32_t num_tokens, const int32_t *slot_mapping,
+                                       int32_t *dev_status, nvfp4kv_stream_t stream)
+{
+    nvfp4kv_status st = check_nvfp4(cache);
+    if (st != NVFP4KV_OK)
+        return st;
+    st = check_append(k_new, v_new, in_dtype, num_tokens, slot_mapping);
+    if (st != NVFP4KV_OK || num_tokens == 0)
+        return st;
+    QuantParams p{};
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.slot_mapping = slot_mapping;
+    p.k_data = static_cast<uint8_t *>(cache->k_data);
+    p.k_scale = static_cast<uint8_t *>(cache->k_scale);
+    p.v_data = static_cast<uint8_t *>(cache->v_data);
+    p.v_scale = static_cast<uint8_t *>(cache->v_scale);
+    p.dev_status = dev_status;
+    p.num_tokens = num_tokens;
+    p.hkv = cache->num_kv_heads;
+    p.num_pages = cache->num_pages;
+    p.in_bf16 = in_dtype == NVFP4KV_BF16;
+    return from_cuda(launch_quantize_append_nvfp4(p, to_cuda(stream)));
+}
+
+size_t nvfp4kv_decode_workspace_size(int32_t num_workers)
+{
+    return decode_workspace_bytes(num_workers < 0 ? 0 : num_workers);
+}
+
+nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q, int32_t batch,
+                                    int32_t num_q_heads, const int32_t *block_table, int32_t max_pages_per_seq,
+                                    const int32_t *seq_lens, float sm_scale, void *out, nvfp4kv_dtype out_dtype,
+                                    void *workspace, size_t workspace_bytes, int32_t num_workers,
+                                    int32_t *dev_status, nvfp4kv_stream_t stream)
+{
+    nvfp4kv_status st = check_nvfp4(cache);
+    if (st != NVFP4KV_OK)
+        return st;
+    DecodeParams p;
+    st = check_decode(cache->num_kv_heads, cache->num_pages, q, batch, num_q_heads, block_table,
+                      max_pages_per_seq, seq_lens, sm_scale, out, out_dtype, workspace, workspace_bytes,
+                      num_workers, dev_status, p);
+    if (st != NVFP4KV_OK || batch == 0)
+        return st;
+    p.k_scale = static_cast<const uint8_t *>(cache->k_scale);
+    p.v_scale = static_cast<const uint8_t *>(cache->v_scale);
+    const int64_t page_heads = static_cast<int64_t>(cache->num_pages) * cache->num_kv_heads;
+    CUtensorMap tk, tv;
+    if (!make_page_map(&tk, cache->k_data, page_heads, kHeadDim / 2) ||
+        !make_page_map(&tv, cache->v_data, page_heads, kHeadDim / 2))
+        return NVFP4KV_ERR_CUDA;
+    cudaError_t e = launch_decode_nvfp4(p, tk, tv, to_cuda(stream));
+    if (e == cudaSuccess)
+        e = launch_merge(p, to_cuda(stream));
+    return from_cuda(e);
+}
+
+nvfp4kv_status nvfp4kv_dequant_prefix_fp8(const nvfp4kv_cache *cache, const int32_t *block_table,
+                                          int32_t max_pages_per_seq, const int32_t *prefix_lens,
+                                          const int32_t *kv_indptr, int32_t batch, void *k_fp8_out,
+                                          void *v_fp8_out, int32_t *dev_status, nvfp4kv_stream_t stream)
+{
+    nvfp4kv_status st = check_nvfp4(cache);
+    if (st != NVFP4KV_OK)
+        return st;
+    if (batch < 0 || max_pages_per_seq <= 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_pages_per_seq) * kPageSize > (int64_t{1} << 30))
+        return NVFP4KV_ERR_UNSUPPORTED;
+    if (batch == 0)
+        return NVFP4KV_OK;
+    if (block_table == nullptr || prefix_lens == nullptr || kv_indptr == nullptr || k_fp8_out == nullptr ||
+        v_fp8_out == nullptr)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (!aligned16(k_fp8_out) || !aligned16(v_fp8_out) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+        (reinterpret_cast<uintptr_t>(prefix_lens) & 3u) || (reinterpret_cast<uintptr_t>(kv_indptr) & 3u))
+        return NVFP4KV_ERR_INVALID_ARG;
+    PrefixParams p{};
+    p.k_data = static_cast<const uint8_t *>(cache->k_data);
+    p.k_scale = static_cast<const uint8_t *>(cache->k_scale);
+    p.v_data = static_cast<const uint8_t *>(cache->v_data);
+    p.v_scale = static_cast<const uint8_t *>(cache->v_scale);
+    p.block_table = block_table;
+    p.prefix_lens = prefix_lens;
+    p.kv_indptr = kv_indptr;
+    p.k_out = static_cast<uint8_t *>(k_fp8_out);
+    p.v_out = static_cast<uint8_t *>(v_fp8_out);
+    p.dev_status = dev_status;
+    p.batch = batch;
+    p.hkv = cache->num_kv_heads;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = cache->num_pages;
+    return from_cuda(launch_dequant_prefix_fp8(p, to_cuda(stream)));
+}
+
+nvfp4kv_status fp8kv_quantize_append(const fp8kv_cache *cache, const void *k_new, const void *v_new,
+                                     nvfp4kv_dtype in_dtype, int32_t num_tokens, const int32_t *slot_mapping,
+                                     int32_t *dev_status, nvfp4kv_stream_t stream)
+{
+    nvfp4kv_status st = check_fp8(cache);
+    if (st != NVFP4KV_OK)
+        return st;
+    st = check_append(k_new, v_new, in_dtype, num_tokens, slot_mapping);
+    if (st != NVFP4KV_OK || num_tokens == 0)
+        return st;
+    QuantParams p{};
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.slot_mapping = slot_mapping;
+    p.k_data = static_cast<uint8_t *>(cache->k);
+    p.v_data = static_cast<uint8_t *>(cache->v);
+    p.dev_status = dev_status;
+    p.num_tokens = num_tokens;
+    p.hkv = cache->num_kv_heads;
+    p.num_pages = cache->num_pages;
+    p.in_bf16 = in_dtype == NVFP4KV_BF16;
+    return from_cuda(launch_quantize_append_fp8(p, to_cuda(stream)));
+}
+
+nvfp4kv_status fp8kv_paged_decode(const fp8kv_cache *cache, const void *q, int32_t batch, int32_t num_q_heads,
+                                  const int32_t *block_table, int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                  float sm_scale, void *out, nvfp4kv_dtype out_dtype, void *workspace,
+                                  size_t workspace_bytes, int32_t num_workers, int32_t *dev_status,
+                                  nvfp4kv_stream_t stream)
+{
+    nvfp4kv_status st = check_fp8(cache);
+    if (st != NVFP4KV_OK)
+        return st;
+    DecodeParams p;
+    st = check_decode(cache->num_kv_heads, cache->num_pages, q, batch, num_q_heads, block_table,
+                      max_pages_per_seq, seq_lens, sm_scale, out, out_dtype, workspace, workspace_bytes,
+                      num_workers, dev_status, p);
+    if (st != NVFP4KV_OK || batch == 0)
+        return st;
+    const int64_t page_heads = static_cast<int64_t>(cache->num_pages) * cache->num_kv_heads;
+    CUtensorMap tk, tv;
+    if (!make_page_map(&tk, cache->k, page_heads, kHeadDim) || !make_page_map(&tv, cache->v, page_heads, kHeadDim))
+        return NVFP4KV_ERR_CUDA;
+    cudaError_t e = launch_decode_fp8(p, tk, tv, to_cuda(stream));
+    if (e == cudaSuccess)
+        e = launch_merge(p, to_cuda(stream));
+    return from_cuda(e);
+}
+
+int64_t nvfp4kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t head_dim)
+{
+    if (num_pages < 0 || num_kv_heads < 0 || page_size < 0 || head_dim < 0 || head_dim % 16 != 0)
+        return -1;
+    const int64_t rows = static_cast<int64_t>(num_pages) * num_kv_heads * page_size;
+    return 2 * rows * (head_dim / 2 + head_dim / 16);
+}
+
+int64_t fp8kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t head_dim)
+{
+    if (num_pages < 0 || num_kv_heads < 0 || page_size < 0 || head_dim < 0)
+        return -1;
+    return 2 * static_cast<int64_t>(num_pages) * num_kv_heads * page_size * head_dim;
+}
+
+const char *nvfp4kv_status_string(nvfp4kv_status status)
+{
+    switch (status) {
+    case NVFP4KV_OK:
+        return "ok";
+    case NVFP4KV_ERR_INVALID_ARG:
+        return "invalid argument";
+    case NVFP4KV_ERR_UNSUPPORTED:
+        return "unsupported geometry or option";
+    case NVFP4KV_ERR_WORKSPACE:
+        return "decode workspace missing, misaligned or too small";
+    case NVFP4KV_ERR_CUDA:
+        return "CUDA runtime error";
+    }
+    return "unknown status";
+}
+
+int32_t nvfp4kv_version(void)
+{
+    return 100;
+}
+
+} // extern "C"

@@ -1,0 +1,26 @@
+// FP8-E4M3 paged decode (comparison kernel): instantiation and launcher.
+#include "decode_common.cuh"
+
+namespace nvfp4kv {
+
+template <class Fmt>
+static cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 cudaStream_t s)
+{
+    const size_t smem = decode_smem_bytes<Fmt>(p.batch);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<Fmt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess)
+        return e;
+    const int grid = (p.num_workers + kDecodeWarps - 1) / kDecodeWarps;
+    decode_kernel<Fmt><<<grid, kDecodeWarps * 32, smem, s>>>(tk, tv, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_fp8(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                                cudaStream_t s)
+{
+    return launch_decode<Fp8Format>(p, tk, tv, s);
+}
+
+} // namespace nvfp4kv

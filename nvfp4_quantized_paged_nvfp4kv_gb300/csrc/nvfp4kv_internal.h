@@ -1,0 +1,85 @@
+// Internal interface between the C ABI (abi.cpp) and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace nvfp4kv {
+
+constexpr int kPageSize = 16;
+constexpr int kHeadDim = 128;
+constexpr int kMaxGroup = 8;                 // query heads per kv head handled by one warp
+constexpr int kDecodeWarps = 4;              // warps (independent workers) per decode CTA
+constexpr int kDecodeCtasPerSm = 4;          // occupancy the default worker count assumes
+constexpr int kPartialFloats = kMaxGroup * kHeadDim + 2 * kMaxGroup;  // O[8][128], m[8], l[8]
+constexpr int kMaxBatch = 16384;             // prefix table lives in shared memory
+
+// Split-KV decode over either cache format.
+struct DecodeParams {
+    const uint8_t *k_scale;      // NVFP4 only
+    const uint8_t *v_scale;      // NVFP4 only
+    const uint16_t *q;           // bf16 [batch][hq][128]
+    void *out;                   // [batch][hq][128] bf16 or f32
+    const int32_t *block_table;  // [batch][max_pages]
+    const int32_t *seq_lens;     // [batch]
+    int32_t *dev_status;         // nullable
+    float *partials;             // [2 * num_workers][kPartialFloats]
+    int batch;
+    int hq;
+    int hkv;
+    int group;
+    int max_pages;
+    int num_pages;
+    int out_bf16;
+    int num_workers;
+    float qscale;                // sm_scale * log2(e)
+};
+
+struct QuantParams {
+    const void *k_new;
+    const void *v_new;
+    const int32_t *slot_mapping;
+    uint8_t *k_data;             // NVFP4 data pool, or the FP8 pool
+    uint8_t *k_scale;            // NVFP4 only
+    uint8_t *v_data;
+    uint8_t *v_scale;
+    int32_t *dev_status;
+    int num_tokens;
+    int hkv;
+    int num_pages;
+    int in_bf16;
+};
+
+struct PrefixParams {
+    const uint8_t *k_data;
+    const uint8_t *k_scale;
+    const uint8_t *v_data;
+    const uint8_t *v_scale;
+    const int32_t *block_table;
+    const int32_t *prefix_lens;
+    const int32_t *kv_indptr;
+    uint8_t *k_out;
+    uint8_t *v_out;
+    int32_t *dev_status;
+    int batch;
+    int hkv;
+    int max_pages;
+    int num_pages;
+};
+
+int sm_count();                  // current device, cached
+int default_num_workers();       // sm_count * kDecodeCtasPerSm * kDecodeWarps
+size_t decode_workspace_bytes(int num_workers);
+
+cudaError_t launch_quantize_append_nvfp4(const QuantParams &p, cudaStream_t s);
+cudaError_t launch_quantize_append_fp8(const QuantParams &p, cudaStream_t s);
+cudaError_t launch_decode_nvfp4(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                                cudaStream_t s);
+cudaError_t launch_decode_fp8(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                              cudaStream_t s);
+cudaError_t launch_merge(const DecodeParams &p, cudaStream_t s);
+cudaError_t launch_dequant_prefix_fp8(const PrefixParams &p, cudaStream_t s);
+
+} // namespace nvfp4kv

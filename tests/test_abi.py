@@ -1,0 +1,152 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/nvfp4kv.h declares, and rejects bad arguments on the host before it
+touches the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+from nvfp4_quantized_paged_nvfp4kv_gb300 import _Fp8Cache, _Nvfp4Cache
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(HEADER_DIR):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = re.sub(r"#[^\n]*", "", text)
+        for m in re.finditer(r"\b([A-Za-z_]\w*)\s*\(", text):
+            name = m.group(1)
+            if name not in ("sizeof",) and not name.startswith("__"):
+                names.add(name)
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("nvfp4kv_quantize_append", "nvfp4kv_paged_decode", "nvfp4kv_dequant_prefix_fp8",
+              "fp8kv_paged_decode", "fp8kv_quantize_append", "nvfp4kv_decode_workspace_size"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = nv.load()
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", nv.library_path()], capture_output=True,
+                         text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in declared_functions():
+        assert n in exported, n
+
+
+FAKE = 0x7F0000000000          # a 16-byte aligned address that is never dereferenced
+
+
+def cache(**kw):
+    c = dict(k_data=FAKE, k_scale=FAKE + 4096, v_data=FAKE + 8192, v_scale=FAKE + 12288,
+             num_pages=10, num_kv_heads=2, page_size=16, head_dim=128, global_scale=1.0)
+    c.update(kw)
+    return _Nvfp4Cache(**c)
+
+
+def fp8cache(**kw):
+    c = dict(k=FAKE, v=FAKE + 4096, num_pages=10, num_kv_heads=2, page_size=16, head_dim=128)
+    c.update(kw)
+    return _Fp8Cache(**c)
+
+
+def append(c, k=FAKE, v=FAKE, n=4, slots=FAKE, dtype=nv.F32):
+    return nv.load().nvfp4kv_quantize_append(ctypes.byref(c) if c is not None else None, k, v, dtype,
+                                             n, slots, None, None)
+
+
+def decode(c, hq=4, batch=2, bt=FAKE, mp=4, sl=FAKE, out=FAKE, ws=FAKE, wsb=1 << 30, nw=0,
+           q=FAKE, scale=0.088, dtype=nv.BF16):
+    return nv.load().nvfp4kv_paged_decode(ctypes.byref(c), q, batch, hq, bt, mp, sl, scale, out, dtype,
+                                          ws, wsb, nw, None, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(head_dim=64), nv.ERR_UNSUPPORTED),
+    (dict(page_size=32), nv.ERR_UNSUPPORTED),
+    (dict(global_scale=2.0), nv.ERR_UNSUPPORTED),
+    (dict(num_pages=0), nv.ERR_INVALID_ARG),
+    (dict(num_kv_heads=-1), nv.ERR_INVALID_ARG),
+    (dict(k_scale=FAKE + 8), nv.ERR_INVALID_ARG),
+    (dict(v_data=None), nv.ERR_INVALID_ARG),
+])
+def test_cache_validation(kw, want):
+    assert append(cache(**kw)) == want
+    assert decode(cache(**kw)) == want
+
+
+def test_append_validation():
+    assert append(None) == nv.ERR_INVALID_ARG
+    assert append(cache(), n=-1) == nv.ERR_INVALID_ARG
+    assert append(cache(), k=FAKE + 4) == nv.ERR_INVALID_ARG
+    assert append(cache(), slots=None) == nv.ERR_INVALID_ARG
+    assert append(cache(), dtype=7) == nv.ERR_INVALID_ARG
+    assert append(cache(), n=0, k=None, v=None, slots=None) == nv.OK     # nothing to do
+    c8 = fp8cache(head_dim=256)
+    assert nv.load().fp8kv_quantize_append(ctypes.byref(c8), FAKE, FAKE, nv.F32, 1, FAKE, None,
+                                           None) == nv.ERR_UNSUPPORTED
+
+
+def test_decode_validation():
+    c = cache()
+    assert decode(c, hq=5) == nv.ERR_INVALID_ARG            # Hq % Hkv != 0
+    assert decode(c, hq=18) == nv.ERR_UNSUPPORTED           # group 9 > 8
+    assert decode(c, batch=-1) == nv.ERR_INVALID_ARG
+    assert decode(c, mp=0) == nv.ERR_INVALID_ARG
+    assert decode(c, q=FAKE + 2) == nv.ERR_INVALID_ARG
+    assert decode(c, out=None) == nv.ERR_INVALID_ARG
+    assert decode(c, scale=float("nan")) == nv.ERR_INVALID_ARG
+    assert decode(c, dtype=9) == nv.ERR_INVALID_ARG
+    assert decode(c, ws=None) == nv.ERR_WORKSPACE
+    assert decode(c, ws=FAKE + 16) == nv.ERR_WORKSPACE      # not 256-byte aligned
+    assert decode(c, wsb=16) == nv.ERR_WORKSPACE
+    assert decode(c, batch=0, q=None, out=None, bt=None, sl=None, ws=None) == nv.OK
+    assert decode(c, batch=20000) == nv.ERR_UNSUPPORTED
+
+
+def test_prefix_validation():
+    lib = nv.load()
+    c = cache()
+    f = lib.nvfp4kv_dequant_prefix_fp8
+    assert f(ctypes.byref(c), FAKE, 4, FAKE, FAKE, -1, FAKE, FAKE, None, None) == nv.ERR_INVALID_ARG
+    assert f(ctypes.byref(c), FAKE, 0, FAKE, FAKE, 1, FAKE, FAKE, None, None) == nv.ERR_INVALID_ARG
+    assert f(ctypes.byref(c), FAKE, 4, FAKE, FAKE, 1, FAKE + 1, FAKE, None, None) == nv.ERR_INVALID_ARG
+    assert f(ctypes.byref(c), FAKE, 4, FAKE, None, 1, FAKE, FAKE, None, None) == nv.ERR_INVALID_ARG
+    assert f(ctypes.byref(c), FAKE, 4, FAKE, FAKE, 0, FAKE, FAKE, None, None) == nv.OK
+
+
+def test_status_strings_and_version():
+    for s in range(5):
+        assert nv.status_string(s)
+    assert nv.status_string(99) == "unknown status"
+    assert nv.nvfp4kv_version() >= 100
+
+
+def test_cache_bytes_match_the_printed_figures():
+    """Pool sizes for Llama 3.3 70B (80 layers x 8 kv heads x d 128): 1.25 GiB
+    per 8K session in FP8 and 0.5625 of that in NVFP4 ("NVFP4-KV-Cache auf der
+    NVIDIA RTX PRO 6000 Blackwell Server Edition", "Bytes pro Token" and
+    "Sitzungen pro Karte"); 9 bytes per 16 values."""
+    pages_8k = 8192 // 16
+    nv_layer = nv.nvfp4kv_cache_bytes(pages_8k, 8)
+    f8_layer = nv.fp8kv_cache_bytes(pages_8k, 8)
+    assert 80 * f8_layer == 1.25 * 2 ** 30
+    assert nv_layer / f8_layer == 0.5625
+    assert nv.nvfp4kv_cache_bytes(1, 1) == 2 * 16 * 9 * 8           # 16 tokens x 128 ch x (K,V)
+    assert 80 * nv.nvfp4kv_cache_bytes(131072 // 16, 8) == 11.25 * 2 ** 30
+    assert nv.nvfp4kv_cache_bytes(1, 1, 16, 100) == -1

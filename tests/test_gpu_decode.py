@@ -1,0 +1,108 @@
+"""GPU parity of the paged decode (NVFP4 and the FP8 comparison kernel) against
+the oracle, elementwise within |d| <= 2e-3 + 1e-2 |ref|.
+
+Decode: "SGLang stores KV cache in 4 bits" (LMSYS summary), Interpretation --
+the decode path dequantises inside the attention kernel."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+import workloads
+from gpu_util import Built, assert_close, oracle_full, oracle_single_head
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_tiny_workload_all_outputs(fp8):
+    b = Built(workloads.make("tiny"), spare_pages=0)
+    want, _ = oracle_full(b, fp8=fp8)
+    assert_close(b.decode(torch.float32, fp8=fp8), want, "fp32 out")
+    assert_close(b.decode(torch.bfloat16, fp8=fp8), want, "bf16 out")
+    assert int(b.status.item()) == 0
+
+
+GEOMS = [
+    # (Hq, Hkv, lengths)
+    (8, 8, (1, 15, 16, 17)),
+    (16, 8, (33, 0, 100)),
+    (12, 4, (250, 1, 64)),
+    (16, 4, (513, 77)),
+    (48, 8, (300, 129, 16)),
+    (64, 8, (200, 5)),
+    (24, 3, (47, 1000)),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,lens", GEOMS)
+@pytest.mark.parametrize("num_workers", [0, 1, 7])
+def test_geometries_and_worker_counts(hq, hkv, lens, num_workers):
+    w = workloads.custom(len(lens), hq, hkv, lens, seed=hq * 31 + hkv)
+    b = Built(w, garbage=True)
+    want, _ = oracle_full(b)
+    got = b.decode(torch.float32, num_workers=num_workers)
+    assert_close(got, want, f"nvfp4 workers={num_workers}")
+    got8 = b.decode(torch.float32, num_workers=num_workers, fp8=True)
+    want8, _ = oracle_full(b, fp8=True)
+    assert_close(got8, want8, f"fp8 workers={num_workers}")
+    assert int(b.status.item()) == 0
+
+
+def test_worker_count_invariance():
+    """The split changes the result only through rounding: P is rounded to
+    fp16 against a running maximum that depends on where a split starts."""
+    w = workloads.custom(3, 32, 4, (2000, 37, 900), seed=3)
+    b = Built(w)
+    ref = b.decode(torch.float32, num_workers=1)
+    for nw in (2, 5, 64, 333, 0):
+        np.testing.assert_allclose(b.decode(torch.float32, num_workers=nw), ref, rtol=2e-3, atol=2e-4)
+
+
+def test_bad_page_and_length_are_reported_not_faulted():
+    w = workloads.custom(2, 8, 2, (40, 40), seed=5)
+    b = Built(w)
+    bt = b.bt.copy()
+    bt[1, 1] = b.num_pages + 7
+    b.bt_d = torch.from_numpy(bt).to("cuda")
+    out = b.decode(torch.float32)
+    assert int(b.status.item()) & nv.DEV_BAD_PAGE
+    assert np.isfinite(out[0]).all()
+    b.status.zero_()
+    b.bt_d = torch.from_numpy(b.bt).to("cuda")
+    b.sl_d = torch.tensor([40, 10 ** 6], dtype=torch.int32, device="cuda")
+    b.decode(torch.float32)
+    assert int(b.status.item()) & nv.DEV_BAD_LEN
+
+
+@pytest.mark.parametrize("name,batch", [("llama70b", 12), ("llama70b", 21)])
+def test_llama70b_layer_sampled(name, batch):
+    """Full-size Llama-3.3-70B-shaped layer (Hq=64, Hkv=8, 8192 tokens), as
+    the bench launches it; oracle on sampled (sequence, kv head) pairs."""
+    w = workloads.make(name, batch=batch)
+    b = Built(w, spare_pages=0)
+    got = b.decode(torch.bfloat16)
+    got8 = b.decode(torch.bfloat16, fp8=True)
+    rng = np.random.default_rng(batch)
+    for seq, h in [(0, 0), (batch - 1, 7)] + [tuple(x) for x in rng.integers([0, 0], [batch, 8], (2, 2))]:
+        g = w.group
+        want = oracle_single_head(b, seq, h)
+        assert_close(got[seq, h * g:(h + 1) * g], want, f"nvfp4 seq {seq} kv head {h}")
+        want8 = oracle_single_head(b, seq, h, fp8=True)
+        assert_close(got8[seq, h * g:(h + 1) * g], want8, f"fp8 seq {seq} kv head {h}")
+    assert int(b.status.item()) == 0
+
+
+@pytest.mark.parametrize("name,batch", [("ctx32k", 44), ("ctx160k", 10), ("ctx1m", 1)])
+def test_long_context_sampled(name, batch):
+    w = workloads.make(name, batch=batch)
+    b = Built(w, spare_pages=0, fp8=(name != "ctx160k"))
+    got = b.decode(torch.bfloat16)
+    got8 = b.decode(torch.bfloat16, fp8=True) if b.fp8 is not None else None
+    for seq, h in [(0, 3), (batch - 1, 6)]:
+        g = w.group
+        assert_close(got[seq, h * g:(h + 1) * g], oracle_single_head(b, seq, h), f"{name} seq {seq} h {h}")
+        if got8 is not None:
+            assert_close(got8[seq, h * g:(h + 1) * g], oracle_single_head(b, seq, h, fp8=True),
+                         f"{name} fp8 seq {seq} h {h}")
+    assert int(b.status.item()) == 0

@@ -1,0 +1,172 @@
+"""GPU parity of the write side (quantize_append, NVFP4 and FP8): bit-exact
+against the oracle ("SGLang stores KV cache in 4 bits" (LMSYS summary),
+Interpretation: new K/V are quantised into the NVFP4 cache)."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_gpu(x_k, x_v, slots, num_pages, hkv, fp8=False):
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sm = torch.from_numpy(np.asarray(slots, np.int32)).to(DEV)
+    if fp8:
+        c = nv.FP8Cache.allocate(num_pages, hkv, device=DEV)
+        nv.fp8kv_quantize_append(c, x_k.to(DEV), x_v.to(DEV), sm, status)
+        torch.cuda.synchronize()
+        return [c.k.cpu().numpy(), c.v.cpu().numpy()], int(status.item())
+    c = nv.NVFP4Cache.allocate(num_pages, hkv, device=DEV)
+    nv.nvfp4kv_quantize_append(c, x_k.to(DEV), x_v.to(DEV), sm, status)
+    torch.cuda.synchronize()
+    return [t.cpu().numpy() for t in (c.k_data, c.k_scale, c.v_data, c.v_scale)], int(status.item())
+
+
+def run_oracle(x_k, x_v, slots, num_pages, hkv, fp8=False):
+    kf = x_k.float().numpy()
+    vf = x_v.float().numpy()
+    slots = np.asarray(slots, np.int32)
+    if fp8:
+        kc = np.zeros((num_pages, hkv, 16, 128), np.uint8)
+        vc = np.zeros_like(kc)
+        oracle.fp8_quantize_append(kf, slots, kc)
+        oracle.fp8_quantize_append(vf, slots, vc)
+        return [kc, vc]
+    pools = [np.zeros((num_pages, hkv, 16, s), np.uint8) for s in (64, 8, 64, 8)]
+    oracle.quantize_append(kf, slots, pools[0], pools[1])
+    oracle.quantize_append(vf, slots, pools[2], pools[3])
+    return pools
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_tiny_workload_bit_exact(dtype, fp8):
+    w = workloads.make("tiny")
+    bt, num_pages = workloads.block_table(w, spare_pages=2)
+    ks, vs, slots = [], [], []
+    for b in range(w.batch):
+        L = w.seq_lens[b]
+        ks.append(workloads.kv_rows(w, "k", b, 0, L))
+        vs.append(workloads.kv_rows(w, "v", b, 0, L))
+        slots.append(workloads.slot_mapping(w, bt, b, 0, L))
+    k = torch.cat(ks).to(dtype)
+    v = torch.cat(vs).to(dtype)
+    slots = np.concatenate(slots)
+    got, st = run_gpu(k, v, slots, num_pages, w.num_kv_heads, fp8)
+    want = run_oracle(k, v, slots, num_pages, w.num_kv_heads, fp8)
+    assert st == 0
+    for g_, w_ in zip(got, want):
+        np.testing.assert_array_equal(g_, w_)
+
+
+@pytest.mark.parametrize("name", ["llama70b", "ctx32k", "ctx1m"])
+def test_distributions_bit_exact(name):
+    """Outlier channels, per-head scales, Student-t tails: 3000 tokens."""
+    w = workloads.make(name, batch=1, seq_len=3000)
+    L = w.seq_lens[0]
+    bt, num_pages = workloads.block_table(w)
+    k = workloads.kv_rows(w, "k", 0, 0, L)
+    v = workloads.kv_rows(w, "v", 0, 0, L)
+    slots = workloads.slot_mapping(w, bt, 0, 0, L)
+    for fp8 in (False, True):
+        got, st = run_gpu(k, v, slots, num_pages, w.num_kv_heads, fp8)
+        want = run_oracle(k, v, slots, num_pages, w.num_kv_heads, fp8)
+        assert st == 0
+        for g_, w_ in zip(got, want):
+            np.testing.assert_array_equal(g_, w_)
+
+
+def test_skipped_and_out_of_range_slots():
+    rng = np.random.default_rng(0)
+    T, hkv, pages = 40, 2, 4
+    k = torch.from_numpy(rng.standard_normal((T, hkv, 128)).astype(np.float32))
+    v = torch.from_numpy(rng.standard_normal((T, hkv, 128)).astype(np.float32))
+    slots = rng.permutation(pages * 16)[:T].astype(np.int32)
+    slots[3] = -1
+    slots[7] = -5
+    good = slots.copy()
+    slots[11] = pages * 16 + 3            # out of range: skipped and reported
+    good[11] = -1
+    got, st = run_gpu(k, v, slots, pages, hkv)
+    want = run_oracle(k, v, good, pages, hkv)
+    assert st == nv.DEV_BAD_SLOT
+    for g_, w_ in zip(got, want):
+        np.testing.assert_array_equal(g_, w_)
+
+
+def _blocks_to_gpu_codes(blocks):
+    """Quantise float32 blocks [N][16] (N multiple of 8) as rows of one kv head."""
+    n = blocks.shape[0]
+    T = n // 8
+    pages = (T + 15) // 16
+    x = torch.from_numpy(blocks.reshape(T, 1, 128)).to(DEV)
+    c = nv.NVFP4Cache.allocate(pages, 1, device=DEV)
+    sm = torch.arange(T, dtype=torch.int32, device=DEV)
+    nv.nvfp4kv_quantize_append(c, x, x, sm)
+    data = c.k_data.reshape(-1, 64)[:T].reshape(n, 8)
+    scale = c.k_scale.reshape(-1, 8)[:T].reshape(n)
+    codes = torch.stack([data & 15, data >> 4], -1).reshape(n, 16)
+    return codes, scale
+
+
+def test_every_element_value_at_unit_scale():
+    """Every finite fp32 with |x| <= 6 (about 2.2e9 values) is quantised at
+    block scale 1 (each block holds 15 test values and one 6.0) and compared
+    with the oracle's E2M1 encoder, value by value."""
+    six = np.float32(6.0)
+    lim = int(np.float32(6.0).view(np.uint32))           # all non-negative patterns <= 6.0
+    step = 15 * 8 * (1 << 18)                            # values per chunk (multiple of 15*8)
+    total_checked = 0
+    for sign in (0, 0x80000000):
+        for start in range(0, lim + 1, step):
+            stop = min(lim + 1, start + step)
+            bits = np.arange(start, stop, dtype=np.uint64).astype(np.uint32) | np.uint32(sign)
+            vals = bits.view(np.float32)
+            pad = (-len(vals)) % (15 * 8)
+            vals_p = np.concatenate([vals, np.zeros(pad, np.float32)])
+            blocks = np.empty((len(vals_p) // 15, 16), np.float32)
+            blocks[:, :15] = vals_p.reshape(-1, 15)
+            blocks[:, 15] = six
+            codes, scale = _blocks_to_gpu_codes(blocks)
+            assert bool((scale == 0x38).all())            # E4M3(1.0)
+            got = codes[:, :15].reshape(-1)[:len(vals)].cpu().numpy()
+            want = oracle.e2m1_encode(vals)
+            np.testing.assert_array_equal(got, want)
+            total_checked += len(vals)
+    assert total_checked == 2 * (lim + 1)
+
+
+def test_block_scale_sweep():
+    """amax over every fp32 exponent from 2^-14 to 2^12 with the mantissa
+    patterns next to every E4M3 rounding boundary, plus random amax: scale
+    byte and all codes against the oracle's block quantiser."""
+    mant = []
+    for hi in range(1 << 16):
+        for lo in (0, 1, 0x3F, 0x40, 0x41, 0x7F):
+            mant.append((hi << 7) | lo)
+    mant = np.array(mant, np.uint32)
+    exps = np.arange(127 - 14, 127 + 13, dtype=np.uint32)
+    amax = ((exps[:, None] << 23) | mant[None, :]).reshape(-1).view(np.float32)
+    rng = np.random.default_rng(1)
+    amax = np.concatenate([amax, np.exp2(rng.uniform(-20, 13, 1 << 20)).astype(np.float32)])
+    n = len(amax) - len(amax) % 8
+    amax = amax[:n]
+    frac = rng.uniform(-1, 1, (n, 16)).astype(np.float32)
+    blocks = (frac * amax[:, None]).astype(np.float32)
+    blocks[np.arange(n), rng.integers(0, 16, n)] = amax * np.where(rng.integers(0, 2, n) == 1, 1, -1)
+    for lo in range(0, n, 1 << 22):
+        hi = min(n, lo + (1 << 22))
+        codes, scale = _blocks_to_gpu_codes(blocks[lo:hi])
+        x = blocks[lo:hi].reshape(-1, 1, 128)
+        T = x.shape[0]
+        data = np.zeros((T, 1, 1, 64), np.uint8)
+        sc = np.zeros((T, 1, 1, 8), np.uint8)
+        oracle.quantize_append(x, np.arange(T, dtype=np.int32), data, sc, page_size=1)
+        np.testing.assert_array_equal(scale.cpu().numpy(), sc.reshape(-1))
+        want = np.stack([data & 15, data >> 4], -1).reshape(hi - lo, 16)
+        np.testing.assert_array_equal(codes.cpu().numpy(), want)
