@@ -59,6 +59,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--num-workers", type=int, default=0)
+    ap.add_argument("--soak-seconds", type=float, default=1.0,
+                    help="untimed load before the timed region so clock samples see load clocks")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -320,7 +324,7 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(local)
     sampler.start()
     # soak: keep the GPU loaded for ~1 s so the clock samples see load clocks
-    t_end = time.time() + 1.0
+    t_end = time.time() + args.soak_seconds
     i = 0
     while time.time() < t_end:
         setup.step(i)
@@ -332,9 +336,12 @@ def run_ours(args, world, rank, local):
     total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
     value = tokens * world / (ms_per_step / 1e3)
-    e2e_ms, h2d, d2h = time_e2e(setup, args.steps, world)
-    e2e_ms = max_over_ranks(e2e_ms, world)
-    e2e_value = tokens * world / (e2e_ms / args.steps / 1e3)
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = time_e2e(setup, args.steps, world)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        e2e = {"value": tokens * world / (e2e_ms / args.steps / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     st = int(setup.status.item())
     hbm = (measured_peaks() or {}).get("hbm_gbs")
     peak_src = "measured"
@@ -363,7 +370,7 @@ def run_ours(args, world, rank, local):
                      "frac": achieved / hbm, "frac_of_8tbs_nominal": achieved / 8000.0,
                      "alg_bytes_per_launch": alg_bytes, "decode_ms": dec_ms,
                      "traffic": profiled_traffic("decode_nvfp4", args.workload)},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "device_status": st,
@@ -382,7 +389,8 @@ def run_ours(args, world, rank, local):
             "value": f_value, "unit": UNIT, "ms_per_step": f_total / args.steps, "decode_ms": f_dec,
             "achieved_gbs": f_bytes / (f_dec / 1e3) / 1e9,
             "nvfp4_over_fp8_step": value / f_value, "nvfp4_over_fp8_decode": f_dec / dec_ms}
-    cpu = cpu_baseline(w, budget_s=10.0) if rank == 0 and world == 1 else None
+    cpu = (cpu_baseline(w, budget_s=10.0)
+           if rank == 0 and world == 1 and not args.no_cpu_baseline else None)
     if cpu is not None:
         result["cpu_baseline"] = cpu
     return result

@@ -118,6 +118,17 @@ __device__ __forceinline__ int tok_perm(int t)
 
 // ---- per-format page staging and dequantisation ----------------------------
 
+// Shared-memory byte offsets a lane reads inside one stage; they depend only on
+// the lane, so they are computed once.
+struct LaneOffsets {
+    uint32_t k[4];    // K data (NVFP4: rows A, B; FP8: rows A, A, B, B chunks)
+    uint32_t ks[2];   // K scales (NVFP4)
+    uint32_t v[4];    // V data of tokens t0, t1, t0+8, t1+8
+    uint32_t vs[4];   // V scales (NVFP4)
+    int tt[4];        // physical tokens of the V reads
+    int tA;           // physical token of logical QK row gid (row gid+8 is tA+8)
+};
+
 // NVFP4: a page-head stages K data (16 rows x 64 B), V data (same), both via
 // TMA with the 64-byte swizzle, and K / V scales (16 x 8 B) via bulk copies.
 struct Nvfp4Format {
@@ -136,16 +147,36 @@ struct Nvfp4Format {
         return (t << 6) + ((c ^ ((t >> 1) & 3)) << 4);
     }
 
+    __device__ static __forceinline__ LaneOffsets offsets(int gid, int tig)
+    {
+        LaneOffsets o;
+        o.tA = tok_perm(gid);
+        const int tB = o.tA + 8;
+        o.k[0] = sw(o.tA, tig);
+        o.k[1] = sw(tB, tig);
+        o.k[2] = o.k[3] = 0;
+        o.ks[0] = o.tA * 8 + 2 * tig;
+        o.ks[1] = tB * 8 + 2 * tig;
+        const int t0 = tok_perm(2 * tig), t1 = tok_perm(2 * tig + 1);
+        const int tt[4] = {t0, t1, t0 + 8, t1 + 8};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            o.tt[i] = tt[i];
+            o.v[i] = kTileBytes + sw(tt[i], gid >> 1) + ((gid & 1) << 3);
+            o.vs[i] = 128 + tt[i] * 8 + gid;
+        }
+        return o;
+    }
+
     // K fragments of logical rows gid (fa) and gid+8 (fb): f16x2 of channels
     // 32*tig + 2m, 2m+1 for m = 0..15.
-    __device__ static __forceinline__ void load_k(uint32_t data, uint32_t scale, int tA, int tig,
+    __device__ static __forceinline__ void load_k(uint32_t data, uint32_t scale, const LaneOffsets &o,
                                                   uint32_t (&fa)[16], uint32_t (&fb)[16])
     {
-        const int tB = tA + 8;
-        const uint4 ka = lds128(data + sw(tA, tig));
-        const uint4 kb = lds128(data + sw(tB, tig));
-        const uint32_t sa = e4m3x2_to_f16x2(lds_u16(scale + tA * 8 + 2 * tig));
-        const uint32_t sb = e4m3x2_to_f16x2(lds_u16(scale + tB * 8 + 2 * tig));
+        const uint4 ka = lds128(data + o.k[0]);
+        const uint4 kb = lds128(data + o.k[1]);
+        const uint32_t sa = e4m3x2_to_f16x2(lds_u16(scale + o.ks[0]));
+        const uint32_t sb = e4m3x2_to_f16x2(lds_u16(scale + o.ks[1]));
         const uint32_t sa0 = __byte_perm(sa, 0, 0x1010), sa1 = __byte_perm(sa, 0, 0x3232);
         const uint32_t sb0 = __byte_perm(sb, 0, 0x1010), sb1 = __byte_perm(sb, 0, 0x3232);
         const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w};
@@ -165,24 +196,20 @@ struct Nvfp4Format {
     // V^T A-fragments for the 8 m-tiles: tile j, row gid <-> channel
     // 16*gid + 2j, row gid+8 <-> 16*gid + 2j + 1; columns = logical tokens
     // (2tig, 2tig+1) in a0/a1 and (2tig+8, 2tig+9) in a2/a3.
-    __device__ static __forceinline__ void load_v(uint32_t data, uint32_t scale, int gid, int tig,
+    __device__ static __forceinline__ void load_v(uint32_t data, uint32_t scale, const LaneOffsets &o,
                                                   int valid, uint32_t (&va)[8][4])
     {
-        const uint32_t vbase = data + kTileBytes;
-        const uint32_t sbase = scale + 128;
-        const int t0 = tok_perm(2 * tig), t1 = tok_perm(2 * tig + 1);
-        const int tt[4] = {t0, t1, t0 + 8, t1 + 8};
         uint2 v[4];
         uint32_t s[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            v[i] = lds64(vbase + sw(tt[i], gid >> 1) + ((gid & 1) << 3));
-            s[i] = lds_u8(sbase + tt[i] * 8 + gid);
+            v[i] = lds64(data + o.v[i]);
+            s[i] = lds_u8(scale + o.vs[i]);
         }
         if (valid < kPageSize) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                if (tt[i] >= valid) {
+                if (o.tt[i] >= valid) {
                     v[i] = make_uint2(0u, 0u);
                     s[i] = 0u;
                 }
@@ -227,12 +254,32 @@ struct Fp8Format {
         return (t << 7) + ((c ^ (t & 7)) << 4);
     }
 
-    __device__ static __forceinline__ void load_k(uint32_t data, uint32_t, int tA, int tig,
+    __device__ static __forceinline__ LaneOffsets offsets(int gid, int tig)
+    {
+        LaneOffsets o;
+        o.tA = tok_perm(gid);
+        const int tB = o.tA + 8;
+        o.k[0] = sw(o.tA, 2 * tig);
+        o.k[1] = sw(o.tA, 2 * tig + 1);
+        o.k[2] = sw(tB, 2 * tig);
+        o.k[3] = sw(tB, 2 * tig + 1);
+        o.ks[0] = o.ks[1] = 0;
+        const int t0 = tok_perm(2 * tig), t1 = tok_perm(2 * tig + 1);
+        const int tt[4] = {t0, t1, t0 + 8, t1 + 8};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            o.tt[i] = tt[i];
+            o.v[i] = kTileBytes + sw(tt[i], gid);
+            o.vs[i] = 0;
+        }
+        return o;
+    }
+
+    __device__ static __forceinline__ void load_k(uint32_t data, uint32_t, const LaneOffsets &o,
                                                   uint32_t (&fa)[16], uint32_t (&fb)[16])
     {
-        const int tB = tA + 8;
-        const uint4 a0 = lds128(data + sw(tA, 2 * tig)), a1 = lds128(data + sw(tA, 2 * tig + 1));
-        const uint4 b0 = lds128(data + sw(tB, 2 * tig)), b1 = lds128(data + sw(tB, 2 * tig + 1));
+        const uint4 a0 = lds128(data + o.k[0]), a1 = lds128(data + o.k[1]);
+        const uint4 b0 = lds128(data + o.k[2]), b1 = lds128(data + o.k[3]);
         const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -242,20 +289,17 @@ struct Fp8Format {
         }
     }
 
-    __device__ static __forceinline__ void load_v(uint32_t data, uint32_t, int gid, int tig, int valid,
+    __device__ static __forceinline__ void load_v(uint32_t data, uint32_t, const LaneOffsets &o, int valid,
                                                   uint32_t (&va)[8][4])
     {
-        const uint32_t vbase = data + kTileBytes;
-        const int t0 = tok_perm(2 * tig), t1 = tok_perm(2 * tig + 1);
-        const int tt[4] = {t0, t1, t0 + 8, t1 + 8};
         uint4 v[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            v[i] = lds128(vbase + sw(tt[i], gid));
+            v[i] = lds128(data + o.v[i]);
         if (valid < kPageSize) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                if (tt[i] >= valid)
+                if (o.tt[i] >= valid)
                     v[i] = make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
@@ -319,6 +363,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
+    // everything below reads data the previous kernel in the stream may write
+    pdl_wait();
     const int max_len = p.max_pages * kPageSize;
     build_prefix(p.seq_lens, p.batch, p.hkv, max_len, prefix, scratch,
                  blockIdx.x == 0 ? p.dev_status : nullptr);
@@ -351,7 +397,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     lookup(win + lane, cur_phys, cur_h);
     lookup(win + 32 + lane, nxt_phys, nxt_h);
 
-    auto issue = [&](int j) {
+    // Stage `st` receives page-head j (called by the whole warp, in order of j).
+    auto issue = [&](int j, int st) {
         int rel = j - win;
         if (rel >= 32) {
             win += 32;
@@ -367,7 +414,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
                 report(p.dev_status, NVFP4KV_DEV_BAD_PAGE);
                 phys = 0;
             }
-            const int st = (j - lo) % S;
             const uint32_t bar = wbar + 8 * st;
             const int z = phys * p.hkv + hh;
             mbar_arrive_expect_tx(bar, Fmt::kStageTx);
@@ -391,12 +437,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
 
     const int npro = min(S, hi - lo);
     for (int j = lo; j < lo + npro; ++j)
-        issue(j);
+        issue(j, j - lo);
 
     uint32_t qf[16];
     float m0, m1, l0, l1;
     float oacc[8][4];
     const int g = p.group;
+    const LaneOffsets off = Fmt::offsets(gid, tig);
 
     auto start_segment = [&]() {
         if (gid < g) {
@@ -489,18 +536,28 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     };
 
     start_segment();
-    const int tA = tok_perm(gid);
 
+    int st = 0;            // ring stage of page-head j
+    uint32_t ph = 0;       // phase parity of that stage's barrier
     for (int j = lo; j < hi; ++j) {
-        const int st = (j - lo) % S;
-        const uint32_t parity = static_cast<uint32_t>(((j - lo) / S) & 1);
-        if (!mbar_wait_bounded(wbar + 8 * st, parity, kWaitLimit)) {
+        // Lanes poll independently and may leave the loop at different polls;
+        // the vote reconverges the warp before the warp-wide MMAs below and
+        // makes the give-up decision uniform.
+        const bool arrived = mbar_wait_bounded(wbar + 8 * st, ph, kWaitLimit);
+        if (!__all_sync(kFullMask, arrived)) {
             // staged data never arrived: report, let the copies in flight land, stop
             if (lane == 0)
                 report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
-            for (int jj = j; jj < min(j + S, hi); ++jj)
-                mbar_wait_bounded(wbar + 8 * ((jj - lo) % S), static_cast<uint32_t>(((jj - lo) / S) & 1),
-                                  kWaitLimit);
+            const int pending = min(S, hi - j);
+            for (int k = 0; k < pending; ++k) {
+                int s2 = st + k;
+                uint32_t p2 = ph;
+                if (s2 >= S) {
+                    s2 -= S;
+                    p2 ^= 1u;
+                }
+                mbar_wait_bounded(wbar + 8 * s2, p2, kWaitLimit);
+            }
             return;
         }
         const int valid = (pg == n - 1) ? (L - pg * kPageSize) : kPageSize;
@@ -511,26 +568,27 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
         {
             uint32_t fa[16], fb[16];
-            Fmt::load_k(sdata, sscale, tA, tig, fa, fb);
+            Fmt::load_k(sdata, sscale, off, fa, fb);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
                 mma_f16_16816(sc, fa[2 * s], fb[2 * s], fa[2 * s + 1], fb[2 * s + 1], qf[2 * s], qf[2 * s + 1]);
         }
         if (valid < kPageSize) {
-            if (tA >= valid)
+            if (off.tA >= valid)
                 sc[0] = sc[1] = -INFINITY;
-            if (tA + 8 >= valid)
+            if (off.tA + 8 >= valid)
                 sc[2] = sc[3] = -INFINITY;
         }
-        // online softmax over the 16 tokens of this page, per head (2tig, 2tig+1)
+        // Online softmax, heads (2tig, 2tig+1).  The running maximum is only
+        // moved when some score exceeds it by more than 2^kLazyRescale, so the
+        // common page needs no cross-lane reduction; P then stays <= 2^8.
         float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+        if (__any_sync(kFullMask, (mx0 > m0 + kLazyRescale) || (mx1 > m1 + kLazyRescale))) {
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, o));
-        }
-        const bool grow = (mx0 > m0 + kLazyRescale) || (mx1 > m1 + kLazyRescale);
-        if (__any_sync(kFullMask, grow)) {
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, o));
+            }
             const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
             const float a0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - n0);
             const float a1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - n1);
@@ -556,7 +614,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         // O^T += V^T . P^T
         {
             uint32_t va[8][4];
-            Fmt::load_v(sdata, sscale, gid, tig, valid, va);
+            Fmt::load_v(sdata, sscale, off, valid, va);
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj)
                 mma_f16_16816(oacc[jj], va[jj][0], va[jj][1], va[jj][2], va[jj][3], pb0, pb1);
@@ -564,7 +622,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
 
         __syncwarp();
         if (j + S < hi)
-            issue(j + S);
+            issue(j + S, st);
+        if (++st == S) {
+            st = 0;
+            ph ^= 1u;
+        }
 
         ++pg;
         if (pg == n || j + 1 == hi) {
@@ -585,12 +647,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
             }
         }
     }
+    pdl_launch_dependents();
 }
 
 // ---- split merge ---------------------------------------------------------------
-// One CTA of 128 threads per (sequence, kv head, query head of the group).
-// Segments that one worker covered were written by the decode kernel; empty
-// sequences get zeros here.
-__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p);
+// One CTA of kMergeThreads threads per (sequence, kv head, query head of the
+// group).  Segments that one worker covered were written by the decode kernel;
+// empty sequences get zeros here.
+constexpr int kMergeThreads = 256;
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p);
 
 } // namespace nvfp4kv

@@ -13,8 +13,7 @@ static cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, c
     if (e != cudaSuccess)
         return e;
     const int grid = (p.num_workers + kDecodeWarps - 1) / kDecodeWarps;
-    decode_kernel<Fmt><<<grid, kDecodeWarps * 32, smem, s>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_pdl(decode_kernel<Fmt>, dim3(grid), dim3(kDecodeWarps * 32), smem, s, tk, tv, p);
 }
 
 cudaError_t launch_decode_nvfp4(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,

@@ -16,6 +16,7 @@ namespace nvfp4kv {
 
 __global__ void __launch_bounds__(128) dequant_prefix_kernel(const PrefixParams p)
 {
+    pdl_wait();
     const int tok = threadIdx.x >> 3, blk = threadIdx.x & 7;
     const long long units = static_cast<long long>(p.batch) * p.max_pages * p.hkv * 2;
     const int max_len = p.max_pages * kPageSize;
@@ -72,8 +73,7 @@ cudaError_t launch_dequant_prefix_fp8(const PrefixParams &p, cudaStream_t s)
     long long grid = static_cast<long long>(sms > 0 ? sms : 1) * 16;
     if (grid > units)
         grid = units;
-    dequant_prefix_kernel<<<static_cast<unsigned>(grid), 128, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(dequant_prefix_kernel, dim3(static_cast<unsigned>(grid)), dim3(128), 0, s, p);
 }
 
 } // namespace nvfp4kv

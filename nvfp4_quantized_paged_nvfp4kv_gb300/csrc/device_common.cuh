@@ -232,6 +232,18 @@ __device__ __forceinline__ uint32_t lds_u8(uint32_t addr)
     return v;
 }
 
+// Programmatic dependent launch: wait for the preceding kernel in the stream
+// (no-op when the launch did not allow overlap) / let the next one start.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void report(int32_t *dev_status, int32_t bits)
 {
     if (dev_status != nullptr)

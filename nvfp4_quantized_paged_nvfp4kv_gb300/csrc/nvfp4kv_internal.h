@@ -69,6 +69,27 @@ struct PrefixParams {
     int num_pages;
 };
 
+// Launch with programmatic stream serialisation allowed, so the kernel's
+// prologue may overlap the tail of the previous kernel in the stream; every
+// kernel launched this way calls pdl_wait() before touching data that the
+// previous kernel may still write or read.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 int sm_count();                  // current device, cached
 int default_num_workers();       // sm_count * kDecodeCtasPerSm * kDecodeWarps
 size_t decode_workspace_bytes(int num_workers);

@@ -49,8 +49,12 @@ struct BlockSite {
     int blk;            // block within the row (0..7)
 };
 
+// The cache rows written here may still be read by the previous kernel in the
+// stream (a decode of the last step): wait for it, then let the next start.
 __device__ __forceinline__ BlockSite locate(const QuantParams &p, long long idx)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     BlockSite s{false, 0, 0, 0};
     const long long rows = static_cast<long long>(p.num_tokens) * p.hkv;
     if (idx >= rows * 8)
@@ -132,8 +136,7 @@ static cudaError_t launch_blocks(K kernel, const QuantParams &p, cudaStream_t s)
     const long long grid = (blocks + 255) / 256;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidValue;
-    kernel<<<dim3(static_cast<unsigned>(grid), 2), 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kernel, dim3(static_cast<unsigned>(grid), 2), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_quantize_append_nvfp4(const QuantParams &p, cudaStream_t s)

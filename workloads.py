@@ -74,7 +74,9 @@ class Workload:
 
 
 def _seed(*parts) -> int:
-    return zlib.crc32(repr(parts).encode()) & 0x7FFFFFFF
+    # integers of any type (Python or numpy) seed identically
+    norm = tuple(int(x) if isinstance(x, (int, np.integer)) else x for x in parts)
+    return zlib.crc32(repr(norm).encode()) & 0x7FFFFFFF
 
 
 def make(name: str, batch: int | None = None, seq_len: int | None = None) -> Workload:
