@@ -3,7 +3,8 @@
  *
  * C ABI.  Plain pointers and sizes only.  Every device pointer is a CUDA
  * device address owned by the caller; the library allocates no device memory
- * and keeps no state between calls except a per-device cache of the SM count.
+ * and keeps no state between calls except a per-device cache of the SM count
+ * and the fixed scratch array of nvfp4kv_paged_decode_static_scratch.
  * Every launching call is asynchronous on the given stream: it validates its
  * arguments on the host first (returning an error and launching nothing when
  * they are bad), then enqueues its kernels and returns.  A NULL stream is the
@@ -143,7 +144,7 @@ size_t nvfp4kv_decode_workspace_size(int32_t num_workers);
  *   aligned; its contents need no initialisation and are overwritten.  Two
  *   calls in flight at once must not share a workspace.
  * num_workers: 0 = automatic; otherwise the number of warp workers the
- *   page-heads are balanced over (results agree to fp32 rounding for any
+ *   page-heads are balanced over (results agree up to rounding for any
  *   value).
  * Launches two kernels (split-KV attention, then the split merge). */
 nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q,
@@ -153,6 +154,29 @@ nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q,
                                     nvfp4kv_dtype out_dtype, void *workspace,
                                     size_t workspace_bytes, int32_t num_workers,
                                     int32_t *dev_status, nvfp4kv_stream_t stream);
+
+/* Decode without a caller-provided workspace, for callers that cannot
+ * allocate device memory (for example a serving engine whose device memory is
+ * all reserved for weights and KV cache at start-up).  The pages have no
+ * counterpart to this call; it exists for such callers.
+ * Same arguments and result as nvfp4kv_paged_decode, minus the workspace: the
+ * split-KV scratch comes from one array of NVFP4KV_STATIC_SCRATCH_BYTES that
+ * the library keeps on every device that loads it, until the process exits.
+ * num_workers may be at most NVFP4KV_STATIC_SCRATCH_MAX_WORKERS (a larger
+ * value returns NVFP4KV_ERR_WORKSPACE); 0 picks the automatic count, capped at
+ * that maximum.  The first call on a device looks the array up with that
+ * device current, so make it before any stream capture.  All calls on a
+ * device share the array: calls whose kernels can overlap on the GPU race and
+ * must be serialised (for example, issue them on one stream).  Allocates no
+ * memory. */
+#define NVFP4KV_STATIC_SCRATCH_BYTES (16u << 20)
+#define NVFP4KV_STATIC_SCRATCH_MAX_WORKERS 2016
+nvfp4kv_status nvfp4kv_paged_decode_static_scratch(const nvfp4kv_cache *cache, const void *q, int32_t batch,
+                                                   int32_t num_q_heads, const int32_t *block_table,
+                                                   int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                                   float sm_scale, void *out, nvfp4kv_dtype out_dtype,
+                                                   int32_t num_workers, int32_t *dev_status,
+                                                   nvfp4kv_stream_t stream);
 
 /* Extend path ("SGLang stores KV cache in 4 bits", Interpretation ¶2: the
  * cached prefix is dequantised into one FP8 workspace shared across layers).

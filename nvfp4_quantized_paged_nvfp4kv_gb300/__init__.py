@@ -86,6 +86,9 @@ def load(build_if_missing: bool = True):
             "nvfp4kv_decode_workspace_size": (ctypes.c_size_t, [_i32]),
             "nvfp4kv_paged_decode": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _i32, _i32, _vp, _i32, _vp,
                                            ctypes.c_float, _vp, _st, _vp, ctypes.c_size_t, _i32, _vp, _vp]),
+            "nvfp4kv_paged_decode_static_scratch": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _i32, _i32, _vp,
+                                                          _i32, _vp, ctypes.c_float, _vp, _st, _i32, _vp,
+                                                          _vp]),
             "nvfp4kv_dequant_prefix_fp8": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _i32, _vp, _vp, _i32,
                                                  _vp, _vp, _vp, _vp]),
             "fp8kv_quantize_append": (_st, [ctypes.POINTER(_Fp8Cache), _vp, _vp, _st, _i32, _vp, _vp, _vp]),
@@ -227,6 +230,21 @@ def fp8kv_paged_decode(cache: FP8Cache, q, block_table, seq_lens, out, workspace
                        sm_scale=None, num_workers=0, dev_status=None, stream=None) -> None:
     _decode(load().fp8kv_paged_decode, "fp8kv_paged_decode", cache, q, block_table, seq_lens,
             out, workspace, sm_scale, num_workers, dev_status, stream)
+
+
+def nvfp4kv_paged_decode_static_scratch(cache: NVFP4Cache, q, block_table, seq_lens, out,
+                                        sm_scale=None, num_workers=0, dev_status=None,
+                                        stream=None) -> None:
+    """Decode for callers that cannot allocate device memory: the split-KV
+    scratch is the library's own fixed array (see include/nvfp4kv.h)."""
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    B, Hq, _ = q.shape
+    st = load().nvfp4kv_paged_decode_static_scratch(
+        cache.c, _ptr(q), B, Hq, _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        float(sm_scale), _ptr(out), _dtype_code(out), int(num_workers), _ptr(dev_status),
+        _stream(stream))
+    _check(st, "nvfp4kv_paged_decode_static_scratch")
 
 
 def nvfp4kv_dequant_prefix_fp8(cache: NVFP4Cache, block_table, prefix_lens, kv_indptr, k_out, v_out,
