@@ -220,10 +220,7 @@ class DecodeSetup:
         return c
 
     def _clone(self, c):
-        nv = self.nv
-        if self.fmt == "nvfp4":
-            return nv.NVFP4Cache(c.k_data.clone(), c.k_scale.clone(), c.v_data.clone(), c.v_scale.clone())
-        return nv.FP8Cache(c.k.clone(), c.v.clone())
+        return type(c)(c.pool.clone())
 
     def cache_bytes(self):
         return self.caches[0].nbytes()

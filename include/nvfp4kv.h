@@ -34,11 +34,35 @@
  *     q_i = E2M1_rn_satfinite(fl32(x_i / s)), or 0 for all i if s == 0.
  *     Packed byte j = q_{2j} | q_{2j+1} << 4 (low nibble = even channel).
  *
- * NVFP4 cache layout (HND, per K and per V):
- *   data [num_pages][num_kv_heads][page_size][head_dim/2]  uint8
- *   scale[num_pages][num_kv_heads][page_size][head_dim/16] uint8 (E4M3)
- *   A token's slot is physical_page * page_size + offset_in_page.
- * FP8 cache layout: k, v [num_pages][num_kv_heads][page_size][head_dim] E4M3.
+ * Cache layout.  The cache is one pool of page-head records: the record of
+ * kv head h of physical page P starts at byte (P * num_kv_heads + h) * R and
+ * holds the 16 tokens of that page for that head (token t of the page is the
+ * one at slot P * 16 + t).  The pages give only the storage cost (8 packed
+ * bytes + 1 scale byte per 16 values); the arrangement inside a record is this
+ * library's, chosen so the decode stages a record with one bulk copy and reads
+ * it without shared-memory bank conflicts.
+ *
+ * NVFP4 record, R = NVFP4KV_RECORD_BYTES = 2304:
+ *   [0, 1024)     K data: 16 rows of 64 bytes, row t = token t; byte 8*b + i
+ *                 of a row holds channels 16*b + 2i (low nibble) and
+ *                 16*b + 2i + 1 (high nibble).
+ *   [1024, 2048)  V data: 8 rows of 128 bytes; row p holds tokens 2p (low
+ *                 nibbles) and 2p + 1 (high nibbles) of the same channel.  A row
+ *                 is 8 chunks of 16 bytes; group g (0..7) sits in the chunk at
+ *                 position (g + 2p) mod 8, and byte 2j + w of group g is
+ *                 channel 16j + g + 8w.
+ *   [2048, 2176)  K scales: [16 tokens][8 blocks] E4M3 (block b = channels
+ *                 16b .. 16b + 15).
+ *   [2176, 2304)  V scales: [8 rows p][8 blocks][2]; byte (p, b, w) is the scale
+ *                 of token 2p + w, block b.
+ * FP8 record, R = FP8KV_RECORD_BYTES = 4096 (E4M3 at scale 1.0):
+ *   [0, 2048)     K: 16 rows of 128 bytes, row t = token t; the 16-byte chunk
+ *                 at position (c + (t mod 2)) mod 8
+ *                 holds channels 16c .. 16c + 15.
+ *   [2048, 4096)  V: 8 rows of 256 bytes, row p = tokens 2p and 2p + 1; the
+ *                 16-byte chunk at position (c + f(p)) mod 16, with
+ *                 f(p) = (p mod 2) + 4 * (floor(p / 2) mod 2), holds channels
+ *                 8c .. 8c + 7, byte 2i + w being channel 8c + i of token 2p + w.
  *
  * Supported geometry: head_dim 128, page_size 16, num_q_heads a multiple of
  * num_kv_heads with group g = num_q_heads / num_kv_heads in 1..8,
@@ -78,13 +102,13 @@ typedef enum {
 
 typedef enum { NVFP4KV_F32 = 0, NVFP4KV_BF16 = 1 } nvfp4kv_dtype;
 
-/* NVFP4 cache: four pools laid out as above.  Every pool pointer must be
+#define NVFP4KV_RECORD_BYTES 2304
+#define FP8KV_RECORD_BYTES 4096
+
+/* NVFP4 cache: pool of num_pages * num_kv_heads records laid out as above,
  * 16-byte aligned.  global_scale must be 1.0f. */
 typedef struct {
-    void *k_data;
-    void *k_scale;
-    void *v_data;
-    void *v_scale;
+    void *pool;
     int32_t num_pages;
     int32_t num_kv_heads;
     int32_t page_size;
@@ -92,10 +116,10 @@ typedef struct {
     float global_scale;
 } nvfp4kv_cache;
 
-/* FP8-E4M3 comparison cache (scale 1.0).  Pointers 16-byte aligned. */
+/* FP8-E4M3 comparison cache (scale 1.0): pool of records as above, 16-byte
+ * aligned. */
 typedef struct {
-    void *k;
-    void *v;
+    void *pool;
     int32_t num_pages;
     int32_t num_kv_heads;
     int32_t page_size;
@@ -146,7 +170,9 @@ size_t nvfp4kv_decode_workspace_size(int32_t num_workers);
  * num_workers: 0 = automatic; otherwise the number of warp workers the
  *   page-heads are balanced over (results agree up to rounding for any
  *   value).
- * Launches two kernels (split-KV attention, then the split merge). */
+ * Launches two kernels (split-KV attention, then the split merge), both with
+ * programmatic dependent launch allowed, so each may start its prologue while
+ * the previous kernel in the stream drains. */
 nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q,
                                     int32_t batch, int32_t num_q_heads,
                                     const int32_t *block_table, int32_t max_pages_per_seq,
@@ -211,14 +237,16 @@ nvfp4kv_status fp8kv_paged_decode(const fp8kv_cache *cache, const void *q, int32
                                   int32_t num_workers, int32_t *dev_status,
                                   nvfp4kv_stream_t stream);
 
-/* Bytes of all four NVFP4 pools (K and V data and scales) for a geometry:
+/* Bytes of an NVFP4 pool (K and V data and scales) for a geometry:
  * num_pages * num_kv_heads * page_size * 2 * (head_dim/2 + head_dim/16),
  * i.e. 9 bytes per 16 values ("SGLang stores KV cache in 4 bits",
- * Interpretation).  Returns -1 for invalid arguments.  Host only. */
+ * Interpretation); for the supported geometry that is num_pages *
+ * num_kv_heads * NVFP4KV_RECORD_BYTES.  Returns -1 for invalid arguments.
+ * Host only. */
 int64_t nvfp4kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
                             int32_t head_dim);
 
-/* Bytes of both FP8 pools: num_pages * num_kv_heads * page_size * 2 * head_dim. */
+/* Bytes of an FP8 pool: num_pages * num_kv_heads * page_size * 2 * head_dim. */
 int64_t fp8kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
                           int32_t head_dim);
 

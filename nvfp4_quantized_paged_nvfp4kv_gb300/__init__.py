@@ -43,16 +43,19 @@ class Nvfp4kvError(RuntimeError):
         super().__init__(f"{what}: status {status} ({status_string(status)})")
 
 
+NVFP4_RECORD_BYTES = 2304      # one page-head record: K, V data and scales
+FP8_RECORD_BYTES = 4096
+
+
 class _Nvfp4Cache(ctypes.Structure):
-    _fields_ = [("k_data", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
-                ("v_data", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+    _fields_ = [("pool", ctypes.c_void_p),
                 ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("global_scale", ctypes.c_float)]
 
 
 class _Fp8Cache(ctypes.Structure):
-    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+    _fields_ = [("pool", ctypes.c_void_p),
                 ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
@@ -135,55 +138,43 @@ def _dtype_code(t) -> int:
 # --- caches -----------------------------------------------------------------
 
 class NVFP4Cache:
-    """The four NVFP4 pools: data [pages][Hkv][16][64] and scale [pages][Hkv][16][8]."""
+    """An NVFP4 pool: uint8 [num_pages][num_kv_heads][NVFP4_RECORD_BYTES] page-head
+    records (layout in include/nvfp4kv.h)."""
 
-    def __init__(self, k_data, k_scale, v_data, v_scale):
-        self.k_data, self.k_scale, self.v_data, self.v_scale = k_data, k_scale, v_data, v_scale
-        self.num_pages, self.num_kv_heads, self.page_size, half = k_data.shape
-        self.head_dim = half * 2
-        self._c = _Nvfp4Cache(k_data.data_ptr(), k_scale.data_ptr(), v_data.data_ptr(),
-                              v_scale.data_ptr(), self.num_pages, self.num_kv_heads, self.page_size,
-                              self.head_dim, 1.0)
+    record_bytes = NVFP4_RECORD_BYTES
+
+    def __init__(self, pool):
+        self.pool = pool
+        self.num_pages, self.num_kv_heads, rb = pool.shape
+        assert rb == self.record_bytes
+        self.page_size, self.head_dim = PAGE_SIZE, HEAD_DIM
+        self._c = _Nvfp4Cache(pool.data_ptr(), self.num_pages, self.num_kv_heads, PAGE_SIZE, HEAD_DIM, 1.0)
 
     @classmethod
     def allocate(cls, num_pages, num_kv_heads, device="cuda", zero=True):
         import torch
         f = torch.zeros if zero else torch.empty
-        d = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM // 2)
-        s = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM // 16)
-        return cls(f(d, dtype=torch.uint8, device=device), f(s, dtype=torch.uint8, device=device),
-                   f(d, dtype=torch.uint8, device=device), f(s, dtype=torch.uint8, device=device))
+        return cls(f((num_pages, num_kv_heads, cls.record_bytes), dtype=torch.uint8, device=device))
 
     @property
     def c(self):
         return ctypes.byref(self._c)
 
     def nbytes(self) -> int:
-        return sum(t.numel() for t in (self.k_data, self.k_scale, self.v_data, self.v_scale))
+        return self.pool.numel()
 
 
-class FP8Cache:
-    """The two FP8-E4M3 pools [pages][Hkv][16][128]."""
+class FP8Cache(NVFP4Cache):
+    """An FP8-E4M3 pool: uint8 [num_pages][num_kv_heads][FP8_RECORD_BYTES] records."""
 
-    def __init__(self, k, v):
-        self.k, self.v = k, v
-        self.num_pages, self.num_kv_heads, self.page_size, self.head_dim = k.shape
-        self._c = _Fp8Cache(k.data_ptr(), v.data_ptr(), self.num_pages, self.num_kv_heads,
-                            self.page_size, self.head_dim)
+    record_bytes = FP8_RECORD_BYTES
 
-    @classmethod
-    def allocate(cls, num_pages, num_kv_heads, device="cuda", zero=True):
-        import torch
-        f = torch.zeros if zero else torch.empty
-        shape = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM)
-        return cls(f(shape, dtype=torch.uint8, device=device), f(shape, dtype=torch.uint8, device=device))
-
-    @property
-    def c(self):
-        return ctypes.byref(self._c)
-
-    def nbytes(self) -> int:
-        return self.k.numel() + self.v.numel()
+    def __init__(self, pool):
+        self.pool = pool
+        self.num_pages, self.num_kv_heads, rb = pool.shape
+        assert rb == self.record_bytes
+        self.page_size, self.head_dim = PAGE_SIZE, HEAD_DIM
+        self._c = _Fp8Cache(pool.data_ptr(), self.num_pages, self.num_kv_heads, PAGE_SIZE, HEAD_DIM)
 
 
 # --- entry points -------------------------------------------------------------

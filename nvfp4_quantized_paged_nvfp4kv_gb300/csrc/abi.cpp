@@ -1,12 +1,9 @@
-// C ABI of the library: argument validation, tensor-map set-up and launches.
+// C ABI of the library: argument validation and launches.
 // The contract of every entry point is documented in include/nvfp4kv.h.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "nvfp4kv.h"
 #include "nvfp4kv_internal.h"
@@ -51,10 +48,8 @@ nvfp4kv_status check_nvfp4(const nvfp4kv_cache *c)
         return st;
     if (!(c->global_scale == 1.0f))
         return NVFP4KV_ERR_UNSUPPORTED;
-    const void *ptrs[4] = {c->k_data, c->k_scale, c->v_data, c->v_scale};
-    for (const void *p : ptrs)
-        if (p == nullptr || !aligned16(p))
-            return NVFP4KV_ERR_INVALID_ARG;
+    if (c->pool == nullptr || !aligned16(c->pool))
+        return NVFP4KV_ERR_INVALID_ARG;
     return NVFP4KV_OK;
 }
 
@@ -65,7 +60,7 @@ nvfp4kv_status check_fp8(const fp8kv_cache *c)
     nvfp4kv_status st = check_geometry(c->num_pages, c->num_kv_heads, c->page_size, c->head_dim);
     if (st != NVFP4KV_OK)
         return st;
-    if (c->k == nullptr || c->v == nullptr || !aligned16(c->k) || !aligned16(c->v))
+    if (c->pool == nullptr || !aligned16(c->pool))
         return NVFP4KV_ERR_INVALID_ARG;
     return NVFP4KV_OK;
 }
@@ -154,40 +149,6 @@ nvfp4kv_status check_decode(int32_t hkv, int32_t num_pages, const void *q, int32
     return NVFP4KV_OK;
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// Tensor map over one data pool viewed as [page-heads][16 rows][row_bytes]
-// bytes, box = one page-head, swizzle span = row width (64 or 128 bytes).
-bool make_page_map(CUtensorMap *map, const void *pool, int64_t page_heads, uint32_t row_bytes)
-{
-    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-    if (fn == nullptr)
-        return false;
-    cuuint64_t dims[3] = {row_bytes, static_cast<cuuint64_t>(kPageSize), static_cast<cuuint64_t>(page_heads)};
-    cuuint64_t strides[2] = {row_bytes, static_cast<cuuint64_t>(row_bytes) * kPageSize};
-    cuuint32_t box[3] = {row_bytes, static_cast<cuuint32_t>(kPageSize), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(pool), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 } // namespace
 
 extern "C" {
@@ -206,10 +167,7 @@ nvfp4kv_status nvfp4kv_quantize_append(const nvfp4kv_cache *cache, const void *k
     p.k_new = k_new;
     p.v_new = v_new;
     p.slot_mapping = slot_mapping;
-    p.k_data = static_cast<uint8_t *>(cache->k_data);
-    p.k_scale = static_cast<uint8_t *>(cache->k_scale);
-    p.v_data = static_cast<uint8_t *>(cache->v_data);
-    p.v_scale = static_cast<uint8_t *>(cache->v_scale);
+    p.pool = static_cast<uint8_t *>(cache->pool);
     p.dev_status = dev_status;
     p.num_tokens = num_tokens;
     p.hkv = cache->num_kv_heads;
@@ -238,14 +196,8 @@ nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q, i
                       num_workers, dev_status, p);
     if (st != NVFP4KV_OK || batch == 0)
         return st;
-    p.k_scale = static_cast<const uint8_t *>(cache->k_scale);
-    p.v_scale = static_cast<const uint8_t *>(cache->v_scale);
-    const int64_t page_heads = static_cast<int64_t>(cache->num_pages) * cache->num_kv_heads;
-    CUtensorMap tk, tv;
-    if (!make_page_map(&tk, cache->k_data, page_heads, kHeadDim / 2) ||
-        !make_page_map(&tv, cache->v_data, page_heads, kHeadDim / 2))
-        return NVFP4KV_ERR_CUDA;
-    cudaError_t e = launch_decode_nvfp4(p, tk, tv, to_cuda(stream));
+    p.pool = static_cast<const uint8_t *>(cache->pool);
+    cudaError_t e = launch_decode_nvfp4(p, to_cuda(stream));
     if (e == cudaSuccess)
         e = launch_merge(p, to_cuda(stream));
     return from_cuda(e);
@@ -272,10 +224,7 @@ nvfp4kv_status nvfp4kv_dequant_prefix_fp8(const nvfp4kv_cache *cache, const int3
         (reinterpret_cast<uintptr_t>(prefix_lens) & 3u) || (reinterpret_cast<uintptr_t>(kv_indptr) & 3u))
         return NVFP4KV_ERR_INVALID_ARG;
     PrefixParams p{};
-    p.k_data = static_cast<const uint8_t *>(cache->k_data);
-    p.k_scale = static_cast<const uint8_t *>(cache->k_scale);
-    p.v_data = static_cast<const uint8_t *>(cache->v_data);
-    p.v_scale = static_cast<const uint8_t *>(cache->v_scale);
+    p.pool = static_cast<const uint8_t *>(cache->pool);
     p.block_table = block_table;
     p.prefix_lens = prefix_lens;
     p.kv_indptr = kv_indptr;
@@ -303,8 +252,7 @@ nvfp4kv_status fp8kv_quantize_append(const fp8kv_cache *cache, const void *k_new
     p.k_new = k_new;
     p.v_new = v_new;
     p.slot_mapping = slot_mapping;
-    p.k_data = static_cast<uint8_t *>(cache->k);
-    p.v_data = static_cast<uint8_t *>(cache->v);
+    p.pool = static_cast<uint8_t *>(cache->pool);
     p.dev_status = dev_status;
     p.num_tokens = num_tokens;
     p.hkv = cache->num_kv_heads;
@@ -328,11 +276,8 @@ nvfp4kv_status fp8kv_paged_decode(const fp8kv_cache *cache, const void *q, int32
                       num_workers, dev_status, p);
     if (st != NVFP4KV_OK || batch == 0)
         return st;
-    const int64_t page_heads = static_cast<int64_t>(cache->num_pages) * cache->num_kv_heads;
-    CUtensorMap tk, tv;
-    if (!make_page_map(&tk, cache->k, page_heads, kHeadDim) || !make_page_map(&tv, cache->v, page_heads, kHeadDim))
-        return NVFP4KV_ERR_CUDA;
-    cudaError_t e = launch_decode_fp8(p, tk, tv, to_cuda(stream));
+    p.pool = static_cast<const uint8_t *>(cache->pool);
+    cudaError_t e = launch_decode_fp8(p, to_cuda(stream));
     if (e == cudaSuccess)
         e = launch_merge(p, to_cuda(stream));
     return from_cuda(e);

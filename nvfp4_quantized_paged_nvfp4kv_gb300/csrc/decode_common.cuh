@@ -10,9 +10,9 @@
 // sequence: 16 tokens.  Page-heads are numbered sequence-major, then kv head,
 // then page, so the page-heads of one (sequence, kv head) pair -- a "segment"
 // -- are contiguous.  The T page-heads are split evenly over NW warp workers:
-// worker w takes [T*w/NW, T*(w+1)/NW).  Each warp stages its page-heads through
-// its own ring of shared-memory buffers filled by TMA (lane 0 issues), and
-// computes for the g <= 8 query heads of the kv head:
+// worker w takes [T*w/NW, T*(w+1)/NW).  Each warp stages its page-head records
+// through its own ring of shared-memory buffers, one bulk copy per record
+// (lane 0 issues), and computes for the g <= 8 query heads of the kv head:
 //   S^T[16 tok x 8 heads] = K[16 x 128] . Q^T          (8 x mma m16n8k16)
 //   online softmax (fp32, exp2 domain, lazy rescale)
 //   O^T[128 x 8]        += V^T[128 x 16] . P^T[16 x 8]  (8 x mma m16n8k16)
@@ -21,13 +21,18 @@
 // others leave (O, m, l) partials in the workspace for the merge kernel.
 #pragma once
 
+#include <type_traits>
+
 #include "device_common.cuh"
 #include "nvfp4kv.h"
 
 namespace nvfp4kv {
 
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a staged-data wait gives up
-constexpr float kLazyRescale = 8.0f;       // rescale O only when the max grows by > 2^8
+// The running max is moved only when a score exceeds it by more than this
+// (log2 units), so P <= 2^7; with a V block scale <= 448, P * scale <= 57344
+// stays finite in fp16.
+constexpr float kLazyRescale = 7.0f;
 
 __device__ __forceinline__ int clamp_len(int L, int max_len)
 {
@@ -108,75 +113,58 @@ __device__ __forceinline__ int partial_slot(int w, int seg_begin, long long T, l
     return 2 * w + (lo_w >= seg_begin ? 0 : 1);
 }
 
-// Logical token row -> physical token of the page (bit 0 ^= bit 1).  Used for
-// both QK rows and PV columns so the two stay consistent; it spreads the rows a
-// warp touches over different shared-memory banks.
-__device__ __forceinline__ int tok_perm(int t)
-{
-    return t ^ ((t >> 1) & 1);
-}
-
 // ---- per-format page staging and dequantisation ----------------------------
+//
+// A warp stages one whole page-head record (layout in include/nvfp4kv.h) with a
+// single bulk copy and reads it from shared memory.  Lane (gid = lane/4,
+// tig = lane%4) holds the MMA fragments:
+//   QK^T  A = K rows gid and gid+8 (tokens), channels 32*tig .. 32*tig + 31;
+//         B = Q^T, the same 32 channels of query head gid.
+//   PV    A = V^T, columns (tokens) 2tig, 2tig+1 (a0/a1) and 2tig+8, 2tig+9
+//         (a2/a3); the channel of m-tile j, row r is Fmt::channel(j, r).
+// The record arrangement (chosen by the writer) makes every shared-memory read
+// below conflict-free and hands cvt.f16x2 the two tokens of a V column pair in
+// one byte (NVFP4) or one 16-bit unit (FP8).
 
-// Shared-memory byte offsets a lane reads inside one stage; they depend only on
-// the lane, so they are computed once.
 struct LaneOffsets {
-    uint32_t k[4];    // K data (NVFP4: rows A, B; FP8: rows A, A, B, B chunks)
-    uint32_t ks[2];   // K scales (NVFP4)
-    uint32_t v[4];    // V data of tokens t0, t1, t0+8, t1+8
-    uint32_t vs[4];   // V scales (NVFP4)
-    int tt[4];        // physical tokens of the V reads
-    int tA;           // physical token of logical QK row gid (row gid+8 is tA+8)
+    uint32_t k[4];    // K data (NVFP4: rows gid, gid+8; FP8: rows gid, gid+8, two chunks each)
+    uint32_t ks[2];   // K scales of rows gid, gid+8 (NVFP4)
+    uint32_t v[4];    // V data (NVFP4: rows tig, tig+4; FP8: two chunks of each)
+    uint32_t vs[2];   // V scale rows tig, tig+4 (NVFP4)
 };
 
-// NVFP4: a page-head stages K data (16 rows x 64 B), V data (same), both via
-// TMA with the 64-byte swizzle, and K / V scales (16 x 8 B) via bulk copies.
 struct Nvfp4Format {
     static constexpr int kStages = 5;
-    static constexpr int kTileBytes = 1024;
-    static constexpr int kStageData = 2 * kTileBytes;
-    static constexpr int kStageScale = 256;
-    static constexpr uint32_t kStageTx = 2 * kTileBytes + 2 * 128;
+    static constexpr int kRecord = 2304;
 
-    // Byte offset of 16-byte chunk c of 64-byte row t in a tile written with
-    // the 64-byte swizzle (address bits [5:4] ^= bits [8:7]).  With tok_perm
-    // the K reads (two rows of one 128-byte line per quarter warp) and the V
-    // reads (rows 0,3,4,7 or 1,2,5,6 per half warp) are free of bank conflicts.
-    __device__ static __forceinline__ uint32_t sw(int t, int c)
-    {
-        return (t << 6) + ((c ^ ((t >> 1) & 3)) << 4);
-    }
+    // m-tile j, row r (0..15) is channel 16j + r: each m-tile is one scale block.
+    __device__ static __forceinline__ int channel(int j, int gid, int w) { return 16 * j + gid + 8 * w; }
 
     __device__ static __forceinline__ LaneOffsets offsets(int gid, int tig)
     {
         LaneOffsets o;
-        o.tA = tok_perm(gid);
-        const int tB = o.tA + 8;
-        o.k[0] = sw(o.tA, tig);
-        o.k[1] = sw(tB, tig);
+        o.k[0] = gid * 64 + 16 * tig;
+        o.k[1] = o.k[0] + 512;
         o.k[2] = o.k[3] = 0;
-        o.ks[0] = o.tA * 8 + 2 * tig;
-        o.ks[1] = tB * 8 + 2 * tig;
-        const int t0 = tok_perm(2 * tig), t1 = tok_perm(2 * tig + 1);
-        const int tt[4] = {t0, t1, t0 + 8, t1 + 8};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            o.tt[i] = tt[i];
-            o.v[i] = kTileBytes + sw(tt[i], gid >> 1) + ((gid & 1) << 3);
-            o.vs[i] = 128 + tt[i] * 8 + gid;
-        }
+        o.ks[0] = 2048 + gid * 8 + 2 * tig;
+        o.ks[1] = o.ks[0] + 64;
+        o.v[0] = 1024 + tig * 128 + ((gid + 2 * tig) & 7) * 16;
+        o.v[1] = o.v[0] + 512;                           // row tig + 4, same chunk position
+        o.v[2] = o.v[3] = 0;
+        o.vs[0] = 2176 + tig * 16;
+        o.vs[1] = o.vs[0] + 64;
         return o;
     }
 
-    // K fragments of logical rows gid (fa) and gid+8 (fb): f16x2 of channels
-    // 32*tig + 2m, 2m+1 for m = 0..15.
-    __device__ static __forceinline__ void load_k(uint32_t data, uint32_t scale, const LaneOffsets &o,
-                                                  uint32_t (&fa)[16], uint32_t (&fb)[16])
+    // K fragments of rows gid (fa) and gid+8 (fb): f16x2 of channels
+    // 32*tig + 2m, 2m+1 for m = 0..15, scaled exactly.
+    __device__ static __forceinline__ void load_k(uint32_t rec, const LaneOffsets &o, uint32_t (&fa)[16],
+                                                  uint32_t (&fb)[16])
     {
-        const uint4 ka = lds128(data + o.k[0]);
-        const uint4 kb = lds128(data + o.k[1]);
-        const uint32_t sa = e4m3x2_to_f16x2(lds_u16(scale + o.ks[0]));
-        const uint32_t sb = e4m3x2_to_f16x2(lds_u16(scale + o.ks[1]));
+        const uint4 ka = lds128(rec + o.k[0]);
+        const uint4 kb = lds128(rec + o.k[1]);
+        const uint32_t sa = e4m3x2_to_f16x2(lds_u16(rec + o.ks[0]));
+        const uint32_t sb = e4m3x2_to_f16x2(lds_u16(rec + o.ks[1]));
         const uint32_t sa0 = __byte_perm(sa, 0, 0x1010), sa1 = __byte_perm(sa, 0, 0x3232);
         const uint32_t sb0 = __byte_perm(sb, 0, 0x1010), sb1 = __byte_perm(sb, 0, 0x3232);
         const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w};
@@ -193,93 +181,74 @@ struct Nvfp4Format {
         }
     }
 
-    // V^T A-fragments for the 8 m-tiles: tile j, row gid <-> channel
-    // 16*gid + 2j, row gid+8 <-> 16*gid + 2j + 1; columns = logical tokens
-    // (2tig, 2tig+1) in a0/a1 and (2tig+8, 2tig+9) in a2/a3.
-    __device__ static __forceinline__ void load_v(uint32_t data, uint32_t scale, const LaneOffsets &o,
-                                                  int valid, uint32_t (&va)[8][4])
+    // V^T fragments, unscaled E2M1 values (exact in fp16), and the block scales
+    // of the four tokens: sv[0][j] = (scale of token 2tig, 2tig+1 in block j),
+    // sv[1][j] the same for tokens 2tig+8, 2tig+9.  The scales are applied to P.
+    __device__ static __forceinline__ void load_v(uint32_t rec, const LaneOffsets &o, int tig, int valid,
+                                                  uint32_t (&va)[8][4], uint32_t (&sv)[2][8])
     {
-        uint2 v[4];
-        uint32_t s[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[i] = lds64(data + o.v[i]);
-            s[i] = lds_u8(scale + o.vs[i]);
-        }
+        uint4 x = lds128(rec + o.v[0]), y = lds128(rec + o.v[1]);
+        uint4 s0 = lds128(rec + o.vs[0]), s1 = lds128(rec + o.vs[1]);
         if (valid < kPageSize) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (o.tt[i] >= valid) {
-                    v[i] = make_uint2(0u, 0u);
-                    s[i] = 0u;
-                }
+            // tokens at or past `valid` read as zero codes with zero scales
+            auto keep = [&](int t0, uint32_t &nib, uint32_t &byt) {
+                nib = (t0 >= valid) ? 0u : ((t0 + 1 >= valid) ? 0x0F0F0F0Fu : 0xFFFFFFFFu);
+                byt = (t0 >= valid) ? 0u : ((t0 + 1 >= valid) ? 0x00FF00FFu : 0xFFFFFFFFu);
+            };
+            uint32_t n0, b0, n1, b1;
+            keep(2 * tig, n0, b0);
+            keep(2 * tig + 8, n1, b1);
+            x = make_uint4(x.x & n0, x.y & n0, x.z & n0, x.w & n0);
+            y = make_uint4(y.x & n1, y.y & n1, y.z & n1, y.w & n1);
+            s0 = make_uint4(s0.x & b0, s0.y & b0, s0.z & b0, s0.w & b0);
+            s1 = make_uint4(s1.x & b1, s1.y & b1, s1.z & b1, s1.w & b1);
         }
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-            const uint2 x = v[2 * pr], y = v[2 * pr + 1];
-            const uint32_t sp = e4m3x2_to_f16x2(s[2 * pr] | (s[2 * pr + 1] << 8));
-            // nibble interleave: byte k of E = (x ch 2k | y ch 2k << 4), O = odd channels
-            const uint32_t E0 = (x.x & 0x0F0F0F0Fu) | ((y.x << 4) & 0xF0F0F0F0u);
-            const uint32_t O0 = ((x.x >> 4) & 0x0F0F0F0Fu) | (y.x & 0xF0F0F0F0u);
-            const uint32_t E1 = (x.y & 0x0F0F0F0Fu) | ((y.y << 4) & 0xF0F0F0F0u);
-            const uint32_t O1 = ((x.y >> 4) & 0x0F0F0F0Fu) | (y.y & 0xF0F0F0F0u);
-            uint32_t e0[4], o0[4], e1[4], o1[4];
-            e2m1x8_to_f16x2x4(E0, e0[0], e0[1], e0[2], e0[3]);
-            e2m1x8_to_f16x2x4(O0, o0[0], o0[1], o0[2], o0[3]);
-            e2m1x8_to_f16x2x4(E1, e1[0], e1[1], e1[2], e1[3]);
-            e2m1x8_to_f16x2x4(O1, o1[0], o1[1], o1[2], o1[3]);
+        for (int k = 0; k < 4; ++k) {
+            // bytes 4k .. 4k+3 = (m-tile 2k, w 0), (2k, 1), (2k+1, 0), (2k+1, 1)
+            e2m1x8_to_f16x2x4(xw[k], va[2 * k][0], va[2 * k][1], va[2 * k + 1][0], va[2 * k + 1][1]);
+            e2m1x8_to_f16x2x4(yw[k], va[2 * k][2], va[2 * k][3], va[2 * k + 1][2], va[2 * k + 1][3]);
+        }
+        const uint32_t s0w[4] = {s0.x, s0.y, s0.z, s0.w}, s1w[4] = {s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                va[k][2 * pr] = hmul2(e0[k], sp);
-                va[k][2 * pr + 1] = hmul2(o0[k], sp);
-                va[k + 4][2 * pr] = hmul2(e1[k], sp);
-                va[k + 4][2 * pr + 1] = hmul2(o1[k], sp);
-            }
+        for (int k = 0; k < 4; ++k) {
+            e4m3x4_to_f16x2x2(s0w[k], sv[0][2 * k], sv[0][2 * k + 1]);
+            e4m3x4_to_f16x2x2(s1w[k], sv[1][2 * k], sv[1][2 * k + 1]);
         }
     }
 };
 
-// FP8: a page-head stages K and V data (16 rows x 128 B each) via TMA with the
-// 128-byte swizzle (address bits [6:4] ^= bits [9:7]); values are E4M3 at
-// scale 1.0.
 struct Fp8Format {
     static constexpr int kStages = 3;
-    static constexpr int kTileBytes = 2048;
-    static constexpr int kStageData = 2 * kTileBytes;
-    static constexpr int kStageScale = 0;
-    static constexpr uint32_t kStageTx = 2 * kTileBytes;
+    static constexpr int kRecord = 4096;
 
-    __device__ static __forceinline__ uint32_t sw(int t, int c)
-    {
-        return (t << 7) + ((c ^ (t & 7)) << 4);
-    }
+    // m-tile j: row gid is channel 16*gid + 2j, row gid+8 is 16*gid + 2j + 1.
+    __device__ static __forceinline__ int channel(int j, int gid, int w) { return 16 * gid + 2 * j + w; }
 
     __device__ static __forceinline__ LaneOffsets offsets(int gid, int tig)
     {
         LaneOffsets o;
-        o.tA = tok_perm(gid);
-        const int tB = o.tA + 8;
-        o.k[0] = sw(o.tA, 2 * tig);
-        o.k[1] = sw(o.tA, 2 * tig + 1);
-        o.k[2] = sw(tB, 2 * tig);
-        o.k[3] = sw(tB, 2 * tig + 1);
+        const int par = gid & 1;
+        o.k[0] = gid * 128 + ((2 * tig + par) & 7) * 16;
+        o.k[1] = gid * 128 + ((2 * tig + 1 + par) & 7) * 16;
+        o.k[2] = o.k[0] + 1024;                          // row gid + 8, same parity
+        o.k[3] = o.k[1] + 1024;
         o.ks[0] = o.ks[1] = 0;
-        const int t0 = tok_perm(2 * tig), t1 = tok_perm(2 * tig + 1);
-        const int tt[4] = {t0, t1, t0 + 8, t1 + 8};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            o.tt[i] = tt[i];
-            o.v[i] = kTileBytes + sw(tt[i], gid);
-            o.vs[i] = 0;
-        }
+        const int f = (tig & 1) + 4 * ((tig >> 1) & 1);  // rows tig and tig+4 share f
+        o.v[0] = 2048 + tig * 256 + ((2 * gid + f) & 15) * 16;
+        o.v[1] = 2048 + tig * 256 + ((2 * gid + 1 + f) & 15) * 16;
+        o.v[2] = o.v[0] + 1024;
+        o.v[3] = o.v[1] + 1024;
+        o.vs[0] = o.vs[1] = 0;
         return o;
     }
 
-    __device__ static __forceinline__ void load_k(uint32_t data, uint32_t, const LaneOffsets &o,
-                                                  uint32_t (&fa)[16], uint32_t (&fb)[16])
+    __device__ static __forceinline__ void load_k(uint32_t rec, const LaneOffsets &o, uint32_t (&fa)[16],
+                                                  uint32_t (&fb)[16])
     {
-        const uint4 a0 = lds128(data + o.k[0]), a1 = lds128(data + o.k[1]);
-        const uint4 b0 = lds128(data + o.k[2]), b1 = lds128(data + o.k[3]);
+        const uint4 a0 = lds128(rec + o.k[0]), a1 = lds128(rec + o.k[1]);
+        const uint4 b0 = lds128(rec + o.k[2]), b1 = lds128(rec + o.k[3]);
         const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -289,30 +258,30 @@ struct Fp8Format {
         }
     }
 
-    __device__ static __forceinline__ void load_v(uint32_t data, uint32_t, const LaneOffsets &o, int valid,
-                                                  uint32_t (&va)[8][4])
+    __device__ static __forceinline__ void load_v(uint32_t rec, const LaneOffsets &o, int tig, int valid,
+                                                  uint32_t (&va)[8][4], uint32_t (&)[2][8])
     {
-        uint4 v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            v[i] = lds128(data + o.v[i]);
+        uint4 x0 = lds128(rec + o.v[0]), x1 = lds128(rec + o.v[1]);
+        uint4 y0 = lds128(rec + o.v[2]), y1 = lds128(rec + o.v[3]);
         if (valid < kPageSize) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (o.tt[i] >= valid)
-                    v[i] = make_uint4(0u, 0u, 0u, 0u);
+            auto keep = [&](int t0) {
+                return (t0 >= valid) ? 0u : ((t0 + 1 >= valid) ? 0x00FF00FFu : 0xFFFFFFFFu);
+            };
+            const uint32_t m0 = keep(2 * tig), m1 = keep(2 * tig + 8);
+            x0 = make_uint4(x0.x & m0, x0.y & m0, x0.z & m0, x0.w & m0);
+            x1 = make_uint4(x1.x & m0, x1.y & m0, x1.z & m0, x1.w & m0);
+            y0 = make_uint4(y0.x & m1, y0.y & m1, y0.z & m1, y0.w & m1);
+            y1 = make_uint4(y1.x & m1, y1.y & m1, y1.z & m1, y1.w & m1);
         }
+        const uint32_t x0w[4] = {x0.x, x0.y, x0.z, x0.w}, x1w[4] = {x1.x, x1.y, x1.z, x1.w};
+        const uint32_t y0w[4] = {y0.x, y0.y, y0.z, y0.w}, y1w[4] = {y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-            const uint4 x = v[2 * pr], y = v[2 * pr + 1];
-            const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t lo = __byte_perm(xw[k], yw[k], 0x5140);
-                const uint32_t hi = __byte_perm(xw[k], yw[k], 0x7362);
-                e4m3x4_to_f16x2x2(lo, va[2 * k][2 * pr], va[2 * k][2 * pr + 1]);
-                e4m3x4_to_f16x2x2(hi, va[2 * k + 1][2 * pr], va[2 * k + 1][2 * pr + 1]);
-            }
+        for (int k = 0; k < 4; ++k) {
+            // word k: channels 16gid + 2k (tokens t0, t1) and 16gid + 2k + 1
+            e4m3x4_to_f16x2x2(x0w[k], va[k][0], va[k][1]);
+            e4m3x4_to_f16x2x2(x1w[k], va[k + 4][0], va[k + 4][1]);
+            e4m3x4_to_f16x2x2(y0w[k], va[k][2], va[k][3]);
+            e4m3x4_to_f16x2x2(y1w[k], va[k + 4][2], va[k + 4][3]);
         }
     }
 };
@@ -320,8 +289,7 @@ struct Fp8Format {
 template <class Fmt>
 __host__ __device__ constexpr size_t decode_smem_fixed()
 {
-    return 1024 /* alignment slack */ +
-           static_cast<size_t>(kDecodeWarps) * Fmt::kStages * (Fmt::kStageData + Fmt::kStageScale + 8) +
+    return 128 /* alignment slack */ + static_cast<size_t>(kDecodeWarps) * Fmt::kStages * (Fmt::kRecord + 8) +
            8 * sizeof(int32_t);
 }
 
@@ -334,34 +302,27 @@ size_t decode_smem_bytes(int batch)
 // ---- the decode kernel -------------------------------------------------------
 
 template <class Fmt>
-__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
-    decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                  const DecodeParams p)
+__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_kernel(const DecodeParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
-    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t *smem = smem_raw + ((128u - (raw_addr & 127u)) & 127u);
     constexpr int S = Fmt::kStages;
+    constexpr int R = Fmt::kRecord;
     uint8_t *data_base = smem;
-    uint8_t *scale_base = data_base + kDecodeWarps * S * Fmt::kStageData;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(scale_base + kDecodeWarps * S * Fmt::kStageScale);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(data_base + kDecodeWarps * S * R);
     int32_t *scratch = reinterpret_cast<int32_t *>(bars + kDecodeWarps * S);
     int32_t *prefix = scratch + 8;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
-    const uint32_t wdata = smem_addr(data_base) + warp * S * Fmt::kStageData;
-    const uint32_t wscale = smem_addr(scale_base) + warp * S * Fmt::kStageScale;
+    const uint32_t wdata = smem_addr(data_base) + warp * S * R;
     const uint32_t wbar = smem_addr(bars) + warp * S * 8;
 
     if (lane == 0) {
         for (int s = 0; s < S; ++s)
             mbar_init(wbar + 8 * s, 1);
         fence_mbar_init();
-    }
-    if (threadIdx.x == 0) {
-        prefetch_tensormap(&tmap_k);
-        prefetch_tensormap(&tmap_v);
     }
     // everything below reads data the previous kernel in the stream may write
     pdl_wait();
@@ -415,15 +376,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
                 phys = 0;
             }
             const uint32_t bar = wbar + 8 * st;
-            const int z = phys * p.hkv + hh;
-            mbar_arrive_expect_tx(bar, Fmt::kStageTx);
-            tma_load_3d(wdata + st * Fmt::kStageData, &tmap_k, 0, 0, z, bar);
-            tma_load_3d(wdata + st * Fmt::kStageData + Fmt::kTileBytes, &tmap_v, 0, 0, z, bar);
-            if constexpr (Fmt::kStageScale > 0) {
-                bulk_g2s(wscale + st * Fmt::kStageScale, p.k_scale + static_cast<size_t>(z) * 128, 128, bar);
-                bulk_g2s(wscale + st * Fmt::kStageScale + 128, p.v_scale + static_cast<size_t>(z) * 128, 128,
-                         bar);
-            }
+            const size_t z = static_cast<size_t>(phys) * p.hkv + hh;
+            mbar_arrive_expect_tx(bar, R);
+            bulk_g2s(wdata + st * R, p.pool + z * R, R, bar);
         }
     };
 
@@ -491,40 +446,33 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
                 if (head >= g)
                     continue;
                 const float r = which ? r1 : r0;
-                const size_t o = (static_cast<size_t>(b) * p.hq + h * g + head) * kHeadDim + 16 * gid;
-                float v[16];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    v[2 * j] = oacc[j][which] * r;
-                    v[2 * j + 1] = oacc[j][2 + which] * r;
-                }
+                const size_t o = (static_cast<size_t>(b) * p.hq + h * g + head) * kHeadDim;
                 if (p.out_bf16) {
-                    uint32_t pk[8];
+                    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) + o;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        __nv_bfloat162 t = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
-                        pk[k] = *reinterpret_cast<uint32_t *>(&t);
+                    for (int j = 0; j < 8; ++j) {
+                        dst[Fmt::channel(j, gid, 0)] = __float2bfloat16_rn(oacc[j][which] * r);
+                        dst[Fmt::channel(j, gid, 1)] = __float2bfloat16_rn(oacc[j][2 + which] * r);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + o);
-                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 } else {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o);
+                    float *dst = static_cast<float *>(p.out) + o;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                    for (int j = 0; j < 8; ++j) {
+                        dst[Fmt::channel(j, gid, 0)] = oacc[j][which] * r;
+                        dst[Fmt::channel(j, gid, 1)] = oacc[j][2 + which] * r;
+                    }
                 }
             }
         } else {
             float *slot = p.partials + static_cast<size_t>(partial_slot(w, seg_begin, T, NW)) * kPartialFloats;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
-                const int head = which ? hB : hA;
-                float4 *dst = reinterpret_cast<float4 *>(slot + head * kHeadDim + 16 * gid);
+                float *dst = slot + (which ? hB : hA) * kHeadDim;
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    dst[k] = make_float4(oacc[2 * k][which], oacc[2 * k][2 + which], oacc[2 * k + 1][which],
-                                         oacc[2 * k + 1][2 + which]);
+                for (int j = 0; j < 8; ++j) {
+                    dst[Fmt::channel(j, gid, 0)] = oacc[j][which];
+                    dst[Fmt::channel(j, gid, 1)] = oacc[j][2 + which];
+                }
             }
             if (gid == 0) {
                 slot[kMaxGroup * kHeadDim + hA] = m0;
@@ -537,52 +485,35 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
 
     start_segment();
 
-    int st = 0;            // ring stage of page-head j
-    uint32_t ph = 0;       // phase parity of that stage's barrier
-    for (int j = lo; j < hi; ++j) {
-        // Lanes poll independently and may leave the loop at different polls;
-        // the vote reconverges the warp before the warp-wide MMAs below and
-        // makes the give-up decision uniform.
-        const bool arrived = mbar_wait_bounded(wbar + 8 * st, ph, kWaitLimit);
-        if (!__all_sync(kFullMask, arrived)) {
-            // staged data never arrived: report, let the copies in flight land, stop
-            if (lane == 0)
-                report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
-            const int pending = min(S, hi - j);
-            for (int k = 0; k < pending; ++k) {
-                int s2 = st + k;
-                uint32_t p2 = ph;
-                if (s2 >= S) {
-                    s2 -= S;
-                    p2 ^= 1u;
-                }
-                mbar_wait_bounded(wbar + 8 * s2, p2, kWaitLimit);
-            }
-            return;
-        }
-        const int valid = (pg == n - 1) ? (L - pg * kPageSize) : kPageSize;
-        const uint32_t sdata = wdata + st * Fmt::kStageData;
-        const uint32_t sscale = wscale + st * Fmt::kStageScale;
-
+    // One step handles one page-head, or two of the same segment.
+    auto step = [&](auto npc, uint32_t rec0, uint32_t rec1, int last_valid) {
+        constexpr int NP = decltype(npc)::value;
         // S^T = K . Q^T
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-        {
+        float sc[NP][4];
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
             uint32_t fa[16], fb[16];
-            Fmt::load_k(sdata, sscale, off, fa, fb);
+            Fmt::load_k(q == 0 ? rec0 : rec1, off, fa, fb);
+            sc[q][0] = sc[q][1] = sc[q][2] = sc[q][3] = 0.f;
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma_f16_16816(sc, fa[2 * s], fb[2 * s], fa[2 * s + 1], fb[2 * s + 1], qf[2 * s], qf[2 * s + 1]);
+                mma_f16_16816(sc[q], fa[2 * s], fb[2 * s], fa[2 * s + 1], fb[2 * s + 1], qf[2 * s], qf[2 * s + 1]);
         }
-        if (valid < kPageSize) {
-            if (off.tA >= valid)
-                sc[0] = sc[1] = -INFINITY;
-            if (off.tA + 8 >= valid)
-                sc[2] = sc[3] = -INFINITY;
+        if (last_valid < kPageSize) {
+            if (gid >= last_valid)
+                sc[NP - 1][0] = sc[NP - 1][1] = -INFINITY;
+            if (gid + 8 >= last_valid)
+                sc[NP - 1][2] = sc[NP - 1][3] = -INFINITY;
         }
         // Online softmax, heads (2tig, 2tig+1).  The running maximum is only
-        // moved when some score exceeds it by more than 2^kLazyRescale, so the
-        // common page needs no cross-lane reduction; P then stays <= 2^8.
-        float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+        // moved when some score exceeds it by more than kLazyRescale, so the
+        // common step needs no cross-lane reduction.
+        float mx0 = fmaxf(sc[0][0], sc[0][2]), mx1 = fmaxf(sc[0][1], sc[0][3]);
+#pragma unroll
+        for (int q = 1; q < NP; ++q) {
+            mx0 = fmaxf(mx0, fmaxf(sc[q][0], sc[q][2]));
+            mx1 = fmaxf(mx1, fmaxf(sc[q][1], sc[q][3]));
+        }
         if (__any_sync(kFullMask, (mx0 > m0 + kLazyRescale) || (mx1 > m1 + kLazyRescale))) {
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) {
@@ -604,34 +535,89 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
             m0 = n0;
             m1 = n1;
         }
-        const float p0 = fast_exp2(sc[0] - m0), p1 = fast_exp2(sc[1] - m1);
-        const float p2 = fast_exp2(sc[2] - m0), p3 = fast_exp2(sc[3] - m1);
-        l0 += p0 + p2;
-        l1 += p1 + p3;
-        const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
-        const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
-
-        // O^T += V^T . P^T
-        {
-            uint32_t va[8][4];
-            Fmt::load_v(sdata, sscale, off, valid, va);
+        uint32_t pb[NP][2];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-                mma_f16_16816(oacc[jj], va[jj][0], va[jj][1], va[jj][2], va[jj][3], pb0, pb1);
+        for (int q = 0; q < NP; ++q) {
+            const float p0 = fast_exp2(sc[q][0] - m0), p1 = fast_exp2(sc[q][1] - m1);
+            const float p2 = fast_exp2(sc[q][2] - m0), p3 = fast_exp2(sc[q][3] - m1);
+            l0 += p0 + p2;
+            l1 += p1 + p3;
+            pb[q][0] = movmatrix_trans(pack_f16x2(p0, p1));
+            pb[q][1] = movmatrix_trans(pack_f16x2(p2, p3));
         }
+        // O^T += V^T . P^T; for NVFP4 each m-tile is one scale block, so the
+        // block scales of the tokens multiply the P^T columns instead of V.
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            uint32_t va[8][4], sv[2][8];
+            Fmt::load_v(q == 0 ? rec0 : rec1, off, tig, q == NP - 1 ? last_valid : kPageSize, va, sv);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                if constexpr (Fmt::kRecord == Nvfp4Format::kRecord)
+                    mma_f16_16816(oacc[jj], va[jj][0], va[jj][1], va[jj][2], va[jj][3],
+                                  hmul2(pb[q][0], sv[0][jj]), hmul2(pb[q][1], sv[1][jj]));
+                else
+                    mma_f16_16816(oacc[jj], va[jj][0], va[jj][1], va[jj][2], va[jj][3], pb[q][0], pb[q][1]);
+            }
+        }
+    };
+
+    int st = 0;            // ring stage of page-head j
+    uint32_t ph = 0;       // phase parity of that stage's barrier
+    int j = lo;
+    while (j < hi) {
+        const int np = (j + 1 < hi && pg + 1 < n) ? 2 : 1;
+        int st1 = st + 1;
+        uint32_t ph1 = ph;
+        if (st1 == S) {
+            st1 = 0;
+            ph1 ^= 1u;
+        }
+        // Lanes poll independently and may leave the loop at different polls;
+        // the vote reconverges the warp before the warp-wide MMAs below and
+        // makes the give-up decision uniform.
+        bool arrived = mbar_wait_bounded(wbar + 8 * st, ph, kWaitLimit);
+        if (np == 2)
+            arrived = arrived && mbar_wait_bounded(wbar + 8 * st1, ph1, kWaitLimit);
+        if (!__all_sync(kFullMask, arrived)) {
+            // staged data never arrived: report, let the copies in flight land, stop
+            if (lane == 0)
+                report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
+            const int pending = min(S, hi - j);
+            for (int k = 0; k < pending; ++k) {
+                int s2 = st + k;
+                uint32_t p2 = ph;
+                if (s2 >= S) {
+                    s2 -= S;
+                    p2 ^= 1u;
+                }
+                mbar_wait_bounded(wbar + 8 * s2, p2, kWaitLimit);
+            }
+            return;
+        }
+        const int plast = pg + np - 1;
+        const int last_valid = (plast == n - 1) ? (L - plast * kPageSize) : kPageSize;
+        if (np == 2)
+            step(std::integral_constant<int, 2>(), wdata + st * R, wdata + st1 * R, last_valid);
+        else
+            step(std::integral_constant<int, 1>(), wdata + st * R, wdata + st * R, last_valid);
 
         __syncwarp();
         if (j + S < hi)
             issue(j + S, st);
-        if (++st == S) {
-            st = 0;
+        if (np == 2 && j + 1 + S < hi)
+            issue(j + 1 + S, st1);
+        st += np;
+        if (st >= S) {
+            st -= S;
             ph ^= 1u;
         }
 
-        ++pg;
-        if (pg == n || j + 1 == hi) {
+        j += np;
+        pg += np;
+        if (pg == n || j == hi) {
             finish_segment();
-            if (j + 1 < hi) {
+            if (j < hi) {
                 ++h;
                 pg = 0;
                 if (h == p.hkv) {

@@ -4,8 +4,7 @@
 namespace nvfp4kv {
 
 template <class Fmt>
-static cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                                 cudaStream_t s)
+static cudaError_t launch_decode(const DecodeParams &p, cudaStream_t s)
 {
     const size_t smem = decode_smem_bytes<Fmt>(p.batch);
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<Fmt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -13,13 +12,12 @@ static cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, c
     if (e != cudaSuccess)
         return e;
     const int grid = (p.num_workers + kDecodeWarps - 1) / kDecodeWarps;
-    return launch_pdl(decode_kernel<Fmt>, dim3(grid), dim3(kDecodeWarps * 32), smem, s, tk, tv, p);
+    return launch_pdl(decode_kernel<Fmt>, dim3(grid), dim3(kDecodeWarps * 32), smem, s, p);
 }
 
-cudaError_t launch_decode_fp8(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                                cudaStream_t s)
+cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t s)
 {
-    return launch_decode<Fp8Format>(p, tk, tv, s);
+    return launch_decode<Fp8Format>(p, s);
 }
 
 } // namespace nvfp4kv

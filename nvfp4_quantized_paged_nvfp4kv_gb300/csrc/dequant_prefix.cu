@@ -8,7 +8,8 @@
 //
 // Work unit: one page-head of K or V (16 tokens x 8 blocks) per 128-thread
 // CTA iteration, grid-stride over (sequence, page, kv head, K|V).  Each thread
-// reads 8 packed bytes and one scale byte and writes 16 E4M3 bytes.
+// gathers the 16 codes and the scale of one (token, block) from the record
+// (layout in include/nvfp4kv.h) and writes 16 E4M3 bytes.
 #include "device_common.cuh"
 #include "nvfp4kv.h"
 
@@ -44,11 +45,29 @@ __global__ void __launch_bounds__(128) dequant_prefix_kernel(const PrefixParams 
                 report(p.dev_status, NVFP4KV_DEV_BAD_PAGE);
             phys = 0;
         }
-        const size_t row = (static_cast<size_t>(phys) * p.hkv + h) * kPageSize + tok;
-        const uint8_t *data = kv ? p.v_data : p.k_data;
-        const uint8_t *scale = kv ? p.v_scale : p.k_scale;
-        const uint2 packed = __ldg(reinterpret_cast<const uint2 *>(data + row * (kHeadDim / 2) + blk * 8));
-        const uint32_t sbyte = __ldg(scale + row * (kHeadDim / 16) + blk);
+        const uint8_t *rec = p.pool + (static_cast<size_t>(phys) * p.hkv + h) * kNvfp4Record;
+        uint2 packed;
+        uint32_t sbyte;
+        if (kv == 0) {
+            packed = __ldg(reinterpret_cast<const uint2 *>(rec + tok * 64 + blk * 8));
+            sbyte = __ldg(rec + 2048 + tok * 8 + blk);
+        } else {
+            // channel 16*blk + g + 8w: row tok/2, chunk (g + 2*row) mod 8, byte
+            // 2*blk + w, nibble tok & 1; repack into natural order
+            const int row = tok >> 1, half = tok & 1;
+            uint32_t lo = 0u, hi = 0u;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const uint32_t unit = __ldg(reinterpret_cast<const uint16_t *>(
+                    rec + 1024 + row * 128 + ((g + 2 * row) & 7) * 16 + 2 * blk));
+                const uint32_t c0 = (unit >> (4 * half)) & 15u;        // channel g
+                const uint32_t c1 = (unit >> (8 + 4 * half)) & 15u;    // channel g + 8
+                lo |= c0 << (4 * g);
+                hi |= c1 << (4 * g);
+            }
+            packed = make_uint2(lo, hi);
+            sbyte = __ldg(rec + 2176 + row * 16 + blk * 2 + half);
+        }
         const uint32_t s2 = e4m3x2_to_f16x2(sbyte | (sbyte << 8));
         uint32_t f[8];
         e2m1x8_to_f16x2x4(packed.x, f[0], f[1], f[2], f[3]);

@@ -14,12 +14,13 @@ constexpr int kMaxGroup = 8;                 // query heads per kv head handled 
 constexpr int kDecodeWarps = 4;              // warps (independent workers) per decode CTA
 constexpr int kDecodeCtasPerSm = 4;          // occupancy the default worker count assumes
 constexpr int kPartialFloats = kMaxGroup * kHeadDim + 2 * kMaxGroup;  // O[8][128], m[8], l[8]
+constexpr int kNvfp4Record = 2304;           // bytes of an NVFP4 page-head record
+constexpr int kFp8Record = 4096;             // bytes of an FP8 page-head record
 constexpr int kMaxBatch = 16384;             // prefix table lives in shared memory
 
 // Split-KV decode over either cache format.
 struct DecodeParams {
-    const uint8_t *k_scale;      // NVFP4 only
-    const uint8_t *v_scale;      // NVFP4 only
+    const uint8_t *pool;         // page-head records [num_pages][hkv][record]
     const uint16_t *q;           // bf16 [batch][hq][128]
     void *out;                   // [batch][hq][128] bf16 or f32
     const int32_t *block_table;  // [batch][max_pages]
@@ -41,10 +42,7 @@ struct QuantParams {
     const void *k_new;
     const void *v_new;
     const int32_t *slot_mapping;
-    uint8_t *k_data;             // NVFP4 data pool, or the FP8 pool
-    uint8_t *k_scale;            // NVFP4 only
-    uint8_t *v_data;
-    uint8_t *v_scale;
+    uint8_t *pool;               // page-head records [num_pages][hkv][record]
     int32_t *dev_status;
     int num_tokens;
     int hkv;
@@ -53,10 +51,7 @@ struct QuantParams {
 };
 
 struct PrefixParams {
-    const uint8_t *k_data;
-    const uint8_t *k_scale;
-    const uint8_t *v_data;
-    const uint8_t *v_scale;
+    const uint8_t *pool;         // NVFP4 page-head records
     const int32_t *block_table;
     const int32_t *prefix_lens;
     const int32_t *kv_indptr;
@@ -96,10 +91,8 @@ size_t decode_workspace_bytes(int num_workers);
 
 cudaError_t launch_quantize_append_nvfp4(const QuantParams &p, cudaStream_t s);
 cudaError_t launch_quantize_append_fp8(const QuantParams &p, cudaStream_t s);
-cudaError_t launch_decode_nvfp4(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                                cudaStream_t s);
-cudaError_t launch_decode_fp8(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                              cudaStream_t s);
+cudaError_t launch_decode_nvfp4(const DecodeParams &p, cudaStream_t s);
+cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_merge(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_dequant_prefix_fp8(const PrefixParams &p, cudaStream_t s);
 

@@ -40,11 +40,9 @@ class Built:
         self.cache = nv.NVFP4Cache.allocate(self.num_pages, w.num_kv_heads, device=DEV)
         self.fp8 = nv.FP8Cache.allocate(self.num_pages, w.num_kv_heads, device=DEV) if fp8 else None
         if garbage:                   # unused slots hold bytes that decode to NaN scales
-            for t in (self.cache.k_data, self.cache.k_scale, self.cache.v_data, self.cache.v_scale):
-                t.fill_(0xFF)
+            self.cache.pool.fill_(0xFF)
             if fp8:
-                self.fp8.k.fill_(0xFF)
-                self.fp8.v.fill_(0xFF)
+                self.fp8.pool.fill_(0xFF)
         self.status = torch.zeros(1, dtype=torch.int32, device=DEV)
         self.rows = {}
         for b in range(w.batch):

@@ -53,14 +53,13 @@ FAKE = 0x7F0000000000          # a 16-byte aligned address that is never derefer
 
 
 def cache(**kw):
-    c = dict(k_data=FAKE, k_scale=FAKE + 4096, v_data=FAKE + 8192, v_scale=FAKE + 12288,
-             num_pages=10, num_kv_heads=2, page_size=16, head_dim=128, global_scale=1.0)
+    c = dict(pool=FAKE, num_pages=10, num_kv_heads=2, page_size=16, head_dim=128, global_scale=1.0)
     c.update(kw)
     return _Nvfp4Cache(**c)
 
 
 def fp8cache(**kw):
-    c = dict(k=FAKE, v=FAKE + 4096, num_pages=10, num_kv_heads=2, page_size=16, head_dim=128)
+    c = dict(pool=FAKE, num_pages=10, num_kv_heads=2, page_size=16, head_dim=128)
     c.update(kw)
     return _Fp8Cache(**c)
 
@@ -82,8 +81,8 @@ def decode(c, hq=4, batch=2, bt=FAKE, mp=4, sl=FAKE, out=FAKE, ws=FAKE, wsb=1 <<
     (dict(global_scale=2.0), nv.ERR_UNSUPPORTED),
     (dict(num_pages=0), nv.ERR_INVALID_ARG),
     (dict(num_kv_heads=-1), nv.ERR_INVALID_ARG),
-    (dict(k_scale=FAKE + 8), nv.ERR_INVALID_ARG),
-    (dict(v_data=None), nv.ERR_INVALID_ARG),
+    (dict(pool=FAKE + 8), nv.ERR_INVALID_ARG),
+    (dict(pool=None), nv.ERR_INVALID_ARG),
 ])
 def test_cache_validation(kw, want):
     assert append(cache(**kw)) == want
@@ -148,5 +147,7 @@ def test_cache_bytes_match_the_printed_figures():
     assert 80 * f8_layer == 1.25 * 2 ** 30
     assert nv_layer / f8_layer == 0.5625
     assert nv.nvfp4kv_cache_bytes(1, 1) == 2 * 16 * 9 * 8           # 16 tokens x 128 ch x (K,V)
+    assert nv.nvfp4kv_cache_bytes(1, 1) == nv.NVFP4_RECORD_BYTES
+    assert nv.fp8kv_cache_bytes(1, 1) == nv.FP8_RECORD_BYTES
     assert 80 * nv.nvfp4kv_cache_bytes(131072 // 16, 8) == 11.25 * 2 ** 30
     assert nv.nvfp4kv_cache_bytes(1, 1, 16, 100) == -1

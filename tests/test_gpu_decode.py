@@ -56,7 +56,7 @@ def test_worker_count_invariance():
     b = Built(w)
     ref = b.decode(torch.float32, num_workers=1)
     for nw in (2, 5, 64, 333, 0):
-        np.testing.assert_allclose(b.decode(torch.float32, num_workers=nw), ref, rtol=2e-3, atol=2e-4)
+        np.testing.assert_allclose(b.decode(torch.float32, num_workers=nw), ref, rtol=5e-3, atol=5e-4)
 
 
 def test_bad_page_and_length_are_reported_not_faulted():

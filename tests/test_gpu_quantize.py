@@ -8,6 +8,7 @@ import torch
 import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
 import oracle
 import workloads
+from layout import fp8_planes, nvfp4_planes
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -20,11 +21,11 @@ def run_gpu(x_k, x_v, slots, num_pages, hkv, fp8=False):
         c = nv.FP8Cache.allocate(num_pages, hkv, device=DEV)
         nv.fp8kv_quantize_append(c, x_k.to(DEV), x_v.to(DEV), sm, status)
         torch.cuda.synchronize()
-        return [c.k.cpu().numpy(), c.v.cpu().numpy()], int(status.item())
+        return list(fp8_planes(c.pool.cpu().numpy())), int(status.item())
     c = nv.NVFP4Cache.allocate(num_pages, hkv, device=DEV)
     nv.nvfp4kv_quantize_append(c, x_k.to(DEV), x_v.to(DEV), sm, status)
     torch.cuda.synchronize()
-    return [t.cpu().numpy() for t in (c.k_data, c.k_scale, c.v_data, c.v_scale)], int(status.item())
+    return list(nvfp4_planes(c.pool.cpu().numpy())), int(status.item())
 
 
 def run_oracle(x_k, x_v, slots, num_pages, hkv, fp8=False):
@@ -81,6 +82,28 @@ def test_distributions_bit_exact(name):
             np.testing.assert_array_equal(g_, w_)
 
 
+def test_v_nibble_pairs_written_by_separate_calls():
+    """The two tokens of a V token pair share bytes; writing them in separate
+    calls, in either order and over stale bytes, gives the oracle's result."""
+    rng = np.random.default_rng(3)
+    T, hkv, pages = 32, 2, 2
+    k = torch.from_numpy(rng.standard_normal((T, hkv, 128)).astype(np.float32))
+    v = torch.from_numpy(rng.standard_normal((T, hkv, 128)).astype(np.float32))
+    slots = np.arange(T, dtype=np.int32)
+    for fp8 in (False, True):
+        c = (nv.FP8Cache if fp8 else nv.NVFP4Cache).allocate(pages, hkv, device=DEV)
+        c.pool.fill_(0xA5)
+        order = [1, 0, 3, 2] + list(range(4, T))           # odd token first for the first pairs
+        for t in order:
+            app = nv.fp8kv_quantize_append if fp8 else nv.nvfp4kv_quantize_append
+            app(c, k[t:t + 1].to(DEV), v[t:t + 1].to(DEV), torch.from_numpy(slots[t:t + 1]).to(DEV))
+        torch.cuda.synchronize()
+        got = (fp8_planes if fp8 else nvfp4_planes)(c.pool.cpu().numpy())
+        want = run_oracle(k, v, slots, pages, hkv, fp8)
+        for g_, w_ in zip(got, want):
+            np.testing.assert_array_equal(g_, w_)
+
+
 def test_skipped_and_out_of_range_slots():
     rng = np.random.default_rng(0)
     T, hkv, pages = 40, 2, 4
@@ -100,7 +123,8 @@ def test_skipped_and_out_of_range_slots():
 
 
 def _blocks_to_gpu_codes(blocks):
-    """Quantise float32 blocks [N][16] (N multiple of 8) as rows of one kv head."""
+    """Quantise float32 blocks [N][16] (N multiple of 8) as rows of one kv head;
+    returns the K codes and scales (K rows of a record are in natural order)."""
     n = blocks.shape[0]
     T = n // 8
     pages = (T + 15) // 16
@@ -108,8 +132,9 @@ def _blocks_to_gpu_codes(blocks):
     c = nv.NVFP4Cache.allocate(pages, 1, device=DEV)
     sm = torch.arange(T, dtype=torch.int32, device=DEV)
     nv.nvfp4kv_quantize_append(c, x, x, sm)
-    data = c.k_data.reshape(-1, 64)[:T].reshape(n, 8)
-    scale = c.k_scale.reshape(-1, 8)[:T].reshape(n)
+    rec = c.pool.reshape(-1, nv.NVFP4_RECORD_BYTES)                   # one kv head: page = record
+    data = rec[:, :1024].reshape(-1, 64)[:T].reshape(n, 8)
+    scale = rec[:, 2048:2176].reshape(-1, 8)[:T].reshape(n)
     codes = torch.stack([data & 15, data >> 4], -1).reshape(n, 16)
     return codes, scale
 
