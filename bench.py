@@ -1,9 +1,9 @@
 """Benchmark of the NVFP4 paged-KV decode step on GB300.
 
-A step is one pass of the hot path over one batch: quantize_append of the
-newest token of every sequence into the NVFP4 cache, then the paged decode
-(split-KV attention + merge) of one query token per sequence over the whole
-cache.  value = KV-tokens attended per second per layer (sum of sequence
+A step is one pass of the hot path over one batch: the newest token of every
+sequence is quantised into the NVFP4 cache and one query token per sequence
+attends over the whole cache (nvfp4kv_append_paged_decode: the fused
+append + split-KV attention kernel, then the merge kernel).  value = KV-tokens attended per second per layer (sum of sequence
 lengths / step time), summed over ranks.  The same step over the FP8-E4M3
 comparison cache is timed beside it, and the dominant kernel's achieved HBM
 bandwidth is reported against the measured copy bandwidth.
@@ -63,6 +63,7 @@ def parse():
                     help="untimed load before the timed region so clock samples see load clocks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-rows", action="store_true", help="skip the quantize / prefix-dequant rows")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -239,9 +240,14 @@ class DecodeSetup:
         fn(c, self.q if q is None else q, self.bt, self.sl if sl is None else sl, self.out, self.ws,
            num_workers=self.num_workers, dev_status=self.status)
 
-    def step(self, i):
-        self.append(i)
-        self.decode(i)
+    def step(self, i, q=None, k=None, v=None, sl=None):
+        """quantize the newest token of every sequence and decode, one fused call"""
+        nv = self.nv
+        c = self.caches[i % len(self.caches)]
+        fn = nv.nvfp4kv_append_paged_decode if self.fmt == "nvfp4" else nv.fp8kv_append_paged_decode
+        fn(c, self.k_new if k is None else k, self.v_new if v is None else v, self.q if q is None else q,
+           self.bt, self.sl if sl is None else sl, self.out, self.ws, num_workers=self.num_workers,
+           dev_status=self.status)
 
 
 def time_steps(setup: DecodeSetup, steps: int, warmup: int, world: int):
@@ -257,9 +263,8 @@ def time_steps(setup: DecodeSetup, steps: int, warmup: int, world: int):
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(steps):
-        setup.append(i)
         ev[i][0].record(stream)
-        setup.decode(i)
+        setup.step(i)
         ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -271,22 +276,20 @@ def time_steps(setup: DecodeSetup, steps: int, warmup: int, world: int):
 
 def time_e2e(setup: DecodeSetup, steps: int, world: int):
     """Same step through the public API with the step's inputs in pinned host
-    memory: H2D of queries, new K/V rows, slots and lengths; D2H of the output."""
+    memory: H2D of queries, new K/V rows and lengths; D2H of the output."""
     dev = setup.dev
     hq = setup.q.cpu().pin_memory()
     hk = setup.k_new.cpu().pin_memory()
     hv = setup.v_new.cpu().pin_memory()
-    hs = setup.new_slots.cpu().pin_memory()
     hl = setup.sl.cpu().pin_memory()
     hout = torch.empty(setup.out.shape, dtype=setup.out.dtype).pin_memory()
     dq, dk, dv = torch.empty_like(setup.q), torch.empty_like(setup.k_new), torch.empty_like(setup.v_new)
-    ds, dl = torch.empty_like(setup.new_slots), torch.empty_like(setup.sl)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hl))
+    dl = torch.empty_like(setup.sl)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl))
     d2h = hout.numel() * hout.element_size()
     stream = torch.cuda.current_stream()
     for i in range(3):
-        setup.append(i)
-        setup.decode(i)
+        setup.step(i)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -295,10 +298,8 @@ def time_e2e(setup: DecodeSetup, steps: int, world: int):
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
-        ds.copy_(hs, non_blocking=True)
         dl.copy_(hl, non_blocking=True)
-        setup.append(i, dk, dv, ds)
-        setup.decode(i, dq, dl)
+        setup.step(i, dq, dk, dv, dl)
         hout.copy_(setup.out, non_blocking=True)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -344,9 +345,10 @@ def run_ours(args, world, rank, local):
     peak_src = "measured"
     if hbm is None:
         hbm, peak_src = 6800.0, "fallback"
-    alg_bytes = (tokens * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
-                 + 2 * w.batch * w.num_q_heads * w.head_dim * 2
-                 + w.batch * w.max_pages * 4 + w.batch * 4)
+    alg_bytes = (tokens * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD       # K/V pages read
+                 + 2 * w.batch * w.num_q_heads * w.head_dim * 2                 # q in, out
+                 + w.batch * w.max_pages * 4 + w.batch * 4                      # block table, lengths
+                 + w.batch * w.num_kv_heads * w.head_dim * 2 * 4)               # new K/V rows (fp32)
     achieved = alg_bytes / (dec_ms / 1e3) / 1e9
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -361,14 +363,15 @@ def run_ours(args, world, rank, local):
                           f"(L2 {l2 / 1e6:.0f} MB)") if replicas > 1 else
                          f"cache {setup.cache_bytes() / 1e6:.1f} MB > 4x L2",
                    "parallelism": f"replicas x{world} (each rank its own sequences)",
-                   "step": "quantize_append(newest token per sequence) + paged_decode"},
-        "roofline": {"bound": "hbm", "kernel": "nvfp4 paged decode (split-KV attention + merge)",
+                   "step": "append_paged_decode: newest token per sequence quantised into the cache, "
+                           "then split-KV decode + merge (2 kernels)"},
+        "roofline": {"bound": "hbm", "kernel": "nvfp4 append + paged decode (split-KV attention + merge)",
                      "achieved": achieved, "peak": hbm, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / hbm, "frac_of_8tbs_nominal": achieved / 8000.0,
                      "alg_bytes_per_launch": alg_bytes, "decode_ms": dec_ms,
                      "traffic": profiled_traffic("decode_nvfp4", args.workload)},
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "device_status": st,
     }
@@ -386,11 +389,65 @@ def run_ours(args, world, rank, local):
             "value": f_value, "unit": UNIT, "ms_per_step": f_total / args.steps, "decode_ms": f_dec,
             "achieved_gbs": f_bytes / (f_dec / 1e3) / 1e9,
             "nvfp4_over_fp8_step": value / f_value, "nvfp4_over_fp8_decode": f_dec / dec_ms}
+    if not args.no_rows:
+        result["other_rows"] = other_rows(dev)
     cpu = (cpu_baseline(w, budget_s=10.0)
            if rank == 0 and world == 1 and not args.no_cpu_baseline else None)
     if cpu is not None:
         result["cpu_baseline"] = cpu
     return result
+
+
+def other_rows(dev):
+    """The write side and the extend path on the long-context workload: quantize_append
+    of one 8192-token bf16 prefill chunk (Hkv=8) and dequant_prefix_fp8 of a
+    163840-token prefix, each timed with CUDA events (mean of 20 after 3 warm-ups)."""
+    import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+    w = workloads.make("ctx160k", batch=1)
+    bt, num_pages = workloads.block_table(w)
+    cache = nv.NVFP4Cache.allocate(num_pages, w.num_kv_heads, device=dev, zero=False)
+    bt_d = torch.from_numpy(bt).to(dev)
+    for t0 in range(0, w.seq_lens[0], workloads.CHUNK):
+        t1 = min(w.seq_lens[0], t0 + workloads.CHUNK)
+        sm = torch.from_numpy(workloads.slot_mapping(w, bt, 0, t0, t1)).to(dev)
+        nv.nvfp4kv_quantize_append(cache, workloads.kv_rows(w, "k", 0, t0, t1, device=dev).to(torch.bfloat16),
+                                   workloads.kv_rows(w, "v", 0, t0, t1, device=dev).to(torch.bfloat16), sm)
+    T = 8192
+    k = workloads.kv_rows(w, "k", 0, 0, T, device=dev).to(torch.bfloat16)
+    v = workloads.kv_rows(w, "v", 0, 0, T, device=dev).to(torch.bfloat16)
+    sm = torch.from_numpy(workloads.slot_mapping(w, bt, 0, 0, T)).to(dev)
+    L = w.seq_lens[0]
+    kf = torch.empty((L, w.num_kv_heads, 128), dtype=torch.uint8, device=dev)
+    vf = torch.empty_like(kf)
+    pl = torch.tensor([L], dtype=torch.int32, device=dev)
+    ip = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ms = []
+        for _ in range(20):
+            flush.fill_(1)                                   # evict the inputs from L2
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        return statistics.mean(ms)
+
+    q_ms = timed(lambda: nv.nvfp4kv_quantize_append(cache, k, v, sm))
+    q_bytes = T * w.num_kv_heads * (2 * 128 * 2 + NVFP4_BYTES_PER_TOKEN_HEAD) + T * 4
+    p_ms = timed(lambda: nv.nvfp4kv_dequant_prefix_fp8(cache, bt_d, pl, ip, kf, vf))
+    p_bytes = L * w.num_kv_heads * (NVFP4_BYTES_PER_TOKEN_HEAD + 2 * 128)
+    return {
+        "quantize_append_8k_bf16": {"us": q_ms * 1e3, "tokens_per_s": T / (q_ms / 1e3),
+                                    "alg_gbs": q_bytes / (q_ms / 1e3) / 1e9, "alg_bytes": q_bytes},
+        "dequant_prefix_fp8_160k": {"us": p_ms * 1e3, "tokens_per_s": L / (p_ms / 1e3),
+                                    "alg_gbs": p_bytes / (p_ms / 1e3) / 1e9, "alg_bytes": p_bytes},
+        "timing": "CUDA events per call, 256 MB buffer written before each call to evict L2",
+    }
 
 
 # ---------------------------------------------------------------------------

@@ -181,6 +181,25 @@ nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q,
                                     size_t workspace_bytes, int32_t num_workers,
                                     int32_t *dev_status, nvfp4kv_stream_t stream);
 
+/* One decode step: append each sequence's newest token, then attend.
+ * For every sequence b with seq_lens[b] > 0, the K and V rows k_new[b],
+ * v_new[b] ([batch][num_kv_heads][128], fp32 or bf16 per in_dtype, 16-byte
+ * aligned) are quantised into the cache at position seq_lens[b] - 1 (page
+ * block_table[b][(seq_lens[b]-1)/16], offset (seq_lens[b]-1)%16) exactly as
+ * nvfp4kv_quantize_append would, and then the decode of nvfp4kv_paged_decode
+ * runs over all seq_lens[b] tokens, including the new one.  The append is done
+ * inside the decode kernel by the warp that streams that page, so the step is
+ * two kernels instead of three.  The page that receives a sequence's new
+ * token must not appear in another sequence's block table in the same call.
+ * Other arguments and results as for nvfp4kv_paged_decode. */
+nvfp4kv_status nvfp4kv_append_paged_decode(const nvfp4kv_cache *cache, const void *k_new, const void *v_new,
+                                           nvfp4kv_dtype in_dtype, const void *q, int32_t batch,
+                                           int32_t num_q_heads, const int32_t *block_table,
+                                           int32_t max_pages_per_seq, const int32_t *seq_lens, float sm_scale,
+                                           void *out, nvfp4kv_dtype out_dtype, void *workspace,
+                                           size_t workspace_bytes, int32_t num_workers, int32_t *dev_status,
+                                           nvfp4kv_stream_t stream);
+
 /* Decode without a caller-provided workspace, for callers that cannot
  * allocate device memory (for example a serving engine whose device memory is
  * all reserved for weights and KV cache at start-up).  The pages have no
@@ -236,6 +255,15 @@ nvfp4kv_status fp8kv_paged_decode(const fp8kv_cache *cache, const void *q, int32
                                   void *workspace, size_t workspace_bytes,
                                   int32_t num_workers, int32_t *dev_status,
                                   nvfp4kv_stream_t stream);
+
+/* The same fused step over the FP8 comparison cache. */
+nvfp4kv_status fp8kv_append_paged_decode(const fp8kv_cache *cache, const void *k_new, const void *v_new,
+                                         nvfp4kv_dtype in_dtype, const void *q, int32_t batch,
+                                         int32_t num_q_heads, const int32_t *block_table,
+                                         int32_t max_pages_per_seq, const int32_t *seq_lens, float sm_scale,
+                                         void *out, nvfp4kv_dtype out_dtype, void *workspace,
+                                         size_t workspace_bytes, int32_t num_workers, int32_t *dev_status,
+                                         nvfp4kv_stream_t stream);
 
 /* Bytes of an NVFP4 pool (K and V data and scales) for a geometry:
  * num_pages * num_kv_heads * page_size * 2 * (head_dim/2 + head_dim/16),

@@ -9,6 +9,7 @@ Functions carry the C names and take torch tensors:
 
   nvfp4kv_quantize_append(cache, k_new, v_new, slot_mapping, dev_status=None)
   nvfp4kv_paged_decode(cache, q, block_table, seq_lens, out, workspace, ...)
+  nvfp4kv_append_paged_decode(cache, k_new, v_new, q, block_table, seq_lens, out, workspace, ...)
   nvfp4kv_dequant_prefix_fp8(cache, block_table, prefix_lens, kv_indptr, k_out, v_out)
   fp8kv_quantize_append(cache, k_new, v_new, slot_mapping, dev_status=None)
   fp8kv_paged_decode(cache, q, block_table, seq_lens, out, workspace, ...)
@@ -89,6 +90,12 @@ def load(build_if_missing: bool = True):
             "nvfp4kv_decode_workspace_size": (ctypes.c_size_t, [_i32]),
             "nvfp4kv_paged_decode": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _i32, _i32, _vp, _i32, _vp,
                                            ctypes.c_float, _vp, _st, _vp, ctypes.c_size_t, _i32, _vp, _vp]),
+            "nvfp4kv_append_paged_decode": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _vp, _st, _vp, _i32, _i32,
+                                                  _vp, _i32, _vp, ctypes.c_float, _vp, _st, _vp,
+                                                  ctypes.c_size_t, _i32, _vp, _vp]),
+            "fp8kv_append_paged_decode": (_st, [ctypes.POINTER(_Fp8Cache), _vp, _vp, _st, _vp, _i32, _i32,
+                                                _vp, _i32, _vp, ctypes.c_float, _vp, _st, _vp,
+                                                ctypes.c_size_t, _i32, _vp, _vp]),
             "nvfp4kv_paged_decode_static_scratch": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _i32, _i32, _vp,
                                                           _i32, _vp, ctypes.c_float, _vp, _st, _i32, _vp,
                                                           _vp]),
@@ -221,6 +228,35 @@ def fp8kv_paged_decode(cache: FP8Cache, q, block_table, seq_lens, out, workspace
                        sm_scale=None, num_workers=0, dev_status=None, stream=None) -> None:
     _decode(load().fp8kv_paged_decode, "fp8kv_paged_decode", cache, q, block_table, seq_lens,
             out, workspace, sm_scale, num_workers, dev_status, stream)
+
+
+def _append_decode(fn, name, cache, k_new, v_new, q, block_table, seq_lens, out, workspace, sm_scale,
+                   num_workers, dev_status, stream):
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    B, Hq, _ = q.shape
+    st = fn(cache.c, _ptr(k_new), _ptr(v_new), _dtype_code(k_new), _ptr(q), B, Hq, _ptr(block_table),
+            block_table.shape[1], _ptr(seq_lens), float(sm_scale), _ptr(out), _dtype_code(out),
+            _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+            int(num_workers), _ptr(dev_status), _stream(stream))
+    _check(st, name)
+
+
+def nvfp4kv_append_paged_decode(cache: NVFP4Cache, k_new, v_new, q, block_table, seq_lens, out,
+                                workspace, sm_scale=None, num_workers=0, dev_status=None,
+                                stream=None) -> None:
+    """One decode step: append k_new/v_new [B][Hkv][128] at position seq_lens-1, then decode."""
+    _append_decode(load().nvfp4kv_append_paged_decode, "nvfp4kv_append_paged_decode", cache, k_new,
+                   v_new, q, block_table, seq_lens, out, workspace, sm_scale, num_workers, dev_status,
+                   stream)
+
+
+def fp8kv_append_paged_decode(cache: FP8Cache, k_new, v_new, q, block_table, seq_lens, out,
+                              workspace, sm_scale=None, num_workers=0, dev_status=None,
+                              stream=None) -> None:
+    _append_decode(load().fp8kv_append_paged_decode, "fp8kv_append_paged_decode", cache, k_new,
+                   v_new, q, block_table, seq_lens, out, workspace, sm_scale, num_workers, dev_status,
+                   stream)
 
 
 def nvfp4kv_paged_decode_static_scratch(cache: NVFP4Cache, q, block_table, seq_lens, out,

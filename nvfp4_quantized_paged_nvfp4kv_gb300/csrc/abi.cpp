@@ -283,6 +283,68 @@ nvfp4kv_status fp8kv_paged_decode(const fp8kv_cache *cache, const void *q, int32
     return from_cuda(e);
 }
 
+nvfp4kv_status nvfp4kv_append_paged_decode(const nvfp4kv_cache *cache, const void *k_new, const void *v_new,
+                                           nvfp4kv_dtype in_dtype, const void *q, int32_t batch,
+                                           int32_t num_q_heads, const int32_t *block_table,
+                                           int32_t max_pages_per_seq, const int32_t *seq_lens, float sm_scale,
+                                           void *out, nvfp4kv_dtype out_dtype, void *workspace,
+                                           size_t workspace_bytes, int32_t num_workers, int32_t *dev_status,
+                                           nvfp4kv_stream_t stream)
+{
+    nvfp4kv_status st = check_nvfp4(cache);
+    if (st != NVFP4KV_OK)
+        return st;
+    st = check_append(k_new, v_new, in_dtype, batch, block_table);
+    if (st != NVFP4KV_OK)
+        return st;
+    DecodeParams p;
+    st = check_decode(cache->num_kv_heads, cache->num_pages, q, batch, num_q_heads, block_table,
+                      max_pages_per_seq, seq_lens, sm_scale, out, out_dtype, workspace, workspace_bytes,
+                      num_workers, dev_status, p);
+    if (st != NVFP4KV_OK || batch == 0)
+        return st;
+    p.pool = static_cast<const uint8_t *>(cache->pool);
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.append = 1;
+    p.new_bf16 = in_dtype == NVFP4KV_BF16;
+    cudaError_t e = launch_decode_nvfp4(p, to_cuda(stream));
+    if (e == cudaSuccess)
+        e = launch_merge(p, to_cuda(stream));
+    return from_cuda(e);
+}
+
+nvfp4kv_status fp8kv_append_paged_decode(const fp8kv_cache *cache, const void *k_new, const void *v_new,
+                                         nvfp4kv_dtype in_dtype, const void *q, int32_t batch,
+                                         int32_t num_q_heads, const int32_t *block_table,
+                                         int32_t max_pages_per_seq, const int32_t *seq_lens, float sm_scale,
+                                         void *out, nvfp4kv_dtype out_dtype, void *workspace,
+                                         size_t workspace_bytes, int32_t num_workers, int32_t *dev_status,
+                                         nvfp4kv_stream_t stream)
+{
+    nvfp4kv_status st = check_fp8(cache);
+    if (st != NVFP4KV_OK)
+        return st;
+    st = check_append(k_new, v_new, in_dtype, batch, block_table);
+    if (st != NVFP4KV_OK)
+        return st;
+    DecodeParams p;
+    st = check_decode(cache->num_kv_heads, cache->num_pages, q, batch, num_q_heads, block_table,
+                      max_pages_per_seq, seq_lens, sm_scale, out, out_dtype, workspace, workspace_bytes,
+                      num_workers, dev_status, p);
+    if (st != NVFP4KV_OK || batch == 0)
+        return st;
+    p.pool = static_cast<const uint8_t *>(cache->pool);
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.append = 1;
+    p.new_bf16 = in_dtype == NVFP4KV_BF16;
+    cudaError_t e = launch_decode_fp8(p, to_cuda(stream));
+    if (e == cudaSuccess)
+        e = launch_merge(p, to_cuda(stream));
+    return from_cuda(e);
+}
+
 int64_t nvfp4kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t head_dim)
 {
     if (num_pages < 0 || num_kv_heads < 0 || page_size < 0 || head_dim < 0 || head_dim % 16 != 0)

@@ -25,6 +25,7 @@
 
 #include "device_common.cuh"
 #include "nvfp4kv.h"
+#include "record_write.cuh"
 
 namespace nvfp4kv {
 
@@ -137,6 +138,12 @@ struct Nvfp4Format {
     static constexpr int kStages = 5;
     static constexpr int kRecord = 2304;
 
+    __device__ static __forceinline__ void write_block(uint8_t *rec, bool is_v, int tok, int blk,
+                                                       const float (&x)[16])
+    {
+        write_nvfp4_block(rec, is_v, tok, blk, x);
+    }
+
     // m-tile j, row r (0..15) is channel 16j + r: each m-tile is one scale block.
     __device__ static __forceinline__ int channel(int j, int gid, int w) { return 16 * j + gid + 8 * w; }
 
@@ -222,6 +229,12 @@ struct Nvfp4Format {
 struct Fp8Format {
     static constexpr int kStages = 3;
     static constexpr int kRecord = 4096;
+
+    __device__ static __forceinline__ void write_block(uint8_t *rec, bool is_v, int tok, int blk,
+                                                       const float (&x)[16])
+    {
+        write_fp8_block(rec, is_v, tok, blk, x);
+    }
 
     // m-tile j: row gid is channel 16*gid + 2j, row gid+8 is 16*gid + 2j + 1.
     __device__ static __forceinline__ int channel(int j, int gid, int w) { return 16 * gid + 2 * j + w; }
@@ -324,19 +337,22 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
             mbar_init(wbar + 8 * s, 1);
         fence_mbar_init();
     }
-    // everything below reads data the previous kernel in the stream may write
+    // everything below reads data the previous kernel in the stream may write;
+    // the merge kernel that follows may start its own prologue meanwhile
     pdl_wait();
+    pdl_launch_dependents();
     const int max_len = p.max_pages * kPageSize;
     build_prefix(p.seq_lens, p.batch, p.hkv, max_len, prefix, scratch,
                  blockIdx.x == 0 ? p.dev_status : nullptr);
 
     const int w = blockIdx.x * kDecodeWarps + warp;
-    if (w >= p.num_workers)
-        return;
     const long long T = prefix[p.batch];
     const long long NW = p.num_workers;
-    const int lo = static_cast<int>((T * w) / NW);
-    const int hi = static_cast<int>((T * (w + 1)) / NW);
+    const int lo = w < p.num_workers ? static_cast<int>((T * w) / NW) : 0;
+    const int hi = w < p.num_workers ? static_cast<int>((T * (w + 1)) / NW) : 0;
+
+    // The worker: this warp's page-heads [lo, hi).
+    auto run_worker = [&]() {
     if (lo >= hi)
         return;
 
@@ -389,6 +405,40 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
     int pg = lo - prefix[b] - h * n;
     int L = clamp_len(p.seq_lens[b], max_len);
     int seg_begin = prefix[b] + h * n;
+
+    if (p.append) {
+        // Fused append: the warp that streams the last page-head of a segment
+        // first writes that sequence's new token (position seq_len - 1) into
+        // it, one 16-value block per lane, before any copy of that page.
+        for (int idx = lo; idx < hi;) {
+            const int bb = find_seq(prefix, p.batch, idx);
+            const int nn = (prefix[bb + 1] - prefix[bb]) / p.hkv;
+            const int hh = (idx - prefix[bb]) / nn;
+            const int last = prefix[bb] + hh * nn + nn - 1;
+            if (last < hi && lane < 16) {
+                int phys = __ldg(p.block_table + static_cast<size_t>(bb) * p.max_pages + nn - 1);
+                if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_pages)) {
+                    if (lane == 0)
+                        report(p.dev_status, NVFP4KV_DEV_BAD_PAGE);
+                } else {
+                    const int tok = (clamp_len(p.seq_lens[bb], max_len) - 1) & (kPageSize - 1);
+                    const bool is_v = lane >= 8;
+                    const int blk = lane & 7;
+                    const size_t src = (static_cast<size_t>(bb) * p.hkv + hh) * kHeadDim + blk * 16;
+                    float x[16];
+                    if (p.new_bf16)
+                        load16<true>(is_v ? p.v_new : p.k_new, src, x);
+                    else
+                        load16<false>(is_v ? p.v_new : p.k_new, src, x);
+                    Fmt::write_block(const_cast<uint8_t *>(p.pool) + (static_cast<size_t>(phys) * p.hkv + hh) * R,
+                                     is_v, tok, blk, x);
+                    fence_proxy_async_global();
+                }
+            }
+            idx = last + 1;
+        }
+        __syncwarp();
+    }
 
     const int npro = min(S, hi - lo);
     for (int j = lo; j < lo + npro; ++j)
@@ -464,7 +514,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
                 }
             }
         } else {
-            float *slot = p.partials + static_cast<size_t>(partial_slot(w, seg_begin, T, NW)) * kPartialFloats;
+            float *slot = p.partials + static_cast<size_t>(2 * w + (lo >= seg_begin ? 0 : 1)) * kPartialFloats;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 float *dst = slot + (which ? hB : hA) * kHeadDim;
@@ -633,7 +683,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
             }
         }
     }
-    pdl_launch_dependents();
+    };  // run_worker
+    run_worker();
 }
 
 // ---- split merge ---------------------------------------------------------------

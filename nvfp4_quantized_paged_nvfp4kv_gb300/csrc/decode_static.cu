@@ -28,6 +28,7 @@ namespace nvfp4kv {
 namespace {
 
 constexpr size_t kStaticScratchBytes = NVFP4KV_STATIC_SCRATCH_BYTES;
+// two partial slots per worker
 static_assert(kStaticScratchBytes / (2 * kPartialFloats * sizeof(float)) >= NVFP4KV_STATIC_SCRATCH_MAX_WORKERS,
               "static scratch too small for its advertised worker count");
 

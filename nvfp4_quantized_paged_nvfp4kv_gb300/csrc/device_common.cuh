@@ -232,6 +232,13 @@ __device__ __forceinline__ uint32_t lds_u8(uint32_t addr)
     return v;
 }
 
+// Orders this thread's earlier generic-proxy global writes before its (and,
+// after a warp barrier, its warp's) later asynchronous bulk copies.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding kernel in the stream
 // (no-op when the launch did not allow overlap) / let the next one start.
 __device__ __forceinline__ void pdl_wait()

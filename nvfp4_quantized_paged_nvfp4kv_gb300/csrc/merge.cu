@@ -1,6 +1,6 @@
 // Split-KV merge (flash-decoding log-sum-exp combine) and the decode workspace
-// arithmetic.  For a segment (sequence b, kv head h) split over workers
-// wf..wl, each left (O_w, m_w, l_w) with O_w = sum_j 2^(s_j - m_w) v_j and
+// arithmetic.  For a segment (sequence b, kv head h) split over the decode
+// workers wf..wl, each left one partial (O_w, m_w, l_w) with O_w = sum_j 2^(s_j - m_w) v_j and
 // l_w = sum_j 2^(s_j - m_w) (scores s in log2 units).  Then
 //   M = max_w m_w,   o = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w.
 #include "decode_common.cuh"
@@ -8,16 +8,18 @@
 namespace nvfp4kv {
 
 // Thread t works on channels 4*(t%32) .. +3 of the CTA's query head for the
-// contributors k = t/32, t/32 + 8, ...; the 8 contributor groups are summed in
-// shared memory.  Warp 0 first finds M and the denominator.
+// contributors k = t/32, t/32 + 8, ...; each of the 8 contributor groups keeps
+// its own running maximum (one pass over the partials), and the groups are
+// combined in shared memory at the end.
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p)
 {
     constexpr int kGroups = kMergeThreads / 32;
     extern __shared__ int32_t msmem[];
     __shared__ float4 part[kGroups][32];
-    __shared__ float s_max, s_den;
+    __shared__ float part_m[kGroups], part_l[kGroups];
     int32_t *scratch = msmem;
     int32_t *prefix = msmem + 32;
+    pdl_launch_dependents();                 // the next kernel may start its prologue
     build_prefix(p.seq_lens, p.batch, p.hkv, p.max_pages * kPageSize, prefix, scratch, nullptr);
 
     const int b = blockIdx.x / p.hkv;
@@ -38,56 +40,54 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
             return;                              // written by the decode kernel
         pdl_wait();                              // the partials come from the decode kernel
         const int nc = wl - wf + 1;
-        auto slot_of = [&](int k) {
-            return p.partials + static_cast<size_t>(partial_slot(wf + k, seg_begin, T, NW)) * kPartialFloats;
-        };
-        if (grp == 0) {
-            float M = -INFINITY;
-            for (int k = lane; k < nc; k += 32)
-                M = fmaxf(M, __ldcg(slot_of(k) + kMaxGroup * kHeadDim + i));
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
-            float den = 0.f;
-            for (int k = lane; k < nc; k += 32) {
-                const float *sl = slot_of(k);
-                den += fast_exp2(__ldcg(sl + kMaxGroup * kHeadDim + i) - M) *
-                       __ldcg(sl + kMaxGroup * kHeadDim + kMaxGroup + i);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                den += __shfl_xor_sync(kFullMask, den, off);
-            if (lane == 0) {
-                s_max = M;
-                s_den = den;
-            }
-        }
-        __syncthreads();
-        const float M = s_max;
+        float M = -INFINITY, den = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
         for (int k = grp; k < nc; k += kGroups) {
-            const float *sl = slot_of(k);
-            const float e = fast_exp2(__ldcg(sl + kMaxGroup * kHeadDim + i) - M);
+            const float *sl =
+                p.partials + static_cast<size_t>(partial_slot(wf + k, seg_begin, T, NW)) * kPartialFloats;
+            const float mk = __ldcg(sl + kMaxGroup * kHeadDim + i);
+            const float lk = __ldcg(sl + kMaxGroup * kHeadDim + kMaxGroup + i);
             const float4 v = __ldcg(reinterpret_cast<const float4 *>(sl + i * kHeadDim) + lane);
+            if (mk > M) {                        // uniform across the warp
+                const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mk);
+                acc = make_float4(acc.x * a, acc.y * a, acc.z * a, acc.w * a);
+                den *= a;
+                M = mk;
+            }
+            const float e = fast_exp2(mk - M);
             acc.x += e * v.x;
             acc.y += e * v.y;
             acc.z += e * v.z;
             acc.w += e * v.w;
+            den += e * lk;
         }
         part[grp][lane] = acc;
+        if (lane == 0) {
+            part_m[grp] = M;
+            part_l[grp] = den;
+        }
         __syncthreads();
         if (grp != 0)
             return;
-        for (int k = 1; k < kGroups; ++k) {
+        float Mall = part_m[0];
+        for (int k = 1; k < kGroups; ++k)
+            Mall = fmaxf(Mall, part_m[k]);
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        float dsum = 0.f;
+        for (int k = 0; k < kGroups; ++k) {
+            if (part_m[k] == -INFINITY)
+                continue;                        // a group with no contributor
+            const float e = fast_exp2(part_m[k] - Mall);
             const float4 v = part[k][lane];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            sum.x += e * v.x;
+            sum.y += e * v.y;
+            sum.z += e * v.z;
+            sum.w += e * v.w;
+            dsum += e * part_l[k];
         }
-        const float r = 1.f / s_den;
-        res = make_float4(acc.x * r, acc.y * r, acc.z * r, acc.w * r);
+        const float r = 1.f / dsum;
+        res = make_float4(sum.x * r, sum.y * r, sum.z * r, sum.w * r);
     } else if (grp != 0) {
         return;
     }
@@ -134,11 +134,12 @@ int default_num_workers()
     return (sms > 0 ? sms : 1) * kDecodeCtasPerSm * kDecodeWarps;
 }
 
+// Two partial slots per warp worker.
 size_t decode_workspace_bytes(int num_workers)
 {
     if (num_workers <= 0)
         num_workers = default_num_workers();
-    return static_cast<size_t>(2) * num_workers * kPartialFloats * sizeof(float);
+    return 2 * static_cast<size_t>(num_workers) * kPartialFloats * sizeof(float);
 }
 
 } // namespace nvfp4kv

@@ -36,6 +36,12 @@ struct DecodeParams {
     int out_bf16;
     int num_workers;
     float qscale;                // sm_scale * log2(e)
+    // fused append: new K/V rows [batch][hkv][128] written at position
+    // seq_lens[b] - 1 before the decode reads the page (append != 0)
+    const void *k_new;
+    const void *v_new;
+    int append;
+    int new_bf16;
 };
 
 struct QuantParams {

@@ -1,0 +1,116 @@
+// Writing one 16-value block of a token-head row into a page-head record
+// (layout in include/nvfp4kv.h), shared by the quantize-append kernels and the
+// append step of the fused append + decode kernel.
+#pragma once
+
+#include "device_common.cuh"
+
+namespace nvfp4kv {
+
+template <bool kBf16>
+__device__ __forceinline__ void load16(const void *src, size_t elem_off, float (&x)[16])
+{
+    if constexpr (kBf16) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(src) + elem_off);
+        const uint4 a = __ldg(p), b = __ldg(p + 1);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            x[2 * k] = __uint_as_float(w[k] << 16);
+            x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+    } else {
+        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + elem_off);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 v = __ldg(p + k);
+            x[4 * k] = v.x;
+            x[4 * k + 1] = v.y;
+            x[4 * k + 2] = v.z;
+            x[4 * k + 3] = v.w;
+        }
+    }
+}
+
+// amax -> E4M3 block scale -> 16 E2M1 codes (code i in bits 4i .. 4i+3).
+__device__ __forceinline__ void quantize_block(const float (&x)[16], uint32_t &scale_byte, uint32_t (&packed)[2])
+{
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        amax = fmaxf(amax, fabsf(x[i]));
+    const float s32 = __fdiv_rn(amax, 6.0f);
+    scale_byte = f32x2_to_e4m3x2(s32, 0.f) & 0xffu;
+    const float sc = e4m3_to_f32(scale_byte);
+    packed[0] = packed[1] = 0u;
+    if (sc != 0.f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t byte = f32x2_to_e2m1x2(__fdiv_rn(x[2 * j], sc), __fdiv_rn(x[2 * j + 1], sc));
+            packed[j >> 2] |= byte << (8 * (j & 3));
+        }
+    }
+}
+
+// NVFP4: quantise x (block blk of token tok of the record) and write it.  K
+// rows are natural (one 8-byte store); a V block is merged into the 8 words
+// that hold its token pair with atomic AND/OR on the thread's own nibbles.
+__device__ __forceinline__ void write_nvfp4_block(uint8_t *rec, bool is_v, int tok, int blk, const float (&x)[16])
+{
+    uint32_t S, packed[2];
+    quantize_block(x, S, packed);
+    if (!is_v) {
+        *reinterpret_cast<uint2 *>(rec + tok * 64 + blk * 8) = make_uint2(packed[0], packed[1]);
+        rec[2048 + tok * 8 + blk] = static_cast<uint8_t>(S);
+        return;
+    }
+    // channel 16*blk + r (r = g + 8w) goes to row tok/2, group g at chunk
+    // position (g + 2*row) mod 8, byte 2*blk + w, nibble (tok & 1).
+    const int row = tok >> 1, half = tok & 1;
+    const uint64_t codes = (static_cast<uint64_t>(packed[1]) << 32) | packed[0];
+    const uint32_t shift = 16u * (blk & 1);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const uint32_t c0 = static_cast<uint32_t>(codes >> (4 * g)) & 15u;        // channel 16blk + g
+        const uint32_t c1 = static_cast<uint32_t>(codes >> (4 * (g + 8))) & 15u;  // channel 16blk + g + 8
+        const uint32_t unit = (c0 << (4 * half)) | (c1 << (8 + 4 * half));
+        const uint32_t mask = (0xFu << (4 * half)) | (0xFu << (8 + 4 * half));
+        unsigned int *word = reinterpret_cast<unsigned int *>(
+            rec + 1024 + row * 128 + ((g + 2 * row) & 7) * 16 + ((2 * blk) & ~3));
+        atomicAnd(word, ~(mask << shift));
+        atomicOr(word, unit << shift);
+    }
+    rec[2176 + row * 16 + blk * 2 + half] = static_cast<uint8_t>(S);
+}
+
+// FP8: each value E4M3_rn_satfinite(x); K chunk blk of row tok sits at position
+// (blk + (tok & 1)) mod 8; V channel 8c + i of token 2*row + half is byte
+// 2i + half of chunk c, at chunk position (c + f(row)) mod 16.
+__device__ __forceinline__ void write_fp8_block(uint8_t *rec, bool is_v, int tok, int blk, const float (&x)[16])
+{
+    if (!is_v) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = f32x2_to_e4m3x2(x[4 * k], x[4 * k + 1]) | (f32x2_to_e4m3x2(x[4 * k + 2], x[4 * k + 3]) << 16);
+        *reinterpret_cast<uint4 *>(rec + tok * 128 + ((blk + (tok & 1)) & 7) * 16) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+        return;
+    }
+    const int row = tok >> 1, half = tok & 1;
+    const int f = (row & 1) + 4 * ((row >> 1) & 1);
+    uint8_t *vrow = rec + 2048 + row * 256;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * blk + cc;
+        uint8_t *chunk = vrow + ((c + f) & 15) * 16;
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const uint32_t two = f32x2_to_e4m3x2(x[8 * cc + i], x[8 * cc + i + 1]);
+            chunk[2 * i + half] = static_cast<uint8_t>(two & 0xffu);
+            chunk[2 * (i + 1) + half] = static_cast<uint8_t>(two >> 8);
+        }
+    }
+}
+
+} // namespace nvfp4kv

@@ -106,3 +106,37 @@ def test_long_context_sampled(name, batch):
             assert_close(got8[seq, h * g:(h + 1) * g], oracle_single_head(b, seq, h, fp8=True),
                          f"{name} fp8 seq {seq} h {h}")
     assert int(b.status.item()) == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("lens", [(37, 16, 1, 300, 0), (8192, 8191, 8177)])
+def test_append_decode_equals_append_then_decode(fp8, lens):
+    """The fused step writes exactly the bytes quantize_append would and then
+    decodes exactly as paged_decode does."""
+    w = workloads.custom(len(lens), 32, 4, lens, seed=21)
+    full = Built(w)                                     # all tokens appended by quantize_append
+    cache = (nv.FP8Cache if fp8 else nv.NVFP4Cache).allocate(full.num_pages, w.num_kv_heads, device="cuda")
+    app = nv.fp8kv_quantize_append if fp8 else nv.nvfp4kv_quantize_append
+    k_new = torch.zeros((w.batch, w.num_kv_heads, 128), dtype=torch.float32, device="cuda")
+    v_new = torch.zeros_like(k_new)
+    for b, L in enumerate(w.seq_lens):
+        if L == 0:
+            continue
+        if L > 1:
+            sm = torch.from_numpy(workloads.slot_mapping(w, full.bt, b, 0, L - 1)).cuda()
+            app(cache, workloads.kv_rows(w, "k", b, 0, L - 1, device="cuda"),
+                workloads.kv_rows(w, "v", b, 0, L - 1, device="cuda"), sm)
+        k_new[b] = workloads.kv_rows(w, "k", b, L - 1, L, device="cuda")[0]
+        v_new[b] = workloads.kv_rows(w, "v", b, L - 1, L, device="cuda")[0]
+    out = torch.full((w.batch, w.num_q_heads, 128), float("nan"), dtype=torch.float32, device="cuda")
+    ws = nv.new_workspace(device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    step = nv.fp8kv_append_paged_decode if fp8 else nv.nvfp4kv_append_paged_decode
+    step(cache, k_new, v_new, full.q, full.bt_d, full.sl_d, out, ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref_pool = (full.fp8 if fp8 else full.cache).pool
+    np.testing.assert_array_equal(cache.pool.cpu().numpy(), ref_pool.cpu().numpy())
+    np.testing.assert_array_equal(out.cpu().numpy(), full.decode(torch.float32, fp8=fp8))
+    want, _ = oracle_full(full, fp8=fp8)
+    assert_close(out.cpu().numpy(), want, "fused append + decode")
