@@ -100,6 +100,14 @@ __device__ __forceinline__ int find_seq(const int32_t *prefix, int batch, int j)
     return lo;
 }
 
+// Workers that take part: never more than there are page-heads, so that every
+// worker's range [T*w/NW, T*(w+1)/NW) is non-empty and the contributors to a
+// segment are exactly the workers owner_of(first) .. owner_of(last).
+__device__ __forceinline__ long long effective_workers(int num_workers, long long T)
+{
+    return num_workers < T ? num_workers : (T > 0 ? T : 1);
+}
+
 // Worker that owns page-head index x (balanced split of T over NW).
 __device__ __forceinline__ int owner_of(long long x, long long T, long long NW)
 {
@@ -347,9 +355,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
 
     const int w = blockIdx.x * kDecodeWarps + warp;
     const long long T = prefix[p.batch];
-    const long long NW = p.num_workers;
-    const int lo = w < p.num_workers ? static_cast<int>((T * w) / NW) : 0;
-    const int hi = w < p.num_workers ? static_cast<int>((T * (w + 1)) / NW) : 0;
+    const long long NW = effective_workers(p.num_workers, T);
+    const int lo = w < NW ? static_cast<int>((T * w) / NW) : 0;
+    const int hi = w < NW ? static_cast<int>((T * (w + 1)) / NW) : 0;
 
     // The worker: this warp's page-heads [lo, hi).
     auto run_worker = [&]() {
@@ -441,8 +449,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
     }
 
     const int npro = min(S, hi - lo);
-    for (int j = lo; j < lo + npro; ++j)
-        issue(j, j - lo);
+    for (int x = lo; x < lo + npro; ++x)
+        issue(x, x - lo);
 
     uint32_t qf[16];
     float m0, m1, l0, l1;
@@ -539,15 +547,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
     auto step = [&](auto npc, uint32_t rec0, uint32_t rec1, int last_valid) {
         constexpr int NP = decltype(npc)::value;
         // S^T = K . Q^T
+        // (two accumulators per page-head halve the dependent MMA chain)
         float sc[NP][4];
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             uint32_t fa[16], fb[16];
             Fmt::load_k(q == 0 ? rec0 : rec1, off, fa, fb);
+            float sd[4] = {0.f, 0.f, 0.f, 0.f};
             sc[q][0] = sc[q][1] = sc[q][2] = sc[q][3] = 0.f;
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma_f16_16816(sc[q], fa[2 * s], fb[2 * s], fa[2 * s + 1], fb[2 * s + 1], qf[2 * s], qf[2 * s + 1]);
+                mma_f16_16816((s & 1) ? sd : sc[q], fa[2 * s], fb[2 * s], fa[2 * s + 1], fb[2 * s + 1], qf[2 * s],
+                              qf[2 * s + 1]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sc[q][e] += sd[e];
         }
         if (last_valid < kPageSize) {
             if (gid >= last_valid)

@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
     if (n > 0) {
         const long long T = prefix[p.batch];
-        const long long NW = p.num_workers;
+        const long long NW = effective_workers(p.num_workers, T);
         const int seg_begin = prefix[b] + h * n;
         const int wf = owner_of(seg_begin, T, NW);
         const int wl = owner_of(static_cast<long long>(seg_begin) + n - 1, T, NW);
@@ -40,27 +40,51 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
             return;                              // written by the decode kernel
         pdl_wait();                              // the partials come from the decode kernel
         const int nc = wl - wf + 1;
+        // Worker wf reached this segment from an earlier one unless it starts
+        // exactly at seg_begin; every later contributor starts inside the
+        // segment, so this is its first partial (slot 2w).
+        const int slot_wf = partial_slot(wf, seg_begin, T, NW);
+        // Contributors k = grp, grp + 8, ...: four per group are loaded before
+        // any is used, so one pass costs one memory round trip.
+        constexpr int kUnroll = 4;
         float M = -INFINITY, den = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int k = grp; k < nc; k += kGroups) {
-            const float *sl =
-                p.partials + static_cast<size_t>(partial_slot(wf + k, seg_begin, T, NW)) * kPartialFloats;
-            const float mk = __ldcg(sl + kMaxGroup * kHeadDim + i);
-            const float lk = __ldcg(sl + kMaxGroup * kHeadDim + kMaxGroup + i);
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(sl + i * kHeadDim) + lane);
-            if (mk > M) {                        // uniform across the warp
-                const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mk);
-                acc = make_float4(acc.x * a, acc.y * a, acc.z * a, acc.w * a);
-                den *= a;
-                M = mk;
+        for (int k0 = grp; k0 < nc; k0 += kGroups * kUnroll) {
+            float mk[kUnroll], lk[kUnroll];
+            float4 v[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int k = k0 + u * kGroups;
+                mk[u] = -INFINITY;
+                lk[u] = 0.f;
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (k < nc) {
+                    const int slot = k == 0 ? slot_wf : 2 * (wf + k);
+                    const float *sl = p.partials + static_cast<size_t>(slot) * kPartialFloats;
+                    mk[u] = __ldcg(sl + kMaxGroup * kHeadDim + i);
+                    lk[u] = __ldcg(sl + kMaxGroup * kHeadDim + kMaxGroup + i);
+                    v[u] = __ldcg(reinterpret_cast<const float4 *>(sl + i * kHeadDim) + lane);
+                }
             }
-            const float e = fast_exp2(mk - M);
-            acc.x += e * v.x;
-            acc.y += e * v.y;
-            acc.z += e * v.z;
-            acc.w += e * v.w;
-            den += e * lk;
+            float mx = M;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+                mx = fmaxf(mx, mk[u]);
+            if (mx == -INFINITY)
+                continue;
+            const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mx);
+            acc = make_float4(acc.x * a, acc.y * a, acc.z * a, acc.w * a);
+            den *= a;
+            M = mx;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const float e = (mk[u] == -INFINITY) ? 0.f : fast_exp2(mk[u] - M);
+                acc.x += e * v[u].x;
+                acc.y += e * v[u].y;
+                acc.z += e * v[u].z;
+                acc.w += e * v[u].w;
+                den += e * lk[u];
+            }
         }
         part[grp][lane] = acc;
         if (lane == 0) {

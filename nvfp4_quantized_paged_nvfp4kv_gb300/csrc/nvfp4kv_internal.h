@@ -1,7 +1,6 @@
 // Internal interface between the C ABI (abi.cpp) and the kernel launchers.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>

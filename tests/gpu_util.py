@@ -81,6 +81,7 @@ class Built:
         w = self.w
         out = torch.full((w.batch, w.num_q_heads, w.head_dim), float("nan"), dtype=out_dtype, device=DEV)
         ws = nv.new_workspace(num_workers, device=DEV)
+        ws.fill_(0xFF)               # NaN everywhere: a partial read before it is written shows
         q = self.q if q is None else q
         if fp8:
             nv.fp8kv_paged_decode(self.fp8, q, self.bt_d, self.sl_d, out, ws, num_workers=num_workers,

@@ -59,6 +59,22 @@ def test_worker_count_invariance():
         np.testing.assert_allclose(b.decode(torch.float32, num_workers=nw), ref, rtol=5e-3, atol=5e-4)
 
 
+def test_more_workers_than_page_heads():
+    """One long sequence among many short ones: the automatic worker count,
+    bounded by the largest batch the block table allows, and an explicit one
+    both exceed the number of page-heads, so the split must leave no worker
+    between two contributors of a segment without a range."""
+    lens = (3000,) + tuple(range(1, 24))
+    w = workloads.custom(len(lens), 16, 4, lens, seed=11)
+    b = Built(w, garbage=True)
+    want, _ = oracle_full(b)
+    want8, _ = oracle_full(b, fp8=True)
+    for nw in (0, 2000):
+        assert_close(b.decode(torch.float32, num_workers=nw), want, f"nvfp4 workers={nw}")
+        assert_close(b.decode(torch.float32, num_workers=nw, fp8=True), want8, f"fp8 workers={nw}")
+    assert int(b.status.item()) == 0
+
+
 def test_bad_page_and_length_are_reported_not_faulted():
     w = workloads.custom(2, 8, 2, (40, 40), seed=5)
     b = Built(w)
