@@ -31,8 +31,8 @@ namespace nvfp4kv {
 
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a staged-data wait gives up
 // The running max is moved only when a score exceeds it by more than this
-// (log2 units), so P <= 2^7; with a V block scale <= 448, P * scale <= 57344
-// stays finite in fp16.
+// (log2 units), so P <= 2^7 and its fp16 rounding stays relative (far from the
+// fp16 overflow and subnormal ranges for the terms that matter).
 constexpr float kLazyRescale = 7.0f;
 
 __device__ __forceinline__ int clamp_len(int L, int max_len)
@@ -196,11 +196,13 @@ struct Nvfp4Format {
         }
     }
 
-    // V^T fragments, unscaled E2M1 values (exact in fp16), and the block scales
-    // of the four tokens: sv[0][j] = (scale of token 2tig, 2tig+1 in block j),
-    // sv[1][j] the same for tokens 2tig+8, 2tig+9.  The scales are applied to P.
+    // V^T fragments, dequantised exactly: the E2M1 value (at most two
+    // significant bits) times the E4M3 block scale (four) is exact in fp16.
+    // va[j][0..1] hold tokens 2tig, 2tig+1 and va[j][2..3] tokens 2tig+8,
+    // 2tig+9 of m-tile j, which is scale block j; the scales of those token
+    // pairs come as f16x2 from one cvt each.
     __device__ static __forceinline__ void load_v(uint32_t rec, const LaneOffsets &o, int tig, int valid,
-                                                  uint32_t (&va)[8][4], uint32_t (&sv)[2][8])
+                                                  uint32_t (&va)[8][4])
     {
         uint4 x = lds128(rec + o.v[0]), y = lds128(rec + o.v[1]);
         uint4 s0 = lds128(rec + o.vs[0]), s1 = lds128(rec + o.vs[1]);
@@ -219,17 +221,23 @@ struct Nvfp4Format {
             s1 = make_uint4(s1.x & b1, s1.y & b1, s1.z & b1, s1.w & b1);
         }
         const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+        const uint32_t s0w[4] = {s0.x, s0.y, s0.z, s0.w}, s1w[4] = {s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             // bytes 4k .. 4k+3 = (m-tile 2k, w 0), (2k, 1), (2k+1, 0), (2k+1, 1)
             e2m1x8_to_f16x2x4(xw[k], va[2 * k][0], va[2 * k][1], va[2 * k + 1][0], va[2 * k + 1][1]);
             e2m1x8_to_f16x2x4(yw[k], va[2 * k][2], va[2 * k][3], va[2 * k + 1][2], va[2 * k + 1][3]);
-        }
-        const uint32_t s0w[4] = {s0.x, s0.y, s0.z, s0.w}, s1w[4] = {s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            e4m3x4_to_f16x2x2(s0w[k], sv[0][2 * k], sv[0][2 * k + 1]);
-            e4m3x4_to_f16x2x2(s1w[k], sv[1][2 * k], sv[1][2 * k + 1]);
+            uint32_t sa, sb, sc, sd;   // scale pairs of m-tiles 2k, 2k+1 for the two token pairs
+            e4m3x4_to_f16x2x2(s0w[k], sa, sb);
+            e4m3x4_to_f16x2x2(s1w[k], sc, sd);
+            va[2 * k][0] = hmul2(va[2 * k][0], sa);
+            va[2 * k][1] = hmul2(va[2 * k][1], sa);
+            va[2 * k + 1][0] = hmul2(va[2 * k + 1][0], sb);
+            va[2 * k + 1][1] = hmul2(va[2 * k + 1][1], sb);
+            va[2 * k][2] = hmul2(va[2 * k][2], sc);
+            va[2 * k][3] = hmul2(va[2 * k][3], sc);
+            va[2 * k + 1][2] = hmul2(va[2 * k + 1][2], sd);
+            va[2 * k + 1][3] = hmul2(va[2 * k + 1][3], sd);
         }
     }
 };
@@ -280,7 +288,7 @@ struct Fp8Format {
     }
 
     __device__ static __forceinline__ void load_v(uint32_t rec, const LaneOffsets &o, int tig, int valid,
-                                                  uint32_t (&va)[8][4], uint32_t (&)[2][8])
+                                                  uint32_t (&va)[8][4])
     {
         uint4 x0 = lds128(rec + o.v[0]), x1 = lds128(rec + o.v[1]);
         uint4 y0 = lds128(rec + o.v[2]), y1 = lds128(rec + o.v[3]);
@@ -600,29 +608,26 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
             m1 = n1;
         }
         uint32_t pb[NP][2];
+        float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             const float p0 = fast_exp2(sc[q][0] - m0), p1 = fast_exp2(sc[q][1] - m1);
             const float p2 = fast_exp2(sc[q][2] - m0), p3 = fast_exp2(sc[q][3] - m1);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
+            ls0 += p0 + p2;
+            ls1 += p1 + p3;
             pb[q][0] = movmatrix_trans(pack_f16x2(p0, p1));
             pb[q][1] = movmatrix_trans(pack_f16x2(p2, p3));
         }
-        // O^T += V^T . P^T; for NVFP4 each m-tile is one scale block, so the
-        // block scales of the tokens multiply the P^T columns instead of V.
+        l0 += ls0;
+        l1 += ls1;
+        // O^T += V^T . P^T (V arrives scaled)
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
-            uint32_t va[8][4], sv[2][8];
-            Fmt::load_v(q == 0 ? rec0 : rec1, off, tig, q == NP - 1 ? last_valid : kPageSize, va, sv);
+            uint32_t va[8][4];
+            Fmt::load_v(q == 0 ? rec0 : rec1, off, tig, q == NP - 1 ? last_valid : kPageSize, va);
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                if constexpr (Fmt::kRecord == Nvfp4Format::kRecord)
-                    mma_f16_16816(oacc[jj], va[jj][0], va[jj][1], va[jj][2], va[jj][3],
-                                  hmul2(pb[q][0], sv[0][jj]), hmul2(pb[q][1], sv[1][jj]));
-                else
-                    mma_f16_16816(oacc[jj], va[jj][0], va[jj][1], va[jj][2], va[jj][3], pb[q][0], pb[q][1]);
-            }
+            for (int jj = 0; jj < 8; ++jj)
+                mma_f16_16816(oacc[jj], va[jj][0], va[jj][1], va[jj][2], va[jj][3], pb[q][0], pb[q][1]);
         }
     };
 

@@ -10,43 +10,52 @@ namespace nvfp4kv {
 // Thread t works on channels 4*(t%32) .. +3 of the CTA's query head for the
 // contributors k = t/32, t/32 + 8, ...; each of the 8 contributor groups keeps
 // its own running maximum (one pass over the partials), and the groups are
-// combined in shared memory at the end.
+// combined in shared memory at the end.  The segment's contributor range is
+// worked out once per CTA, before the wait for the decode kernel.
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p)
 {
     constexpr int kGroups = kMergeThreads / 32;
+    constexpr int kUnroll = 8;                   // contributors a thread loads before using any
     extern __shared__ int32_t msmem[];
     __shared__ float4 part[kGroups][32];
     __shared__ float part_m[kGroups], part_l[kGroups];
+    __shared__ int seg[3];                       // first contributor, count (-1: empty sequence), its slot
     int32_t *scratch = msmem;
     int32_t *prefix = msmem + 32;
-    pdl_launch_dependents();                 // the next kernel may start its prologue
+    pdl_launch_dependents();                     // the next kernel may start its prologue
     build_prefix(p.seq_lens, p.batch, p.hkv, p.max_pages * kPageSize, prefix, scratch, nullptr);
 
     const int b = blockIdx.x / p.hkv;
     const int h = blockIdx.x - b * p.hkv;
     const int i = blockIdx.y;
     const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
-    const int n = (prefix[b + 1] - prefix[b]) / p.hkv;
+    if (threadIdx.x == 0) {
+        const int n = (prefix[b + 1] - prefix[b]) / p.hkv;
+        int wf = 0, nc = -1, slot = 0;
+        if (n > 0) {
+            const long long T = prefix[p.batch];
+            const long long NW = effective_workers(p.num_workers, T);
+            const int seg_begin = prefix[b] + h * n;
+            wf = owner_of(seg_begin, T, NW);
+            nc = owner_of(static_cast<long long>(seg_begin) + n - 1, T, NW) - wf + 1;
+            // wf reached this segment from an earlier one unless it starts at
+            // seg_begin; every later contributor starts inside the segment, so
+            // this is its first partial (slot 2w)
+            slot = partial_slot(wf, seg_begin, T, NW);
+        }
+        seg[0] = wf;
+        seg[1] = nc;
+        seg[2] = slot;
+    }
+    __syncthreads();
+    const int wf = seg[0], nc = seg[1], slot_wf = seg[2];
+    if (nc == 1)
+        return;                                  // written by the decode kernel
     const size_t o = (static_cast<size_t>(b) * p.hq + h * p.group + i) * kHeadDim + 4 * lane;
 
     float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (n > 0) {
-        const long long T = prefix[p.batch];
-        const long long NW = effective_workers(p.num_workers, T);
-        const int seg_begin = prefix[b] + h * n;
-        const int wf = owner_of(seg_begin, T, NW);
-        const int wl = owner_of(static_cast<long long>(seg_begin) + n - 1, T, NW);
-        if (wf == wl)
-            return;                              // written by the decode kernel
+    if (nc > 1) {
         pdl_wait();                              // the partials come from the decode kernel
-        const int nc = wl - wf + 1;
-        // Worker wf reached this segment from an earlier one unless it starts
-        // exactly at seg_begin; every later contributor starts inside the
-        // segment, so this is its first partial (slot 2w).
-        const int slot_wf = partial_slot(wf, seg_begin, T, NW);
-        // Contributors k = grp, grp + 8, ...: four per group are loaded before
-        // any is used, so one pass costs one memory round trip.
-        constexpr int kUnroll = 4;
         float M = -INFINITY, den = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k0 = grp; k0 < nc; k0 += kGroups * kUnroll) {
@@ -70,8 +79,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u)
                 mx = fmaxf(mx, mk[u]);
-            if (mx == -INFINITY)
-                continue;
             const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mx);
             acc = make_float4(acc.x * a, acc.y * a, acc.z * a, acc.w * a);
             den *= a;
@@ -113,7 +120,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
         const float r = 1.f / dsum;
         res = make_float4(sum.x * r, sum.y * r, sum.z * r, sum.w * r);
     } else if (grp != 0) {
-        return;
+        return;                                  // empty sequence: zeros
     }
     if (p.out_bf16) {
         __nv_bfloat162 a = __floats2bfloat162_rn(res.x, res.y), c = __floats2bfloat162_rn(res.z, res.w);
