@@ -456,8 +456,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         __syncwarp();
     }
 
+    // The first two records go out at once, the rest of the ring once the
+    // first has landed: when every warp asks for its whole ring together,
+    // each warp's first record would arrive late in that burst.
     const int npro = min(S, hi - lo);
-    for (int x = lo; x < lo + npro; ++x)
+    for (int x = lo; x < lo + min(2, npro); ++x)
         issue(x, x - lo);
 
     uint32_t qf[16];
@@ -550,6 +553,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
     };
 
     start_segment();
+    if (npro > 2) {
+        // (a wait that gives up here gives up again, reported, in the loop)
+        mbar_wait_bounded(wbar, 0, kWaitLimit);
+        __syncwarp();
+        for (int x = lo + 2; x < lo + npro; ++x)
+            issue(x, x - lo);
+    }
 
     // One step handles one page-head, or two of the same segment.
     auto step = [&](auto npc, uint32_t rec0, uint32_t rec1, int last_valid) {
