@@ -140,6 +140,11 @@ nvfp4kv_status nvfp4kv_quantize_append(const nvfp4kv_cache *cache, const void *k
                                        int32_t num_tokens, const int32_t *slot_mapping,
                                        int32_t *dev_status, nvfp4kv_stream_t stream);
 
+/* Largest batch one decode call takes (the per-sequence page-head offsets are
+ * kept in shared memory next to the staging ring); a larger batch returns
+ * NVFP4KV_ERR_UNSUPPORTED. */
+#define NVFP4KV_MAX_BATCH 8192
+
 /* Bytes of decode workspace needed by nvfp4kv_paged_decode / fp8kv_paged_decode
  * when called with the same num_workers on the current device (num_workers 0 =
  * the automatic choice, whose need is bounded by this value).  Host only; the
@@ -214,8 +219,8 @@ nvfp4kv_status nvfp4kv_append_paged_decode(const nvfp4kv_cache *cache, const voi
  * device share the array: calls whose kernels can overlap on the GPU race and
  * must be serialised (for example, issue them on one stream).  Allocates no
  * memory. */
-#define NVFP4KV_STATIC_SCRATCH_BYTES (16u << 20)
-#define NVFP4KV_STATIC_SCRATCH_MAX_WORKERS 2016
+#define NVFP4KV_STATIC_SCRATCH_BYTES (24u << 20)
+#define NVFP4KV_STATIC_SCRATCH_MAX_WORKERS 3024
 nvfp4kv_status nvfp4kv_paged_decode_static_scratch(const nvfp4kv_cache *cache, const void *q, int32_t batch,
                                                    int32_t num_q_heads, const int32_t *block_table,
                                                    int32_t max_pages_per_seq, const int32_t *seq_lens,

@@ -328,6 +328,12 @@ size_t decode_smem_bytes(int batch)
     return decode_smem_fixed<Fmt>() + static_cast<size_t>(batch + 1) * sizeof(int32_t);
 }
 
+// one CTA per SM: the staging rings of all its warps plus the largest prefix table
+static_assert(decode_smem_fixed<Nvfp4Format>() + (kMaxBatch + 1) * sizeof(int32_t) <= 227 * 1024,
+              "NVFP4 decode shared memory");
+static_assert(decode_smem_fixed<Fp8Format>() + (kMaxBatch + 1) * sizeof(int32_t) <= 227 * 1024,
+              "FP8 decode shared memory");
+
 // ---- the decode kernel -------------------------------------------------------
 
 template <class Fmt>

@@ -5,17 +5,19 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "nvfp4kv.h"
+
 namespace nvfp4kv {
 
 constexpr int kPageSize = 16;
 constexpr int kHeadDim = 128;
 constexpr int kMaxGroup = 8;                 // query heads per kv head handled by one warp
-constexpr int kDecodeWarps = 4;              // warps (independent workers) per decode CTA
-constexpr int kDecodeCtasPerSm = 4;          // occupancy the default worker count assumes
+constexpr int kDecodeWarps = 16;             // warps (independent workers) per decode CTA
+constexpr int kDecodeCtasPerSm = 1;          // occupancy the default worker count assumes
 constexpr int kPartialFloats = kMaxGroup * kHeadDim + 2 * kMaxGroup;  // O[8][128], m[8], l[8]
 constexpr int kNvfp4Record = 2304;           // bytes of an NVFP4 page-head record
 constexpr int kFp8Record = 4096;             // bytes of an FP8 page-head record
-constexpr int kMaxBatch = 16384;             // prefix table lives in shared memory
+constexpr int kMaxBatch = NVFP4KV_MAX_BATCH; // prefix table lives in shared memory
 
 // Split-KV decode over either cache format.
 struct DecodeParams {

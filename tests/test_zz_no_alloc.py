@@ -45,5 +45,5 @@ def test_static_scratch_rejects_too_many_workers():
     b = Built(workloads.make("tiny"), fp8=False)
     out = torch.empty((2, 8, 128), dtype=torch.float32, device="cuda")
     assert static_decode(b, out, num_workers=100000) == nv.ERR_WORKSPACE
-    assert static_decode(b, out, num_workers=2016) == nv.OK
+    assert static_decode(b, out, num_workers=3024) == nv.OK
     torch.cuda.synchronize()
