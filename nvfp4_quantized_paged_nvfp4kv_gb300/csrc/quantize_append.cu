@@ -8,80 +8,116 @@
 //   byte j = q_2j | q_2j+1 << 4.
 // FP8 (the comparison cache): each value E4M3_rn_satfinite(x), scale 1.0.
 //
-// One thread per 16-value block of one token-head row of K or V.  Records are
-// laid out as documented in include/nvfp4kv.h: K rows are natural (8 bytes per
-// block, one 8-byte store); V bytes hold the two tokens of a token pair in their
-// two nibbles, so a V block is merged into its 8 words with atomic AND/OR on the
-// thread's own nibbles (the other token of the pair may be written by another
-// thread or another call).
+// Records are laid out as documented in include/nvfp4kv.h: K rows are natural
+// (8 bytes per block, one 8-byte store); V bytes hold the two tokens of a token
+// pair in their two nibbles.  A pair whose two tokens are neighbours in this
+// call is written whole by one thread; a lone token's V block is merged into
+// its 8 words with atomic AND/OR on its own nibbles (its partner may come from
+// another call).
 #include "nvfp4kv.h"
 #include "record_write.cuh"
 
 namespace nvfp4kv {
 
-// Shared front part: which block this thread owns and where it goes.
-struct BlockSite {
-    bool active;
-    size_t src_off;     // element offset of the block in k_new / v_new
-    size_t record;      // byte offset of the page-head record
-    int tok;            // token within the page (0..15)
-    int blk;            // block within the row (0..7)
-};
-
-// The cache records written here may still be read by the previous kernel in
-// the stream (a decode of the last step): wait for it, then let the next start.
-__device__ __forceinline__ BlockSite locate(const QuantParams &p, long long idx, int record_bytes)
+// Where the block of input token t lands: the byte offset of its page-head
+// record and its token within the page, or false when the slot is skipped
+// (negative) or out of range (reported).
+__device__ __forceinline__ bool site_of(const QuantParams &p, int slot, int h, int record_bytes, size_t &record,
+                                        int &tok, bool report_bad)
 {
-    pdl_wait();
-    pdl_launch_dependents();
-    BlockSite s{false, 0, 0, 0, 0};
-    const long long rows = static_cast<long long>(p.num_tokens) * p.hkv;
-    if (idx >= rows * 8)
-        return s;
-    const long long th = idx >> 3;                   // token-head row of the input
-    s.blk = static_cast<int>(idx & 7);
-    const int t = static_cast<int>(th / p.hkv);
-    const int h = static_cast<int>(th - static_cast<long long>(t) * p.hkv);
-    const int slot = __ldg(p.slot_mapping + t);
     if (slot < 0)
-        return s;
+        return false;
     if (slot >= p.num_pages * kPageSize) {
-        if (s.blk == 0 && h == 0)
+        if (report_bad)
             report(p.dev_status, NVFP4KV_DEV_BAD_SLOT);
-        return s;
+        return false;
     }
     const int page = slot / kPageSize;
-    s.tok = slot - page * kPageSize;
-    s.active = true;
-    s.src_off = static_cast<size_t>(th) * kHeadDim + s.blk * 16;
-    s.record = (static_cast<size_t>(page) * p.hkv + h) * record_bytes;
-    return s;
+    tok = slot - page * kPageSize;
+    record = (static_cast<size_t>(page) * p.hkv + h) * record_bytes;
+    return true;
 }
 
+// NVFP4.  blockIdx.y == 0: K, one thread per (token, kv head, block).
+// blockIdx.y == 1: V, one thread per (token pair, kv head, block).  V pairs are
+// taken in input order, starting one token early when the first slot is odd,
+// so that consecutive slots (the usual prefill order) form the record's token
+// pairs; such a pair is written whole, any other token through the atomic
+// nibble merge.  Each thread issues its data loads together with its slot
+// loads (the source offset does not depend on the slot).
 template <bool kBf16>
 __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const QuantParams p)
 {
+    pdl_wait();                  // the records may still be read by the previous kernel
+    pdl_launch_dependents();
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const BlockSite s = locate(p, idx, kNvfp4Record);
-    if (!s.active)
+    const int blk = static_cast<int>(idx & 7);
+    const long long unit = idx >> 3;                 // (token or pair) * hkv + h
+    const int h = static_cast<int>(unit % p.hkv);
+    const long long tu = unit / p.hkv;
+    if (blockIdx.y == 0) {
+        if (tu >= p.num_tokens)
+            return;
+        const int t = static_cast<int>(tu);
+        float x[16];
+        load16<kBf16>(p.k_new, (static_cast<size_t>(t) * p.hkv + h) * kHeadDim + blk * 16, x);
+        size_t record;
+        int tok;
+        if (!site_of(p, __ldg(p.slot_mapping + t), h, kNvfp4Record, record, tok, blk == 0 && h == 0))
+            return;
+        write_nvfp4_block(p.pool + record, false, tok, blk, x);
         return;
-    const bool is_v = blockIdx.y == 1;
-    float x[16];
-    load16<kBf16>(is_v ? p.v_new : p.k_new, s.src_off, x);
-    write_nvfp4_block(p.pool + s.record, is_v, s.tok, s.blk, x);
+    }
+    const int first = __ldg(p.slot_mapping);
+    const int o = first >= 0 ? (first & 1) : 0;
+    const long long pairs = (static_cast<long long>(p.num_tokens) + o + 1) / 2;
+    if (tu >= pairs)
+        return;
+    const int t0 = static_cast<int>(2 * tu) - o, t1 = t0 + 1;
+    const bool has0 = t0 >= 0, has1 = t1 < p.num_tokens;
+    float x0[16], x1[16];
+    if (has0)
+        load16<kBf16>(p.v_new, (static_cast<size_t>(t0) * p.hkv + h) * kHeadDim + blk * 16, x0);
+    if (has1)
+        load16<kBf16>(p.v_new, (static_cast<size_t>(t1) * p.hkv + h) * kHeadDim + blk * 16, x1);
+    const int s0 = has0 ? __ldg(p.slot_mapping + t0) : -1;
+    const int s1 = has1 ? __ldg(p.slot_mapping + t1) : -1;
+    size_t r0 = 0, r1 = 0;
+    int tok0 = 0, tok1 = 0;
+    const bool ok0 = has0 && site_of(p, s0, h, kNvfp4Record, r0, tok0, blk == 0 && h == 0);
+    const bool ok1 = has1 && site_of(p, s1, h, kNvfp4Record, r1, tok1, blk == 0 && h == 0);
+    if (ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
+        write_nvfp4_v_pair(p.pool + r0, tok0, blk, x0, x1);
+        return;
+    }
+    if (ok0)
+        write_nvfp4_block(p.pool + r0, true, tok0, blk, x0);
+    if (ok1)
+        write_nvfp4_block(p.pool + r1, true, tok1, blk, x1);
 }
 
+// FP8: one thread per (token, kv head, block) of K (y == 0) or V (y == 1).
 template <bool kBf16>
 __global__ void __launch_bounds__(256) quantize_fp8_kernel(const QuantParams p)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const BlockSite s = locate(p, idx, kFp8Record);
-    if (!s.active)
+    const int blk = static_cast<int>(idx & 7);
+    const long long unit = idx >> 3;
+    const int h = static_cast<int>(unit % p.hkv);
+    const long long tu = unit / p.hkv;
+    if (tu >= p.num_tokens)
         return;
+    const int t = static_cast<int>(tu);
     const bool is_v = blockIdx.y == 1;
     float x[16];
-    load16<kBf16>(is_v ? p.v_new : p.k_new, s.src_off, x);
-    write_fp8_block(p.pool + s.record, is_v, s.tok, s.blk, x);
+    load16<kBf16>(is_v ? p.v_new : p.k_new, (static_cast<size_t>(t) * p.hkv + h) * kHeadDim + blk * 16, x);
+    size_t record;
+    int tok;
+    if (!site_of(p, __ldg(p.slot_mapping + t), h, kFp8Record, record, tok, !is_v && blk == 0 && h == 0))
+        return;
+    write_fp8_block(p.pool + record, is_v, tok, blk, x);
 }
 
 template <class K>

@@ -33,6 +33,14 @@ __device__ __forceinline__ void load16(const void *src, size_t elem_off, float (
 }
 
 // amax -> E4M3 block scale -> 16 E2M1 codes (code i in bits 4i .. 4i+3).
+//
+// Each code is decided on the IEEE quotient fl32(x / s).  It is computed
+// without a division per element: with r = RN(1/s), q0 = RN(x r) is within an
+// ulp of x / s, the remainder x - q0 s is exact through one FMA, and
+// RN(q0 + (x - q0 s) r) is the correctly rounded quotient (Markstein's
+// correction step).  s has at most four significant bits, so only eight
+// mantissas occur; every fp32 quotient in the range that decides a code is
+// compared against an IEEE division for all eight in the GPU tests.
 __device__ __forceinline__ void quantize_block(const float (&x)[16], uint32_t &scale_byte, uint32_t (&packed)[2])
 {
     float amax = 0.f;
@@ -44,9 +52,15 @@ __device__ __forceinline__ void quantize_block(const float (&x)[16], uint32_t &s
     const float sc = e4m3_to_f32(scale_byte);
     packed[0] = packed[1] = 0u;
     if (sc != 0.f) {
+        const float r = __frcp_rn(sc);
+        auto quotient = [&](float v) {
+            const float q0 = __fmul_rn(v, r);
+            // the correction step turns a -0 quotient into +0: restore the sign
+            return copysignf(__fmaf_rn(__fmaf_rn(-q0, sc, v), r, q0), v);
+        };
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const uint32_t byte = f32x2_to_e2m1x2(__fdiv_rn(x[2 * j], sc), __fdiv_rn(x[2 * j + 1], sc));
+            const uint32_t byte = f32x2_to_e2m1x2(quotient(x[2 * j]), quotient(x[2 * j + 1]));
             packed[j >> 2] |= byte << (8 * (j & 3));
         }
     }
@@ -81,6 +95,31 @@ __device__ __forceinline__ void write_nvfp4_block(uint8_t *rec, bool is_v, int t
         atomicOr(word, unit << shift);
     }
     rec[2176 + row * 16 + blk * 2 + half] = static_cast<uint8_t>(S);
+}
+
+// NVFP4, V block blk of both tokens of a token pair (tok0 even, tok0 + 1) at
+// once: every byte of theirs is written whole, no atomics.
+__device__ __forceinline__ void write_nvfp4_v_pair(uint8_t *rec, int tok0, int blk, const float (&x0)[16],
+                                                   const float (&x1)[16])
+{
+    uint32_t S0, S1, p0[2], p1[2];
+    quantize_block(x0, S0, p0);
+    quantize_block(x1, S1, p1);
+    const int row = tok0 >> 1;
+    const uint64_t c0 = (static_cast<uint64_t>(p0[1]) << 32) | p0[0];
+    const uint64_t c1 = (static_cast<uint64_t>(p1[1]) << 32) | p1[0];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        // bytes 2*blk (channel 16blk + g) and 2*blk + 1 (channel 16blk + g + 8);
+        // low nibble token tok0, high nibble token tok0 + 1
+        const uint32_t lo = (static_cast<uint32_t>(c0 >> (4 * g)) & 15u) |
+                            ((static_cast<uint32_t>(c1 >> (4 * g)) & 15u) << 4);
+        const uint32_t hi = (static_cast<uint32_t>(c0 >> (4 * (g + 8))) & 15u) |
+                            ((static_cast<uint32_t>(c1 >> (4 * (g + 8))) & 15u) << 4);
+        *reinterpret_cast<uint16_t *>(rec + 1024 + row * 128 + ((g + 2 * row) & 7) * 16 + 2 * blk) =
+            static_cast<uint16_t>(lo | (hi << 8));
+    }
+    *reinterpret_cast<uint16_t *>(rec + 2176 + row * 16 + blk * 2) = static_cast<uint16_t>(S0 | (S1 << 8));
 }
 
 // FP8: each value E4M3_rn_satfinite(x); K chunk blk of row tok sits at position

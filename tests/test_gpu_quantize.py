@@ -104,6 +104,24 @@ def test_v_nibble_pairs_written_by_separate_calls():
             np.testing.assert_array_equal(g_, w_)
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_odd_first_slot_and_broken_pairs(fp8):
+    """Slots that start odd, jump, skip a token, swap a pair's order and run
+    backwards, so that tokens taken in input order both do and do not form
+    the record's token pairs."""
+    slots = (list(range(5, 25)) + [-1] + list(range(41, 51)) + [60, 62, 61, 63] + [3, 2]
+             + list(range(80, 87)))
+    T, hkv, pages = len(slots), 2, 6
+    rng = np.random.default_rng(11)
+    k = torch.from_numpy(rng.standard_normal((T, hkv, 128)).astype(np.float32))
+    v = torch.from_numpy((rng.standard_normal((T, hkv, 128)) * 3).astype(np.float32))
+    got, st = run_gpu(k, v, slots, pages, hkv, fp8=fp8)
+    want = run_oracle(k, v, slots, pages, hkv, fp8=fp8)
+    assert st == 0
+    for g_, w_ in zip(got, want):
+        np.testing.assert_array_equal(g_, w_)
+
+
 def test_skipped_and_out_of_range_slots():
     rng = np.random.default_rng(0)
     T, hkv, pages = 40, 2, 4
@@ -164,6 +182,36 @@ def test_every_element_value_at_unit_scale():
             np.testing.assert_array_equal(got, want)
             total_checked += len(vals)
     assert total_checked == 2 * (lim + 1)
+
+
+def test_element_rounding_for_every_scale_mantissa():
+    """Each code is decided on the IEEE quotient fl32(x / s), which the kernel
+    forms without a division instruction.  An E4M3 scale has one of eight
+    mantissas (s = 1 + m/8 up to a power of two, which scales every quotient
+    exactly).  For each, every fp32 x with 1/8 <= x/s <= 6 (and the negatives
+    for one of them) is quantised in blocks of 15 test values plus one 6s,
+    and every code is compared with the oracle's encoder of the quotient."""
+    step = 15 * 8 * (1 << 18)
+    for m in range(8):
+        s = np.float32(1 + m / 8)
+        anchor = np.float32(s * np.float32(6.0))
+        lo = int(np.float32(s * np.float32(0.125)).view(np.uint32))
+        hi = int(anchor.view(np.uint32))
+        for sign in ((0, 0x80000000) if m == 5 else (0,)):
+            for start in range(lo, hi + 1, step):
+                stop = min(hi + 1, start + step)
+                bits = np.arange(start, stop, dtype=np.uint64).astype(np.uint32) | np.uint32(sign)
+                vals = bits.view(np.float32)
+                pad = (-len(vals)) % (15 * 8)
+                vals_p = np.concatenate([vals, np.zeros(pad, np.float32)])
+                blocks = np.empty((len(vals_p) // 15, 16), np.float32)
+                blocks[:, :15] = vals_p.reshape(-1, 15)
+                blocks[:, 15] = anchor
+                codes, scale = _blocks_to_gpu_codes(blocks)
+                assert bool((scale == 0x38 + m).all())
+                got = codes[:, :15].reshape(-1)[:len(vals)].cpu().numpy()
+                want = oracle.e2m1_encode((vals / s).astype(np.float32))
+                np.testing.assert_array_equal(got, want)
 
 
 def test_block_scale_sweep():
