@@ -177,7 +177,10 @@ size_t nvfp4kv_decode_workspace_size(int32_t num_workers);
  *   value).
  * Launches two kernels (split-KV attention, then the split merge), both with
  * programmatic dependent launch allowed, so each may start its prologue while
- * the previous kernel in the stream drains. */
+ * the previous kernel in the stream drains.  seq_lens and block_table are read
+ * in that prologue: a kernel earlier in the stream that writes them must not
+ * let its dependents start before it has written them (no kernel of this
+ * library writes them). */
 nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q,
                                     int32_t batch, int32_t num_q_heads,
                                     const int32_t *block_table, int32_t max_pages_per_seq,

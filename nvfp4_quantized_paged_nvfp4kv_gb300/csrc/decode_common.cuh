@@ -359,10 +359,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
             mbar_init(wbar + 8 * s, 1);
         fence_mbar_init();
     }
-    // everything below reads data the previous kernel in the stream may write;
-    // the merge kernel that follows may start its own prologue meanwhile
-    pdl_wait();
+    // The merge kernel that follows may start its own prologue meanwhile.
     pdl_launch_dependents();
+    // The work split and the block-table lookups read only the lengths and the
+    // block table, which no kernel of this library writes; they run before the
+    // wait for the previous kernel in the stream, overlapping its tail.  The
+    // cache records, q, the new K/V, the output and the workspace are touched
+    // only after the wait.
     const int max_len = p.max_pages * kPageSize;
     build_prefix(p.seq_lens, p.batch, p.hkv, max_len, prefix, scratch,
                  blockIdx.x == 0 ? p.dev_status : nullptr);
@@ -428,6 +431,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
     int L = clamp_len(p.seq_lens[b], max_len);
     int seg_begin = prefix[b] + h * n;
 
+    pdl_wait();
     if (p.append) {
         // Fused append: the warp that streams the last page-head of a segment
         // first writes that sequence's new token (position seq_len - 1) into
