@@ -29,7 +29,6 @@
 
 namespace nvfp4kv {
 
-constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a staged-data wait gives up
 // The running max is moved only when a score exceeds it by more than this
 // (log2 units), so P <= 2^7 and its fp16 rounding stays relative (far from the
 // fp16 overflow and subnormal ranges for the terms that matter).

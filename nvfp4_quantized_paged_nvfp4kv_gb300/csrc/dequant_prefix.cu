@@ -6,19 +6,23 @@
 // The product has at most 6 significant bits and lies in [2^-10, 2688], so it
 // is exact in fp16; the only rounding is the final one to E4M3.
 //
-// Work unit: one page-head (16 tokens x 8 blocks of K and of V) per 128-thread
-// CTA iteration, grid-stride over (sequence, page, kv head).  Thread (token,
-// block) gathers the 16 K codes and the 16 V codes of its (token, block) from
-// the record (layout in include/nvfp4kv.h) with independent loads, and writes
-// 16 E4M3 bytes to each workspace.  The unit's length, block-table entry and
-// output offset are read together, and those of the CTA's next unit are
-// fetched while the current one is being converted.
+// Work unit: one page-head record (16 tokens of one kv head, K and V), grid-
+// stride over (sequence, page, kv head).  A CTA of 64 threads stages the
+// record of its next unit in shared memory with one bulk copy (double
+// buffered) while it converts the current one.  Thread t converts K blocks
+// (token t/8, block t%8) and (token t/8 + 8, block t%8), and V block t%8 of the
+// token pair t/8: a V byte holds one channel of both tokens, so the pair is
+// dequantised together (one cvt per channel) and split into the two tokens'
+// rows when the E4M3 bytes are packed.
 #include "device_common.cuh"
 #include "nvfp4kv.h"
 
 namespace nvfp4kv {
 
 namespace {
+
+constexpr int kPrefixThreads = 64;
+constexpr int kPrefixCtasPerSm = 24;
 
 struct PrefixUnit {
     int b, pg, h;
@@ -39,75 +43,151 @@ __device__ __forceinline__ PrefixUnit prefix_unit(const PrefixParams &p, long lo
     return t;
 }
 
-// 16 E2M1 codes (natural channel order) x scale -> 16 E4M3 bytes
-__device__ __forceinline__ uint4 codes_to_e4m3(uint2 packed, uint32_t sbyte)
+// Two bytes of 8 E4M3 values each from 8 f16x2 (low halves -> first word pair).
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t h2a, uint32_t h2b)
 {
-    const uint32_t s2 = e4m3x2_to_f16x2(sbyte | (sbyte << 8));
-    uint32_t f[8];
-    e2m1x8_to_f16x2x4(packed.x, f[0], f[1], f[2], f[3]);
-    e2m1x8_to_f16x2x4(packed.y, f[4], f[5], f[6], f[7]);
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        w[k] = f16x2_to_e4m3x2(hmul2(f[2 * k], s2)) | (f16x2_to_e4m3x2(hmul2(f[2 * k + 1], s2)) << 16);
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    return f16x2_to_e4m3x2(h2a) | (f16x2_to_e4m3x2(h2b) << 16);
 }
 
 } // namespace
 
-__global__ void __launch_bounds__(128) dequant_prefix_kernel(const PrefixParams p)
+__global__ void __launch_bounds__(kPrefixThreads) dequant_prefix_kernel(const PrefixParams p)
 {
-    pdl_wait();
-    const int tok = threadIdx.x >> 3, blk = threadIdx.x & 7;
-    const int row = tok >> 1, half = tok & 1;
+    __shared__ __align__(128) uint8_t buf[2][kNvfp4Record];
+    __shared__ __align__(8) uint64_t bars[2];
+    const int t = threadIdx.x;
+    const int row = t >> 3, blk = t & 7;
     const long long units = static_cast<long long>(p.batch) * p.max_pages * p.hkv;
     const int max_len = p.max_pages * kPageSize;
-    long long u = blockIdx.x;
-    PrefixUnit cur{};
-    if (u < units)
-        cur = prefix_unit(p, u);
-    for (; u < units; u += gridDim.x) {
-        PrefixUnit nxt{};
-        if (u + gridDim.x < units)
-            nxt = prefix_unit(p, u + gridDim.x);
-        int L = cur.len;
+    const uint32_t bar0 = smem_addr(&bars[0]);
+    if (t == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();                  // the records may come from the previous kernel
+
+    // Length of the unit's sequence (clamped, reported) and whether its page
+    // holds any prefix token; issues the unit's copy into buffer k if so.
+    auto stage = [&](const PrefixUnit &x, int k, int &L) {
+        L = x.len;
         if (L < 0 || L > max_len) {
-            if (threadIdx.x == 0 && cur.pg == 0 && cur.h == 0)
+            if (t == 0 && x.pg == 0 && x.h == 0)
                 report(p.dev_status, NVFP4KV_DEV_BAD_LEN);
             L = L < 0 ? 0 : max_len;
         }
-        const int j = cur.pg * kPageSize + tok;
-        if (j < L) {
-            int phys = cur.phys;
-            if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_pages)) {
-                if (tok == 0 && blk == 0)
-                    report(p.dev_status, NVFP4KV_DEV_BAD_PAGE);
-                phys = 0;
-            }
-            const uint8_t *rec = p.pool + (static_cast<size_t>(phys) * p.hkv + cur.h) * kNvfp4Record;
-            // K: natural rows
-            const uint2 kpacked = __ldg(reinterpret_cast<const uint2 *>(rec + tok * 64 + blk * 8));
-            const uint32_t ks = __ldg(rec + 2048 + tok * 8 + blk);
-            // V: channel 16*blk + g + 8w sits in row tok/2, chunk (g + 2*row) mod
-            // 8, byte 2*blk + w, nibble tok & 1; repacked into natural order
-            uint32_t units16[8];
-#pragma unroll
-            for (int g = 0; g < 8; ++g)
-                units16[g] = __ldg(reinterpret_cast<const uint16_t *>(
-                    rec + 1024 + row * 128 + ((g + 2 * row) & 7) * 16 + 2 * blk));
-            const uint32_t vs = __ldg(rec + 2176 + row * 16 + blk * 2 + half);
-            uint32_t lo = 0u, hi = 0u;
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                lo |= ((units16[g] >> (4 * half)) & 15u) << (4 * g);        // channel g
-                hi |= ((units16[g] >> (8 + 4 * half)) & 15u) << (4 * g);    // channel g + 8
-            }
-            const size_t orow = (static_cast<size_t>(cur.base) + j) * p.hkv + cur.h;
-            *reinterpret_cast<uint4 *>(p.k_out + orow * kHeadDim + blk * 16) = codes_to_e4m3(kpacked, ks);
-            *reinterpret_cast<uint4 *>(p.v_out + orow * kHeadDim + blk * 16) =
-                codes_to_e4m3(make_uint2(lo, hi), vs);
+        if (x.pg * kPageSize >= L)
+            return false;
+        int phys = x.phys;
+        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_pages)) {
+            if (t == 0)
+                report(p.dev_status, NVFP4KV_DEV_BAD_PAGE);
+            phys = 0;
         }
+        if (t == 0) {
+            const uint32_t bar = bar0 + 8 * k;
+            mbar_arrive_expect_tx(bar, kNvfp4Record);
+            bulk_g2s(smem_addr(buf[k]), p.pool + (static_cast<size_t>(phys) * p.hkv + x.h) * kNvfp4Record,
+                     kNvfp4Record, bar);
+        }
+        return true;
+    };
+
+    long long u = blockIdx.x;
+    if (u >= units)
+        return;
+    PrefixUnit cur = prefix_unit(p, u);
+    int L = 0;
+    bool staged = stage(cur, 0, L);
+    uint32_t parity = 0u;        // bit k: phase parity of buffer k's barrier
+    int k = 0;
+    for (; u < units; u += gridDim.x) {
+        const long long un = u + gridDim.x;
+        PrefixUnit nxt{};
+        int Ln = 0;
+        bool staged_n = false;
+        if (un < units) {
+            nxt = prefix_unit(p, un);
+            staged_n = stage(nxt, k ^ 1, Ln);
+        }
+        if (staged) {
+            const bool arrived = mbar_wait_bounded(bar0 + 8 * k, (parity >> k) & 1u, kWaitLimit);
+            parity ^= 1u << k;
+            if (!__syncthreads_and(arrived)) {
+                // staged data never arrived: report, let the other copy land, stop
+                if (t == 0)
+                    report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
+                if (staged_n)
+                    mbar_wait_bounded(bar0 + 8 * (k ^ 1), (parity >> (k ^ 1)) & 1u, kWaitLimit);
+                return;
+            }
+            const uint32_t rec = smem_addr(buf[k]);
+            const int j0 = cur.pg * kPageSize;
+            const size_t rows = static_cast<size_t>(cur.base) + j0;     // output row of token 0
+            // K: tokens row and row + 8, block blk (natural rows)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int tok = row + 8 * half;
+                if (j0 + tok < L) {
+                    const uint2 packed = lds64(rec + tok * 64 + blk * 8);
+                    const uint32_t sb = lds_u8(rec + 2048 + tok * 8 + blk);
+                    const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
+                    uint32_t f[8];
+                    e2m1x8_to_f16x2x4(packed.x, f[0], f[1], f[2], f[3]);
+                    e2m1x8_to_f16x2x4(packed.y, f[4], f[5], f[6], f[7]);
+                    const size_t o = ((rows + tok) * p.hkv + cur.h) * kHeadDim + blk * 16;
+                    *reinterpret_cast<uint4 *>(p.k_out + o) =
+                        make_uint4(e4m3_pair(hmul2(f[0], s2), hmul2(f[1], s2)), e4m3_pair(hmul2(f[2], s2), hmul2(f[3], s2)),
+                                   e4m3_pair(hmul2(f[4], s2), hmul2(f[5], s2)), e4m3_pair(hmul2(f[6], s2), hmul2(f[7], s2)));
+                }
+            }
+            // V: tokens 2*row (low nibbles) and 2*row + 1 (high nibbles), block blk.
+            // Unit g (bytes 2*blk, 2*blk + 1 of group g's chunk) holds channels
+            // 16*blk + g and 16*blk + g + 8 of both tokens.
+            const int t0 = 2 * row;
+            if (j0 + t0 < L) {
+                uint32_t unitw[4];   // units (g, g + 1) for g = 0, 2, 4, 6
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int g = 2 * q;
+                    const uint32_t a = lds_u16(rec + 1024 + row * 128 + ((g + 2 * row) & 7) * 16 + 2 * blk);
+                    const uint32_t c = lds_u16(rec + 1024 + row * 128 + ((g + 1 + 2 * row) & 7) * 16 + 2 * blk);
+                    unitw[q] = a | (c << 16);
+                }
+                const uint32_t s2 = e4m3x2_to_f16x2(lds_u16(rec + 2176 + row * 16 + blk * 2));   // (s_t0, s_t1)
+                // e8[r]: E4M3 bytes of channel 16*blk + r, low byte token t0, high byte t0 + 1
+                uint32_t e8[16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t f0, f1, f2, f3;   // channels g, g + 8, g + 1, g + 9 (g = 2q), tokens (t0, t0 + 1)
+                    e2m1x8_to_f16x2x4(unitw[q], f0, f1, f2, f3);
+                    e8[2 * q] = f16x2_to_e4m3x2(hmul2(f0, s2));
+                    e8[2 * q + 8] = f16x2_to_e4m3x2(hmul2(f1, s2));
+                    e8[2 * q + 1] = f16x2_to_e4m3x2(hmul2(f2, s2));
+                    e8[2 * q + 9] = f16x2_to_e4m3x2(hmul2(f3, s2));
+                }
+                uint32_t w0[4], w1[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t lo = e8[4 * q] | (e8[4 * q + 1] << 16);
+                    const uint32_t hi = e8[4 * q + 2] | (e8[4 * q + 3] << 16);
+                    w0[q] = __byte_perm(lo, hi, 0x6420);   // token t0: the low bytes
+                    w1[q] = __byte_perm(lo, hi, 0x7531);   // token t0 + 1: the high bytes
+                }
+                const size_t o0 = ((rows + t0) * p.hkv + cur.h) * kHeadDim + blk * 16;
+                *reinterpret_cast<uint4 *>(p.v_out + o0) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+                if (j0 + t0 + 1 < L) {
+                    const size_t o1 = ((rows + t0 + 1) * p.hkv + cur.h) * kHeadDim + blk * 16;
+                    *reinterpret_cast<uint4 *>(p.v_out + o1) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                }
+            }
+        }
+        __syncthreads();         // buffer k is free for the unit after next
         cur = nxt;
+        L = Ln;
+        staged = staged_n;
+        k ^= 1;
     }
 }
 
@@ -117,10 +197,10 @@ cudaError_t launch_dequant_prefix_fp8(const PrefixParams &p, cudaStream_t s)
     if (units == 0)
         return cudaSuccess;
     const int sms = sm_count();
-    long long grid = static_cast<long long>(sms > 0 ? sms : 1) * 16;
+    long long grid = static_cast<long long>(sms > 0 ? sms : 1) * kPrefixCtasPerSm;
     if (grid > units)
         grid = units;
-    return launch_pdl(dequant_prefix_kernel, dim3(static_cast<unsigned>(grid)), dim3(128), 0, s, p);
+    return launch_pdl(dequant_prefix_kernel, dim3(static_cast<unsigned>(grid)), dim3(kPrefixThreads), 0, s, p);
 }
 
 } // namespace nvfp4kv

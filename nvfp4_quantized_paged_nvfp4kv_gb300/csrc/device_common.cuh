@@ -50,6 +50,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait for phase `parity` of a barrier, giving up after `limit` polls.
+constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a staged-data wait gives up
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit)
 {
     for (uint32_t i = 0; i < limit; ++i)

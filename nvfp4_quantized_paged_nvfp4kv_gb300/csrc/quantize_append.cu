@@ -38,62 +38,62 @@ __device__ __forceinline__ bool site_of(const QuantParams &p, int slot, int h, i
     return true;
 }
 
-// NVFP4.  blockIdx.y == 0: K, one thread per (token, kv head, block).
-// blockIdx.y == 1: V, one thread per (token pair, kv head, block).  V pairs are
-// taken in input order, starting one token early when the first slot is odd,
-// so that consecutive slots (the usual prefill order) form the record's token
-// pairs; such a pair is written whole, any other token through the atomic
-// nibble merge.  Each thread issues its data loads together with its slot
+// NVFP4: one thread per (token pair, kv head, block) of K (blockIdx.y == 0)
+// or V (y == 1), so that each thread has both tokens' loads in flight at once.
+// V pairs are taken in input order, starting one token early when the first
+// slot is odd, so that consecutive slots (the usual prefill order) form the
+// record's token pairs; such a pair is written whole, any other token through
+// the atomic nibble merge.  Data loads are issued together with the slot
 // loads (the source offset does not depend on the slot).
 template <bool kBf16>
 __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const QuantParams p)
 {
     pdl_wait();                  // the records may still be read by the previous kernel
     pdl_launch_dependents();
-    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int blk = static_cast<int>(idx & 7);
-    const long long unit = idx >> 3;                 // (token or pair) * hkv + h
-    const int h = static_cast<int>(unit % p.hkv);
-    const long long tu = unit / p.hkv;
-    if (blockIdx.y == 0) {
-        if (tu >= p.num_tokens)
-            return;
-        const int t = static_cast<int>(tu);
-        float x[16];
-        load16<kBf16>(p.k_new, (static_cast<size_t>(t) * p.hkv + h) * kHeadDim + blk * 16, x);
-        size_t record;
-        int tok;
-        if (!site_of(p, __ldg(p.slot_mapping + t), h, kNvfp4Record, record, tok, blk == 0 && h == 0))
-            return;
-        write_nvfp4_block(p.pool + record, false, tok, blk, x);
-        return;
-    }
+    const unsigned idx = blockIdx.x * blockDim.x + threadIdx.x;
+    const int blk = static_cast<int>(idx & 7u);
+    const unsigned unit = idx >> 3;                  // pair * hkv + h
+    const int h = static_cast<int>(unit % static_cast<unsigned>(p.hkv));
+    const unsigned pr = unit / static_cast<unsigned>(p.hkv);
+    const bool is_v = blockIdx.y == 1;
     const int first = __ldg(p.slot_mapping);
-    const int o = first >= 0 ? (first & 1) : 0;
-    const long long pairs = (static_cast<long long>(p.num_tokens) + o + 1) / 2;
-    if (tu >= pairs)
+    const int o = (is_v && first >= 0) ? (first & 1) : 0;
+    const unsigned pairs = (static_cast<unsigned>(p.num_tokens) + o + 1) / 2;
+    if (pr >= pairs)
         return;
-    const int t0 = static_cast<int>(2 * tu) - o, t1 = t0 + 1;
+    const int t0 = static_cast<int>(2 * pr) - o, t1 = t0 + 1;
     const bool has0 = t0 >= 0, has1 = t1 < p.num_tokens;
-    float x0[16], x1[16];
+    const void *src = is_v ? p.v_new : p.k_new;
+    RawBlock<kBf16> r0, r1;
     if (has0)
-        load16<kBf16>(p.v_new, (static_cast<size_t>(t0) * p.hkv + h) * kHeadDim + blk * 16, x0);
+        load_raw<kBf16>(src, (static_cast<size_t>(t0) * p.hkv + h) * kHeadDim + blk * 16, r0);
     if (has1)
-        load16<kBf16>(p.v_new, (static_cast<size_t>(t1) * p.hkv + h) * kHeadDim + blk * 16, x1);
+        load_raw<kBf16>(src, (static_cast<size_t>(t1) * p.hkv + h) * kHeadDim + blk * 16, r1);
     const int s0 = has0 ? __ldg(p.slot_mapping + t0) : -1;
     const int s1 = has1 ? __ldg(p.slot_mapping + t1) : -1;
-    size_t r0 = 0, r1 = 0;
+    size_t rec0 = 0, rec1 = 0;
     int tok0 = 0, tok1 = 0;
-    const bool ok0 = has0 && site_of(p, s0, h, kNvfp4Record, r0, tok0, blk == 0 && h == 0);
-    const bool ok1 = has1 && site_of(p, s1, h, kNvfp4Record, r1, tok1, blk == 0 && h == 0);
-    if (ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
-        write_nvfp4_v_pair(p.pool + r0, tok0, blk, x0, x1);
+    const bool rep = !is_v && blk == 0 && h == 0;
+    const bool ok0 = has0 && site_of(p, s0, h, kNvfp4Record, rec0, tok0, rep);
+    const bool ok1 = has1 && site_of(p, s1, h, kNvfp4Record, rec1, tok1, rep);
+    float x[16];
+    if (is_v && ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
+        uint32_t S0, S1, c0[2], c1[2];
+        unpack<kBf16>(r0, x);
+        quantize_block(x, S0, c0);
+        unpack<kBf16>(r1, x);
+        quantize_block(x, S1, c1);
+        write_nvfp4_v_pair(p.pool + rec0, tok0, blk, S0, c0, S1, c1);
         return;
     }
-    if (ok0)
-        write_nvfp4_block(p.pool + r0, true, tok0, blk, x0);
-    if (ok1)
-        write_nvfp4_block(p.pool + r1, true, tok1, blk, x1);
+    if (ok0) {
+        unpack<kBf16>(r0, x);
+        write_nvfp4_block(p.pool + rec0, is_v, tok0, blk, x);
+    }
+    if (ok1) {
+        unpack<kBf16>(r1, x);
+        write_nvfp4_block(p.pool + rec1, is_v, tok1, blk, x);
+    }
 }
 
 // FP8: one thread per (token, kv head, block) of K (y == 0) or V (y == 1).
@@ -121,11 +121,14 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(const QuantParams p)
 }
 
 template <class K>
-static cudaError_t launch_blocks(K kernel, const QuantParams &p, cudaStream_t s)
+static cudaError_t launch_blocks(K kernel, const QuantParams &p, cudaStream_t s, bool pairs)
 {
-    const long long blocks = static_cast<long long>(p.num_tokens) * p.hkv * 8;
+    const long long units = pairs ? (static_cast<long long>(p.num_tokens) + 2) / 2 : p.num_tokens;
+    const long long blocks = units * p.hkv * 8;
     if (blocks == 0)
         return cudaSuccess;
+    if (blocks >= (1LL << 32))
+        return cudaErrorInvalidValue;        // thread indices are 32-bit
     const long long grid = (blocks + 255) / 256;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidValue;
@@ -134,14 +137,14 @@ static cudaError_t launch_blocks(K kernel, const QuantParams &p, cudaStream_t s)
 
 cudaError_t launch_quantize_append_nvfp4(const QuantParams &p, cudaStream_t s)
 {
-    return p.in_bf16 ? launch_blocks(quantize_nvfp4_kernel<true>, p, s)
-                     : launch_blocks(quantize_nvfp4_kernel<false>, p, s);
+    return p.in_bf16 ? launch_blocks(quantize_nvfp4_kernel<true>, p, s, true)
+                     : launch_blocks(quantize_nvfp4_kernel<false>, p, s, true);
 }
 
 cudaError_t launch_quantize_append_fp8(const QuantParams &p, cudaStream_t s)
 {
-    return p.in_bf16 ? launch_blocks(quantize_fp8_kernel<true>, p, s)
-                     : launch_blocks(quantize_fp8_kernel<false>, p, s);
+    return p.in_bf16 ? launch_blocks(quantize_fp8_kernel<true>, p, s, false)
+                     : launch_blocks(quantize_fp8_kernel<false>, p, s, false);
 }
 
 } // namespace nvfp4kv

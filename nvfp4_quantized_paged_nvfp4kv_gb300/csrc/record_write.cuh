@@ -7,29 +7,49 @@
 
 namespace nvfp4kv {
 
+// One 16-value block of an input row, as loaded (fp32 or bf16 bits).
 template <bool kBf16>
-__device__ __forceinline__ void load16(const void *src, size_t elem_off, float (&x)[16])
+struct RawBlock {
+    uint4 v[kBf16 ? 2 : 4];
+};
+
+template <bool kBf16>
+__device__ __forceinline__ void load_raw(const void *src, size_t elem_off, RawBlock<kBf16> &r)
+{
+    const uint4 *p = kBf16 ? reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(src) + elem_off)
+                           : reinterpret_cast<const uint4 *>(static_cast<const float *>(src) + elem_off);
+#pragma unroll
+    for (int i = 0; i < (kBf16 ? 2 : 4); ++i)
+        r.v[i] = __ldg(p + i);
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void unpack(const RawBlock<kBf16> &r, float (&x)[16])
 {
     if constexpr (kBf16) {
-        const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(src) + elem_off);
-        const uint4 a = __ldg(p), b = __ldg(p + 1);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const uint32_t w[8] = {r.v[0].x, r.v[0].y, r.v[0].z, r.v[0].w, r.v[1].x, r.v[1].y, r.v[1].z, r.v[1].w};
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             x[2 * k] = __uint_as_float(w[k] << 16);
             x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
         }
     } else {
-        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + elem_off);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const float4 v = __ldg(p + k);
-            x[4 * k] = v.x;
-            x[4 * k + 1] = v.y;
-            x[4 * k + 2] = v.z;
-            x[4 * k + 3] = v.w;
+            x[4 * k] = __uint_as_float(r.v[k].x);
+            x[4 * k + 1] = __uint_as_float(r.v[k].y);
+            x[4 * k + 2] = __uint_as_float(r.v[k].z);
+            x[4 * k + 3] = __uint_as_float(r.v[k].w);
         }
     }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void load16(const void *src, size_t elem_off, float (&x)[16])
+{
+    RawBlock<kBf16> r;
+    load_raw<kBf16>(src, elem_off, r);
+    unpack<kBf16>(r, x);
 }
 
 // amax -> E4M3 block scale -> 16 E2M1 codes (code i in bits 4i .. 4i+3).
@@ -97,14 +117,11 @@ __device__ __forceinline__ void write_nvfp4_block(uint8_t *rec, bool is_v, int t
     rec[2176 + row * 16 + blk * 2 + half] = static_cast<uint8_t>(S);
 }
 
-// NVFP4, V block blk of both tokens of a token pair (tok0 even, tok0 + 1) at
-// once: every byte of theirs is written whole, no atomics.
-__device__ __forceinline__ void write_nvfp4_v_pair(uint8_t *rec, int tok0, int blk, const float (&x0)[16],
-                                                   const float (&x1)[16])
+// NVFP4, V block blk of both tokens of a token pair (tok0 even, tok0 + 1), from
+// their scale bytes and codes: every byte of theirs is written whole, no atomics.
+__device__ __forceinline__ void write_nvfp4_v_pair(uint8_t *rec, int tok0, int blk, uint32_t S0,
+                                                   const uint32_t (&p0)[2], uint32_t S1, const uint32_t (&p1)[2])
 {
-    uint32_t S0, S1, p0[2], p1[2];
-    quantize_block(x0, S0, p0);
-    quantize_block(x1, S1, p1);
     const int row = tok0 >> 1;
     const uint64_t c0 = (static_cast<uint64_t>(p0[1]) << 32) | p0[0];
     const uint64_t c1 = (static_cast<uint64_t>(p1[1]) << 32) | p1[0];
