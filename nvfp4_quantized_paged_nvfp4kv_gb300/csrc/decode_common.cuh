@@ -381,8 +381,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         return;
 
     // ---- producer: page-head lookahead window, lane l holds index win + l ----
+    // Lane l looks up page-head win + l of the current window and of the next
+    // one; a window's entries are checked and turned into record indices
+    // (page * hkv + head) when it becomes current, long after its block-table
+    // reads were issued.
     int win = lo;
-    int cur_phys = 0, cur_h = 0, nxt_phys = 0, nxt_h = 0;
+    int nxt_phys = 0, nxt_h = 0;
+    uint32_t cur_rec = 0;
     auto lookup = [&](int j, int &phys, int &hh) {
         phys = 0;
         hh = 0;
@@ -395,8 +400,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
             phys = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + pg);
         }
     };
-    lookup(win + lane, cur_phys, cur_h);
-    lookup(win + 32 + lane, nxt_phys, nxt_h);
+    auto record_of = [&](int phys, int hh, int j) {
+        if (j < hi && static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_pages)) {
+            report(p.dev_status, NVFP4KV_DEV_BAD_PAGE);
+            phys = 0;
+        }
+        return static_cast<uint32_t>(phys) * static_cast<uint32_t>(p.hkv) + static_cast<uint32_t>(hh);
+    };
+    {
+        int phys, hh;
+        lookup(win + lane, phys, hh);
+        lookup(win + 32 + lane, nxt_phys, nxt_h);
+        cur_rec = record_of(phys, hh, win + lane);
+    }
 
     // Stage `st` receives page-head j (called by the whole warp, in order of j).
     auto issue = [&](int j, int st) {
@@ -404,21 +420,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         if (rel >= 32) {
             win += 32;
             rel -= 32;
-            cur_phys = nxt_phys;
-            cur_h = nxt_h;
+            cur_rec = record_of(nxt_phys, nxt_h, win + lane);
             lookup(win + 32 + lane, nxt_phys, nxt_h);
         }
-        int phys = __shfl_sync(kFullMask, cur_phys, rel);
-        const int hh = __shfl_sync(kFullMask, cur_h, rel);
+        const uint32_t z = __shfl_sync(kFullMask, cur_rec, rel);
         if (lane == 0) {
-            if (static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_pages)) {
-                report(p.dev_status, NVFP4KV_DEV_BAD_PAGE);
-                phys = 0;
-            }
             const uint32_t bar = wbar + 8 * st;
-            const size_t z = static_cast<size_t>(phys) * p.hkv + hh;
             mbar_arrive_expect_tx(bar, R);
-            bulk_g2s(wdata + st * R, p.pool + z * R, R, bar);
+            bulk_g2s(wdata + st * R, p.pool + static_cast<size_t>(z) * R, R, bar);
         }
     };
 
