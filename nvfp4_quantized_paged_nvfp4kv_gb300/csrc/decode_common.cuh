@@ -673,9 +673,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         // Lanes poll independently and may leave the loop at different polls;
         // the vote reconverges the warp before the warp-wide MMAs below and
         // makes the give-up decision uniform.
-        bool arrived = mbar_wait_bounded(wbar + 8 * st, ph, kWaitLimit);
-        if (np == 2)
-            arrived = arrived && mbar_wait_bounded(wbar + 8 * st1, ph1, kWaitLimit);
+        const bool arrived = np == 2 ? mbar_wait2_bounded(wbar + 8 * st, ph, wbar + 8 * st1, ph1, kWaitLimit)
+                                     : mbar_wait_bounded(wbar + 8 * st, ph, kWaitLimit);
         if (!__all_sync(kFullMask, arrived)) {
             // staged data never arrived: report, let the copies in flight land, stop
             if (lane == 0)

@@ -63,6 +63,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 // ---- asynchronous copies global -> shared ---------------------------------
 
 // Untiled bulk copy; both addresses 16-byte aligned, bytes a multiple of 16.
+// Waits (bounded) until the phases with parity pa of barrier a and pb of
+// barrier b have completed, polling both in one loop.
+__device__ __forceinline__ bool mbar_wait2_bounded(uint32_t a, uint32_t pa, uint32_t b, uint32_t pb, uint32_t limit)
+{
+    bool da = false, db = false;
+    for (uint32_t i = 0; i < limit; ++i) {
+        da = da || mbar_try_wait(a, pa);
+        db = db || mbar_try_wait(b, pb);
+        if (da && db)
+            return true;
+    }
+    return false;
+}
+
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
     asm volatile(
