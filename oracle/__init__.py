@@ -61,16 +61,16 @@ def _load():
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.oracle_e2m1_encode_array.argtypes = [_f32p, _u8p, ctypes.c_int64]
         lib.oracle_e4m3_encode_array.argtypes = [_f32p, _u8p, ctypes.c_int64]
-        lib.oracle_quantize_block16.argtypes = [_f32p, _u8p, _u8p]
+        lib.oracle_quantize_block16.argtypes = [_f32p, _u8p, _u8p, ctypes.c_float]
         lib.oracle_quantize_append.argtypes = [
-            _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _u8p, _u8p]
-        lib.oracle_dequant_rows.argtypes = [_u8p, _u8p, ctypes.c_int64, ctypes.c_int, _f32p]
+            _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _u8p, _u8p, ctypes.c_float]
+        lib.oracle_dequant_rows.argtypes = [_u8p, _u8p, ctypes.c_int64, ctypes.c_int, _f32p, ctypes.c_float]
         lib.oracle_paged_decode.argtypes = [
             _u8p, _u8p, _u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p,
-            ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_double, _f64p]
+            ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_double, _f64p, ctypes.c_float]
         lib.oracle_dequant_prefix_fp8.argtypes = [
             _u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int,
-            _i32p, _i32p, ctypes.c_int, _u8p]
+            _i32p, _i32p, ctypes.c_int, _u8p, ctypes.c_float]
         lib.oracle_fp8_quantize_append.argtypes = [
             _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _u8p]
         lib.oracle_fp8_paged_decode.argtypes = [
@@ -127,38 +127,39 @@ def e4m3_table() -> np.ndarray:
 
 # --- NVFP4 blocks and cache ----------------------------------------------
 
-def quantize_block16(x) -> tuple[np.ndarray, int]:
+def quantize_block16(x, global_scale: float = 1.0) -> tuple[np.ndarray, int]:
     x = _c(x, np.float32).reshape(16)
     packed = np.empty(8, np.uint8)
     scale = np.empty(1, np.uint8)
-    _load().oracle_quantize_block16(_p(x, _f32p), _p(packed, _u8p), _p(scale, _u8p))
+    _load().oracle_quantize_block16(_p(x, _f32p), _p(packed, _u8p), _p(scale, _u8p), float(global_scale))
     return packed, int(scale[0])
 
 
-def quantize_append(x, slot_mapping, data, scale, page_size: int = 16) -> None:
-    """Quantise rows x[T][Hkv][d] into the NVFP4 pools (in place)."""
+def quantize_append(x, slot_mapping, data, scale, page_size: int = 16, global_scale: float = 1.0) -> None:
+    """Quantise rows x[T][Hkv][d] into the NVFP4 pools (in place); values are
+    stored as global_scale * E4M3 scale * E2M1."""
     x = _c(x, np.float32)
     T, Hkv, d = x.shape
     sm = _c(slot_mapping, np.int32)
     assert data.flags.c_contiguous and scale.flags.c_contiguous
     assert data.dtype == np.uint8 and scale.dtype == np.uint8
     _load().oracle_quantize_append(_p(x, _f32p), T, Hkv, d, _p(sm, _i32p), page_size,
-                                   _p(data, _u8p), _p(scale, _u8p))
+                                   _p(data, _u8p), _p(scale, _u8p), float(global_scale))
 
 
-def dequant_rows(data, scale) -> np.ndarray:
+def dequant_rows(data, scale, global_scale: float = 1.0) -> np.ndarray:
     """Dequantise NVFP4 rows (data[..., d/2], scale[..., d/16]) to fp32."""
     data = _c(data, np.uint8)
     scale = _c(scale, np.uint8)
     d = data.shape[-1] * 2
     rows = data.size // (d // 2)
     out = np.empty(data.shape[:-1] + (d,), np.float32)
-    _load().oracle_dequant_rows(_p(data, _u8p), _p(scale, _u8p), rows, d, _p(out, _f32p))
+    _load().oracle_dequant_rows(_p(data, _u8p), _p(scale, _u8p), rows, d, _p(out, _f32p), float(global_scale))
     return out
 
 
 def paged_decode(k_data, k_scale, v_data, v_scale, q, block_table, seq_lens,
-                 sm_scale: float | None = None) -> np.ndarray:
+                 sm_scale: float | None = None, global_scale: float = 1.0) -> np.ndarray:
     """fp64 GQA decode over the NVFP4 pools.  q: float32 [B][Hq][d]."""
     k_data = _c(k_data, np.uint8)
     k_scale = _c(k_scale, np.uint8)
@@ -176,12 +177,12 @@ def paged_decode(k_data, k_scale, v_data, v_scale, q, block_table, seq_lens,
     _load().oracle_paged_decode(_p(k_data, _u8p), _p(k_scale, _u8p), _p(v_data, _u8p),
                                 _p(v_scale, _u8p), Hkv, P, d, _p(q, _f32p), B, Hq,
                                 _p(bt, _i32p), bt.shape[1], _p(sl, _i32p),
-                                float(sm_scale), _p(out, _f64p))
+                                float(sm_scale), _p(out, _f64p), float(global_scale))
     return out
 
 
 def dequant_prefix_fp8(data, scale, block_table, prefix_lens, kv_indptr,
-                       out_rows: int | None = None) -> np.ndarray:
+                       out_rows: int | None = None, global_scale: float = 1.0) -> np.ndarray:
     data = _c(data, np.uint8)
     scale = _c(scale, np.uint8)
     _, Hkv, P, half = data.shape
@@ -194,7 +195,7 @@ def dequant_prefix_fp8(data, scale, block_table, prefix_lens, kv_indptr,
     out = np.zeros((out_rows, Hkv, d), np.uint8)
     _load().oracle_dequant_prefix_fp8(_p(data, _u8p), _p(scale, _u8p), Hkv, P, d,
                                       _p(bt, _i32p), bt.shape[1], _p(pl, _i32p),
-                                      _p(ip, _i32p), len(pl), _p(out, _u8p))
+                                      _p(ip, _i32p), len(pl), _p(out, _u8p), float(global_scale))
     return out
 
 

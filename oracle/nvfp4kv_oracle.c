@@ -150,28 +150,32 @@ void oracle_e4m3_encode_array(const float *y, uint8_t *out, int64_t n)
 /* ------------------------------------------------------------------------ */
 /* NVFP4 block of 16 values ([RTX-PRO-6000] "Bytes pro Token": one E4M3 scale
  * per 16 E2M1 values, FP32 tensor scale above; [LMSYS-summary] Perspective:
- * the tensor scale is left at 1.0).
- *   amax  = max |x_i|
+ * the tensor scale is left at 1.0, calibrating it is the next step).
+ * With tensor scale G (reading: a value is G * s * E2M1, so the block
+ * procedure runs on y_i = fl32(x_i / G), which is x_i itself at G = 1):
+ *   amax  = max |y_i|
  *   S     = E4M3_RNE_sat(fl32(amax / 6))         (6 = largest E2M1 magnitude)
- *   s     = value(S) * global_scale             (global_scale = 1.0)
- *   q_i   = E2M1_RNE_sat(fl32(x_i / s)), or 0 for every i when s == 0
+ *   s     = value(S)
+ *   q_i   = E2M1_RNE_sat(fl32(y_i / s)), or 0 for every i when s == 0
  * Packing (reading): byte j holds element 2j in its low nibble and element
  * 2j+1 in its high nibble.                                                   */
-void oracle_quantize_block16(const float *x, uint8_t *packed8, uint8_t *scale_code)
+void oracle_quantize_block16(const float *x, uint8_t *packed8, uint8_t *scale_code, float global_scale)
 {
-    const float global_scale = 1.0f;
+    float y[16];
+    for (int i = 0; i < 16; ++i)
+        y[i] = (global_scale == 1.0f) ? x[i] : x[i] / global_scale;
     float amax = 0.0f;
     for (int i = 0; i < 16; ++i) {
-        float a = fabsf(x[i]);
+        float a = fabsf(y[i]);
         if (a > amax)
             amax = a;
     }
     float s32 = amax / 6.0f;
     uint8_t S = oracle_e4m3_encode(s32);
-    float s = (float)oracle_e4m3_value(S) * global_scale;
+    float s = (float)oracle_e4m3_value(S);
     uint8_t q[16];
     for (int i = 0; i < 16; ++i)
-        q[i] = (s == 0.0f) ? 0 : oracle_e2m1_encode(x[i] / s);
+        q[i] = (s == 0.0f) ? 0 : oracle_e2m1_encode(y[i] / s);
     for (int j = 0; j < 8; ++j)
         packed8[j] = (uint8_t)(q[2 * j] | (q[2 * j + 1] << 4));
     *scale_code = S;
@@ -192,7 +196,7 @@ static size_t row_index(int64_t page, int h, int off, int Hkv, int P)
  * prefill quantises the same data it attends on into the NVFP4 cache.        */
 void oracle_quantize_append(const float *x, int T, int Hkv, int d,
                             const int32_t *slot_mapping, int P,
-                            uint8_t *data, uint8_t *scale)
+                            uint8_t *data, uint8_t *scale, float global_scale)
 {
     int nb = d / 16;
 #pragma omp parallel for schedule(static)
@@ -208,29 +212,30 @@ void oracle_quantize_append(const float *x, int T, int Hkv, int d,
             for (int blk = 0; blk < nb; ++blk)
                 oracle_quantize_block16(src + 16 * blk,
                                         data + r * (size_t)(d / 2) + 8 * blk,
-                                        scale + r * (size_t)nb + blk);
+                                        scale + r * (size_t)nb + blk, global_scale);
         }
     }
 }
 
-/* Dequantised value of channel c of one cached NVFP4 row: E2M1 x E4M3 x 1.0.
- * The product is exact in double (and in fp32).                             */
-static double nvfp4_row_value(const uint8_t *data_row, const uint8_t *scale_row, int c)
+/* Dequantised value of channel c of one cached NVFP4 row: E2M1 x E4M3 x G.
+ * The product is exact in double (at most 6 + 24 significant bits).          */
+static double nvfp4_row_value(const uint8_t *data_row, const uint8_t *scale_row, int c, float global_scale)
 {
     uint8_t byte = data_row[c / 2];
     uint8_t code = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
-    return oracle_e2m1_value(code) * oracle_e4m3_value(scale_row[c / 16]) * 1.0;
+    return oracle_e2m1_value(code) * oracle_e4m3_value(scale_row[c / 16]) * (double)global_scale;
 }
 
-/* Dequantise a whole row into fp32 (test helper; products are exact). */
+/* Dequantise a whole row into fp32 (test helper; at G = 1 the products are
+ * exact in fp32, otherwise rounded once). */
 void oracle_dequant_rows(const uint8_t *data, const uint8_t *scale, int64_t rows,
-                         int d, float *out)
+                         int d, float *out, float global_scale)
 {
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r)
         for (int c = 0; c < d; ++c)
             out[r * d + c] = (float)nvfp4_row_value(data + r * (d / 2),
-                                                    scale + r * (d / 16), c);
+                                                    scale + r * (d / 16), c, global_scale);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -246,10 +251,10 @@ void oracle_dequant_rows(const uint8_t *data, const uint8_t *scale, int64_t rows
  * sequence (L_b = 0) yields zeros.  kind 0 = NVFP4 pools, kind 1 = FP8 pool
  * (data [pages][Hkv][P][d] E4M3, scale unused).                              */
 static double cache_value(int kind, const uint8_t *data, const uint8_t *scale,
-                          size_t r, int d, int c)
+                          size_t r, int d, int c, float global_scale)
 {
     if (kind == 0)
-        return nvfp4_row_value(data + r * (size_t)(d / 2), scale + r * (size_t)(d / 16), c);
+        return nvfp4_row_value(data + r * (size_t)(d / 2), scale + r * (size_t)(d / 16), c, global_scale);
     return oracle_e4m3_value(data[r * (size_t)d + c]);
 }
 
@@ -260,7 +265,7 @@ static void paged_decode_generic(int kind,
                                  const float *q, int B, int Hq,
                                  const int32_t *block_table, int max_pages,
                                  const int32_t *seq_lens, double sm_scale,
-                                 double *out)
+                                 double *out, float global_scale)
 {
     int g = Hq / Hkv;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -281,7 +286,7 @@ static void paged_decode_generic(int kind,
             size_t r = row_index(page, h, j % P, Hkv, P);
             double dot = 0.0;
             for (int c = 0; c < d; ++c)
-                dot += (double)qv[c] * cache_value(kind, k_data, k_scale, r, d, c);
+                dot += (double)qv[c] * cache_value(kind, k_data, k_scale, r, d, c, global_scale);
             double sj = dot * sm_scale;
             if (sj > smax)
                 smax = sj;
@@ -294,11 +299,11 @@ static void paged_decode_generic(int kind,
             size_t r = row_index(page, h, j % P, Hkv, P);
             double dot = 0.0;
             for (int c = 0; c < d; ++c)
-                dot += (double)qv[c] * cache_value(kind, k_data, k_scale, r, d, c);
+                dot += (double)qv[c] * cache_value(kind, k_data, k_scale, r, d, c, global_scale);
             double p = exp(dot * sm_scale - m);
             denom += p;
             for (int c = 0; c < d; ++c)
-                o[c] += p * cache_value(kind, v_data, v_scale, r, d, c);
+                o[c] += p * cache_value(kind, v_data, v_scale, r, d, c, global_scale);
         }
         for (int c = 0; c < d; ++c)
             o[c] /= denom;
@@ -309,22 +314,23 @@ void oracle_paged_decode(const uint8_t *k_data, const uint8_t *k_scale,
                          const uint8_t *v_data, const uint8_t *v_scale,
                          int Hkv, int P, int d, const float *q, int B, int Hq,
                          const int32_t *block_table, int max_pages,
-                         const int32_t *seq_lens, double sm_scale, double *out)
+                         const int32_t *seq_lens, double sm_scale, double *out, float global_scale)
 {
     paged_decode_generic(0, k_data, k_scale, v_data, v_scale, Hkv, P, d, q, B, Hq,
-                         block_table, max_pages, seq_lens, sm_scale, out);
+                         block_table, max_pages, seq_lens, sm_scale, out, global_scale);
 }
 
 /* ------------------------------------------------------------------------ */
 /* Extend path: dequantise the cached prefix of each sequence into one
  * contiguous FP8 workspace ([LMSYS-summary] Interpretation ¶2).  Reading:
- * each value is E4M3_RNE_sat(E2M1 x scale) at workspace scale 1.0; rows of
- * sequence b go to workspace rows kv_indptr[b] + j, laid out [row][Hkv][d].  */
+ * each value is E4M3_RNE_sat(fl32(E2M1 x scale x G)) at workspace scale 1.0
+ * (the fp32 rounding only acts when G != 1); rows of sequence b go to
+ * workspace rows kv_indptr[b] + j, laid out [row][Hkv][d].                   */
 void oracle_dequant_prefix_fp8(const uint8_t *data, const uint8_t *scale,
                                int Hkv, int P, int d,
                                const int32_t *block_table, int max_pages,
                                const int32_t *prefix_lens, const int32_t *kv_indptr,
-                               int B, uint8_t *out)
+                               int B, uint8_t *out, float global_scale)
 {
     for (int b = 0; b < B; ++b) {
         int L = prefix_lens[b];
@@ -336,7 +342,7 @@ void oracle_dequant_prefix_fp8(const uint8_t *data, const uint8_t *scale,
                 uint8_t *dst = out + (((size_t)kv_indptr[b] + j) * Hkv + h) * d;
                 for (int c = 0; c < d; ++c) {
                     float v = (float)nvfp4_row_value(data + r * (size_t)(d / 2),
-                                                     scale + r * (size_t)(d / 16), c);
+                                                     scale + r * (size_t)(d / 16), c, global_scale);
                     dst[c] = oracle_e4m3_encode(v);
                 }
             }
@@ -373,7 +379,7 @@ void oracle_fp8_paged_decode(const uint8_t *k, const uint8_t *v, int Hkv, int P,
                              const int32_t *seq_lens, double sm_scale, double *out)
 {
     paged_decode_generic(1, k, NULL, v, NULL, Hkv, P, d, q, B, Hq, block_table,
-                         max_pages, seq_lens, sm_scale, out);
+                         max_pages, seq_lens, sm_scale, out, 1.0f);
 }
 
 /* ------------------------------------------------------------------------ */
