@@ -441,11 +441,25 @@ def other_rows(dev):
     q_bytes = T * w.num_kv_heads * (2 * 128 * 2 + NVFP4_BYTES_PER_TOKEN_HEAD) + T * 4
     p_ms = timed(lambda: nv.nvfp4kv_dequant_prefix_fp8(cache, bt_d, pl, ip, kf, vf))
     p_bytes = L * w.num_kv_heads * (NVFP4_BYTES_PER_TOKEN_HEAD + 2 * 128)
+    # the same cache read as one with a calibrated tensor scale G = 0.37: the
+    # decode of the 160K sequence and the quantise path cost what G = 1 costs
+    cache_g = nv.NVFP4Cache(cache.pool, global_scale=0.37)
+    q = workloads.query(w, device=dev)
+    sl = torch.tensor([L], dtype=torch.int32, device=dev)
+    out = torch.empty((1, w.num_q_heads, 128), dtype=torch.bfloat16, device=dev)
+    ws = nv.new_workspace(device=dev)
+    d1_ms = timed(lambda: nv.nvfp4kv_paged_decode(cache, q, bt_d, sl, out, ws))
+    dg_ms = timed(lambda: nv.nvfp4kv_paged_decode(cache_g, q, bt_d, sl, out, ws))
+    qg_ms = timed(lambda: nv.nvfp4kv_quantize_append(cache_g, k, v, sm))
+    d_bytes = L * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
     return {
         "quantize_append_8k_bf16": {"us": q_ms * 1e3, "tokens_per_s": T / (q_ms / 1e3),
                                     "alg_gbs": q_bytes / (q_ms / 1e3) / 1e9, "alg_bytes": q_bytes},
         "dequant_prefix_fp8_160k": {"us": p_ms * 1e3, "tokens_per_s": L / (p_ms / 1e3),
                                     "alg_gbs": p_bytes / (p_ms / 1e3) / 1e9, "alg_bytes": p_bytes},
+        "tensor_scale_0.37": {"decode_160k_b1_us": dg_ms * 1e3, "decode_160k_b1_unit_scale_us": d1_ms * 1e3,
+                              "decode_alg_gbs": d_bytes / (dg_ms / 1e3) / 1e9,
+                              "quantize_append_8k_bf16_us": qg_ms * 1e3},
         "timing": "CUDA events per call, 256 MB buffer written before each call to evict L2",
     }
 

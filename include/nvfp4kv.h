@@ -29,9 +29,13 @@
  *   E2M1 code: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa;
  *     magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
  *   E4M3 (OCP "FN"): bias 7, subnormals m/8 * 2^-6, max 448, 0x7F = NaN.
- *   Block of 16 consecutive channels of one token-head:
- *     S = E4M3_rn_satfinite(fl32(amax / 6)), s = value(S) (x global 1.0),
- *     q_i = E2M1_rn_satfinite(fl32(x_i / s)), or 0 for all i if s == 0.
+ *   Tensor scale G (nvfp4kv_cache.global_scale, FP32; the pages run with
+ *     G = 1.0 and name its calibration as the next step): a cached value is
+ *     G * E4M3 block scale * E2M1 code.
+ *   Block of 16 consecutive channels of one token-head, y_i = fl32(x_i / G)
+ *     (y = x at G = 1):
+ *     S = E4M3_rn_satfinite(fl32(amax_i |y_i| / 6)), s = value(S),
+ *     q_i = E2M1_rn_satfinite(fl32(y_i / s)), or 0 for all i if s == 0.
  *     Packed byte j = q_{2j} | q_{2j+1} << 4 (low nibble = even channel).
  *
  * Cache layout.  The cache is one pool of page-head records: the record of
@@ -66,7 +70,8 @@
  *
  * Supported geometry: head_dim 128, page_size 16, num_q_heads a multiple of
  * num_kv_heads with group g = num_q_heads / num_kv_heads in 1..8,
- * global_scale 1.0.  Anything else returns NVFP4KV_ERR_UNSUPPORTED.
+ * global_scale a positive normal finite fp32.  Anything else returns
+ * NVFP4KV_ERR_UNSUPPORTED.
  *
  * Device-side checks: kernels that read page ids, slots or lengths from
  * device memory check them and, instead of faulting, OR a bit into the
@@ -106,7 +111,7 @@ typedef enum { NVFP4KV_F32 = 0, NVFP4KV_BF16 = 1 } nvfp4kv_dtype;
 #define FP8KV_RECORD_BYTES 4096
 
 /* NVFP4 cache: pool of num_pages * num_kv_heads records laid out as above,
- * 16-byte aligned.  global_scale must be 1.0f. */
+ * 16-byte aligned; global_scale is the tensor scale G described above. */
 typedef struct {
     void *pool;
     int32_t num_pages;
@@ -160,8 +165,10 @@ size_t nvfp4kv_decode_workspace_size(int32_t num_workers);
  *   seq_lens[b] tokens j of sequence b, token j in page block_table[b][j/16]
  *   at offset j%16; no causal mask (the query sees all cached tokens).
  * q: bf16 [batch][num_q_heads][128], 16-byte aligned.  Computation: q is
- *   multiplied by sm_scale*log2(e) and rounded to fp16 (|q * sm_scale| must
- *   stay below 4.5e4); K and V are dequantised exactly to fp16; QK^T and PV run
+ *   multiplied by sm_scale*log2(e)*G (G the tensor scale) and rounded to fp16
+ *   (|q * sm_scale * G| must stay below 4.5e4); K and V are dequantised
+ *   exactly to fp16 (block scale times code) and the output is multiplied by
+ *   G; QK^T and PV run
  *   on tensor cores with fp32 accumulation; softmax in fp32.
  * block_table: int32 [batch][max_pages_per_seq]; only the first
  *   ceil(seq_lens[b]/16) entries of row b are read; an entry outside
@@ -234,7 +241,7 @@ nvfp4kv_status nvfp4kv_paged_decode_static_scratch(const nvfp4kv_cache *cache, c
 /* Extend path ("SGLang stores KV cache in 4 bits", Interpretation ¶2: the
  * cached prefix is dequantised into one FP8 workspace shared across layers).
  * For sequence b, token j < prefix_lens[b], kv head h, channel c:
- *   out[kv_indptr[b] + j][h][c] = E4M3_rn_satfinite(E2M1 x scale x 1.0)
+ *   out[kv_indptr[b] + j][h][c] = E4M3_rn_satfinite(fl32(E2M1 x scale x G))
  * for K into k_fp8_out and V into v_fp8_out (each [rows][num_kv_heads][128]
  * uint8, 16-byte aligned; the caller sizes it to cover every row written).
  * kv_indptr: int32[batch] row offsets; prefix_lens: int32[batch].

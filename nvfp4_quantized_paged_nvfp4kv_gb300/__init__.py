@@ -146,22 +146,25 @@ def _dtype_code(t) -> int:
 
 class NVFP4Cache:
     """An NVFP4 pool: uint8 [num_pages][num_kv_heads][NVFP4_RECORD_BYTES] page-head
-    records (layout in include/nvfp4kv.h)."""
+    records (layout in include/nvfp4kv.h).  global_scale is the FP32 tensor
+    scale G: a cached value is G * E4M3 block scale * E2M1 code."""
 
     record_bytes = NVFP4_RECORD_BYTES
 
-    def __init__(self, pool):
+    def __init__(self, pool, global_scale: float = 1.0):
         self.pool = pool
         self.num_pages, self.num_kv_heads, rb = pool.shape
         assert rb == self.record_bytes
         self.page_size, self.head_dim = PAGE_SIZE, HEAD_DIM
-        self._c = _Nvfp4Cache(pool.data_ptr(), self.num_pages, self.num_kv_heads, PAGE_SIZE, HEAD_DIM, 1.0)
+        self.global_scale = float(global_scale)
+        self._c = _Nvfp4Cache(pool.data_ptr(), self.num_pages, self.num_kv_heads, PAGE_SIZE, HEAD_DIM,
+                              self.global_scale)
 
     @classmethod
-    def allocate(cls, num_pages, num_kv_heads, device="cuda", zero=True):
+    def allocate(cls, num_pages, num_kv_heads, device="cuda", zero=True, **kw):
         import torch
         f = torch.zeros if zero else torch.empty
-        return cls(f((num_pages, num_kv_heads, cls.record_bytes), dtype=torch.uint8, device=device))
+        return cls(f((num_pages, num_kv_heads, cls.record_bytes), dtype=torch.uint8, device=device), **kw)
 
     @property
     def c(self):

@@ -46,7 +46,8 @@ nvfp4kv_status check_nvfp4(const nvfp4kv_cache *c)
     nvfp4kv_status st = check_geometry(c->num_pages, c->num_kv_heads, c->page_size, c->head_dim);
     if (st != NVFP4KV_OK)
         return st;
-    if (!(c->global_scale == 1.0f))
+    // a positive, normal, finite tensor scale
+    if (!(c->global_scale >= 1.17549435e-38f && c->global_scale <= 3.40282347e+38f))
         return NVFP4KV_ERR_UNSUPPORTED;
     if (c->pool == nullptr || !aligned16(c->pool))
         return NVFP4KV_ERR_INVALID_ARG;
@@ -146,7 +147,18 @@ nvfp4kv_status check_decode(int32_t hkv, int32_t num_pages, const void *q, int32
     p.out_bf16 = out_dtype == NVFP4KV_BF16;
     p.num_workers = nw;
     p.qscale = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+    p.out_scale = 1.f;
+    p.gscale = 1.f;
     return NVFP4KV_OK;
+}
+
+// The NVFP4 tensor scale G: scores see G * k, so G joins the query scale;
+// outputs see G * v, so the normaliser carries it.
+void apply_tensor_scale(DecodeParams &p, float sm_scale, float G)
+{
+    p.qscale = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634 * static_cast<double>(G));
+    p.out_scale = G;
+    p.gscale = G;
 }
 
 } // namespace
@@ -173,6 +185,7 @@ nvfp4kv_status nvfp4kv_quantize_append(const nvfp4kv_cache *cache, const void *k
     p.hkv = cache->num_kv_heads;
     p.num_pages = cache->num_pages;
     p.in_bf16 = in_dtype == NVFP4KV_BF16;
+    p.gscale = cache->global_scale;
     return from_cuda(launch_quantize_append_nvfp4(p, to_cuda(stream)));
 }
 
@@ -197,6 +210,7 @@ nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q, i
     if (st != NVFP4KV_OK || batch == 0)
         return st;
     p.pool = static_cast<const uint8_t *>(cache->pool);
+    apply_tensor_scale(p, sm_scale, cache->global_scale);
     cudaError_t e = launch_decode_nvfp4(p, to_cuda(stream));
     if (e == cudaSuccess)
         e = launch_merge(p, to_cuda(stream));
@@ -235,6 +249,7 @@ nvfp4kv_status nvfp4kv_dequant_prefix_fp8(const nvfp4kv_cache *cache, const int3
     p.hkv = cache->num_kv_heads;
     p.max_pages = max_pages_per_seq;
     p.num_pages = cache->num_pages;
+    p.gscale = cache->global_scale;
     return from_cuda(launch_dequant_prefix_fp8(p, to_cuda(stream)));
 }
 
@@ -304,6 +319,7 @@ nvfp4kv_status nvfp4kv_append_paged_decode(const nvfp4kv_cache *cache, const voi
     if (st != NVFP4KV_OK || batch == 0)
         return st;
     p.pool = static_cast<const uint8_t *>(cache->pool);
+    apply_tensor_scale(p, sm_scale, cache->global_scale);
     p.k_new = k_new;
     p.v_new = v_new;
     p.append = 1;

@@ -464,6 +464,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
                         load16<true>(is_v ? p.v_new : p.k_new, src, x);
                     else
                         load16<false>(is_v ? p.v_new : p.k_new, src, x);
+                    divide_by_tensor_scale(x, p.gscale);
                     Fmt::write_block(const_cast<uint8_t *>(p.pool) + (static_cast<size_t>(phys) * p.hkv + hh) * R,
                                      is_v, tok, blk, x);
                     fence_proxy_async_global();
@@ -526,7 +527,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         const bool owned = seg_begin >= lo && seg_begin + n <= hi;
         const int hA = 2 * tig, hB = hA + 1;
         if (owned) {
-            const float r0 = 1.f / L0, r1 = 1.f / L1;
+            const float r0 = p.out_scale / L0, r1 = p.out_scale / L1;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 const int head = which ? hB : hA;

@@ -2,9 +2,10 @@
 // contiguous FP8-E4M3 workspace ("SGLang stores KV cache in 4 bits" (LMSYS
 // summary), Interpretation: the extend path dequantises the cached prefix into
 // one FP8 workspace shared across layers).
-//   out[kv_indptr[b] + j][h][c] = E4M3_rn_satfinite(E2M1(code) x E4M3(scale))
-// The product has at most 6 significant bits and lies in [2^-10, 2688], so it
-// is exact in fp16; the only rounding is the final one to E4M3.
+//   out[kv_indptr[b] + j][h][c] = E4M3_rn_satfinite(fl32(G x E2M1(code) x E4M3(scale)))
+// with G the tensor scale.  The code-scale product has at most 6 significant
+// bits and lies in [2^-10, 2688], so it is exact in fp16; at G = 1 the only
+// rounding is the final one to E4M3.
 //
 // Work unit: one page-head record (16 tokens of one kv head, K and V), grid-
 // stride over (sequence, page, kv head).  A CTA of 64 threads stages the
@@ -43,10 +44,21 @@ __device__ __forceinline__ PrefixUnit prefix_unit(const PrefixParams &p, long lo
     return t;
 }
 
-// Two bytes of 8 E4M3 values each from 8 f16x2 (low halves -> first word pair).
-__device__ __forceinline__ uint32_t e4m3_pair(uint32_t h2a, uint32_t h2b)
+// E4M3 bytes of the exact products in an f16x2 times the tensor scale G:
+// E4M3_rn_satfinite(fl32(G * v)), which at G = 1 is the f16 conversion itself.
+__device__ __forceinline__ uint32_t to_e4m3x2(uint32_t h2, float G)
 {
-    return f16x2_to_e4m3x2(h2a) | (f16x2_to_e4m3x2(h2b) << 16);
+    if (G == 1.f)
+        return f16x2_to_e4m3x2(h2);
+    const float lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
+    const float hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+    return f32x2_to_e4m3x2(__fmul_rn(lo, G), __fmul_rn(hi, G));
+}
+
+// Four E4M3 bytes from two f16x2 (low halves first).
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t h2a, uint32_t h2b, float G)
+{
+    return to_e4m3x2(h2a, G) | (to_e4m3x2(h2b, G) << 16);
 }
 
 } // namespace
@@ -137,9 +149,10 @@ __global__ void __launch_bounds__(kPrefixThreads) dequant_prefix_kernel(const Pr
                     e2m1x8_to_f16x2x4(packed.x, f[0], f[1], f[2], f[3]);
                     e2m1x8_to_f16x2x4(packed.y, f[4], f[5], f[6], f[7]);
                     const size_t o = ((rows + tok) * p.hkv + cur.h) * kHeadDim + blk * 16;
-                    *reinterpret_cast<uint4 *>(p.k_out + o) =
-                        make_uint4(e4m3_pair(hmul2(f[0], s2), hmul2(f[1], s2)), e4m3_pair(hmul2(f[2], s2), hmul2(f[3], s2)),
-                                   e4m3_pair(hmul2(f[4], s2), hmul2(f[5], s2)), e4m3_pair(hmul2(f[6], s2), hmul2(f[7], s2)));
+                    const float G = p.gscale;
+                    *reinterpret_cast<uint4 *>(p.k_out + o) = make_uint4(
+                        e4m3_pair(hmul2(f[0], s2), hmul2(f[1], s2), G), e4m3_pair(hmul2(f[2], s2), hmul2(f[3], s2), G),
+                        e4m3_pair(hmul2(f[4], s2), hmul2(f[5], s2), G), e4m3_pair(hmul2(f[6], s2), hmul2(f[7], s2), G));
                 }
             }
             // V: tokens 2*row (low nibbles) and 2*row + 1 (high nibbles), block blk.
@@ -162,10 +175,10 @@ __global__ void __launch_bounds__(kPrefixThreads) dequant_prefix_kernel(const Pr
                 for (int q = 0; q < 4; ++q) {
                     uint32_t f0, f1, f2, f3;   // channels g, g + 8, g + 1, g + 9 (g = 2q), tokens (t0, t0 + 1)
                     e2m1x8_to_f16x2x4(unitw[q], f0, f1, f2, f3);
-                    e8[2 * q] = f16x2_to_e4m3x2(hmul2(f0, s2));
-                    e8[2 * q + 8] = f16x2_to_e4m3x2(hmul2(f1, s2));
-                    e8[2 * q + 1] = f16x2_to_e4m3x2(hmul2(f2, s2));
-                    e8[2 * q + 9] = f16x2_to_e4m3x2(hmul2(f3, s2));
+                    e8[2 * q] = to_e4m3x2(hmul2(f0, s2), p.gscale);
+                    e8[2 * q + 8] = to_e4m3x2(hmul2(f1, s2), p.gscale);
+                    e8[2 * q + 1] = to_e4m3x2(hmul2(f2, s2), p.gscale);
+                    e8[2 * q + 9] = to_e4m3x2(hmul2(f3, s2), p.gscale);
                 }
                 uint32_t w0[4], w1[4];
 #pragma unroll

@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
             sum.w += e * v.w;
             dsum += e * part_l[k];
         }
-        const float r = 1.f / dsum;
+        const float r = p.out_scale / dsum;
         res = make_float4(sum.x * r, sum.y * r, sum.z * r, sum.w * r);
     } else if (grp != 0) {
         return;                                  // empty sequence: zeros

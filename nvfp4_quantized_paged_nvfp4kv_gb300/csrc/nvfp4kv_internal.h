@@ -36,7 +36,9 @@ struct DecodeParams {
     int num_pages;
     int out_bf16;
     int num_workers;
-    float qscale;                // sm_scale * log2(e)
+    float qscale;                // sm_scale * log2(e) * tensor scale
+    float out_scale;             // tensor scale of V (1 for the FP8 cache)
+    float gscale;                // tensor scale the fused append divides by
     // fused append: new K/V rows [batch][hkv][128] written at position
     // seq_lens[b] - 1 before the decode reads the page (append != 0)
     const void *k_new;
@@ -55,6 +57,7 @@ struct QuantParams {
     int hkv;
     int num_pages;
     int in_bf16;
+    float gscale;                // tensor scale: blocks are taken of x / gscale
 };
 
 struct PrefixParams {
@@ -69,6 +72,7 @@ struct PrefixParams {
     int hkv;
     int max_pages;
     int num_pages;
+    float gscale;                // tensor scale multiplying every value
 };
 
 // Launch with programmatic stream serialisation allowed, so the kernel's

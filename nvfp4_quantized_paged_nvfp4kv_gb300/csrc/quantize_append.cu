@@ -80,18 +80,22 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const QuantParams p
     if (is_v && ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
         uint32_t S0, S1, c0[2], c1[2];
         unpack<kBf16>(r0, x);
+        divide_by_tensor_scale(x, p.gscale);
         quantize_block(x, S0, c0);
         unpack<kBf16>(r1, x);
+        divide_by_tensor_scale(x, p.gscale);
         quantize_block(x, S1, c1);
         write_nvfp4_v_pair(p.pool + rec0, tok0, blk, S0, c0, S1, c1);
         return;
     }
     if (ok0) {
         unpack<kBf16>(r0, x);
+        divide_by_tensor_scale(x, p.gscale);
         write_nvfp4_block(p.pool + rec0, is_v, tok0, blk, x);
     }
     if (ok1) {
         unpack<kBf16>(r1, x);
+        divide_by_tensor_scale(x, p.gscale);
         write_nvfp4_block(p.pool + rec1, is_v, tok1, blk, x);
     }
 }

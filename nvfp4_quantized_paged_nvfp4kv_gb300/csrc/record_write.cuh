@@ -52,6 +52,17 @@ __device__ __forceinline__ void load16(const void *src, size_t elem_off, float (
     unpack<kBf16>(r, x);
 }
 
+// Values relative to the tensor scale G (the block procedure runs on
+// fl32(x / G); nothing to do at G = 1).
+__device__ __forceinline__ void divide_by_tensor_scale(float (&x)[16], float G)
+{
+    if (G != 1.f) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            x[i] = __fdiv_rn(x[i], G);
+    }
+}
+
 // amax -> E4M3 block scale -> 16 E2M1 codes (code i in bits 4i .. 4i+3).
 //
 // Each code is decided on the IEEE quotient fl32(x / s).  It is computed

@@ -78,7 +78,11 @@ def decode(c, hq=4, batch=2, bt=FAKE, mp=4, sl=FAKE, out=FAKE, ws=FAKE, wsb=1 <<
 @pytest.mark.parametrize("kw,want", [
     (dict(head_dim=64), nv.ERR_UNSUPPORTED),
     (dict(page_size=32), nv.ERR_UNSUPPORTED),
-    (dict(global_scale=2.0), nv.ERR_UNSUPPORTED),
+    (dict(global_scale=0.0), nv.ERR_UNSUPPORTED),
+    (dict(global_scale=-2.0), nv.ERR_UNSUPPORTED),
+    (dict(global_scale=float("inf")), nv.ERR_UNSUPPORTED),
+    (dict(global_scale=float("nan")), nv.ERR_UNSUPPORTED),
+    (dict(global_scale=1e-40), nv.ERR_UNSUPPORTED),           # subnormal
     (dict(num_pages=0), nv.ERR_INVALID_ARG),
     (dict(num_kv_heads=-1), nv.ERR_INVALID_ARG),
     (dict(pool=FAKE + 8), nv.ERR_INVALID_ARG),

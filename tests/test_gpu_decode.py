@@ -59,6 +59,18 @@ def test_worker_count_invariance():
         np.testing.assert_allclose(b.decode(torch.float32, num_workers=nw), ref, rtol=5e-3, atol=5e-4)
 
 
+@pytest.mark.parametrize("g", [0.37, 3.1])
+def test_tensor_scale(g):
+    """Decode over a cache with tensor scale G (values G * s * e): the query
+    scale and the normaliser carry G."""
+    w = workloads.custom(3, 16, 4, (300, 17, 1000), seed=23)
+    b = Built(w, fp8=False, global_scale=g, garbage=True)
+    want, _ = oracle_full(b)
+    assert_close(b.decode(torch.float32), want, f"nvfp4 G={g}")
+    assert_close(b.decode(torch.float32, num_workers=7), want, f"nvfp4 G={g} 7 workers")
+    assert int(b.status.item()) == 0
+
+
 def test_more_workers_than_page_heads():
     """One long sequence among many short ones: the automatic worker count,
     bounded by the largest batch the block table allows, and an explicit one
@@ -126,12 +138,13 @@ def test_long_context_sampled(name, batch):
 
 @pytest.mark.parametrize("fp8", [False, True])
 @pytest.mark.parametrize("lens", [(37, 16, 1, 300, 0), (8192, 8191, 8177)])
-def test_append_decode_equals_append_then_decode(fp8, lens):
+def test_append_decode_equals_append_then_decode(fp8, lens, g=1.0):
     """The fused step writes exactly the bytes quantize_append would and then
     decodes exactly as paged_decode does."""
     w = workloads.custom(len(lens), 32, 4, lens, seed=21)
-    full = Built(w)                                     # all tokens appended by quantize_append
-    cache = (nv.FP8Cache if fp8 else nv.NVFP4Cache).allocate(full.num_pages, w.num_kv_heads, device="cuda")
+    full = Built(w, global_scale=g)                     # all tokens appended by quantize_append
+    cache = (nv.FP8Cache.allocate(full.num_pages, w.num_kv_heads, device="cuda") if fp8 else
+             nv.NVFP4Cache.allocate(full.num_pages, w.num_kv_heads, device="cuda", global_scale=g))
     app = nv.fp8kv_quantize_append if fp8 else nv.nvfp4kv_quantize_append
     k_new = torch.zeros((w.batch, w.num_kv_heads, 128), dtype=torch.float32, device="cuda")
     v_new = torch.zeros_like(k_new)
@@ -156,3 +169,7 @@ def test_append_decode_equals_append_then_decode(fp8, lens):
     np.testing.assert_array_equal(out.cpu().numpy(), full.decode(torch.float32, fp8=fp8))
     want, _ = oracle_full(full, fp8=fp8)
     assert_close(out.cpu().numpy(), want, "fused append + decode")
+
+
+def test_append_decode_with_tensor_scale():
+    test_append_decode_equals_append_then_decode(False, (40, 1, 300), g=0.37)

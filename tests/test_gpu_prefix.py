@@ -25,9 +25,28 @@ def run(b: Built, prefix_lens, indptr, rows):
 
 def expected(b: Built, prefix_lens, indptr, rows):
     _, pools = oracle_full(b)
-    k = oracle.dequant_prefix_fp8(pools[0], pools[1], b.bt, np.int32(prefix_lens), np.int32(indptr), rows)
-    v = oracle.dequant_prefix_fp8(pools[2], pools[3], b.bt, np.int32(prefix_lens), np.int32(indptr), rows)
+    g = b.global_scale
+    k = oracle.dequant_prefix_fp8(pools[0], pools[1], b.bt, np.int32(prefix_lens), np.int32(indptr), rows,
+                                  global_scale=g)
+    v = oracle.dequant_prefix_fp8(pools[2], pools[3], b.bt, np.int32(prefix_lens), np.int32(indptr), rows,
+                                  global_scale=g)
     return k, v
+
+
+@pytest.mark.parametrize("g", [0.37, 3.1])
+def test_prefix_with_tensor_scale(g):
+    """Workspace values E4M3(fl32(G s e)) for a tensor scale G != 1."""
+    w = workloads.custom(2, 8, 2, (301, 40), seed=29)
+    b = Built(w, fp8=False, global_scale=g)
+    lens = list(w.seq_lens)
+    indptr = [3, 3 + lens[0]]
+    rows = 3 + sum(lens) + 2
+    got = run(b, lens, indptr, rows)
+    want = expected(b, lens, indptr, rows)
+    for gv, wv in zip(got, want):
+        for s, L in zip(indptr, lens):
+            np.testing.assert_array_equal(gv[s:s + L], wv[s:s + L])
+    assert int(b.status.item()) == 0
 
 
 @pytest.mark.parametrize("name", ["tiny", "llama70b", "ctx32k", "ctx1m"])
