@@ -276,35 +276,70 @@ def time_steps(setup: DecodeSetup, steps: int, warmup: int, world: int):
 
 def time_e2e(setup: DecodeSetup, steps: int, world: int):
     """Same step through the public API with the step's inputs in pinned host
-    memory: H2D of queries, new K/V rows and lengths; D2H of the output."""
-    dev = setup.dev
-    hq = setup.q.cpu().pin_memory()
-    hk = setup.k_new.cpu().pin_memory()
-    hv = setup.v_new.cpu().pin_memory()
-    hl = setup.sl.cpu().pin_memory()
-    hout = torch.empty(setup.out.shape, dtype=setup.out.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(setup.q), torch.empty_like(setup.k_new), torch.empty_like(setup.v_new)
-    dl = torch.empty_like(setup.sl)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl))
-    d2h = hout.numel() * hout.element_size()
+    memory: every step copies its queries, new K/V rows and lengths host to
+    device (one copy of one packed buffer) and its output back; all copies are
+    inside the timed region.  A serving loop would not pay a host launch per
+    call: each step is one CUDA graph (captured once per input slot) that
+    decodes from one device slot while, on a second stream, it copies the next
+    step's inputs into the other slot and reads the previous step's output
+    back."""
+    parts = [setup.q, setup.k_new, setup.v_new, setup.sl]
+    sizes = [t.numel() * t.element_size() for t in parts]
+    offs = [0]
+    for n in sizes:
+        offs.append(offs[-1] + (n + 255) // 256 * 256)
+    host_in = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
+    for t, o, n in zip(parts, offs, sizes):
+        host_in[o:o + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+    dev_in = [torch.empty(offs[-1], dtype=torch.uint8, device=setup.dev) for _ in range(2)]
+    dev_views = [[b[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(parts, offs, sizes)]
+                 for b in dev_in]
+    outs = [torch.empty_like(setup.out) for _ in range(2)]
+    host_out = [torch.empty(setup.out.shape, dtype=setup.out.dtype).pin_memory() for _ in range(2)]
+    h2d, d2h = sum(sizes), host_out[0].numel() * host_out[0].element_size()
+    out_saved = setup.out
+    side = torch.cuda.Stream(device=setup.dev)
+
+    def body(s, i):
+        main = torch.cuda.current_stream()
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            dev_in[1 - s].copy_(host_in, non_blocking=True)      # the next step's inputs
+            host_out[1 - s].copy_(outs[1 - s], non_blocking=True)  # the previous step's output
+        setup.out = outs[s]
+        q, k, v, sl = dev_views[s]
+        setup.step(i, q, k, v, sl)
+        main.wait_stream(side)
+
+    # warm up both slots eagerly, then capture one graph per slot
+    dev_in[0].copy_(host_in)
+    for i in range(4):
+        body(i % 2, i)
+    torch.cuda.synchronize()
+    graphs = []
+    for s in range(2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body(s, s)
+        graphs.append(g)
+    dev_in[0].copy_(host_in)
+    for i in range(4):
+        graphs[i % 2].replay()
+    torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    for i in range(3):
-        setup.step(i)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t0.record(stream)
+    dev_in[0].copy_(host_in, non_blocking=True)                  # step 0's inputs
     for i in range(steps):
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        dl.copy_(hl, non_blocking=True)
-        setup.step(i, dq, dk, dv, dl)
-        hout.copy_(setup.out, non_blocking=True)
+        graphs[i % 2].replay()
+    last = (steps - 1) % 2
+    host_out[last].copy_(outs[last], non_blocking=True)         # the last step's output
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    del dev
+    setup.out = out_saved
     return t0.elapsed_time(t1), h2d, d2h
 
 
