@@ -215,6 +215,27 @@ nvfp4kv_status nvfp4kv_append_paged_decode(const nvfp4kv_cache *cache, const voi
                                            size_t workspace_bytes, int32_t num_workers, int32_t *dev_status,
                                            nvfp4kv_stream_t stream);
 
+/* Multi-query decode (several new tokens per sequence at once, as in
+ * multi-token prediction or speculative decoding): q_len query tokens per
+ * sequence sit at the last q_len positions and attend causally, token t
+ * (0-based) over the seq_lens[b] - q_len + t + 1 first cached tokens (the
+ * new tokens must already be in the cache, e.g. by nvfp4kv_quantize_append).
+ * Same arguments as nvfp4kv_paged_decode except
+ * q: bf16 [batch][q_len][num_q_heads][128] and out: [batch][q_len][num_q_heads]
+ *   [128]; 1 <= q_len <= NVFP4KV_MAX_QUERY_TOKENS (a larger value returns
+ *   NVFP4KV_ERR_UNSUPPORTED).  A query that sees no cached token gets zeros.
+ * The group * q_len query rows of a kv head are processed in row groups of
+ * 8; each row group streams the kv head's pages (the row groups of one kv
+ * head run close together, so the repeats mostly hit L2).  The workspace is
+ * sized as for nvfp4kv_paged_decode. */
+#define NVFP4KV_MAX_QUERY_TOKENS 8
+nvfp4kv_status nvfp4kv_paged_decode_multi(const nvfp4kv_cache *cache, const void *q, int32_t batch,
+                                          int32_t q_len, int32_t num_q_heads, const int32_t *block_table,
+                                          int32_t max_pages_per_seq, const int32_t *seq_lens, float sm_scale,
+                                          void *out, nvfp4kv_dtype out_dtype, void *workspace,
+                                          size_t workspace_bytes, int32_t num_workers, int32_t *dev_status,
+                                          nvfp4kv_stream_t stream);
+
 /* Decode without a caller-provided workspace, for callers that cannot
  * allocate device memory (for example a serving engine whose device memory is
  * all reserved for weights and KV cache at start-up).  The pages have no

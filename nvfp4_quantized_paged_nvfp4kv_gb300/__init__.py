@@ -96,6 +96,9 @@ def load(build_if_missing: bool = True):
             "fp8kv_append_paged_decode": (_st, [ctypes.POINTER(_Fp8Cache), _vp, _vp, _st, _vp, _i32, _i32,
                                                 _vp, _i32, _vp, ctypes.c_float, _vp, _st, _vp,
                                                 ctypes.c_size_t, _i32, _vp, _vp]),
+            "nvfp4kv_paged_decode_multi": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _i32, _i32, _i32, _vp, _i32,
+                                                 _vp, ctypes.c_float, _vp, _st, _vp, ctypes.c_size_t, _i32, _vp,
+                                                 _vp]),
             "nvfp4kv_paged_decode_static_scratch": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _i32, _i32, _vp,
                                                           _i32, _vp, ctypes.c_float, _vp, _st, _i32, _vp,
                                                           _vp]),
@@ -225,6 +228,21 @@ def nvfp4kv_paged_decode(cache: NVFP4Cache, q, block_table, seq_lens, out, works
                          sm_scale=None, num_workers=0, dev_status=None, stream=None) -> None:
     _decode(load().nvfp4kv_paged_decode, "nvfp4kv_paged_decode", cache, q, block_table, seq_lens,
             out, workspace, sm_scale, num_workers, dev_status, stream)
+
+
+def nvfp4kv_paged_decode_multi(cache: NVFP4Cache, q, block_table, seq_lens, out, workspace,
+                               sm_scale=None, num_workers=0, dev_status=None, stream=None) -> None:
+    """q: bf16 [batch][q_len][Hq][128] (the last q_len positions of each
+    sequence, causal); out: [batch][q_len][Hq][128]."""
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    B, T, Hq, _ = q.shape
+    st = load().nvfp4kv_paged_decode_multi(
+        cache.c, _ptr(q), B, T, Hq, _ptr(block_table), block_table.shape[1], _ptr(seq_lens), float(sm_scale),
+        _ptr(out), _dtype_code(out), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), int(num_workers),
+        _ptr(dev_status), _stream(stream))
+    _check(st, "nvfp4kv_paged_decode_multi")
 
 
 def fp8kv_paged_decode(cache: FP8Cache, q, block_table, seq_lens, out, workspace,

@@ -149,6 +149,9 @@ nvfp4kv_status check_decode(int32_t hkv, int32_t num_pages, const void *q, int32
     p.qscale = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
     p.out_scale = 1.f;
     p.gscale = 1.f;
+    p.q_len = 1;
+    p.rows = group;
+    p.row_groups = 1;
     return NVFP4KV_OK;
 }
 
@@ -212,6 +215,38 @@ nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q, i
     p.pool = static_cast<const uint8_t *>(cache->pool);
     apply_tensor_scale(p, sm_scale, cache->global_scale);
     cudaError_t e = launch_decode_nvfp4(p, to_cuda(stream));
+    if (e == cudaSuccess)
+        e = launch_merge(p, to_cuda(stream));
+    return from_cuda(e);
+}
+
+nvfp4kv_status nvfp4kv_paged_decode_multi(const nvfp4kv_cache *cache, const void *q, int32_t batch, int32_t q_len,
+                                          int32_t num_q_heads, const int32_t *block_table,
+                                          int32_t max_pages_per_seq, const int32_t *seq_lens, float sm_scale,
+                                          void *out, nvfp4kv_dtype out_dtype, void *workspace,
+                                          size_t workspace_bytes, int32_t num_workers, int32_t *dev_status,
+                                          nvfp4kv_stream_t stream)
+{
+    nvfp4kv_status st = check_nvfp4(cache);
+    if (st != NVFP4KV_OK)
+        return st;
+    if (q_len < 1 || q_len > NVFP4KV_MAX_QUERY_TOKENS)
+        return q_len < 1 ? NVFP4KV_ERR_INVALID_ARG : NVFP4KV_ERR_UNSUPPORTED;
+    DecodeParams p;
+    st = check_decode(cache->num_kv_heads, cache->num_pages, q, batch, num_q_heads, block_table,
+                      max_pages_per_seq, seq_lens, sm_scale, out, out_dtype, workspace, workspace_bytes,
+                      num_workers, dev_status, p);
+    if (st != NVFP4KV_OK || batch == 0)
+        return st;
+    p.q_len = q_len;
+    p.rows = p.group * q_len;
+    p.row_groups = (p.rows + kMaxGroup - 1) / kMaxGroup;
+    if (static_cast<int64_t>(batch) * cache->num_kv_heads * p.row_groups * max_pages_per_seq >
+        (int64_t{1} << 31) - 1)
+        return NVFP4KV_ERR_UNSUPPORTED;
+    p.pool = static_cast<const uint8_t *>(cache->pool);
+    apply_tensor_scale(p, sm_scale, cache->global_scale);
+    cudaError_t e = launch_decode_nvfp4_multi(p, to_cuda(stream));
     if (e == cudaSuccess)
         e = launch_merge(p, to_cuda(stream));
     return from_cuda(e);

@@ -335,7 +335,19 @@ static_assert(decode_smem_fixed<Fp8Format>() + (kMaxBatch + 1) * sizeof(int32_t)
 
 // ---- the decode kernel -------------------------------------------------------
 
-template <class Fmt>
+// Output element offset of query row r (0 .. rows-1) of kv head hp, sequence b:
+// row r is query token r / group, head r % group of the kv head's group.
+__device__ __forceinline__ size_t out_row(const DecodeParams &p, int b, int hp, int r)
+{
+    const int t = r / p.group, i = r - t * p.group;
+    return ((static_cast<size_t>(b) * p.q_len + t) * p.hq + hp * p.group + i) * kHeadDim;
+}
+
+// kMulti: several query tokens per sequence.  A segment is then one row group
+// of one kv head ("virtual heads" hkv * row_groups per sequence), numbered
+// with the row group innermost so that the row groups of a kv head read the
+// same pages close together in time.
+template <class Fmt, bool kMulti = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_kernel(const DecodeParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -366,7 +378,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
     // cache records, q, the new K/V, the output and the workspace are touched
     // only after the wait.
     const int max_len = p.max_pages * kPageSize;
-    build_prefix(p.seq_lens, p.batch, p.hkv, max_len, prefix, scratch,
+    const int nseg = kMulti ? p.hkv * p.row_groups : p.hkv;   // segments per sequence
+    build_prefix(p.seq_lens, p.batch, nseg, max_len, prefix, scratch,
                  blockIdx.x == 0 ? p.dev_status : nullptr);
 
     const int w = blockIdx.x * kDecodeWarps + warp;
@@ -394,9 +407,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         if (j < hi) {
             const int b = find_seq(prefix, p.batch, j);
             const int r = j - prefix[b];
-            const int n = (prefix[b + 1] - prefix[b]) / p.hkv;
+            const int n = (prefix[b + 1] - prefix[b]) / nseg;
             hh = r / n;
             const int pg = r - hh * n;
+            if constexpr (kMulti)
+                hh /= p.row_groups;                  // the kv head of the row group
             phys = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + pg);
         }
     };
@@ -433,14 +448,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
 
     // ---- consumer bookkeeping (warp-uniform) ----
     int b = find_seq(prefix, p.batch, lo);
-    int n = (prefix[b + 1] - prefix[b]) / p.hkv;
-    int h = (lo - prefix[b]) / n;
+    int n = (prefix[b + 1] - prefix[b]) / nseg;
+    int h = (lo - prefix[b]) / n;                 // segment (kv head, or row group) in the sequence
     int pg = lo - prefix[b] - h * n;
     int L = clamp_len(p.seq_lens[b], max_len);
     int seg_begin = prefix[b] + h * n;
 
     pdl_wait();
-    if (p.append) {
+    if (!kMulti && p.append) {
         // Fused append: the warp that streams the last page-head of a segment
         // first writes that sequence's new token (position seq_len - 1) into
         // it, one 16-value block per lane, before any copy of that page.
@@ -488,10 +503,25 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
     const int g = p.group;
     const LaneOffsets off = Fmt::offsets(gid, tig);
 
+    // multi-query: the segment's kv head and row group, and the number of
+    // keys visible to this lane's two score columns (rows 2tig, 2tig + 1)
+    int hp = h, rg = 0, limA = 0, limB = 0;
     auto start_segment = [&]() {
-        if (gid < g) {
-            const uint4 *qrow = reinterpret_cast<const uint4 *>(
-                p.q + (static_cast<size_t>(b) * p.hq + h * g + gid) * kHeadDim + 32 * tig);
+        bool has_row = gid < g;
+        const uint16_t *qsrc = p.q + (static_cast<size_t>(b) * p.hq + h * g + gid) * kHeadDim;
+        if constexpr (kMulti) {
+            hp = h / p.row_groups;
+            rg = h - hp * p.row_groups;
+            const int r = rg * kMaxGroup + gid;
+            has_row = r < p.rows;
+            qsrc = p.q + out_row(p, b, hp, has_row ? r : 0);
+            // row r is query token t = r / g at position L - q_len + t
+            const int rA = rg * kMaxGroup + 2 * tig, rB = rA + 1;
+            limA = rA < p.rows ? L - p.q_len + rA / g + 1 : 0;
+            limB = rB < p.rows ? L - p.q_len + rB / g + 1 : 0;
+        }
+        if (has_row) {
+            const uint4 *qrow = reinterpret_cast<const uint4 *>(qsrc + 32 * tig);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 r = __ldg(qrow + i);
@@ -527,14 +557,22 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         const bool owned = seg_begin >= lo && seg_begin + n <= hi;
         const int hA = 2 * tig, hB = hA + 1;
         if (owned) {
-            const float r0 = p.out_scale / L0, r1 = p.out_scale / L1;
+            // (a row that saw no key at all -- a multi-query row before its
+            // first visible key -- has l = 0 and gets zeros)
+            const float r0 = L0 > 0.f ? p.out_scale / L0 : 0.f, r1 = L1 > 0.f ? p.out_scale / L1 : 0.f;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 const int head = which ? hB : hA;
-                if (head >= g)
+                size_t o = (static_cast<size_t>(b) * p.hq + h * g + head) * kHeadDim;
+                if constexpr (kMulti) {
+                    const int row = rg * kMaxGroup + head;   // rows beyond the group are later tokens
+                    if (row >= p.rows)
+                        continue;
+                    o = out_row(p, b, hp, row);
+                } else if (head >= g) {
                     continue;
+                }
                 const float r = which ? r1 : r0;
-                const size_t o = (static_cast<size_t>(b) * p.hq + h * g + head) * kHeadDim;
                 if (p.out_bf16) {
                     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) + o;
 #pragma unroll
@@ -581,7 +619,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
     }
 
     // One step handles one page-head, or two of the same segment.
-    auto step = [&](auto npc, uint32_t rec0, uint32_t rec1, int last_valid) {
+    auto step = [&](auto npc, uint32_t rec0, uint32_t rec1, int last_valid, int pos0) {
         constexpr int NP = decltype(npc)::value;
         // S^T = K . Q^T
         // (two accumulators per page-head halve the dependent MMA chain)
@@ -600,7 +638,23 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
             for (int e = 0; e < 4; ++e)
                 sc[q][e] += sd[e];
         }
-        if (last_valid < kPageSize) {
+        if constexpr (kMulti) {
+            // key pos0 + 16q + token against each column's visible count
+            if (pos0 + NP * kPageSize > min(limA, limB)) {
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    const int k0 = pos0 + q * kPageSize + gid, k1 = k0 + 8;
+                    if (k0 >= limA)
+                        sc[q][0] = -INFINITY;
+                    if (k0 >= limB)
+                        sc[q][1] = -INFINITY;
+                    if (k1 >= limA)
+                        sc[q][2] = -INFINITY;
+                    if (k1 >= limB)
+                        sc[q][3] = -INFINITY;
+                }
+            }
+        } else if (last_valid < kPageSize) {
             if (gid >= last_valid)
                 sc[NP - 1][0] = sc[NP - 1][1] = -INFINITY;
             if (gid + 8 >= last_valid)
@@ -640,8 +694,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
-            const float p0 = fast_exp2(sc[q][0] - m0), p1 = fast_exp2(sc[q][1] - m1);
-            const float p2 = fast_exp2(sc[q][2] - m0), p3 = fast_exp2(sc[q][3] - m1);
+            float p0 = fast_exp2(sc[q][0] - m0), p1 = fast_exp2(sc[q][1] - m1);
+            float p2 = fast_exp2(sc[q][2] - m0), p3 = fast_exp2(sc[q][3] - m1);
+            if constexpr (kMulti) {
+                // a masked score against a maximum that is still -inf
+                p0 = sc[q][0] == -INFINITY ? 0.f : p0;
+                p1 = sc[q][1] == -INFINITY ? 0.f : p1;
+                p2 = sc[q][2] == -INFINITY ? 0.f : p2;
+                p3 = sc[q][3] == -INFINITY ? 0.f : p3;
+            }
             ls0 += p0 + p2;
             ls1 += p1 + p3;
             pb[q][0] = movmatrix_trans(pack_f16x2(p0, p1));
@@ -695,9 +756,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         const int plast = pg + np - 1;
         const int last_valid = (plast == n - 1) ? (L - plast * kPageSize) : kPageSize;
         if (np == 2)
-            step(std::integral_constant<int, 2>(), wdata + st * R, wdata + st1 * R, last_valid);
+            step(std::integral_constant<int, 2>(), wdata + st * R, wdata + st1 * R, last_valid, pg * kPageSize);
         else
-            step(std::integral_constant<int, 1>(), wdata + st * R, wdata + st * R, last_valid);
+            step(std::integral_constant<int, 1>(), wdata + st * R, wdata + st * R, last_valid, pg * kPageSize);
 
         __syncwarp();
         if (j + S < hi)
@@ -717,12 +778,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
             if (j < hi) {
                 ++h;
                 pg = 0;
-                if (h == p.hkv) {
+                if (h == nseg) {
                     h = 0;
                     do {
                         ++b;
                     } while (prefix[b + 1] == prefix[b]);
-                    n = (prefix[b + 1] - prefix[b]) / p.hkv;
+                    n = (prefix[b + 1] - prefix[b]) / nseg;
                     L = clamp_len(p.seq_lens[b], max_len);
                 }
                 seg_begin = prefix[b] + h * n;

@@ -7,12 +7,12 @@ template <class Fmt>
 static cudaError_t launch_decode(const DecodeParams &p, cudaStream_t s)
 {
     const size_t smem = decode_smem_bytes<Fmt>(p.batch);
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<Fmt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<Fmt, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
     const int grid = (p.num_workers + kDecodeWarps - 1) / kDecodeWarps;
-    return launch_pdl(decode_kernel<Fmt>, dim3(grid), dim3(kDecodeWarps * 32), smem, s, p);
+    return launch_pdl(decode_kernel<Fmt, false>, dim3(grid), dim3(kDecodeWarps * 32), smem, s, p);
 }
 
 cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t s)

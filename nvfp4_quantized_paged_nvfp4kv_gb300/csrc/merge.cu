@@ -23,14 +23,18 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     int32_t *scratch = msmem;
     int32_t *prefix = msmem + 32;
     pdl_launch_dependents();                     // the next kernel may start its prologue
-    build_prefix(p.seq_lens, p.batch, p.hkv, p.max_pages * kPageSize, prefix, scratch, nullptr);
+    const int nseg = p.hkv * p.row_groups;       // segments per sequence (row groups of kv heads)
+    build_prefix(p.seq_lens, p.batch, nseg, p.max_pages * kPageSize, prefix, scratch, nullptr);
 
-    const int b = blockIdx.x / p.hkv;
-    const int h = blockIdx.x - b * p.hkv;
-    const int i = blockIdx.y;
+    const int b = blockIdx.x / nseg;
+    const int h = blockIdx.x - b * nseg;
+    const int i = blockIdx.y;                    // row of the segment's row group
+    const int hp = h / p.row_groups, row = (h - hp * p.row_groups) * kMaxGroup + i;
+    if (row >= p.rows)
+        return;
     const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        const int n = (prefix[b + 1] - prefix[b]) / p.hkv;
+        const int n = (prefix[b + 1] - prefix[b]) / nseg;
         int wf = 0, nc = -1, slot = 0;
         if (n > 0) {
             const long long T = prefix[p.batch];
@@ -51,7 +55,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     const int wf = seg[0], nc = seg[1], slot_wf = seg[2];
     if (nc == 1)
         return;                                  // written by the decode kernel
-    const size_t o = (static_cast<size_t>(b) * p.hq + h * p.group + i) * kHeadDim + 4 * lane;
+    const size_t o = out_row(p, b, hp, row) + 4 * lane;
 
     float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
     if (nc > 1) {
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
             sum.w += e * v.w;
             dsum += e * part_l[k];
         }
-        const float r = p.out_scale / dsum;
+        const float r = dsum > 0.f ? p.out_scale / dsum : 0.f;   // a row that saw no key: zeros
         res = make_float4(sum.x * r, sum.y * r, sum.z * r, sum.w * r);
     } else if (grp != 0) {
         return;                                  // empty sequence: zeros
@@ -140,7 +144,8 @@ cudaError_t launch_merge(const DecodeParams &p, cudaStream_t s)
         if (e != cudaSuccess)
             return e;
     }
-    return launch_pdl(merge_kernel, dim3(p.batch * p.hkv, p.group), dim3(kMergeThreads), smem, s, p);
+    return launch_pdl(merge_kernel, dim3(p.batch * p.hkv * p.row_groups, p.rows < kMaxGroup ? p.rows : kMaxGroup),
+                      dim3(kMergeThreads), smem, s, p);
 }
 
 int sm_count()

@@ -45,6 +45,12 @@ struct DecodeParams {
     const void *v_new;
     int append;
     int new_bf16;
+    // multi-query decode: q_len query tokens per sequence (the last q_len
+    // positions, causal among themselves); rows = group * q_len query rows
+    // per kv head, taken in row groups of kMaxGroup
+    int q_len;
+    int rows;
+    int row_groups;
 };
 
 struct QuantParams {
@@ -103,6 +109,7 @@ size_t decode_workspace_bytes(int num_workers);
 cudaError_t launch_quantize_append_nvfp4(const QuantParams &p, cudaStream_t s);
 cudaError_t launch_quantize_append_fp8(const QuantParams &p, cudaStream_t s);
 cudaError_t launch_decode_nvfp4(const DecodeParams &p, cudaStream_t s);
+cudaError_t launch_decode_nvfp4_multi(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_merge(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_dequant_prefix_fp8(const PrefixParams &p, cudaStream_t s);

@@ -8,6 +8,7 @@ import pytest
 import torch
 
 import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+import oracle
 import workloads
 from gpu_util import Built, assert_close, oracle_full, oracle_single_head
 
@@ -173,3 +174,33 @@ def test_append_decode_equals_append_then_decode(fp8, lens, g=1.0):
 
 def test_append_decode_with_tensor_scale():
     test_append_decode_equals_append_then_decode(False, (40, 1, 300), g=0.37)
+
+
+@pytest.mark.parametrize("hq,hkv,q_len,lens", [
+    (64, 8, 2, (300, 17, 1000)),      # group 8: two row groups per kv head
+    (16, 4, 2, (129, 64)),            # group 4: both tokens in one row group
+    (48, 8, 3, (500, 3, 2)),          # group 6, 18 rows; a sequence shorter than q_len
+    (8, 8, 8, (40, 1000)),            # group 1, 8 tokens
+])
+def test_multi_query_decode(hq, hkv, q_len, lens):
+    """Several query tokens per sequence at its last q_len positions, causal:
+    token t attends over the first L - q_len + t + 1 tokens, i.e. the oracle's
+    single-token decode at that length."""
+    w = workloads.custom(len(lens), hq, hkv, lens, seed=31 + q_len)
+    b = Built(w, fp8=False, garbage=True)
+    rng = np.random.default_rng(7)
+    q = torch.from_numpy(rng.standard_normal((w.batch, q_len, hq, 128)).astype(np.float32)).to(torch.bfloat16)
+    want, pools = oracle_full(b)
+    ref = np.zeros((w.batch, q_len, hq, 128))
+    for t in range(q_len):
+        lt = np.maximum(np.int32(w.seq_lens) - q_len + t + 1, 0).astype(np.int32)
+        ref[:, t] = oracle.paged_decode(*pools, q[:, t].float().numpy(), b.bt, lt)
+    for nw in (0, 7):
+        out = torch.full((w.batch, q_len, hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+        ws = nv.new_workspace(nw, device="cuda")
+        ws.fill_(0xFF)
+        nv.nvfp4kv_paged_decode_multi(b.cache, q.cuda(), b.bt_d, b.sl_d, out, ws, num_workers=nw,
+                                      dev_status=b.status)
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy(), ref, f"multi-query q_len={q_len} workers={nw}")
+    assert int(b.status.item()) == 0
