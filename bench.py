@@ -487,6 +487,7 @@ def other_rows(dev):
     dg_ms = timed(lambda: nv.nvfp4kv_paged_decode(cache_g, q, bt_d, sl, out, ws))
     qg_ms = timed(lambda: nv.nvfp4kv_quantize_append(cache_g, k, v, sm))
     d_bytes = L * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
+    multi = multi_query_rows(dev, timed)
     return {
         "quantize_append_8k_bf16": {"us": q_ms * 1e3, "tokens_per_s": T / (q_ms / 1e3),
                                     "alg_gbs": q_bytes / (q_ms / 1e3) / 1e9, "alg_bytes": q_bytes},
@@ -495,8 +496,50 @@ def other_rows(dev):
         "tensor_scale_0.37": {"decode_160k_b1_us": dg_ms * 1e3, "decode_160k_b1_unit_scale_us": d1_ms * 1e3,
                               "decode_alg_gbs": d_bytes / (dg_ms / 1e3) / 1e9,
                               "quantize_append_8k_bf16_us": qg_ms * 1e3},
+        "multi_query": multi,
         "timing": "CUDA events per call, 256 MB buffer written before each call to evict L2",
     }
+
+
+def multi_query_rows(dev, timed):
+    """Multi-query decode (q_len new tokens per sequence, causal) against q_len
+    single-token decodes of the same cache: Llama-3.3-70B layer (group 8, two
+    row groups per kv head at q_len 2) and the 32K workload shape with group 4
+    (Hq 32, Hkv 8: both tokens' rows share one row group)."""
+    import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+    res = {}
+    for name, w in (("llama70b_b12_q2", workloads.make("llama70b", batch=12)),
+                    ("g4_b12_8k_q2", workloads.custom(12, 32, 8, (8192,) * 12, seed=41))):
+        q_len = 2
+        bt, num_pages = workloads.block_table(w)
+        cache = nv.NVFP4Cache.allocate(num_pages, w.num_kv_heads, device=dev, zero=False)
+        for b in range(w.batch):
+            for t0 in range(0, w.seq_lens[b], workloads.CHUNK):
+                t1 = min(w.seq_lens[b], t0 + workloads.CHUNK)
+                sm = torch.from_numpy(workloads.slot_mapping(w, bt, b, t0, t1)).to(dev)
+                nv.nvfp4kv_quantize_append(cache, workloads.kv_rows(w, "k", b, t0, t1, device=dev),
+                                           workloads.kv_rows(w, "v", b, t0, t1, device=dev), sm)
+        bt_d = torch.from_numpy(bt).to(dev)
+        sl = torch.tensor(w.seq_lens, dtype=torch.int32, device=dev)
+        sl_prev = sl - 1
+        q2 = torch.randn((w.batch, q_len, w.num_q_heads, 128), device=dev).to(torch.bfloat16)
+        q1 = q2[:, 0].contiguous()
+        out2 = torch.empty((w.batch, q_len, w.num_q_heads, 128), dtype=torch.bfloat16, device=dev)
+        out1 = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.bfloat16, device=dev)
+        ws = nv.new_workspace(device=dev)
+        m_ms = timed(lambda: nv.nvfp4kv_paged_decode_multi(cache, q2, bt_d, sl, out2, ws))
+
+        def two_singles():
+            nv.nvfp4kv_paged_decode(cache, q1, bt_d, sl_prev, out1, ws)
+            nv.nvfp4kv_paged_decode(cache, q1, bt_d, sl, out1, ws)
+        s_ms = timed(two_singles)
+        kv = sum(w.seq_lens) * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
+        res[name] = {"us": m_ms * 1e3, "two_single_decodes_us": s_ms * 1e3,
+                     "query_tokens_per_s": w.batch * q_len / (m_ms / 1e3),
+                     "kv_alg_gbs": kv / (m_ms / 1e3) / 1e9}
+        del cache
+        torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------
