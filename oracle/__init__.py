@@ -76,6 +76,9 @@ def _load():
         lib.oracle_fp8_paged_decode.argtypes = [
             _u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p, ctypes.c_int,
             ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_double, _f64p]
+        lib.oracle_extend_attention.argtypes = [
+            _f32p, _i32p, _u8p, _u8p, _i32p, _i32p, _f32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_double, _f64p]
         lib.oracle_nvfp4_bytes.restype = ctypes.c_int64
         lib.oracle_nvfp4_bytes.argtypes = [ctypes.c_int64]
         lib.oracle_fp8_bytes.restype = ctypes.c_int64
@@ -223,6 +226,32 @@ def fp8_paged_decode(k, v, q, block_table, seq_lens, sm_scale: float | None = No
     out = np.empty((B, Hq, d), np.float64)
     _load().oracle_fp8_paged_decode(_p(k, _u8p), _p(v, _u8p), Hkv, P, d, _p(q, _f32p), B, Hq,
                                     _p(bt, _i32p), bt.shape[1], _p(sl, _i32p),
+                                    float(sm_scale), _p(out, _f64p))
+    return out
+
+
+# --- extend attention ---------------------------------------------------------
+
+def extend_attention(q, q_indptr, k_prefix, v_prefix, kv_indptr, prefix_lens, k_chunk, v_chunk,
+                     sm_scale: float | None = None) -> np.ndarray:
+    """fp64 attention of each chunk token over its sequence's FP8 prefix rows
+    and the chunk's keys up to itself.  q, k_chunk, v_chunk: float32
+    [rows][H][d]; k_prefix, v_prefix: E4M3 bytes [rows][Hkv][d]."""
+    q = _c(q, np.float32)
+    rows, Hq, d = q.shape
+    kc = _c(k_chunk, np.float32)
+    vc = _c(v_chunk, np.float32)
+    Hkv = kc.shape[1]
+    kp = _c(k_prefix, np.uint8)
+    vp = _c(v_prefix, np.uint8)
+    qi = _c(q_indptr, np.int32)
+    ki = _c(kv_indptr, np.int32)
+    pl = _c(prefix_lens, np.int32)
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(d)
+    out = np.zeros((rows, Hq, d), np.float64)
+    _load().oracle_extend_attention(_p(q, _f32p), _p(qi, _i32p), _p(kp, _u8p), _p(vp, _u8p), _p(ki, _i32p),
+                                    _p(pl, _i32p), _p(kc, _f32p), _p(vc, _f32p), len(pl), Hq, Hkv, d,
                                     float(sm_scale), _p(out, _f64p))
     return out
 

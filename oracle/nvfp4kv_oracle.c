@@ -33,6 +33,7 @@
  * precision the kernels use, since the pages do not fix one.
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <string.h>
@@ -380,6 +381,64 @@ void oracle_fp8_paged_decode(const uint8_t *k, const uint8_t *v, int Hkv, int P,
 {
     paged_decode_generic(1, k, NULL, v, NULL, Hkv, P, d, q, B, Hq, block_table,
                          max_pages, seq_lens, sm_scale, out, 1.0f);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Extend attention ([LMSYS-summary] Interpretation ¶2: an extend step attends
+ * over the cached prefix, dequantised into the FP8 workspace, plus the new
+ * chunk).  For sequence b with prefix length P_b (workspace rows kv_indptr[b]
+ * .. + P_b, E4M3 at scale 1.0) and chunk rows q_indptr[b] .. q_indptr[b+1]
+ * (queries and the chunk's own K/V, given as floats), chunk token i and query
+ * head hq (kv head hq / g) attend over the P_b prefix keys and chunk keys
+ * 0 .. i (causal within the chunk):
+ *   s_j = sm_scale * q . k_j,   o = sum_j softmax(s)_j v_j   (all in double)  */
+void oracle_extend_attention(const float *q, const int32_t *q_indptr,
+                             const uint8_t *k_prefix, const uint8_t *v_prefix,
+                             const int32_t *kv_indptr, const int32_t *prefix_lens,
+                             const float *k_chunk, const float *v_chunk,
+                             int B, int Hq, int Hkv, int d, double sm_scale, double *out)
+{
+    int g = Hq / Hkv;
+    for (int b = 0; b < B; ++b) {
+        int c0 = q_indptr[b], C = q_indptr[b + 1] - q_indptr[b];
+        int P = prefix_lens[b];
+        size_t p0 = (size_t)kv_indptr[b];
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int ti = 0; ti < C * Hq; ++ti) {
+            int i = ti / Hq, hq = ti % Hq, h = hq / g;
+            const float *qv = q + ((size_t)(c0 + i) * Hq + hq) * d;
+            double *o = out + ((size_t)(c0 + i) * Hq + hq) * d;
+            int n = P + i + 1;
+            double smax = -INFINITY;
+            double *sc = (double *)malloc(sizeof(double) * (size_t)n);
+            for (int j = 0; j < n; ++j) {
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c) {
+                    double kv = j < P ? oracle_e4m3_value(k_prefix[((p0 + j) * Hkv + h) * d + c])
+                                      : (double)k_chunk[((size_t)(c0 + j - P) * Hkv + h) * d + c];
+                    dot += (double)qv[c] * kv;
+                }
+                sc[j] = dot * sm_scale;
+                if (sc[j] > smax)
+                    smax = sc[j];
+            }
+            double denom = 0.0;
+            for (int c = 0; c < d; ++c)
+                o[c] = 0.0;
+            for (int j = 0; j < n; ++j) {
+                double pj = exp(sc[j] - smax);
+                denom += pj;
+                for (int c = 0; c < d; ++c) {
+                    double vv = j < P ? oracle_e4m3_value(v_prefix[((p0 + j) * Hkv + h) * d + c])
+                                      : (double)v_chunk[((size_t)(c0 + j - P) * Hkv + h) * d + c];
+                    o[c] += pj * vv;
+                }
+            }
+            for (int c = 0; c < d; ++c)
+                o[c] /= denom;
+            free(sc);
+        }
+    }
 }
 
 /* ------------------------------------------------------------------------ */
