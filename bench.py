@@ -488,6 +488,7 @@ def other_rows(dev):
     qg_ms = timed(lambda: nv.nvfp4kv_quantize_append(cache_g, k, v, sm))
     d_bytes = L * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
     multi = multi_query_rows(dev, timed)
+    extend = extend_rows(dev)
     return {
         "quantize_append_8k_bf16": {"us": q_ms * 1e3, "tokens_per_s": T / (q_ms / 1e3),
                                     "alg_gbs": q_bytes / (q_ms / 1e3) / 1e9, "alg_bytes": q_bytes},
@@ -497,8 +498,58 @@ def other_rows(dev):
                               "decode_alg_gbs": d_bytes / (dg_ms / 1e3) / 1e9,
                               "quantize_append_8k_bf16_us": qg_ms * 1e3},
         "multi_query": multi,
+        "extend_160k_chunk8k": extend,
         "timing": "CUDA events per call, 256 MB buffer written before each call to evict L2",
     }
+
+
+def extend_flops(e) -> float:
+    """Algorithmic FLOPs of extend attention: 2 d for q.k and 2 d for p.v per
+    (chunk token, query head, visible key); token t sees P + t + 1 keys."""
+    tot = 0
+    for P, C in zip(e.prefix_lens, e.chunk_lens):
+        tot += C * P + C * (C + 1) // 2
+    return 4.0 * e.head_dim * e.num_q_heads * tot
+
+
+def extend_rows(dev):
+    """Extend attention of the last 8,192-token chunk of a 163,840-token
+    prefill (Hq 48, Hkv 8) over the 155,648-row FP8 prefix workspace (319 MB,
+    larger than L2) and the chunk, bf16 out; mean of 5 launches after 3
+    warm-ups, CUDA events on the launching stream."""
+    import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+    e = workloads.extend_make("ext160k")
+    x = workloads.extend_inputs(e, device=dev)
+    out = torch.empty((e.q_rows, e.num_q_heads, e.head_dim), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    mql = max(e.chunk_lens)
+
+    def call():
+        nv.nvfp4kv_extend_attention_fp8(x["q"], x["q_indptr"], x["k_prefix"], x["v_prefix"], x["kv_indptr"],
+                                        x["prefix_lens"], x["k_chunk"], x["v_chunk"], out, max_q_len=mql,
+                                        dev_status=status)
+    for _ in range(3):
+        call()
+    ms = []
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    t = statistics.mean(ms)
+    flops = extend_flops(e)
+    peaks = measured_peaks() or {}
+    peak = peaks.get("bf16_tflops")
+    src = "measured"
+    if peak is None:
+        peak, src = 1900.0, "fallback"
+    tf = flops / (t / 1e3) / 1e12
+    return {"us": t * 1e3, "chunk_tokens_per_s": e.q_rows / (t / 1e3), "alg_tflops": tf,
+            "alg_flops": flops, "bound": "tensor", "peak_tflops": peak, "peak_source": src,
+            "frac": tf / peak, "mma": "mma.sync m16n8k16 f16 (peak: bf16 dense, same rate)",
+            "device_status": int(status.item())}
 
 
 def multi_query_rows(dev, timed):

@@ -275,6 +275,48 @@ nvfp4kv_status nvfp4kv_dequant_prefix_fp8(const nvfp4kv_cache *cache,
                                           void *k_fp8_out, void *v_fp8_out,
                                           int32_t *dev_status, nvfp4kv_stream_t stream);
 
+/* Extend attention over the FP8 prefix workspace and the current chunk
+ * ("SGLang stores KV cache in 4 bits", Interpretation: the extend path
+ * dequantises the cached prefix into one FP8 workspace and attends over it
+ * together with the new chunk).  For sequence b with chunk rows
+ * [q_indptr[b], q_indptr[b+1]) and prefix length P = prefix_lens[b], chunk
+ * token t (row q_indptr[b] + t) and query head i (kv head h = i / g):
+ *   keys   = k_prefix[kv_indptr[b] + j][h] for j < P, then k_chunk[q_indptr[b] + u][h] for u <= t
+ *   values = the same rows of v_prefix / v_chunk
+ *   out[q_indptr[b] + t][i] = softmax_j(sm_scale * q . key_j) . value_j
+ * Prefix keys and values are E4M3 bytes (the workspace written by
+ * nvfp4kv_dequant_prefix_fp8, with the same kv_indptr and prefix_lens);
+ * chunk keys and values and q are bf16.
+ *   q        bf16 [q_rows][num_q_heads][128]
+ *   k_chunk, v_chunk  bf16 [q_rows][num_kv_heads][128]
+ *   out      [q_rows][num_q_heads][128], out_dtype bf16 or fp32; rows outside
+ *            every [q_indptr[b], q_indptr[b+1]) are not written
+ *   k_prefix, v_prefix  uint8 E4M3 [prefix_rows][num_kv_heads][128]
+ *   q_indptr int32 [batch + 1] (device), kv_indptr and prefix_lens int32
+ *            [batch] (device)
+ *   max_q_len  host bound on every q_indptr[b+1] - q_indptr[b]; it sizes the
+ *            launch
+ * Arithmetic: q * sm_scale * log2(e) and the chunk's keys and values are
+ * rounded to fp16 (exact for bf16 values of magnitude 2^-14 .. 65504; the
+ * caller keeps |q * sm_scale| and the chunk's values below 65504), E4M3 to
+ * fp16 is exact, scores and outputs accumulate in fp32, softmax weights are
+ * rounded to fp16 for the value product.
+ * Pointers 16-byte aligned (index arrays 4-byte).  Group g = num_q_heads /
+ * num_kv_heads in 1..8; batch and num_kv_heads at most 65535.  Device check:
+ * a sequence whose q_indptr range is not inside [0, q_rows] or longer than
+ * max_q_len, or whose prefix rows are not inside [0, prefix_rows), sets
+ * NVFP4KV_DEV_BAD_LEN and its output rows are not written.  A sequence with
+ * an empty chunk writes nothing; with an empty prefix it is causal
+ * attention over the chunk alone. */
+nvfp4kv_status nvfp4kv_extend_attention_fp8(const void *q, const int32_t *q_indptr, int32_t q_rows,
+                                            int32_t max_q_len, const void *k_prefix,
+                                            const void *v_prefix, const int32_t *kv_indptr,
+                                            const int32_t *prefix_lens, int64_t prefix_rows,
+                                            const void *k_chunk, const void *v_chunk, int32_t batch,
+                                            int32_t num_q_heads, int32_t num_kv_heads, float sm_scale,
+                                            void *out, nvfp4kv_dtype out_dtype, int32_t *dev_status,
+                                            nvfp4kv_stream_t stream);
+
 /* FP8-E4M3 comparison cache, written and read the same way ("NVFP4-KV-Cache
  * auf der ...", "Unterstuetzung in den Engines": the FP8 baseline runs with
  * --kv-cache-dtype fp8_e4m3; "Bytes pro Token": scales 1.0 uncalibrated).

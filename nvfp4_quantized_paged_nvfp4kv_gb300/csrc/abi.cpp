@@ -288,6 +288,65 @@ nvfp4kv_status nvfp4kv_dequant_prefix_fp8(const nvfp4kv_cache *cache, const int3
     return from_cuda(launch_dequant_prefix_fp8(p, to_cuda(stream)));
 }
 
+nvfp4kv_status nvfp4kv_extend_attention_fp8(const void *q, const int32_t *q_indptr, int32_t q_rows,
+                                            int32_t max_q_len, const void *k_prefix, const void *v_prefix,
+                                            const int32_t *kv_indptr, const int32_t *prefix_lens,
+                                            int64_t prefix_rows, const void *k_chunk, const void *v_chunk,
+                                            int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                            float sm_scale, void *out, nvfp4kv_dtype out_dtype,
+                                            int32_t *dev_status, nvfp4kv_stream_t stream)
+{
+    if (batch < 0 || q_rows < 0 || max_q_len < 0 || prefix_rows < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4KV_F32 && out_dtype != NVFP4KV_BF16)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale))
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    if (group > kMaxGroup || num_kv_heads > 65535 || batch > 65535)
+        return NVFP4KV_ERR_UNSUPPORTED;
+    // element offsets of q / out rows and the workspace stay within int64; rows
+    // of one sequence and kv head (chunk length x group) within int32
+    if (static_cast<int64_t>(max_q_len) * group > (int64_t{1} << 31) - kMaxGroup * 128)
+        return NVFP4KV_ERR_UNSUPPORTED;
+    if (prefix_rows > (int64_t{1} << 40) / (static_cast<int64_t>(num_kv_heads) * kHeadDim))
+        return NVFP4KV_ERR_UNSUPPORTED;
+    if (batch == 0 || max_q_len == 0)
+        return NVFP4KV_OK;
+    if (q == nullptr || q_indptr == nullptr || kv_indptr == nullptr || prefix_lens == nullptr || k_chunk == nullptr ||
+        v_chunk == nullptr || out == nullptr)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (prefix_rows > 0 && (k_prefix == nullptr || v_prefix == nullptr))
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_chunk) || !aligned16(v_chunk) || !aligned16(out) || !aligned16(k_prefix) ||
+        !aligned16(v_prefix) || (reinterpret_cast<uintptr_t>(q_indptr) & 3u) ||
+        (reinterpret_cast<uintptr_t>(kv_indptr) & 3u) || (reinterpret_cast<uintptr_t>(prefix_lens) & 3u))
+        return NVFP4KV_ERR_INVALID_ARG;
+    ExtendParams p{};
+    p.q = static_cast<const uint16_t *>(q);
+    p.q_indptr = q_indptr;
+    p.k_prefix = static_cast<const uint8_t *>(k_prefix);
+    p.v_prefix = static_cast<const uint8_t *>(v_prefix);
+    p.kv_indptr = kv_indptr;
+    p.prefix_lens = prefix_lens;
+    p.k_chunk = static_cast<const uint16_t *>(k_chunk);
+    p.v_chunk = static_cast<const uint16_t *>(v_chunk);
+    p.out = out;
+    p.dev_status = dev_status;
+    p.batch = batch;
+    p.hq = num_q_heads;
+    p.hkv = num_kv_heads;
+    p.group = group;
+    p.q_rows = q_rows;
+    p.max_q_len = max_q_len;
+    p.prefix_rows = prefix_rows;
+    p.qscale = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+    p.out_f32 = out_dtype == NVFP4KV_F32;
+    return from_cuda(launch_extend_attention(p, to_cuda(stream)));
+}
+
 nvfp4kv_status fp8kv_quantize_append(const fp8kv_cache *cache, const void *k_new, const void *v_new,
                                      nvfp4kv_dtype in_dtype, int32_t num_tokens, const int32_t *slot_mapping,
                                      int32_t *dev_status, nvfp4kv_stream_t stream)

@@ -81,6 +81,28 @@ struct PrefixParams {
     float gscale;                // tensor scale multiplying every value
 };
 
+struct ExtendParams {
+    const uint16_t *q;           // bf16 [q rows][hq][128]
+    const int32_t *q_indptr;     // [batch + 1] chunk row ranges
+    const uint8_t *k_prefix;     // E4M3 [prefix rows][hkv][128]
+    const uint8_t *v_prefix;
+    const int32_t *kv_indptr;    // [batch] first prefix row of each sequence
+    const int32_t *prefix_lens;  // [batch]
+    const uint16_t *k_chunk;     // bf16 [q rows][hkv][128]
+    const uint16_t *v_chunk;
+    void *out;                   // [q rows][hq][128], bf16 or fp32
+    int32_t *dev_status;
+    int batch;
+    int hq;
+    int hkv;
+    int group;                   // hq / hkv
+    int q_rows;                  // rows of q, k_chunk, v_chunk and out
+    int max_q_len;               // bound on every chunk length (sizes the grid)
+    int64_t prefix_rows;         // rows of the prefix workspace
+    float qscale;                // sm_scale * log2(e)
+    int out_f32;
+};
+
 // Launch with programmatic stream serialisation allowed, so the kernel's
 // prologue may overlap the tail of the previous kernel in the stream; every
 // kernel launched this way calls pdl_wait() before touching data that the
@@ -113,5 +135,6 @@ cudaError_t launch_decode_nvfp4_multi(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_merge(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_dequant_prefix_fp8(const PrefixParams &p, cudaStream_t s);
+cudaError_t launch_extend_attention(const ExtendParams &p, cudaStream_t s);
 
 } // namespace nvfp4kv

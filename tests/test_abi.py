@@ -133,6 +133,32 @@ def test_prefix_validation():
     assert f(ctypes.byref(c), FAKE, 4, FAKE, FAKE, 0, FAKE, FAKE, None, None) == nv.OK
 
 
+def extend(q=FAKE, qi=FAKE, rows=100, mql=50, kp=FAKE, vp=FAKE, ki=FAKE, pl=FAKE, prows=1000, kc=FAKE, vc=FAKE,
+           batch=2, hq=16, hkv=2, scale=0.088, out=FAKE, dtype=nv.BF16):
+    return nv.load().nvfp4kv_extend_attention_fp8(q, qi, rows, mql, kp, vp, ki, pl, prows, kc, vc, batch, hq,
+                                                  hkv, scale, out, dtype, None, None)
+
+
+def test_extend_validation():
+    assert extend(batch=-1) == nv.ERR_INVALID_ARG
+    assert extend(rows=-1) == nv.ERR_INVALID_ARG
+    assert extend(mql=-1) == nv.ERR_INVALID_ARG
+    assert extend(prows=-1) == nv.ERR_INVALID_ARG
+    assert extend(hq=5) == nv.ERR_INVALID_ARG                  # Hq % Hkv != 0
+    assert extend(hq=18) == nv.ERR_UNSUPPORTED                 # group 9 > 8
+    assert extend(batch=70000) == nv.ERR_UNSUPPORTED
+    assert extend(mql=1 << 30) == nv.ERR_UNSUPPORTED           # chunk rows x group past int32
+    assert extend(scale=float("inf")) == nv.ERR_INVALID_ARG
+    assert extend(dtype=3) == nv.ERR_INVALID_ARG
+    assert extend(q=None) == nv.ERR_INVALID_ARG
+    assert extend(kp=None) == nv.ERR_INVALID_ARG               # prefix rows but no workspace
+    assert extend(q=FAKE + 2) == nv.ERR_INVALID_ARG
+    assert extend(kc=FAKE + 8) == nv.ERR_INVALID_ARG
+    assert extend(qi=FAKE + 2) == nv.ERR_INVALID_ARG
+    assert extend(batch=0, q=None, qi=None, ki=None, pl=None, kc=None, vc=None, out=None) == nv.OK
+    assert extend(mql=0, q=None, out=None) == nv.OK
+
+
 def test_status_strings_and_version():
     for s in range(5):
         assert nv.status_string(s)

@@ -1,0 +1,151 @@
+"""GPU parity of the extend attention against the oracle.
+
+"SGLang stores KV cache in 4 bits" (LMSYS summary), Interpretation: the
+extend path attends each chunk token over its sequence's FP8 prefix workspace
+and the chunk up to itself.  Inputs come from workloads.extend_inputs; the
+oracle runs in fp64 on the same bytes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+import oracle
+import workloads
+from gpu_util import DEV, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def to_dev(x):
+    return {k: v.to(DEV) for k, v in x.items()}
+
+
+def oracle_out(e, x):
+    return oracle.extend_attention(x["q"].float().numpy(), x["q_indptr"].numpy(), x["k_prefix"].numpy(),
+                                   x["v_prefix"].numpy(), x["kv_indptr"].numpy(), x["prefix_lens"].numpy(),
+                                   x["k_chunk"].float().numpy(), x["v_chunk"].float().numpy())
+
+
+def run(e, xd, out_dtype=torch.float32, max_q_len=None, status=None, out=None):
+    if out is None:
+        out = torch.full((e.q_rows, e.num_q_heads, e.head_dim), float("nan"), dtype=out_dtype, device=DEV)
+    nv.nvfp4kv_extend_attention_fp8(xd["q"], xd["q_indptr"], xd["k_prefix"], xd["v_prefix"], xd["kv_indptr"],
+                                    xd["prefix_lens"], xd["k_chunk"], xd["v_chunk"], out,
+                                    max_q_len=max(e.chunk_lens) if max_q_len is None else max_q_len,
+                                    dev_status=status)
+    torch.cuda.synchronize()
+    return out
+
+
+CASES = [
+    # (prefix_lens, chunk_lens, Hq, Hkv): ragged prefixes across 64-key tiles,
+    # chunks across 128-row tiles, groups 1, 3, 6 and 8
+    ((0, 61, 200, 1000), (130, 1, 77, 64), 48, 8),
+    ((64, 65), (128, 129), 8, 8),
+    ((300,), (257,), 24, 8),
+    ((0,), (300,), 8, 1),
+    ((5, 0, 127), (0, 16, 40), 16, 2),
+]
+
+
+@pytest.mark.parametrize("prefix_lens,chunk_lens,hq,hkv", CASES)
+def test_extend_matches_oracle(prefix_lens, chunk_lens, hq, hkv):
+    e = workloads.extend_custom(prefix_lens, chunk_lens, hq, hkv, seed=len(prefix_lens) + hq)
+    x = workloads.extend_inputs(e)
+    want = oracle_out(e, x)
+    got = run(e, to_dev(x)).cpu().numpy()
+    assert_close(got, want, "extend fp32 out")
+
+
+def test_extend_bf16_output():
+    e = workloads.extend_make("ext_small")
+    x = workloads.extend_inputs(e)
+    want = oracle_out(e, x)
+    got = run(e, to_dev(x), out_dtype=torch.bfloat16).float().cpu().numpy()
+    assert_close(got, want, "extend bf16 out")
+
+
+def test_extend_leaves_rows_outside_the_chunks_untouched():
+    """Rows before q_indptr[0] and from q_indptr[batch] on keep their contents."""
+    e = workloads.extend_custom((40, 70), (20, 30), 16, 2, seed=5)
+    x = workloads.extend_inputs(e)
+    want = oracle_out(e, x)
+    xd = to_dev(x)
+    lead, tail = 5, 4
+    pad = lambda t: torch.cat([torch.zeros((lead,) + t.shape[1:], dtype=t.dtype, device=DEV), t,
+                               torch.zeros((tail,) + t.shape[1:], dtype=t.dtype, device=DEV)])
+    for k in ("q", "k_chunk", "v_chunk"):
+        xd[k] = pad(xd[k])
+    xd["q_indptr"] = xd["q_indptr"] + lead
+    out = torch.full((lead + e.q_rows + tail, 16, 128), 7.0, device=DEV)
+    run(e, xd, out=out)
+    got = out.cpu().numpy()
+    assert (got[:lead] == 7.0).all() and (got[lead + e.q_rows:] == 7.0).all()
+    assert_close(got[lead:lead + e.q_rows], want, "extend with offset rows")
+
+
+def test_extend_device_checks():
+    """A chunk range outside q_rows, longer than max_q_len, or prefix rows
+    outside the workspace sets NVFP4KV_DEV_BAD_LEN; that sequence writes
+    nothing while the others are computed."""
+    e = workloads.extend_custom((30, 50), (10, 12), 8, 2, seed=9)
+    x = workloads.extend_inputs(e)
+    want = oracle_out(e, x)
+    for bad in ("q_end", "too_long", "prefix"):
+        xd = to_dev(x)
+        max_q_len = 12
+        if bad == "q_end":
+            xd["q_indptr"] = torch.tensor([0, 10, e.q_rows + 1], dtype=torch.int32, device=DEV)
+        elif bad == "too_long":
+            max_q_len = 11
+        else:
+            xd["prefix_lens"] = torch.tensor([30, e.prefix_rows], dtype=torch.int32, device=DEV)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        out = torch.full((e.q_rows, 8, 128), 5.0, device=DEV)
+        run(e, xd, max_q_len=max_q_len, status=status, out=out)
+        assert status.item() == nv.DEV_BAD_LEN, bad
+        got = out.cpu().numpy()
+        assert (got[10:] == 5.0).all(), bad
+        assert_close(got[:10], want[:10], f"extend good sequence next to a bad one ({bad})")
+
+
+def test_extend_empty_inputs():
+    e = workloads.extend_custom((4,), (0,), 8, 2, seed=1)
+    x = to_dev(workloads.extend_inputs(e))
+    out = torch.zeros((0, 8, 128), device=DEV)
+    nv.nvfp4kv_extend_attention_fp8(x["q"], x["q_indptr"], x["k_prefix"], x["v_prefix"], x["kv_indptr"],
+                                    x["prefix_lens"], x["k_chunk"], x["v_chunk"], out, max_q_len=0)
+    torch.cuda.synchronize()
+
+
+def test_extend_full_size_sampled_tokens():
+    """The 160K workload in the launch configuration the bench times.  Chunk
+    K/V are drawn as E4M3 codes (held in bf16, exactly), so the oracle can
+    take chunk token t alone: its keys are the prefix rows followed by the
+    codes of chunk tokens 0 .. t-1, then token t itself."""
+    e = workloads.extend_make("ext160k")
+    xd = to_dev(workloads.extend_inputs(e, device=DEV))
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(1234)
+    kc = workloads.e4m3_codes((e.q_rows, e.num_kv_heads, 128), gen, DEV)
+    vc = workloads.e4m3_codes((e.q_rows, e.num_kv_heads, 128), gen, DEV)
+    xd["k_chunk"] = kc.view(torch.float8_e4m3fn).to(torch.bfloat16)
+    xd["v_chunk"] = vc.view(torch.float8_e4m3fn).to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(e, xd, out_dtype=torch.bfloat16, status=status)
+    assert status.item() == 0
+    P, p0 = e.prefix_lens[0], int(e.kv_indptr()[0])
+    kp = xd["k_prefix"][p0:p0 + P].cpu().numpy()
+    vp = xd["v_prefix"][p0:p0 + P].cpu().numpy()
+    kcn, vcn = kc.cpu().numpy(), vc.cpu().numpy()
+    q = xd["q"].float().cpu().numpy()
+    got = out.float().cpu().numpy()
+    for t in (0, 63, 64, 4097, 8191):
+        k_pre = np.concatenate([kp, kcn[:t]])
+        v_pre = np.concatenate([vp, vcn[:t]])
+        kt = torch.from_numpy(kcn[t:t + 1]).view(torch.float8_e4m3fn).float().numpy()
+        vt = torch.from_numpy(vcn[t:t + 1]).view(torch.float8_e4m3fn).float().numpy()
+        want = oracle.extend_attention(q[t:t + 1], np.int32([0, 1]), k_pre, v_pre, np.int32([0]),
+                                       np.int32([P + t]), kt, vt)
+        assert_close(got[t:t + 1], want, f"ext160k token {t}")

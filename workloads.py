@@ -203,3 +203,94 @@ def new_tokens(w: Workload, T: int, device="cpu", salt: str = "new"):
     k = torch.randn((T, w.num_kv_heads, w.head_dim), generator=gen, device=device)
     v = torch.randn((T, w.num_kv_heads, w.head_dim), generator=gen, device=device)
     return k, v
+
+
+# --- extend path -------------------------------------------------------------
+#
+# The extend step attends a chunk of new tokens over its sequence's prefix,
+# held in the FP8 workspace, and over the chunk itself.  Inputs: bf16 queries
+# and chunk K/V ~ N(0,1); workspace rows of random finite E4M3 codes (sign
+# random, exponent field uniform in 1..8, mantissa uniform, 1 in 32 zero), i.e.
+# magnitudes log-uniform in [2^-6, 3.75].  Sequences sit in the workspace with
+# EXTEND_GAP unused rows before each, so their row offsets are not contiguous.
+
+EXTEND_GAP = 3
+
+
+@dataclasses.dataclass(frozen=True)
+class ExtendWorkload:
+    name: str
+    prefix_lens: tuple
+    chunk_lens: tuple
+    num_q_heads: int
+    num_kv_heads: int
+    seed: int
+    head_dim: int = HEAD_DIM
+
+    @property
+    def batch(self) -> int:
+        return len(self.prefix_lens)
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def q_rows(self) -> int:
+        return int(sum(self.chunk_lens))
+
+    @property
+    def prefix_rows(self) -> int:
+        return int(sum(self.prefix_lens)) + EXTEND_GAP * (self.batch + 1)
+
+    def q_indptr(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.chunk_lens)]).astype(np.int32)
+
+    def kv_indptr(self) -> np.ndarray:
+        starts = EXTEND_GAP * np.arange(1, self.batch + 1) + np.concatenate([[0], np.cumsum(self.prefix_lens)[:-1]])
+        return starts.astype(np.int32)
+
+
+def extend_make(name: str) -> ExtendWorkload:
+    """ext160k: the last 8,192-token chunk of a 163,840-token prefill (Hq=48,
+    Hkv=8), prefix 155,648.  ext_small: four ragged sequences."""
+    if name == "ext160k":
+        return ExtendWorkload(name, (163840 - 8192,), (8192,), 48, 8, seed=_seed("ext160k"))
+    if name == "ext_small":
+        return ExtendWorkload(name, (0, 61, 200, 1000), (130, 1, 77, 64), 48, 8, seed=_seed("ext_small"))
+    raise ValueError(name)
+
+
+def extend_custom(prefix_lens, chunk_lens, num_q_heads, num_kv_heads, seed=11) -> ExtendWorkload:
+    return ExtendWorkload("custom", tuple(int(x) for x in prefix_lens), tuple(int(x) for x in chunk_lens),
+                          num_q_heads, num_kv_heads, seed=seed)
+
+
+def e4m3_codes(shape, gen, device="cpu") -> torch.Tensor:
+    """Random finite E4M3 bytes as described above (uint8)."""
+    e = torch.randint(1, 9, shape, generator=gen, device=device, dtype=torch.int32)
+    m = torch.randint(0, 8, shape, generator=gen, device=device, dtype=torch.int32)
+    s = torch.randint(0, 2, shape, generator=gen, device=device, dtype=torch.int32)
+    z = torch.randint(0, 32, shape, generator=gen, device=device, dtype=torch.int32) == 0
+    code = (s << 7) | (e << 3) | m
+    return torch.where(z, torch.zeros_like(code), code).to(torch.uint8)
+
+
+def extend_inputs(e: ExtendWorkload, device="cpu") -> dict:
+    """q (bf16 [rows][Hq][d]), k_chunk / v_chunk (bf16 [rows][Hkv][d]),
+    k_prefix / v_prefix (uint8 E4M3 [prefix rows][Hkv][d]) and the int32 index
+    arrays q_indptr, kv_indptr, prefix_lens."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(_seed(e.seed, "extend"))
+    rows, d = e.q_rows, e.head_dim
+    out = {
+        "q": torch.randn((rows, e.num_q_heads, d), generator=gen, device=device).to(torch.bfloat16),
+        "k_chunk": torch.randn((rows, e.num_kv_heads, d), generator=gen, device=device).to(torch.bfloat16),
+        "v_chunk": torch.randn((rows, e.num_kv_heads, d), generator=gen, device=device).to(torch.bfloat16),
+        "k_prefix": e4m3_codes((e.prefix_rows, e.num_kv_heads, d), gen, device),
+        "v_prefix": e4m3_codes((e.prefix_rows, e.num_kv_heads, d), gen, device),
+    }
+    for k, v in (("q_indptr", e.q_indptr()), ("kv_indptr", e.kv_indptr()),
+                 ("prefix_lens", np.asarray(e.prefix_lens, np.int32))):
+        out[k] = torch.from_numpy(v).to(device)
+    return out
