@@ -539,6 +539,35 @@ def extend_rows(dev):
         torch.cuda.synchronize()
         ms.append(a.elapsed_time(b))
     t = statistics.mean(ms)
+
+    # the same step fused with the NVFP4 write of the chunk, against the
+    # attention followed by a separate quantize_append
+    P = e.prefix_lens[0]
+    cache = nv.NVFP4Cache.allocate((P + e.q_rows) // 16 + 1, e.num_kv_heads, device=dev, zero=False)
+    slots = torch.arange(P, P + e.q_rows, dtype=torch.int32, device=dev)
+    args = (x["q"], x["q_indptr"], x["k_prefix"], x["v_prefix"], x["kv_indptr"], x["prefix_lens"],
+            x["k_chunk"], x["v_chunk"], out)
+
+    def fused():
+        nv.nvfp4kv_extend_attention_fp8_append(cache, slots, *args, max_q_len=mql, dev_status=status)
+
+    def separate():
+        nv.nvfp4kv_extend_attention_fp8(*args, max_q_len=mql, dev_status=status)
+        nv.nvfp4kv_quantize_append(cache, x["k_chunk"], x["v_chunk"], slots, status)
+
+    def mean_ms(fn):
+        for _ in range(2):
+            fn()
+        res = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            res.append(a.elapsed_time(b))
+        return statistics.mean(res)
+    f_ms, s_ms = mean_ms(fused), mean_ms(separate)
     flops = extend_flops(e)
     peaks = measured_peaks() or {}
     peak = peaks.get("bf16_tflops")
@@ -549,6 +578,7 @@ def extend_rows(dev):
     return {"us": t * 1e3, "chunk_tokens_per_s": e.q_rows / (t / 1e3), "alg_tflops": tf,
             "alg_flops": flops, "bound": "tensor", "peak_tflops": peak, "peak_source": src,
             "frac": tf / peak, "mma": "mma.sync m16n8k16 f16 (peak: bf16 dense, same rate)",
+            "fused_append_us": f_ms * 1e3, "attention_then_quantize_append_us": s_ms * 1e3,
             "device_status": int(status.item())}
 
 

@@ -317,6 +317,28 @@ nvfp4kv_status nvfp4kv_extend_attention_fp8(const void *q, const int32_t *q_indp
                                             void *out, nvfp4kv_dtype out_dtype, int32_t *dev_status,
                                             nvfp4kv_stream_t stream);
 
+/* Extend attention fused with the NVFP4 write of the chunk ("SGLang stores KV
+ * cache in 4 bits", Interpretation: prefill quantises the new K/V into the
+ * cache; the fusion removes the separate read of the chunk).  Computes out
+ * exactly as nvfp4kv_extend_attention_fp8 (num_kv_heads taken from the cache)
+ * and writes chunk row r's K and V into slot slot_mapping[r] of the cache, as
+ * nvfp4kv_quantize_append would with in_dtype bf16 (same blocks, same bytes,
+ * same tensor scale; slot < 0 skips the token, a slot >= num_pages *
+ * page_size is skipped and sets NVFP4KV_DEV_BAD_SLOT).  slot_mapping: int32
+ * [q_rows] (device, 4-byte aligned), read only for rows inside a sequence's
+ * q_indptr range; slots must be distinct.  The prefix workspace must not
+ * overlap the cache. */
+nvfp4kv_status nvfp4kv_extend_attention_fp8_append(const nvfp4kv_cache *cache,
+                                                   const int32_t *slot_mapping, const void *q,
+                                                   const int32_t *q_indptr, int32_t q_rows,
+                                                   int32_t max_q_len, const void *k_prefix,
+                                                   const void *v_prefix, const int32_t *kv_indptr,
+                                                   const int32_t *prefix_lens, int64_t prefix_rows,
+                                                   const void *k_chunk, const void *v_chunk,
+                                                   int32_t batch, int32_t num_q_heads, float sm_scale,
+                                                   void *out, nvfp4kv_dtype out_dtype,
+                                                   int32_t *dev_status, nvfp4kv_stream_t stream);
+
 /* FP8-E4M3 comparison cache, written and read the same way ("NVFP4-KV-Cache
  * auf der ...", "Unterstuetzung in den Engines": the FP8 baseline runs with
  * --kv-cache-dtype fp8_e4m3; "Bytes pro Token": scales 1.0 uncalibrated).

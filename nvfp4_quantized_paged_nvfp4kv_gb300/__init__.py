@@ -106,6 +106,9 @@ def load(build_if_missing: bool = True):
                                                  _vp, _vp, _vp, _vp]),
             "nvfp4kv_extend_attention_fp8": (_st, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, ctypes.c_int64, _vp,
                                                    _vp, _i32, _i32, _i32, ctypes.c_float, _vp, _st, _vp, _vp]),
+            "nvfp4kv_extend_attention_fp8_append": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _vp, _vp, _i32, _i32,
+                                                          _vp, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp, _i32,
+                                                          _i32, ctypes.c_float, _vp, _st, _vp, _vp]),
             "fp8kv_quantize_append": (_st, [ctypes.POINTER(_Fp8Cache), _vp, _vp, _st, _i32, _vp, _vp, _vp]),
             "fp8kv_paged_decode": (_st, [ctypes.POINTER(_Fp8Cache), _vp, _i32, _i32, _vp, _i32, _vp,
                                          ctypes.c_float, _vp, _st, _vp, ctypes.c_size_t, _i32, _vp, _vp]),
@@ -327,6 +330,24 @@ def nvfp4kv_extend_attention_fp8(q, q_indptr, k_prefix, v_prefix, kv_indptr, pre
         _ptr(prefix_lens), k_prefix.shape[0], _ptr(k_chunk), _ptr(v_chunk), B, Hq, Hkv, float(sm_scale),
         _ptr(out), _dtype_code(out), _ptr(dev_status), _stream(stream))
     _check(st, "nvfp4kv_extend_attention_fp8")
+
+
+def nvfp4kv_extend_attention_fp8_append(cache: NVFP4Cache, slot_mapping, q, q_indptr, k_prefix, v_prefix,
+                                        kv_indptr, prefix_lens, k_chunk, v_chunk, out, max_q_len=None,
+                                        sm_scale=None, dev_status=None, stream=None) -> None:
+    """nvfp4kv_extend_attention_fp8 that also writes the chunk's K/V (bf16) into
+    the NVFP4 cache at slot_mapping (int32 [rows], device)."""
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    rows, Hq, _ = q.shape
+    B = prefix_lens.shape[0]
+    if max_q_len is None:
+        max_q_len = int((q_indptr[1:] - q_indptr[:-1]).max().item()) if B > 0 else 0
+    st = load().nvfp4kv_extend_attention_fp8_append(
+        cache.c, _ptr(slot_mapping), _ptr(q), _ptr(q_indptr), rows, int(max_q_len), _ptr(k_prefix),
+        _ptr(v_prefix), _ptr(kv_indptr), _ptr(prefix_lens), k_prefix.shape[0], _ptr(k_chunk), _ptr(v_chunk), B,
+        Hq, float(sm_scale), _ptr(out), _dtype_code(out), _ptr(dev_status), _stream(stream))
+    _check(st, "nvfp4kv_extend_attention_fp8_append")
 
 
 def nvfp4kv_cache_bytes(num_pages, num_kv_heads, page_size=PAGE_SIZE, head_dim=HEAD_DIM) -> int:

@@ -164,6 +164,67 @@ void apply_tensor_scale(DecodeParams &p, float sm_scale, float G)
     p.gscale = G;
 }
 
+// Extend arguments common to both entry points.  Fills p (attention part)
+// on success; batch == 0 or max_q_len == 0 is valid and launches nothing.
+nvfp4kv_status check_extend(const void *q, const int32_t *q_indptr, int32_t q_rows, int32_t max_q_len,
+                            const void *k_prefix, const void *v_prefix, const int32_t *kv_indptr,
+                            const int32_t *prefix_lens, int64_t prefix_rows, const void *k_chunk,
+                            const void *v_chunk, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                            float sm_scale, void *out, nvfp4kv_dtype out_dtype, int32_t *dev_status,
+                            ExtendParams &p)
+{
+    if (batch < 0 || q_rows < 0 || max_q_len < 0 || prefix_rows < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4KV_F32 && out_dtype != NVFP4KV_BF16)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale))
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    if (group > kMaxGroup || num_kv_heads > 65535 || batch > 65535)
+        return NVFP4KV_ERR_UNSUPPORTED;
+    // rows of one sequence and kv head (chunk length x group) stay within
+    // int32; workspace element offsets within int64
+    if (static_cast<int64_t>(max_q_len) * group > (int64_t{1} << 31) - kMaxGroup * 128)
+        return NVFP4KV_ERR_UNSUPPORTED;
+    if (prefix_rows > (int64_t{1} << 40) / (static_cast<int64_t>(num_kv_heads) * kHeadDim))
+        return NVFP4KV_ERR_UNSUPPORTED;
+    if (batch == 0 || max_q_len == 0)
+        return NVFP4KV_OK;
+    if (q == nullptr || q_indptr == nullptr || kv_indptr == nullptr || prefix_lens == nullptr || k_chunk == nullptr ||
+        v_chunk == nullptr || out == nullptr)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (prefix_rows > 0 && (k_prefix == nullptr || v_prefix == nullptr))
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_chunk) || !aligned16(v_chunk) || !aligned16(out) || !aligned16(k_prefix) ||
+        !aligned16(v_prefix) || (reinterpret_cast<uintptr_t>(q_indptr) & 3u) ||
+        (reinterpret_cast<uintptr_t>(kv_indptr) & 3u) || (reinterpret_cast<uintptr_t>(prefix_lens) & 3u))
+        return NVFP4KV_ERR_INVALID_ARG;
+    p = ExtendParams{};
+    p.q = static_cast<const uint16_t *>(q);
+    p.q_indptr = q_indptr;
+    p.k_prefix = static_cast<const uint8_t *>(k_prefix);
+    p.v_prefix = static_cast<const uint8_t *>(v_prefix);
+    p.kv_indptr = kv_indptr;
+    p.prefix_lens = prefix_lens;
+    p.k_chunk = static_cast<const uint16_t *>(k_chunk);
+    p.v_chunk = static_cast<const uint16_t *>(v_chunk);
+    p.out = out;
+    p.dev_status = dev_status;
+    p.batch = batch;
+    p.hq = num_q_heads;
+    p.hkv = num_kv_heads;
+    p.group = group;
+    p.q_rows = q_rows;
+    p.max_q_len = max_q_len;
+    p.prefix_rows = prefix_rows;
+    p.qscale = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+    p.out_f32 = out_dtype == NVFP4KV_F32;
+    p.gscale = 1.f;
+    return NVFP4KV_OK;
+}
+
 } // namespace
 
 extern "C" {
@@ -296,54 +357,39 @@ nvfp4kv_status nvfp4kv_extend_attention_fp8(const void *q, const int32_t *q_indp
                                             float sm_scale, void *out, nvfp4kv_dtype out_dtype,
                                             int32_t *dev_status, nvfp4kv_stream_t stream)
 {
-    if (batch < 0 || q_rows < 0 || max_q_len < 0 || prefix_rows < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
-        return NVFP4KV_ERR_INVALID_ARG;
-    if (out_dtype != NVFP4KV_F32 && out_dtype != NVFP4KV_BF16)
-        return NVFP4KV_ERR_INVALID_ARG;
-    if (!std::isfinite(sm_scale))
-        return NVFP4KV_ERR_INVALID_ARG;
-    if (num_q_heads % num_kv_heads != 0)
-        return NVFP4KV_ERR_INVALID_ARG;
-    const int group = num_q_heads / num_kv_heads;
-    if (group > kMaxGroup || num_kv_heads > 65535 || batch > 65535)
-        return NVFP4KV_ERR_UNSUPPORTED;
-    // element offsets of q / out rows and the workspace stay within int64; rows
-    // of one sequence and kv head (chunk length x group) within int32
-    if (static_cast<int64_t>(max_q_len) * group > (int64_t{1} << 31) - kMaxGroup * 128)
-        return NVFP4KV_ERR_UNSUPPORTED;
-    if (prefix_rows > (int64_t{1} << 40) / (static_cast<int64_t>(num_kv_heads) * kHeadDim))
-        return NVFP4KV_ERR_UNSUPPORTED;
-    if (batch == 0 || max_q_len == 0)
-        return NVFP4KV_OK;
-    if (q == nullptr || q_indptr == nullptr || kv_indptr == nullptr || prefix_lens == nullptr || k_chunk == nullptr ||
-        v_chunk == nullptr || out == nullptr)
-        return NVFP4KV_ERR_INVALID_ARG;
-    if (prefix_rows > 0 && (k_prefix == nullptr || v_prefix == nullptr))
-        return NVFP4KV_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_chunk) || !aligned16(v_chunk) || !aligned16(out) || !aligned16(k_prefix) ||
-        !aligned16(v_prefix) || (reinterpret_cast<uintptr_t>(q_indptr) & 3u) ||
-        (reinterpret_cast<uintptr_t>(kv_indptr) & 3u) || (reinterpret_cast<uintptr_t>(prefix_lens) & 3u))
-        return NVFP4KV_ERR_INVALID_ARG;
     ExtendParams p{};
-    p.q = static_cast<const uint16_t *>(q);
-    p.q_indptr = q_indptr;
-    p.k_prefix = static_cast<const uint8_t *>(k_prefix);
-    p.v_prefix = static_cast<const uint8_t *>(v_prefix);
-    p.kv_indptr = kv_indptr;
-    p.prefix_lens = prefix_lens;
-    p.k_chunk = static_cast<const uint16_t *>(k_chunk);
-    p.v_chunk = static_cast<const uint16_t *>(v_chunk);
-    p.out = out;
-    p.dev_status = dev_status;
-    p.batch = batch;
-    p.hq = num_q_heads;
-    p.hkv = num_kv_heads;
-    p.group = group;
-    p.q_rows = q_rows;
-    p.max_q_len = max_q_len;
-    p.prefix_rows = prefix_rows;
-    p.qscale = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
-    p.out_f32 = out_dtype == NVFP4KV_F32;
+    const nvfp4kv_status st =
+        check_extend(q, q_indptr, q_rows, max_q_len, k_prefix, v_prefix, kv_indptr, prefix_lens, prefix_rows,
+                     k_chunk, v_chunk, batch, num_q_heads, num_kv_heads, sm_scale, out, out_dtype, dev_status, p);
+    if (st != NVFP4KV_OK || batch == 0 || max_q_len == 0)
+        return st;
+    return from_cuda(launch_extend_attention(p, to_cuda(stream)));
+}
+
+nvfp4kv_status nvfp4kv_extend_attention_fp8_append(const nvfp4kv_cache *cache, const int32_t *slot_mapping,
+                                                   const void *q, const int32_t *q_indptr, int32_t q_rows,
+                                                   int32_t max_q_len, const void *k_prefix, const void *v_prefix,
+                                                   const int32_t *kv_indptr, const int32_t *prefix_lens,
+                                                   int64_t prefix_rows, const void *k_chunk, const void *v_chunk,
+                                                   int32_t batch, int32_t num_q_heads, float sm_scale, void *out,
+                                                   nvfp4kv_dtype out_dtype, int32_t *dev_status,
+                                                   nvfp4kv_stream_t stream)
+{
+    nvfp4kv_status st = check_nvfp4(cache);
+    if (st != NVFP4KV_OK)
+        return st;
+    ExtendParams p{};
+    st = check_extend(q, q_indptr, q_rows, max_q_len, k_prefix, v_prefix, kv_indptr, prefix_lens, prefix_rows,
+                      k_chunk, v_chunk, batch, num_q_heads, cache->num_kv_heads, sm_scale, out, out_dtype,
+                      dev_status, p);
+    if (st != NVFP4KV_OK || batch == 0 || max_q_len == 0)
+        return st;
+    if (slot_mapping == nullptr || (reinterpret_cast<uintptr_t>(slot_mapping) & 3u))
+        return NVFP4KV_ERR_INVALID_ARG;
+    p.pool = static_cast<uint8_t *>(cache->pool);
+    p.slot_mapping = slot_mapping;
+    p.num_pages = cache->num_pages;
+    p.gscale = cache->global_scale;
     return from_cuda(launch_extend_attention(p, to_cuda(stream)));
 }
 

@@ -14,7 +14,14 @@
 // into Q.  The CTA converts every key tile once into f16 shared memory
 // (E4M3 -> f16 and bf16 -> f16, both exact in range), double buffered, while
 // the next tile's raw bytes are in flight by cp.async.
-#include "device_common.cuh"
+//
+// The appending variant also writes the chunk's K/V into the NVFP4 cache
+// ("SGLang stores KV cache in 4 bits", Interpretation: prefill quantises the
+// new K/V into the cache): each chunk key tile has one owning CTA, which
+// stages it through shared memory and quantises it before its attention loop.
+// Every row tile of a kv head reads the same chunk tiles, so the chunk stays
+// in L2 and no separate pass over it is needed.
+#include "record_write.cuh"
 
 namespace nvfp4kv {
 namespace {
@@ -177,6 +184,83 @@ __device__ __forceinline__ void store_tile(const ExtCta &c, int i, uint32_t stag
     }
 }
 
+// Page-head record and token of a chunk token's slot; false when the slot is
+// skipped (negative) or out of range (reported when `rep`).
+__device__ __forceinline__ bool append_site(const ExtendParams &p, int slot, int h, size_t &rec, int &tok, bool rep)
+{
+    if (slot < 0)
+        return false;
+    if (slot >= p.num_pages * kPageSize) {
+        if (rep)
+            report(p.dev_status, NVFP4KV_DEV_BAD_SLOT);
+        return false;
+    }
+    const int page = slot / kPageSize;
+    tok = slot - page * kPageSize;
+    rec = (static_cast<size_t>(page) * p.hkv + h) * kNvfp4Record;
+    return true;
+}
+
+__device__ __forceinline__ void staged_block(const uint8_t *src, float (&x)[16], float G)
+{
+    RawBlock<true> r;
+    r.v[0] = *reinterpret_cast<const uint4 *>(src);
+    r.v[1] = *reinterpret_cast<const uint4 *>(src + 16);
+    unpack<true>(r, x);
+    divide_by_tensor_scale(x, G);
+}
+
+// Quantise chunk keys k0 .. k0 + 63 of kv head h from the staged raw tile (K
+// rows at `raw`, V rows at raw + 64 * 256, 256 bytes a key) into the cache.
+// K: 64 keys x 8 blocks, two a thread.  V: 32 key pairs x 8 blocks, one a
+// thread; a pair on an even slot and its successor is written whole, any
+// other token through the atomic nibble merge.
+__device__ __forceinline__ void append_tile(const ExtendParams &p, const ExtCta &c, int h, int k0, const uint8_t *raw)
+{
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int item = tid + kExtThreads * u;
+        const int key = item >> 3, blk = item & 7;
+        if (k0 + key >= c.C)
+            continue;
+        size_t rec;
+        int tok;
+        if (!append_site(p, p.slot_mapping[c.c0 + k0 + key], h, rec, tok, blk == 0))
+            continue;
+        float x[16];
+        staged_block(raw + key * 256 + blk * 32, x, p.gscale);
+        write_nvfp4_block(p.pool + rec, false, tok, blk, x);
+    }
+    const int key0 = 2 * (tid >> 3), blk = tid & 7;
+    const uint8_t *vraw = raw + kExtKeys * 256;
+    const bool has0 = k0 + key0 < c.C, has1 = k0 + key0 + 1 < c.C;
+    const int s0 = has0 ? p.slot_mapping[c.c0 + k0 + key0] : -1;
+    const int s1 = has1 ? p.slot_mapping[c.c0 + k0 + key0 + 1] : -1;
+    size_t rec0 = 0, rec1 = 0;
+    int tok0 = 0, tok1 = 0;
+    const bool ok0 = has0 && append_site(p, s0, h, rec0, tok0, false);
+    const bool ok1 = has1 && append_site(p, s1, h, rec1, tok1, false);
+    float x[16];
+    if (ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
+        uint32_t S0, S1, c0[2], c1[2];
+        staged_block(vraw + key0 * 256 + blk * 32, x, p.gscale);
+        quantize_block(x, S0, c0);
+        staged_block(vraw + (key0 + 1) * 256 + blk * 32, x, p.gscale);
+        quantize_block(x, S1, c1);
+        write_nvfp4_v_pair(p.pool + rec0, tok0, blk, S0, c0, S1, c1);
+        return;
+    }
+    if (ok0) {
+        staged_block(vraw + key0 * 256 + blk * 32, x, p.gscale);
+        write_nvfp4_block(p.pool + rec0, true, tok0, blk, x);
+    }
+    if (ok1) {
+        staged_block(vraw + (key0 + 1) * 256 + blk * 32, x, p.gscale);
+        write_nvfp4_block(p.pool + rec1, true, tok1, blk, x);
+    }
+}
+
 // One key tile for one warp's 16 rows.  lim_a / lim_b: keys of the tile that
 // rows a (lane / 4) and b (lane / 4 + 8) see, counted from the tile's start;
 // only read when `masked`.
@@ -275,6 +359,7 @@ __device__ __forceinline__ void tile_step(uint32_t kbuf, uint32_t vbuf, const ui
     }
 }
 
+template <bool kAppend>
 __global__ void __launch_bounds__(kExtThreads, 1) extend_kernel(const ExtendParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -307,6 +392,10 @@ __global__ void __launch_bounds__(kExtThreads, 1) extend_kernel(const ExtendPara
     const int t_max = (row_end - 1) / g;
     c.n_pre = (c.P + kExtKeys - 1) / kExtKeys;
     c.n_tiles = c.n_pre + t_max / kExtKeys + 1;
+    // chunk key tiles this CTA appends: those whose first key's first row
+    // (64 kt g) falls in its row range
+    const int own_lo = (row0 + kExtKeys * g - 1) / (kExtKeys * g);
+    const int own_hi = (row0 + kExtRows + kExtKeys * g - 1) / (kExtKeys * g);
 
     // this lane's two rows; rows past the end repeat the last row and are not stored
     const int r_a = row0 + 16 * warp + (lane >> 2);
@@ -344,6 +433,17 @@ __global__ void __launch_bounds__(kExtThreads, 1) extend_kernel(const ExtendPara
 
     const uint32_t sbase = smem_addr(smem);
     const uint32_t stage = sbase + kF16Bytes;
+    if constexpr (kAppend) {
+        // the chunk key tiles this CTA owns go into the cache first, staged
+        // through the same area; the attention below reads them from L2
+        for (int kt = own_lo; kt < own_hi && kt * kExtKeys < c.C; ++kt) {
+            load_tile(p, c, h, c.n_pre + kt, stage);
+            cp_async_wait_all();
+            __syncthreads();
+            append_tile(p, c, h, kt * kExtKeys, smem + kF16Bytes);
+            __syncthreads();
+        }
+    }
     load_tile(p, c, h, 0, stage);
     store_tile(c, 0, stage, sbase);
     __syncthreads();
@@ -410,12 +510,13 @@ __global__ void __launch_bounds__(kExtThreads, 1) extend_kernel(const ExtendPara
 cudaError_t launch_extend_attention(const ExtendParams &p, cudaStream_t s)
 {
     static_assert(kExtSmem <= 227 * 1024, "shared memory");
-    cudaError_t e = cudaFuncSetAttribute(extend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kExtSmem);
+    const auto kernel = p.pool != nullptr ? extend_kernel<true> : extend_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kExtSmem);
     if (e != cudaSuccess)
         return e;
     const int64_t rows = static_cast<int64_t>(p.max_q_len) * p.group;
     const dim3 grid(static_cast<unsigned>((rows + kExtRows - 1) / kExtRows), p.hkv, p.batch);
-    extend_kernel<<<grid, kExtThreads, kExtSmem, s>>>(p);
+    kernel<<<grid, kExtThreads, kExtSmem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -101,6 +101,11 @@ struct ExtendParams {
     int64_t prefix_rows;         // rows of the prefix workspace
     float qscale;                // sm_scale * log2(e)
     int out_f32;
+    // fused NVFP4 append of the chunk (null pool: attention only)
+    uint8_t *pool;               // page-head records [num_pages][hkv][record]
+    const int32_t *slot_mapping; // [q rows]
+    int num_pages;
+    float gscale;                // tensor scale: blocks are taken of x / gscale
 };
 
 // Launch with programmatic stream serialisation allowed, so the kernel's
@@ -135,6 +140,6 @@ cudaError_t launch_decode_nvfp4_multi(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_merge(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_dequant_prefix_fp8(const PrefixParams &p, cudaStream_t s);
-cudaError_t launch_extend_attention(const ExtendParams &p, cudaStream_t s);
+cudaError_t launch_extend_attention(const ExtendParams &p, cudaStream_t s);   // appends when p.pool != null
 
 } // namespace nvfp4kv

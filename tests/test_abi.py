@@ -159,6 +159,21 @@ def test_extend_validation():
     assert extend(mql=0, q=None, out=None) == nv.OK
 
 
+def test_extend_append_validation():
+    f = nv.load().nvfp4kv_extend_attention_fp8_append
+
+    def call(c, slots=FAKE, hq=4, batch=2, mql=50):
+        return f(ctypes.byref(c), slots, FAKE, FAKE, 100, mql, FAKE, FAKE, FAKE, FAKE, 1000, FAKE, FAKE, batch,
+                 hq, 0.088, FAKE, nv.BF16, None, None)
+    assert call(cache(global_scale=0.0)) == nv.ERR_UNSUPPORTED
+    assert call(cache(pool=None)) == nv.ERR_INVALID_ARG
+    assert call(cache(), slots=None) == nv.ERR_INVALID_ARG
+    assert call(cache(), slots=FAKE + 2) == nv.ERR_INVALID_ARG
+    assert call(cache(), hq=5) == nv.ERR_INVALID_ARG          # Hq % Hkv (2 in the cache) != 0
+    assert call(cache(), hq=18) == nv.ERR_UNSUPPORTED
+    assert call(cache(), batch=0, slots=None) == nv.OK
+
+
 def test_status_strings_and_version():
     for s in range(5):
         assert nv.status_string(s)

@@ -149,3 +149,81 @@ def test_extend_full_size_sampled_tokens():
         want = oracle.extend_attention(q[t:t + 1], np.int32([0, 1]), k_pre, v_pre, np.int32([0]),
                                        np.int32([P + t]), kt, vt)
         assert_close(got[t:t + 1], want, f"ext160k token {t}")
+
+
+# --- extend fused with the NVFP4 append of the chunk --------------------------
+
+from layout import nvfp4_planes  # noqa: E402
+
+
+def chunk_slots(e, seed, odd_shift=False):
+    """Slots of each sequence's chunk tokens (positions P .. P + C - 1 of the
+    sequence) on shuffled pages; odd_shift moves every position up by one."""
+    rng = np.random.default_rng(seed)
+    ends = [P + C + 1 for P, C in zip(e.prefix_lens, e.chunk_lens)]
+    pages = [(n + 15) // 16 for n in ends]
+    perm = rng.permutation(sum(pages) + 2).astype(np.int32)
+    slots, k = [], 0
+    for b, (P, C) in enumerate(zip(e.prefix_lens, e.chunk_lens)):
+        table = perm[k:k + pages[b]]
+        k += pages[b]
+        pos = np.arange(P, P + C) + (1 if odd_shift else 0)
+        slots.append(table[pos // 16] * 16 + pos % 16)
+    return np.concatenate(slots).astype(np.int32), len(perm)
+
+
+def run_fused(e, x, slots, num_pages, global_scale=1.0, status=None):
+    xd = to_dev(x)
+    cache = nv.NVFP4Cache.allocate(num_pages, e.num_kv_heads, device=DEV, global_scale=global_scale)
+    out = torch.full((e.q_rows, e.num_q_heads, 128), float("nan"), device=DEV)
+    nv.nvfp4kv_extend_attention_fp8_append(cache, torch.from_numpy(slots).to(DEV), xd["q"], xd["q_indptr"],
+                                           xd["k_prefix"], xd["v_prefix"], xd["kv_indptr"], xd["prefix_lens"],
+                                           xd["k_chunk"], xd["v_chunk"], out, max_q_len=max(e.chunk_lens),
+                                           dev_status=status)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), list(nvfp4_planes(cache.pool.cpu().numpy()))
+
+
+def oracle_planes(e, x, slots, num_pages, global_scale=1.0):
+    pools = [np.zeros((num_pages, e.num_kv_heads, 16, n), np.uint8) for n in (64, 8, 64, 8)]
+    oracle.quantize_append(x["k_chunk"].float().numpy(), slots, pools[0], pools[1], global_scale=global_scale)
+    oracle.quantize_append(x["v_chunk"].float().numpy(), slots, pools[2], pools[3], global_scale=global_scale)
+    return pools
+
+
+@pytest.mark.parametrize("prefix_lens,chunk_lens,hq,hkv,odd", [
+    ((0, 61, 200, 1000), (130, 1, 77, 64), 48, 8, False),
+    ((64, 65), (128, 129), 8, 8, True),                 # pairs broken: atomic nibble merge
+    ((0,), (300,), 8, 1, False),
+    ((5, 0, 127), (0, 16, 40), 16, 2, True),
+])
+def test_fused_append_matches_oracle(prefix_lens, chunk_lens, hq, hkv, odd):
+    """Attention as the oracle's extend; cache bytes as the oracle's
+    quantize_append of the chunk rows, bit for bit."""
+    e = workloads.extend_custom(prefix_lens, chunk_lens, hq, hkv, seed=3 * len(prefix_lens) + hq)
+    x = workloads.extend_inputs(e)
+    slots, num_pages = chunk_slots(e, seed=hq, odd_shift=odd)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got, planes = run_fused(e, x, slots, num_pages, status=status)
+    assert status.item() == 0
+    assert_close(got, oracle_out(e, x), "fused extend out")
+    for g_, w_ in zip(planes, oracle_planes(e, x, slots, num_pages)):
+        np.testing.assert_array_equal(g_, w_)
+
+
+def test_fused_append_tensor_scale_and_skipped_slots():
+    """Tensor scale G = 0.37; slot -1 skips a token; a slot past the pool is
+    skipped and reported."""
+    e = workloads.extend_custom((33, 7), (90, 70), 24, 8, seed=77)
+    x = workloads.extend_inputs(e)
+    slots, num_pages = chunk_slots(e, seed=5)
+    slots[[3, 4, 100]] = -1
+    bad = slots.copy()
+    bad[50] = num_pages * 16 + 3
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got, planes = run_fused(e, x, bad, num_pages, global_scale=0.37, status=status)
+    assert status.item() == nv.DEV_BAD_SLOT
+    slots[50] = -1
+    assert_close(got, oracle_out(e, x), "fused extend out, G = 0.37")
+    for g_, w_ in zip(planes, oracle_planes(e, x, slots, num_pages, global_scale=0.37)):
+        np.testing.assert_array_equal(g_, w_)
