@@ -510,7 +510,9 @@ __global__ void __launch_bounds__(kExtThreads, 1) extend_kernel(const ExtendPara
 cudaError_t launch_extend_attention(const ExtendParams &p, cudaStream_t s)
 {
     static_assert(kExtSmem <= 227 * 1024, "shared memory");
-    const auto kernel = p.pool != nullptr ? extend_kernel<true> : extend_kernel<false>;
+    if (p.pool == nullptr)
+        return launch_extend_attention_tc(p, s);
+    const auto kernel = extend_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kExtSmem);
     if (e != cudaSuccess)
         return e;

@@ -1,0 +1,428 @@
+// Extend attention on the fifth-generation tensor cores (tcgen05).
+//
+// "SGLang stores KV cache in 4 bits" (LMSYS summary), Interpretation: on the
+// extend path the cached prefix is dequantised into one FP8 workspace and the
+// new chunk attends over it and over itself; chunk token t of a sequence with
+// prefix length P sees the P prefix keys and chunk keys 0 .. t.
+//
+// One CTA owns 128 rows of one sequence and one kv head, a row being a
+// (chunk token, query head of the group) pair taken token-major.  Per key
+// tile of 64:
+//   S = Q K^T     tcgen05.mma M128 N64 K16 x 8 into tensor memory (two S
+//                 buffers, so Q K^T of tile i+1 runs during the softmax of i)
+//   softmax       one thread per row reads its S row from tensor memory,
+//                 masks, takes exp2 against a running maximum that is only
+//                 raised when it grows by more than 2^8 (then the O row in
+//                 tensor memory is rescaled), writes P (f16) to shared memory
+//   O += P V      tcgen05.mma M128 N128 K16 x 4, O resident in tensor memory
+// Warps 0-3 run the softmax, warps 4-7 convert key tiles (E4M3 prefix rows or
+// bf16 chunk rows) to f16 in the 128-byte-swizzled operand layout, warp 8
+// allocates tensor memory and issues the MMAs.  mbarriers order the roles;
+// every wait is bounded and a timeout is reported.
+#include "tcgen05.cuh"
+
+namespace nvfp4kv {
+namespace {
+
+constexpr int kTcRows = 128;                  // M: rows per CTA
+constexpr int kTcKeys = 64;                   // keys per tile
+constexpr int kSoftmaxThreads = 128;          // warps 0-3
+constexpr int kProducerThreads = 128;         // warps 4-7
+constexpr int kMmaWarp = 8;
+constexpr int kTcThreads = kSoftmaxThreads + kProducerThreads + 32;
+constexpr float kRescaleLog2 = 8.f;           // raise the running maximum only past this margin
+
+constexpr uint32_t kQBytes = kTcRows * kHeadDim * 2;   // 32 KB
+constexpr uint32_t kKVBytes = kTcKeys * kHeadDim * 2;  // 16 KB per K or V tile
+constexpr uint32_t kPBytes = kTcRows * kTcKeys * 2;    // 16 KB
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kQBytes;            // two buffers
+constexpr uint32_t kOffV = kOffK + 2 * kKVBytes;       // two buffers
+constexpr uint32_t kOffP = kOffV + 2 * kKVBytes;       // two buffers
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+enum { kBarKvFull = 0, kBarSFull = 2, kBarPFull = 4, kBarPvDone = 6, kBarDone = 8, kNumBars = 9 };
+constexpr uint32_t kOffTmemSlot = kOffBar + 8 * kNumBars;
+constexpr uint32_t kOffFail = kOffTmemSlot + 4;
+constexpr uint32_t kTcSmem = kOffFail + 4 + 1024;      // + slack to align the base to 1024 bytes
+constexpr uint32_t kTmemCols = 256;                    // S[2] at columns 0 and 64, O at 128
+
+static_assert(kTcSmem <= 227 * 1024, "shared memory");
+static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms");
+
+// Byte offset of 16-byte chunk c (f16 columns 8c .. 8c + 7) of row r in a
+// 128-byte-swizzled tile of `rows` rows: 64-column blocks of rows x 128
+// bytes, eight-row atoms of 1024 bytes, chunk position c ^ (r mod 8).
+__device__ __forceinline__ uint32_t sw128(uint32_t rows, uint32_t r, uint32_t c)
+{
+    return (c >> 3) * rows * 128u + r * 128u + (((c & 7u) ^ (r & 7u)) << 4);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ldg_nc(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float s)
+{
+    return pack_f16x2(__uint_as_float(w << 16) * s, __uint_as_float(w & 0xffff0000u) * s);
+}
+
+__device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, volatile int *fail, int32_t *dev_status)
+{
+    if (*fail)
+        return false;
+    if (mbar_wait_bounded(bar, parity, kWaitLimit))
+        return true;
+    *fail = 1;
+    report(dev_status, NVFP4KV_DEV_TIMEOUT);
+    return false;
+}
+
+struct TcCta {
+    int c0, C, P;
+    int64_t p0;
+    int n_pre, n_tiles;
+};
+
+// Producer thread pt (0..127): load key tile i, wait until its buffer is
+// free, convert and store it.  FP8 prefix tiles: 64 keys x 8 pieces of 16
+// bytes per K or V, four pieces a thread each; bf16 chunk tiles: 64 keys x 16
+// pieces, eight a thread each.  Keys past the end are zeros.
+__device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta &c, int h, int i, int pt,
+                                             uint32_t base, volatile int *fail)
+{
+    const int b = i & 1;
+    const uint32_t kdst = base + kOffK + b * kKVBytes, vdst = base + kOffV + b * kKVBytes;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    uint4 raw[16];
+    const bool pre = i < c.n_pre;
+    if (pre) {
+        const int k0 = i * kTcKeys;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = pt + kProducerThreads * (u & 3);
+            const int key = idx >> 3, piece = idx & 7;
+            const uint8_t *src = (u < 4 ? p.k_prefix : p.v_prefix) + ((c.p0 + k0 + key) * p.hkv + h) * kHeadDim +
+                                 16 * piece;
+            raw[u] = k0 + key < c.P ? ldg_nc(src) : zero;
+        }
+    } else {
+        const int k0 = (i - c.n_pre) * kTcKeys;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int idx = pt + kProducerThreads * (u & 7);
+            const int key = idx >> 4, piece = idx & 15;
+            const uint16_t *src = (u < 8 ? p.k_chunk : p.v_chunk) +
+                                  (static_cast<int64_t>(c.c0 + k0 + key) * p.hkv + h) * kHeadDim + 8 * piece;
+            raw[u] = k0 + key < c.C ? ldg_nc(src) : zero;
+        }
+    }
+    if (i >= 2 && !wait_or_fail(base + kOffBar + 8 * (kBarPvDone + b), ((i - 2) >> 1) & 1, fail, p.dev_status))
+        return false;
+    if (pre) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = pt + kProducerThreads * (u & 3);
+            const uint32_t key = idx >> 3, piece = idx & 7;
+            uint4 lo, hi;
+            e4m3x4_to_f16x2x2(raw[u].x, lo.x, lo.y);
+            e4m3x4_to_f16x2x2(raw[u].y, lo.z, lo.w);
+            e4m3x4_to_f16x2x2(raw[u].z, hi.x, hi.y);
+            e4m3x4_to_f16x2x2(raw[u].w, hi.z, hi.w);
+            const uint32_t dst = u < 4 ? kdst : vdst;
+            // pieces 4..7 store their high half first: eight lanes, eight bank groups
+            const uint32_t first = (piece >> 2) & 1u;
+            sts128(dst + sw128(kTcKeys, key, 2 * piece + first), first ? hi : lo);
+            sts128(dst + sw128(kTcKeys, key, 2 * piece + 1 - first), first ? lo : hi);
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int idx = pt + kProducerThreads * (u & 7);
+            const uint32_t key = idx >> 4, piece = idx & 15;
+            uint4 f;
+            f.x = bf16x2_to_f16x2(raw[u].x, 1.f);
+            f.y = bf16x2_to_f16x2(raw[u].y, 1.f);
+            f.z = bf16x2_to_f16x2(raw[u].z, 1.f);
+            f.w = bf16x2_to_f16x2(raw[u].w, 1.f);
+            sts128((u < 8 ? kdst : vdst) + sw128(kTcKeys, key, piece), f);
+        }
+    }
+    fence_async_shared();
+    mbar_arrive(base + kOffBar + 8 * (kBarKvFull + b));
+    return true;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw_addr);
+    volatile int *fail = reinterpret_cast<volatile int *>(gbase + kOffFail);
+    const uint32_t bar = base + kOffBar;
+
+    const int b_seq = blockIdx.z;
+    const int h = blockIdx.y;
+    const int tile = static_cast<int>(gridDim.x - 1 - blockIdx.x);  // later rows see more keys: start them first
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+
+    TcCta c;
+    c.c0 = p.q_indptr[b_seq];
+    const int c1 = p.q_indptr[b_seq + 1];
+    c.P = p.prefix_lens[b_seq];
+    const int kv0 = p.kv_indptr[b_seq];
+    if (c.c0 < 0 || c1 < c.c0 || c1 > p.q_rows || c1 - c.c0 > p.max_q_len || c.P < 0 || kv0 < 0 ||
+        static_cast<int64_t>(kv0) + c.P > p.prefix_rows) {
+        if (tid == 0)
+            report(p.dev_status, NVFP4KV_DEV_BAD_LEN);
+        return;
+    }
+    c.C = c1 - c.c0;
+    c.p0 = kv0;
+    const int g = p.group;
+    const int R = c.C * g;
+    const int row0 = tile * kTcRows;
+    if (row0 >= R)
+        return;
+    const int t_max = (min(row0 + kTcRows, R) - 1) / g;
+    c.n_pre = (c.P + kTcKeys - 1) / kTcKeys;
+    c.n_tiles = c.n_pre + t_max / kTcKeys + 1;
+
+    // Q tile: rows past the end are zeros; sm_scale * log2 e folded in
+    for (int idx = tid; idx < kTcRows * 16; idx += kTcThreads) {
+        const int r = idx >> 4, piece = idx & 15;
+        const int row = row0 + r;
+        uint4 f = make_uint4(0, 0, 0, 0);
+        if (row < R) {
+            const int t = row / g;
+            const uint4 w = ldg_nc(p.q + (static_cast<int64_t>(c.c0 + t) * p.hq + h * g + (row - t * g)) * kHeadDim +
+                                   8 * piece);
+            f.x = bf16x2_to_f16x2(w.x, p.qscale);
+            f.y = bf16x2_to_f16x2(w.y, p.qscale);
+            f.z = bf16x2_to_f16x2(w.z, p.qscale);
+            f.w = bf16x2_to_f16x2(w.w, p.qscale);
+        }
+        sts128(base + kOffQ + sw128(kTcRows, r, piece), f);
+    }
+    if (tid == 0) {
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(bar + 8 * (kBarKvFull + k), kProducerThreads);
+            mbar_init(bar + 8 * (kBarSFull + k), 1);
+            mbar_init(bar + 8 * (kBarPFull + k), kSoftmaxThreads);
+            mbar_init(bar + 8 * (kBarPvDone + k), 1);
+        }
+        mbar_init(bar + 8 * kBarDone, 1);
+        *fail = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp)
+        tmem_alloc(base + kOffTmemSlot, kTmemCols);
+    fence_async_shared();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + kOffTmemSlot);
+
+    if (warp == kMmaWarp) {
+        if ((tid & 31) == 0) {
+            constexpr uint32_t i_qk = idesc_f16(kTcRows, kTcKeys, false);
+            constexpr uint32_t i_pv = idesc_f16(kTcRows, kHeadDim, true);
+            bool ok = true;
+            auto issue_qk = [&](int i) {
+                const int b = i & 1;
+                if (!wait_or_fail(bar + 8 * (kBarKvFull + b), (i >> 1) & 1, fail, p.dev_status))
+                    return false;
+                tc_fence_after_sync();
+                const uint32_t kb = base + kOffK + b * kKVBytes;
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    umma_f16(tmem + b * kTcKeys,
+                             smem_desc(base + kOffQ + (s >> 2) * (kTcRows * 128) + (s & 3) * 32, 16, 1024),
+                             smem_desc(kb + (s >> 2) * (kTcKeys * 128) + (s & 3) * 32, 16, 1024), i_qk, s > 0);
+                umma_commit(bar + 8 * (kBarSFull + b));
+                return true;
+            };
+            ok = issue_qk(0);
+            for (int i = 0; ok && i < c.n_tiles; ++i) {
+                const int b = i & 1;
+                if (i + 1 < c.n_tiles && !(ok = issue_qk(i + 1)))
+                    break;
+                if (!(ok = wait_or_fail(bar + 8 * (kBarPFull + b), (i >> 1) & 1, fail, p.dev_status)))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t pb = base + kOffP + b * kPBytes, vb = base + kOffV + b * kKVBytes;
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    umma_f16(tmem + 128, smem_desc(pb + s * 32, 16, 1024),
+                             smem_desc(vb + s * 2048, kTcKeys * 128, 1024), i_pv, i > 0 || s > 0);
+                umma_commit(bar + 8 * (kBarPvDone + b));
+            }
+            // nothing of this thread's may still run when tensor memory is freed
+            umma_commit(bar + 8 * kBarDone);
+            if (!mbar_wait_bounded(bar + 8 * kBarDone, 0, kWaitLimit))
+                report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp >= kSoftmaxThreads / 32) {
+        const int pt = tid - kSoftmaxThreads;
+        for (int i = 0; i < c.n_tiles; ++i)
+            if (!produce_tile(p, c, h, i, pt, base, fail))
+                break;
+    } else {
+        // softmax: thread r owns row row0 + r, tensor-memory lane r
+        const int r = tid;
+        const int row = row0 + r;
+        const int t = min(row, R - 1) / g;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        // the warp leaves together: its tensor-memory accesses are warp-wide
+        auto wait_warp = [&](uint32_t bar_addr, uint32_t parity) {
+            return __all_sync(kFullMask, wait_or_fail(bar_addr, parity, fail, p.dev_status));
+        };
+        for (int i = 0; i < c.n_tiles; ++i) {
+            const int b = i & 1;
+            if (!(ok = wait_warp(bar + 8 * (kBarSFull + b), (i >> 1) & 1)))
+                break;
+            tc_fence_after_sync();
+            uint32_t sr[64];
+            tmem_ld32(lane_base + b * kTcKeys, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(lane_base + b * kTcKeys + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_wait_ld();
+            float s[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+                s[j] = __uint_as_float(sr[j]);
+            const int lim = i < c.n_pre ? c.P - i * kTcKeys : t + 1 - (i - c.n_pre) * kTcKeys;
+            if (lim < kTcKeys) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    if (j >= lim)
+                        s[j] = -INFINITY;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+                mx = fmaxf(mx, s[j]);
+            const bool need = mx > m_used + kRescaleLog2;
+            const float m_new = need ? mx : m_used;
+            const float mbase = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = need ? fast_exp2(m_used - mbase) : 1.f;
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                s[j] = fast_exp2(s[j] - mbase);
+                sum += s[j];
+            }
+            l = l * alpha + sum;
+            m_used = m_new;
+            // P buffer b was last read by the value product of tile i - 2
+            if (i >= 2 && !(ok = wait_warp(bar + 8 * (kBarPvDone + b), ((i - 2) >> 1) & 1)))
+                break;
+            if (__any_sync(kFullMask, need) && i >= 1) {
+                const int pb = (i - 1) & 1;
+                if (!(ok = wait_warp(bar + 8 * (kBarPvDone + pb), ((i - 1) >> 1) & 1)))
+                    break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + 128 + 32 * cb, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                    tmem_st32(lane_base + 128 + 32 * cb, o);
+                }
+                tmem_wait_st();
+            }
+            const uint32_t pdst = base + kOffP + b * kPBytes;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                uint4 w;
+                w.x = pack_f16x2(s[8 * cc], s[8 * cc + 1]);
+                w.y = pack_f16x2(s[8 * cc + 2], s[8 * cc + 3]);
+                w.z = pack_f16x2(s[8 * cc + 4], s[8 * cc + 5]);
+                w.w = pack_f16x2(s[8 * cc + 6], s[8 * cc + 7]);
+                sts128(pdst + sw128(kTcRows, r, cc), w);
+            }
+            fence_async_shared();
+            tc_fence_before_sync();
+            mbar_arrive(bar + 8 * (kBarPFull + b));
+        }
+        if (ok) {
+            const int last = c.n_tiles - 1;
+            ok = wait_warp(bar + 8 * (kBarPvDone + (last & 1)), (last >> 1) & 1);
+        }
+        if (ok) {
+            tc_fence_after_sync();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const bool store = row < R;
+            const int64_t off = (static_cast<int64_t>(c.c0 + t) * p.hq + h * g + (min(row, R - 1) - t * g)) * kHeadDim;
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t o[32];
+                tmem_ld32(lane_base + 128 + 32 * cb, o);
+                tmem_wait_ld();
+                if (!store)
+                    continue;
+                if (p.out_f32) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off + 32 * cb);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                             __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + off + 32 * cb);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint4 v;
+                        uint32_t *vw = &v.x;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            __nv_bfloat162 two = __floats2bfloat162_rn(__uint_as_float(o[8 * k + 2 * e]) * inv,
+                                                                       __uint_as_float(o[8 * k + 2 * e + 1]) * inv);
+                            vw[e] = *reinterpret_cast<uint32_t *>(&two);
+                        }
+                        dst[k] = v;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+} // namespace
+
+cudaError_t launch_extend_attention_tc(const ExtendParams &p, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t rows = static_cast<int64_t>(p.max_q_len) * p.group;
+    const dim3 grid(static_cast<unsigned>((rows + kTcRows - 1) / kTcRows), p.hkv, p.batch);
+    extend_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(p);
+    return cudaGetLastError();
+}
+
+} // namespace nvfp4kv
