@@ -36,11 +36,13 @@ constexpr uint32_t kQBytes = kTcRows * kHeadDim * 2;   // 32 KB
 constexpr uint32_t kKVBytes = kTcKeys * kHeadDim * 2;  // 16 KB per K or V tile
 constexpr uint32_t kPBytes = kTcRows * kTcKeys * 2;    // 16 KB
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;            // two buffers
-constexpr uint32_t kOffV = kOffK + 2 * kKVBytes;       // two buffers
-constexpr uint32_t kOffP = kOffV + 2 * kKVBytes;       // two buffers
+constexpr int kKvStages = 4;                           // converted key tiles in flight
+constexpr uint32_t kOffK = kOffQ + kQBytes;            // kKvStages buffers
+constexpr uint32_t kOffV = kOffK + kKvStages * kKVBytes;
+constexpr uint32_t kOffP = kOffV + kKvStages * kKVBytes;  // two buffers
 constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
-enum { kBarKvFull = 0, kBarSFull = 2, kBarPFull = 4, kBarPvDone = 6, kBarDone = 8, kNumBars = 9 };
+// kv_full / kv_empty per key-tile stage; s_full, p_full, pv_done per S / P buffer
+enum { kBarKvFull = 0, kBarKvEmpty = 4, kBarSFull = 8, kBarPFull = 10, kBarPvDone = 12, kBarDone = 14, kNumBars = 15 };
 constexpr uint32_t kOffTmemSlot = kOffBar + 8 * kNumBars;
 constexpr uint32_t kOffFail = kOffTmemSlot + 4;
 constexpr uint32_t kTcSmem = kOffFail + 4 + 1024;      // + slack to align the base to 1024 bytes
@@ -102,8 +104,8 @@ struct TcCta {
 __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta &c, int h, int i, int pt,
                                              uint32_t base, volatile int *fail)
 {
-    const int b = i & 1;
-    const uint32_t kdst = base + kOffK + b * kKVBytes, vdst = base + kOffV + b * kKVBytes;
+    const int st = i % kKvStages;
+    const uint32_t kdst = base + kOffK + st * kKVBytes, vdst = base + kOffV + st * kKVBytes;
     const uint4 zero = make_uint4(0, 0, 0, 0);
     uint4 raw[16];
     const bool pre = i < c.n_pre;
@@ -128,7 +130,9 @@ __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta 
             raw[u] = k0 + key < c.C ? ldg_nc(src) : zero;
         }
     }
-    if (i >= 2 && !wait_or_fail(base + kOffBar + 8 * (kBarPvDone + b), ((i - 2) >> 1) & 1, fail, p.dev_status))
+    // stage st was last read by the MMAs of tile i - kKvStages
+    if (i >= kKvStages && !wait_or_fail(base + kOffBar + 8 * (kBarKvEmpty + st), ((i / kKvStages) - 1) & 1, fail,
+                                        p.dev_status))
         return false;
     if (pre) {
 #pragma unroll
@@ -160,7 +164,7 @@ __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta 
         }
     }
     fence_async_shared();
-    mbar_arrive(base + kOffBar + 8 * (kBarKvFull + b));
+    mbar_arrive(base + kOffBar + 8 * (kBarKvFull + st));
     return true;
 }
 
@@ -218,8 +222,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
         sts128(base + kOffQ + sw128(kTcRows, r, piece), f);
     }
     if (tid == 0) {
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < kKvStages; ++k) {
             mbar_init(bar + 8 * (kBarKvFull + k), kProducerThreads);
+            mbar_init(bar + 8 * (kBarKvEmpty + k), 1);
+        }
+        for (int k = 0; k < 2; ++k) {
             mbar_init(bar + 8 * (kBarSFull + k), 1);
             mbar_init(bar + 8 * (kBarPFull + k), kSoftmaxThreads);
             mbar_init(bar + 8 * (kBarPvDone + k), 1);
@@ -242,11 +249,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
             constexpr uint32_t i_pv = idesc_f16(kTcRows, kHeadDim, true);
             bool ok = true;
             auto issue_qk = [&](int i) {
-                const int b = i & 1;
-                if (!wait_or_fail(bar + 8 * (kBarKvFull + b), (i >> 1) & 1, fail, p.dev_status))
+                const int b = i & 1, st = i % kKvStages;
+                if (!wait_or_fail(bar + 8 * (kBarKvFull + st), (i / kKvStages) & 1, fail, p.dev_status))
                     return false;
                 tc_fence_after_sync();
-                const uint32_t kb = base + kOffK + b * kKVBytes;
+                const uint32_t kb = base + kOffK + st * kKVBytes;
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
                     umma_f16(tmem + b * kTcKeys,
@@ -263,12 +270,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
                 if (!(ok = wait_or_fail(bar + 8 * (kBarPFull + b), (i >> 1) & 1, fail, p.dev_status)))
                     break;
                 tc_fence_after_sync();
-                const uint32_t pb = base + kOffP + b * kPBytes, vb = base + kOffV + b * kKVBytes;
+                const uint32_t pb = base + kOffP + b * kPBytes, vb = base + kOffV + (i % kKvStages) * kKVBytes;
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     umma_f16(tmem + 128, smem_desc(pb + s * 32, 16, 1024),
                              smem_desc(vb + s * 2048, kTcKeys * 128, 1024), i_pv, i > 0 || s > 0);
                 umma_commit(bar + 8 * (kBarPvDone + b));
+                umma_commit(bar + 8 * (kBarKvEmpty + i % kKvStages));
             }
             // nothing of this thread's may still run when tensor memory is freed
             umma_commit(bar + 8 * kBarDone);
