@@ -321,20 +321,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
                     if (j >= lim)
                         s[j] = -INFINITY;
             }
-            float mx = -INFINITY;
+            // eight independent partial maxima and sums keep the dependency chains short
+            float pm[8];
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-                mx = fmaxf(mx, s[j]);
+            for (int k = 0; k < 8; ++k)
+                pm[k] = fmaxf(fmaxf(fmaxf(s[k], s[k + 8]), fmaxf(s[k + 16], s[k + 24])),
+                              fmaxf(fmaxf(s[k + 32], s[k + 40]), fmaxf(s[k + 48], s[k + 56])));
+            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             const bool need = mx > m_used + kRescaleLog2;
             const float m_new = need ? mx : m_used;
             const float mbase = m_new == -INFINITY ? 0.f : m_new;
             const float alpha = need ? fast_exp2(m_used - mbase) : 1.f;
-            float sum = 0.f;
+            float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
                 s[j] = fast_exp2(s[j] - mbase);
-                sum += s[j];
+                ps[j & 7] += s[j];
             }
+            const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             l = l * alpha + sum;
             m_used = m_new;
             // P buffer b was last read by the value product of tile i - 2
