@@ -13,8 +13,10 @@
 //   softmax       one thread per row reads its S row from tensor memory,
 //                 masks, takes exp2 against a running maximum that is only
 //                 raised when it grows by more than 2^8 (then the O row in
-//                 tensor memory is rescaled), writes P (f16) to shared memory
-//   O += P V      tcgen05.mma M128 N128 K16 x 4, O resident in tensor memory
+//                 tensor memory is rescaled), writes P (f16) back to tensor
+//                 memory
+//   O += P V      tcgen05.mma M128 N128 K16 x 4 with P read from tensor
+//                 memory, O resident in tensor memory
 // Warps 0-3 run the softmax, warps 4-7 convert key tiles (E4M3 prefix rows or
 // bf16 chunk rows) to f16 in the 128-byte-swizzled operand layout, warp 8
 // allocates tensor memory and issues the MMAs.  mbarriers order the roles;
@@ -34,22 +36,24 @@ constexpr float kRescaleLog2 = 8.f;           // raise the running maximum only 
 
 constexpr uint32_t kQBytes = kTcRows * kHeadDim * 2;   // 32 KB
 constexpr uint32_t kKVBytes = kTcKeys * kHeadDim * 2;  // 16 KB per K or V tile
-constexpr uint32_t kPBytes = kTcRows * kTcKeys * 2;    // 16 KB
 constexpr uint32_t kOffQ = 0;
 constexpr int kKvStages = 4;                           // converted key tiles in flight
 constexpr uint32_t kOffK = kOffQ + kQBytes;            // kKvStages buffers
 constexpr uint32_t kOffV = kOffK + kKvStages * kKVBytes;
-constexpr uint32_t kOffP = kOffV + kKvStages * kKVBytes;  // two buffers
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffBar = kOffV + kKvStages * kKVBytes;
 // kv_full / kv_empty per key-tile stage; s_full, p_full, pv_done per S / P buffer
 enum { kBarKvFull = 0, kBarKvEmpty = 4, kBarSFull = 8, kBarPFull = 10, kBarPvDone = 12, kBarDone = 14, kNumBars = 15 };
 constexpr uint32_t kOffTmemSlot = kOffBar + 8 * kNumBars;
 constexpr uint32_t kOffFail = kOffTmemSlot + 4;
 constexpr uint32_t kTcSmem = kOffFail + 4 + 1024;      // + slack to align the base to 1024 bytes
-constexpr uint32_t kTmemCols = 256;                    // S[2] at columns 0 and 64, O at 128
+// tensor-memory columns: O, S[2] (fp32), P[2] (f16 pairs)
+constexpr uint32_t kColO = 0, kColS = 128, kColP = 256;
+constexpr uint32_t kTmemCols = 512;
 
 static_assert(kTcSmem <= 227 * 1024, "shared memory");
-static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms");
+// one CTA per SM: its 512 tensor-memory columns are then always free
+static_assert(2 * kTcSmem > 228 * 1024, "one CTA per SM");
+static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzle atoms");
 
 // Byte offset of 16-byte chunk c (f16 columns 8c .. 8c + 7) of row r in a
 // 128-byte-swizzled tile of `rows` rows: 64-column blocks of rows x 128
@@ -256,7 +260,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
                 const uint32_t kb = base + kOffK + st * kKVBytes;
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    umma_f16(tmem + b * kTcKeys,
+                    umma_f16(tmem + kColS + b * kTcKeys,
                              smem_desc(base + kOffQ + (s >> 2) * (kTcRows * 128) + (s & 3) * 32, 16, 1024),
                              smem_desc(kb + (s >> 2) * (kTcKeys * 128) + (s & 3) * 32, 16, 1024), i_qk, s > 0);
                 umma_commit(bar + 8 * (kBarSFull + b));
@@ -270,11 +274,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
                 if (!(ok = wait_or_fail(bar + 8 * (kBarPFull + b), (i >> 1) & 1, fail, p.dev_status)))
                     break;
                 tc_fence_after_sync();
-                const uint32_t pb = base + kOffP + b * kPBytes, vb = base + kOffV + (i % kKvStages) * kKVBytes;
+                const uint32_t vb = base + kOffV + (i % kKvStages) * kKVBytes;
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    umma_f16(tmem + 128, smem_desc(pb + s * 32, 16, 1024),
-                             smem_desc(vb + s * 2048, kTcKeys * 128, 1024), i_pv, i > 0 || s > 0);
+                    umma_f16_ts(tmem + kColO, tmem + kColP + b * (kTcKeys / 2) + s * 8,
+                                smem_desc(vb + s * 2048, kTcKeys * 128, 1024), i_pv, i > 0 || s > 0);
                 umma_commit(bar + 8 * (kBarPvDone + b));
                 umma_commit(bar + 8 * (kBarKvEmpty + i % kKvStages));
             }
@@ -307,8 +311,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
                 break;
             tc_fence_after_sync();
             uint32_t sr[64];
-            tmem_ld32(lane_base + b * kTcKeys, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(lane_base + b * kTcKeys + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_ld32(lane_base + kColS + b * kTcKeys, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(lane_base + kColS + b * kTcKeys + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
             tmem_wait_ld();
             float s[64];
 #pragma unroll
@@ -353,26 +357,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
 #pragma unroll
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t o[32];
-                    tmem_ld32(lane_base + 128 + 32 * cb, o);
+                    tmem_ld32(lane_base + kColO + 32 * cb, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                    tmem_st32(lane_base + 128 + 32 * cb, o);
+                    tmem_st32(lane_base + kColO + 32 * cb, o);
                 }
                 tmem_wait_st();
             }
-            const uint32_t pdst = base + kOffP + b * kPBytes;
+            // P row into tensor memory, f16 pairs, the A operand of the value product
+            uint32_t pw[32];
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                uint4 w;
-                w.x = pack_f16x2(s[8 * cc], s[8 * cc + 1]);
-                w.y = pack_f16x2(s[8 * cc + 2], s[8 * cc + 3]);
-                w.z = pack_f16x2(s[8 * cc + 4], s[8 * cc + 5]);
-                w.w = pack_f16x2(s[8 * cc + 6], s[8 * cc + 7]);
-                sts128(pdst + sw128(kTcRows, r, cc), w);
-            }
-            fence_async_shared();
+            for (int j = 0; j < 32; ++j)
+                pw[j] = pack_f16x2(s[2 * j], s[2 * j + 1]);
+            tmem_st32(lane_base + kColP + b * (kTcKeys / 2), pw);
+            tmem_wait_st();
             tc_fence_before_sync();
             mbar_arrive(bar + 8 * (kBarPFull + b));
         }
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t o[32];
-                tmem_ld32(lane_base + 128 + 32 * cb, o);
+                tmem_ld32(lane_base + kColO + 32 * cb, o);
                 tmem_wait_ld();
                 if (!store)
                     continue;

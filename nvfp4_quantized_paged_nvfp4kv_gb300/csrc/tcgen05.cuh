@@ -53,6 +53,20 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// D (tensor memory) = A (tensor memory) * B (shared memory) (+ D), one thread.
+// A holds its M rows in lanes, 16-bit elements two to a 32-bit column (the
+// lower half first): a K = 16 step spans eight columns.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
 // Arrive once on an mbarrier when every earlier tcgen05 operation of this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
