@@ -37,7 +37,7 @@ constexpr float kRescaleLog2 = 8.f;           // raise the running maximum only 
 constexpr uint32_t kQBytes = kTcRows * kHeadDim * 2;   // 32 KB
 constexpr uint32_t kKVBytes = kTcKeys * kHeadDim * 2;  // 16 KB per K or V tile
 constexpr uint32_t kOffQ = 0;
-constexpr int kKvStages = 4;                           // converted key tiles in flight
+constexpr int kKvStages = 2;                           // converted key tiles in flight
 constexpr uint32_t kOffK = kOffQ + kQBytes;            // kKvStages buffers
 constexpr uint32_t kOffV = kOffK + kKvStages * kKVBytes;
 constexpr uint32_t kOffBar = kOffV + kKvStages * kKVBytes;
@@ -46,13 +46,17 @@ enum { kBarKvFull = 0, kBarKvEmpty = 4, kBarSFull = 8, kBarPFull = 10, kBarPvDon
 constexpr uint32_t kOffTmemSlot = kOffBar + 8 * kNumBars;
 constexpr uint32_t kOffFail = kOffTmemSlot + 4;
 constexpr uint32_t kTcSmem = kOffFail + 4 + 1024;      // + slack to align the base to 1024 bytes
-// tensor-memory columns: O, S[2] (fp32), P[2] (f16 pairs)
-constexpr uint32_t kColO = 0, kColS = 128, kColP = 256;
-constexpr uint32_t kTmemCols = 512;
+// tensor-memory columns: O, S[2] (fp32); P[b] (f16 pairs) overwrites the first
+// 32 columns of S[b] once the softmax has read them.  The MMAs of a CTA run in
+// issue order, so Q K^T of tile i + 2 (into S[b]) follows P V of tile i.
+constexpr uint32_t kColO = 0, kColS = 128, kColP = 128;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColPStride = kTcKeys;                // P[b] at kColP + b * kColPStride
 
 static_assert(kTcSmem <= 227 * 1024, "shared memory");
-// one CTA per SM: its 512 tensor-memory columns are then always free
-static_assert(2 * kTcSmem > 228 * 1024, "one CTA per SM");
+// two CTAs per SM, no more: their 2 x 256 tensor-memory columns are then
+// always free
+static_assert(2 * kTcSmem <= 228 * 1024 && 3 * kTcSmem > 228 * 1024, "two CTAs per SM");
 static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzle atoms");
 
 // Byte offset of 16-byte chunk c (f16 columns 8c .. 8c + 7) of row r in a
@@ -101,20 +105,22 @@ struct TcCta {
     int n_pre, n_tiles;
 };
 
-// Producer thread pt (0..127): load key tile i, wait until its buffer is
-// free, convert and store it.  FP8 prefix tiles: 64 keys x 8 pieces of 16
-// bytes per K or V, four pieces a thread each; bf16 chunk tiles: 64 keys x 16
-// pieces, eight a thread each.  Keys past the end are zeros.
+// Producer thread pt (0..127): load key tile i, wait until its stage is free,
+// convert it to f16 in the 128-byte-swizzled layout and signal the MMA warp.
+// FP8 prefix tiles: 64 keys x 8 pieces of 16 bytes per K and per V, four
+// pieces a thread each, loaded together.  bf16 chunk tiles: 64 keys x 16
+// pieces per K and per V, eight a thread each, K then V (eight loads in
+// flight a thread keep the register count low).  Keys past the end are zeros.
 __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta &c, int h, int i, int pt,
                                              uint32_t base, volatile int *fail)
 {
     const int st = i % kKvStages;
     const uint32_t kdst = base + kOffK + st * kKVBytes, vdst = base + kOffV + st * kKVBytes;
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    uint4 raw[16];
+    uint4 raw[8];
     const bool pre = i < c.n_pre;
+    const int k0 = (pre ? i : i - c.n_pre) * kTcKeys;
     if (pre) {
-        const int k0 = i * kTcKeys;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int idx = pt + kProducerThreads * (u & 3);
@@ -124,14 +130,13 @@ __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta 
             raw[u] = k0 + key < c.P ? ldg_nc(src) : zero;
         }
     } else {
-        const int k0 = (i - c.n_pre) * kTcKeys;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int idx = pt + kProducerThreads * (u & 7);
+        for (int u = 0; u < 8; ++u) {
+            const int idx = pt + kProducerThreads * u;
             const int key = idx >> 4, piece = idx & 15;
-            const uint16_t *src = (u < 8 ? p.k_chunk : p.v_chunk) +
-                                  (static_cast<int64_t>(c.c0 + k0 + key) * p.hkv + h) * kHeadDim + 8 * piece;
-            raw[u] = k0 + key < c.C ? ldg_nc(src) : zero;
+            raw[u] = k0 + key < c.C ? ldg_nc(p.k_chunk + (static_cast<int64_t>(c.c0 + k0 + key) * p.hkv + h) *
+                                                              kHeadDim + 8 * piece)
+                                    : zero;
         }
     }
     // stage st was last read by the MMAs of tile i - kKvStages
@@ -156,15 +161,28 @@ __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta 
         }
     } else {
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int idx = pt + kProducerThreads * (u & 7);
-            const uint32_t key = idx >> 4, piece = idx & 15;
-            uint4 f;
-            f.x = bf16x2_to_f16x2(raw[u].x, 1.f);
-            f.y = bf16x2_to_f16x2(raw[u].y, 1.f);
-            f.z = bf16x2_to_f16x2(raw[u].z, 1.f);
-            f.w = bf16x2_to_f16x2(raw[u].w, 1.f);
-            sts128((u < 8 ? kdst : vdst) + sw128(kTcKeys, key, piece), f);
+        for (int half = 0; half < 2; ++half) {
+            if (half == 1) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int idx = pt + kProducerThreads * u;
+                    const int key = idx >> 4, piece = idx & 15;
+                    raw[u] = k0 + key < c.C ? ldg_nc(p.v_chunk + (static_cast<int64_t>(c.c0 + k0 + key) * p.hkv + h) *
+                                                                      kHeadDim + 8 * piece)
+                                            : zero;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = pt + kProducerThreads * u;
+                const uint32_t key = idx >> 4, piece = idx & 15;
+                uint4 f;
+                f.x = bf16x2_to_f16x2(raw[u].x, 1.f);
+                f.y = bf16x2_to_f16x2(raw[u].y, 1.f);
+                f.z = bf16x2_to_f16x2(raw[u].z, 1.f);
+                f.w = bf16x2_to_f16x2(raw[u].w, 1.f);
+                sts128((half ? vdst : kdst) + sw128(kTcKeys, key, piece), f);
+            }
         }
     }
     fence_async_shared();
@@ -172,7 +190,7 @@ __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta 
     return true;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendParams p)
+__global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const ExtendParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -277,7 +295,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
                 const uint32_t vb = base + kOffV + (i % kKvStages) * kKVBytes;
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    umma_f16_ts(tmem + kColO, tmem + kColP + b * (kTcKeys / 2) + s * 8,
+                    umma_f16_ts(tmem + kColO, tmem + kColP + b * kColPStride + s * 8,
                                 smem_desc(vb + s * 2048, kTcKeys * 128, 1024), i_pv, i > 0 || s > 0);
                 umma_commit(bar + 8 * (kBarPvDone + b));
                 umma_commit(bar + 8 * (kBarKvEmpty + i % kKvStages));
@@ -310,14 +328,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
             if (!(ok = wait_warp(bar + 8 * (kBarSFull + b), (i >> 1) & 1)))
                 break;
             tc_fence_after_sync();
-            uint32_t sr[64];
-            tmem_ld32(lane_base + kColS + b * kTcKeys, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(lane_base + kColS + b * kTcKeys + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            uint32_t sr0[32], sr1[32];
+            tmem_ld32(lane_base + kColS + b * kTcKeys, sr0);
+            tmem_ld32(lane_base + kColS + b * kTcKeys + 32, sr1);
             tmem_wait_ld();
             float s[64];
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-                s[j] = __uint_as_float(sr[j]);
+            for (int j = 0; j < 32; ++j) {
+                s[j] = __uint_as_float(sr0[j]);
+                s[j + 32] = __uint_as_float(sr1[j]);
+            }
             const int lim = i < c.n_pre ? c.P - i * kTcKeys : t + 1 - (i - c.n_pre) * kTcKeys;
             if (lim < kTcKeys) {
 #pragma unroll
@@ -346,9 +366,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
             const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             l = l * alpha + sum;
             m_used = m_new;
-            // P buffer b was last read by the value product of tile i - 2
-            if (i >= 2 && !(ok = wait_warp(bar + 8 * (kBarPvDone + b), ((i - 2) >> 1) & 1)))
-                break;
+            // P row into tensor memory, f16 pairs, the A operand of the value
+            // product.  P[b] was last read by the value product of tile i - 2,
+            // which ran before Q K^T of tile i (in issue order): it is free.
+            {
+                uint32_t pw[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    pw[j] = pack_f16x2(s[2 * j], s[2 * j + 1]);
+                tmem_st32(lane_base + kColP + b * kColPStride, pw);
+            }
+            // a raised maximum: rescale the O rows of the warp once the value
+            // product of tile i - 1 has landed
             if (__any_sync(kFullMask, need) && i >= 1) {
                 const int pb = (i - 1) & 1;
                 if (!(ok = wait_warp(bar + 8 * (kBarPvDone + pb), ((i - 1) >> 1) & 1)))
@@ -364,14 +393,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
                         o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
                     tmem_st32(lane_base + kColO + 32 * cb, o);
                 }
-                tmem_wait_st();
             }
-            // P row into tensor memory, f16 pairs, the A operand of the value product
-            uint32_t pw[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                pw[j] = pack_f16x2(s[2 * j], s[2 * j + 1]);
-            tmem_st32(lane_base + kColP + b * (kTcKeys / 2), pw);
             tmem_wait_st();
             tc_fence_before_sync();
             mbar_arrive(bar + 8 * (kBarPFull + b));
@@ -400,18 +422,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) extend_tc_kernel(const ExtendPa
                                              __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
                 } else {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + off + 32 * cb);
+                    auto bf2 = [&](int j) {
+                        const __nv_bfloat162 two =
+                            __floats2bfloat162_rn(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
+                        return *reinterpret_cast<const uint32_t *>(&two);
+                    };
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint4 v;
-                        uint32_t *vw = &v.x;
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            __nv_bfloat162 two = __floats2bfloat162_rn(__uint_as_float(o[8 * k + 2 * e]) * inv,
-                                                                       __uint_as_float(o[8 * k + 2 * e + 1]) * inv);
-                            vw[e] = *reinterpret_cast<uint32_t *>(&two);
-                        }
-                        dst[k] = v;
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_uint4(bf2(8 * k), bf2(8 * k + 2), bf2(8 * k + 4), bf2(8 * k + 6));
                 }
             }
         }
