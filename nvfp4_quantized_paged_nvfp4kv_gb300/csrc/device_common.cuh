@@ -159,6 +159,38 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t byte)
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
 }
 
+// max of three fp32 (a NaN operand is ignored, as by fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Two fp32 lanes in one 64-bit register (low lane first): packed add, round
+// to nearest even in each lane.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi)
+{
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ float f32x2_lo(uint64_t v)
+{
+    return __uint_as_float(static_cast<uint32_t>(v));
+}
+
+__device__ __forceinline__ float f32x2_hi(uint64_t v)
+{
+    return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
 {
     uint32_t r;

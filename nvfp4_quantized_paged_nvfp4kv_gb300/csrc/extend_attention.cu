@@ -1,62 +1,76 @@
-// Extend attention over the FP8 prefix workspace and the current chunk.
+// Extend attention on the fifth-generation tensor cores (tcgen05).
 //
 // "SGLang stores KV cache in 4 bits" (LMSYS summary), Interpretation: on the
 // extend path the cached prefix is dequantised into one FP8 workspace and the
-// new chunk attends over it and over itself.  Chunk token t of a sequence
-// with prefix length P sees the P prefix keys and chunk keys 0 .. t.
+// new chunk attends over it and over itself; chunk token t of a sequence with
+// prefix length P sees the P prefix keys and chunk keys 0 .. t.
 //
 // One CTA owns 128 rows of one sequence and one kv head, a row being a
-// (chunk token, query head of the group) pair taken token-major, so the g
-// query heads that share a kv head read each key tile once.  Eight warps own
-// 16 rows each and run a flash-attention forward over key tiles of 64:
-// S = Q K^T and O += P V on mma.sync m16n8k16 (f16 operands, fp32
-// accumulators), online softmax in base 2 with sm_scale * log2(e) folded
-// into Q.  The CTA converts every key tile once into f16 shared memory
-// (E4M3 -> f16 and bf16 -> f16, both exact in range), double buffered, while
-// the next tile's raw bytes are in flight by cp.async.
+// (chunk token, query head of the group) pair taken token-major.  Per key
+// tile of 64:
+//   S = Q K^T     tcgen05.mma M128 N64 K16 x 8 into tensor memory (two S
+//                 buffers, so Q K^T of tile i+1 runs during the softmax of i)
+//   softmax       one thread per row reads its S row from tensor memory,
+//                 masks, takes exp2 against a running maximum that is only
+//                 raised when it grows by more than 2^8 (then the O row in
+//                 tensor memory is rescaled), writes P (f16) back to tensor
+//                 memory
+//   O += P V      tcgen05.mma M128 N128 K16 x 4 with P read from tensor
+//                 memory, O resident in tensor memory
+// Warps 0-3 run the softmax, warps 4-7 convert key tiles (E4M3 prefix rows or
+// bf16 chunk rows) to f16 in the 128-byte-swizzled operand layout, warp 8
+// allocates tensor memory and issues the MMAs.  mbarriers order the roles;
+// every wait is bounded and a timeout is reported.
 //
 // The appending variant also writes the chunk's K/V into the NVFP4 cache
 // ("SGLang stores KV cache in 4 bits", Interpretation: prefill quantises the
-// new K/V into the cache): each chunk key tile has one owning CTA, which
-// stages it through shared memory and quantises it before its attention loop.
-// Every row tile of a kv head reads the same chunk tiles, so the chunk stays
-// in L2 and no separate pass over it is needed.
+// new K/V into the cache): each chunk key tile has one owning CTA, whose
+// converter warps quantise it after their last key tile.
 #include "record_write.cuh"
+#include "tcgen05.cuh"
 
 namespace nvfp4kv {
 namespace {
 
-constexpr int kExtWarps = 8;
-constexpr int kExtThreads = 32 * kExtWarps;
-constexpr int kExtRows = 16 * kExtWarps;                  // rows per CTA
-constexpr int kExtKeys = 64;                              // keys per tile
-constexpr uint32_t kTileBytes = kExtKeys * kHeadDim * 2;  // one f16 K or V tile
-constexpr uint32_t kF16Bytes = 2 * 2 * kTileBytes;        // [buffer][K, V] f16 tiles
+constexpr int kTcRows = 128;                  // M: rows per CTA
+constexpr int kTcKeys = 64;                   // keys per tile
+constexpr int kSoftmaxThreads = 128;          // warps 0-3
+constexpr int kProducerThreads = 128;         // warps 4-7
+constexpr int kMmaWarp = 8;
+constexpr int kTcThreads = kSoftmaxThreads + kProducerThreads + 32;
+constexpr float kRescaleLog2 = 8.f;           // raise the running maximum only past this margin
 
-static_assert(kExtKeys * kHeadDim / 16 == 2 * kExtThreads, "FP8 tile: two 16-byte pieces a thread");
-static_assert(kExtKeys * kHeadDim / 8 == 4 * kExtThreads, "bf16 tile: four 16-byte pieces a thread");
+constexpr uint32_t kQBytes = kTcRows * kHeadDim * 2;   // 32 KB
+constexpr uint32_t kKVBytes = kTcKeys * kHeadDim * 2;  // 16 KB per K or V tile
+constexpr uint32_t kOffQ = 0;
+constexpr int kKvStages = 2;                           // converted key tiles in flight
+constexpr uint32_t kOffK = kOffQ + kQBytes;            // kKvStages buffers
+constexpr uint32_t kOffV = kOffK + kKvStages * kKVBytes;
+constexpr uint32_t kOffBar = kOffV + kKvStages * kKVBytes;
+// kv_full / kv_empty per key-tile stage; s_full, p_full, pv_done per S / P buffer
+enum { kBarKvFull = 0, kBarKvEmpty = 4, kBarSFull = 8, kBarPFull = 10, kBarPvDone = 12, kBarDone = 14, kNumBars = 15 };
+constexpr uint32_t kOffTmemSlot = kOffBar + 8 * kNumBars;
+constexpr uint32_t kOffFail = kOffTmemSlot + 4;
+constexpr uint32_t kTcSmem = kOffFail + 4 + 1024;      // + slack to align the base to 1024 bytes
+// tensor-memory columns: O, S[2] (fp32); P[b] (f16 pairs) overwrites the first
+// 32 columns of S[b] once the softmax has read them.  The MMAs of a CTA run in
+// issue order, so Q K^T of tile i + 2 (into S[b]) follows P V of tile i.
+constexpr uint32_t kColO = 0, kColS = 128, kColP = 128;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColPStride = kTcKeys;                // P[b] at kColP + b * kColPStride
 
-// Byte offset of 16-byte chunk c (channels 8c .. 8c + 7) of key row `key` in
-// an f16 tile: 256-byte rows, chunks XOR-swizzled by the row's low three bits
-// so that eight rows read at one chunk index hit eight different bank groups.
-__device__ __forceinline__ uint32_t tile_off(uint32_t key, uint32_t c)
+static_assert(kTcSmem <= 227 * 1024, "shared memory");
+// two CTAs per SM, no more: their 2 x 256 tensor-memory columns are then
+// always free
+static_assert(2 * kTcSmem <= 228 * 1024 && 3 * kTcSmem > 228 * 1024, "two CTAs per SM");
+static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzle atoms");
+
+// Byte offset of 16-byte chunk c (f16 columns 8c .. 8c + 7) of row r in a
+// 128-byte-swizzled tile of `rows` rows: 64-column blocks of rows x 128
+// bytes, eight-row atoms of 1024 bytes, chunk position c ^ (r mod 8).
+__device__ __forceinline__ uint32_t sw128(uint32_t rows, uint32_t r, uint32_t c)
 {
-    return key * 256u + ((c ^ (key & 7u)) << 4);
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                              uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
+    return (c >> 3) * rows * 128u + r * 128u + (((c & 7u) ^ (r & 7u)) << 4);
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
@@ -66,123 +80,123 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
                  : "memory");
 }
 
-// Two bf16 (low half first) to f16x2, round to nearest even.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
+__device__ __forceinline__ uint4 ldg_nc(const void *p)
 {
-    return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_scaled_f16x2(uint32_t w, float s)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float s)
 {
     return pack_f16x2(__uint_as_float(w << 16) * s, __uint_as_float(w & 0xffff0000u) * s);
 }
 
-// Where the CTA is in its sequence and which tiles it visits.
-struct ExtCta {
-    int c0;          // first chunk row of the sequence
-    int C;           // chunk length
-    int P;           // prefix length
-    int64_t p0;      // first prefix row of the sequence
-    int n_pre;       // prefix tiles
-    int n_tiles;     // prefix tiles + chunk tiles
-    int t_min;       // smallest chunk token among the CTA's rows
+__device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, volatile int *fail, int32_t *dev_status)
+{
+    if (*fail)
+        return false;
+    if (mbar_wait_bounded(bar, parity, kWaitLimit))
+        return true;
+    *fail = 1;
+    report(dev_status, NVFP4KV_DEV_TIMEOUT);
+    return false;
+}
+
+struct TcCta {
+    int c0, C, P;
+    int64_t p0;
+    int n_pre, n_tiles;
 };
 
-// Raw bytes of one key tile are staged with cp.async into a per-thread slot
-// array: piece u of thread tid sits at stage + (u * kExtThreads + tid) * 16.
-// FP8 prefix tiles use pieces 0..3 (K, K, V, V), bf16 chunk tiles 0..7 (K x4,
-// V x4).  Each thread converts only the pieces it copied, so a wait on its own
-// copies is enough before the conversion.
-constexpr uint32_t kStageBytes = 8 * kExtThreads * 16;
-constexpr uint32_t kExtSmem = kF16Bytes + kStageBytes;
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
+// Producer thread pt (0..127): load key tile i, wait until its stage is free,
+// convert it to f16 in the 128-byte-swizzled layout and signal the MMA warp.
+// FP8 prefix tiles: 64 keys x 8 pieces of 16 bytes per K and per V, four
+// pieces a thread each, loaded together.  bf16 chunk tiles: 64 keys x 16
+// pieces per K and per V, eight a thread each, K then V (eight loads in
+// flight a thread keep the register count low).  Keys past the end are zeros.
+__device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta &c, int h, int i, int pt,
+                                             uint32_t base, volatile int *fail)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit()
-{
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all()
-{
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
-// Start the copies of tile i; keys past the prefix or chunk read as zeros.
-__device__ __forceinline__ void load_tile(const ExtendParams &p, const ExtCta &c, int h, int i, uint32_t stage)
-{
-    const int tid = threadIdx.x;
-    if (i < c.n_pre) {
-        const int k0 = i * kExtKeys;
+    const int st = i % kKvStages;
+    const uint32_t kdst = base + kOffK + st * kKVBytes, vdst = base + kOffV + st * kKVBytes;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    uint4 raw[8];
+    const bool pre = i < c.n_pre;
+    const int k0 = (pre ? i : i - c.n_pre) * kTcKeys;
+    if (pre) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = tid + kExtThreads * (u & 1);
+        for (int u = 0; u < 8; ++u) {
+            const int idx = pt + kProducerThreads * (u & 3);
             const int key = idx >> 3, piece = idx & 7;
-            const uint8_t *base = u < 2 ? p.k_prefix : p.v_prefix;
-            const bool ok = k0 + key < c.P;
-            const uint8_t *src = ok ? base + ((c.p0 + k0 + key) * p.hkv + h) * kHeadDim + 16 * piece : base;
-            cp_async16(stage + (u * kExtThreads + tid) * 16u, src, ok);
+            const uint8_t *src = (u < 4 ? p.k_prefix : p.v_prefix) + ((c.p0 + k0 + key) * p.hkv + h) * kHeadDim +
+                                 16 * piece;
+            raw[u] = k0 + key < c.P ? ldg_nc(src) : zero;
         }
     } else {
-        const int k0 = (i - c.n_pre) * kExtKeys;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int idx = tid + kExtThreads * (u & 3);
+            const int idx = pt + kProducerThreads * u;
             const int key = idx >> 4, piece = idx & 15;
-            const uint16_t *base = u < 4 ? p.k_chunk : p.v_chunk;
-            const bool ok = k0 + key < c.C;
-            const uint16_t *src =
-                ok ? base + (static_cast<int64_t>(c.c0 + k0 + key) * p.hkv + h) * kHeadDim + 8 * piece : base;
-            cp_async16(stage + (u * kExtThreads + tid) * 16u, src, ok);
+            raw[u] = k0 + key < c.C ? ldg_nc(p.k_chunk + (static_cast<int64_t>(c.c0 + k0 + key) * p.hkv + h) *
+                                                              kHeadDim + 8 * piece)
+                                    : zero;
         }
     }
-    cp_async_commit();
+    // stage st was last read by the MMAs of tile i - kKvStages
+    if (i >= kKvStages && !wait_or_fail(base + kOffBar + 8 * (kBarKvEmpty + st), ((i / kKvStages) - 1) & 1, fail,
+                                        p.dev_status))
+        return false;
+    if (pre) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = pt + kProducerThreads * (u & 3);
+            const uint32_t key = idx >> 3, piece = idx & 7;
+            uint4 lo, hi;
+            e4m3x4_to_f16x2x2(raw[u].x, lo.x, lo.y);
+            e4m3x4_to_f16x2x2(raw[u].y, lo.z, lo.w);
+            e4m3x4_to_f16x2x2(raw[u].z, hi.x, hi.y);
+            e4m3x4_to_f16x2x2(raw[u].w, hi.z, hi.w);
+            const uint32_t dst = u < 4 ? kdst : vdst;
+            // pieces 4..7 store their high half first: eight lanes, eight bank groups
+            const uint32_t first = (piece >> 2) & 1u;
+            sts128(dst + sw128(kTcKeys, key, 2 * piece + first), first ? hi : lo);
+            sts128(dst + sw128(kTcKeys, key, 2 * piece + 1 - first), first ? lo : hi);
+        }
+    } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            if (half == 1) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int idx = pt + kProducerThreads * u;
+                    const int key = idx >> 4, piece = idx & 15;
+                    raw[u] = k0 + key < c.C ? ldg_nc(p.v_chunk + (static_cast<int64_t>(c.c0 + k0 + key) * p.hkv + h) *
+                                                                      kHeadDim + 8 * piece)
+                                            : zero;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = pt + kProducerThreads * u;
+                const uint32_t key = idx >> 4, piece = idx & 15;
+                uint4 f;
+                f.x = bf16x2_to_f16x2(raw[u].x, 1.f);
+                f.y = bf16x2_to_f16x2(raw[u].y, 1.f);
+                f.z = bf16x2_to_f16x2(raw[u].z, 1.f);
+                f.w = bf16x2_to_f16x2(raw[u].w, 1.f);
+                sts128((half ? vdst : kdst) + sw128(kTcKeys, key, piece), f);
+            }
+        }
+    }
+    fence_async_shared();
+    mbar_arrive(base + kOffBar + 8 * (kBarKvFull + st));
+    return true;
 }
 
-// Wait for this thread's copies of tile i, convert them to f16 and store them
-// into buffer `buf` (K tile at buf, V tile at buf + kTileBytes).
-__device__ __forceinline__ void store_tile(const ExtCta &c, int i, uint32_t stage, uint32_t buf)
-{
-    const int tid = threadIdx.x;
-    cp_async_wait_all();
-    if (i < c.n_pre) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = tid + kExtThreads * (u & 1);
-            const uint32_t key = idx >> 3, piece = idx & 7;
-            const uint32_t dst = buf + (u < 2 ? 0u : kTileBytes);
-            const uint4 w = lds128(stage + (u * kExtThreads + tid) * 16u);
-            uint4 lo, hi;
-            e4m3x4_to_f16x2x2(w.x, lo.x, lo.y);
-            e4m3x4_to_f16x2x2(w.y, lo.z, lo.w);
-            e4m3x4_to_f16x2x2(w.z, hi.x, hi.y);
-            e4m3x4_to_f16x2x2(w.w, hi.z, hi.w);
-            // the upper four pieces of a row store their high half first, so
-            // each group of eight lanes covers all eight bank groups
-            const uint32_t first = (piece >> 2) & 1u;
-            sts128(dst + tile_off(key, 2 * piece + first), first ? hi : lo);
-            sts128(dst + tile_off(key, 2 * piece + 1 - first), first ? lo : hi);
-        }
-    } else {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int idx = tid + kExtThreads * (u & 3);
-            const uint32_t key = idx >> 4, piece = idx & 15;
-            const uint32_t dst = buf + (u < 4 ? 0u : kTileBytes);
-            const uint4 w = lds128(stage + (u * kExtThreads + tid) * 16u);
-            uint4 h;
-            h.x = bf16x2_to_f16x2(w.x);
-            h.y = bf16x2_to_f16x2(w.y);
-            h.z = bf16x2_to_f16x2(w.z);
-            h.w = bf16x2_to_f16x2(w.w);
-            sts128(dst + tile_off(key, piece), h);
-        }
-    }
-}
+// ---- fused NVFP4 append of the chunk ----------------------------------------
 
 // Page-head record and token of a chunk token's slot; false when the slot is
 // skipped (negative) or out of range (reported when `rep`).
@@ -201,307 +215,345 @@ __device__ __forceinline__ bool append_site(const ExtendParams &p, int slot, int
     return true;
 }
 
-__device__ __forceinline__ void staged_block(const uint8_t *src, float (&x)[16], float G)
+// Producer thread pt quantises chunk keys k0 .. k0 + 63 of kv head h into the
+// cache, reading the bf16 rows from global memory (each group of loads issued
+// together).  K: 64 keys x 8 blocks, four a thread.  V: 32 key pairs x 8
+// blocks, two a thread; a pair on an even slot and its successor is written
+// whole, any other token through the atomic nibble merge.
+__device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const TcCta &c, int h, int k0, int pt)
 {
-    RawBlock<true> r;
-    r.v[0] = *reinterpret_cast<const uint4 *>(src);
-    r.v[1] = *reinterpret_cast<const uint4 *>(src + 16);
-    unpack<true>(r, x);
-    divide_by_tensor_scale(x, G);
-}
-
-// Quantise chunk keys k0 .. k0 + 63 of kv head h from the staged raw tile (K
-// rows at `raw`, V rows at raw + 64 * 256, 256 bytes a key) into the cache.
-// K: 64 keys x 8 blocks, two a thread.  V: 32 key pairs x 8 blocks, one a
-// thread; a pair on an even slot and its successor is written whole, any
-// other token through the atomic nibble merge.
-__device__ __forceinline__ void append_tile(const ExtendParams &p, const ExtCta &c, int h, int k0, const uint8_t *raw)
-{
-    const int tid = threadIdx.x;
+    auto offset = [&](int key, int blk) {
+        return (static_cast<size_t>(c.c0 + key) * p.hkv + h) * kHeadDim + blk * 16;
+    };
+    RawBlock<true> r[4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int item = tid + kExtThreads * u;
-        const int key = item >> 3, blk = item & 7;
-        if (k0 + key >= c.C)
-            continue;
+    for (int u = 0; u < 4; ++u) {
+        const int item = pt + kProducerThreads * u;
+        const int key = k0 + (item >> 3), blk = item & 7;
+        if (key < c.C)
+            load_raw<true>(p.k_chunk, offset(key, blk), r[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int item = pt + kProducerThreads * u;
+        const int key = k0 + (item >> 3), blk = item & 7;
         size_t rec;
         int tok;
-        if (!append_site(p, p.slot_mapping[c.c0 + k0 + key], h, rec, tok, blk == 0))
+        if (key >= c.C || !append_site(p, p.slot_mapping[c.c0 + key], h, rec, tok, blk == 0))
             continue;
         float x[16];
-        staged_block(raw + key * 256 + blk * 32, x, p.gscale);
+        unpack<true>(r[u], x);
+        divide_by_tensor_scale(x, p.gscale);
         write_nvfp4_block(p.pool + rec, false, tok, blk, x);
     }
-    const int key0 = 2 * (tid >> 3), blk = tid & 7;
-    const uint8_t *vraw = raw + kExtKeys * 256;
-    const bool has0 = k0 + key0 < c.C, has1 = k0 + key0 + 1 < c.C;
-    const int s0 = has0 ? p.slot_mapping[c.c0 + k0 + key0] : -1;
-    const int s1 = has1 ? p.slot_mapping[c.c0 + k0 + key0 + 1] : -1;
-    size_t rec0 = 0, rec1 = 0;
-    int tok0 = 0, tok1 = 0;
-    const bool ok0 = has0 && append_site(p, s0, h, rec0, tok0, false);
-    const bool ok1 = has1 && append_site(p, s1, h, rec1, tok1, false);
-    float x[16];
-    if (ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
-        uint32_t S0, S1, c0[2], c1[2];
-        staged_block(vraw + key0 * 256 + blk * 32, x, p.gscale);
-        quantize_block(x, S0, c0);
-        staged_block(vraw + (key0 + 1) * 256 + blk * 32, x, p.gscale);
-        quantize_block(x, S1, c1);
-        write_nvfp4_v_pair(p.pool + rec0, tok0, blk, S0, c0, S1, c1);
-        return;
-    }
-    if (ok0) {
-        staged_block(vraw + key0 * 256 + blk * 32, x, p.gscale);
-        write_nvfp4_block(p.pool + rec0, true, tok0, blk, x);
-    }
-    if (ok1) {
-        staged_block(vraw + (key0 + 1) * 256 + blk * 32, x, p.gscale);
-        write_nvfp4_block(p.pool + rec1, true, tok1, blk, x);
-    }
-}
-
-// One key tile for one warp's 16 rows.  lim_a / lim_b: keys of the tile that
-// rows a (lane / 4) and b (lane / 4 + 8) see, counted from the tile's start;
-// only read when `masked`.
-__device__ __forceinline__ void tile_step(uint32_t kbuf, uint32_t vbuf, const uint32_t (&qa)[8][4],
-                                          float (&o)[16][4], float &m_a, float &m_b, float &l_a, float &l_b,
-                                          bool masked, int lim_a, int lim_b)
-{
-    const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t rr = lane & 7u, mi = lane >> 3;
-
-    // S = Q K^T: eight n-tiles of 8 keys
-    float s[8][4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+    for (int u = 0; u < 2; ++u) {
+        const int item = pt + kProducerThreads * u;
+        const int key0 = k0 + 2 * (item >> 3), blk = item & 7;
+        if (key0 < c.C)
+            load_raw<true>(p.v_chunk, offset(key0, blk), r[2 * u]);
+        if (key0 + 1 < c.C)
+            load_raw<true>(p.v_chunk, offset(key0 + 1, blk), r[2 * u + 1]);
+    }
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t chunk = 2 * ks + (mi & 1u);
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-            const uint32_t key = 16 * np + 8 * (mi >> 1) + rr;
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbuf + key * 256u + ((chunk ^ rr) << 4), b0, b1, b2, b3);
-            mma_f16_16816(s[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-            mma_f16_16816(s[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+    for (int u = 0; u < 2; ++u) {
+        const int item = pt + kProducerThreads * u;
+        const int key0 = k0 + 2 * (item >> 3), blk = item & 7;
+        const bool has0 = key0 < c.C, has1 = key0 + 1 < c.C;
+        const int s0 = has0 ? p.slot_mapping[c.c0 + key0] : -1;
+        const int s1 = has1 ? p.slot_mapping[c.c0 + key0 + 1] : -1;
+        size_t rec0 = 0, rec1 = 0;
+        int tok0 = 0, tok1 = 0;
+        const bool ok0 = has0 && append_site(p, s0, h, rec0, tok0, false);
+        const bool ok1 = has1 && append_site(p, s1, h, rec1, tok1, false);
+        float x[16];
+        if (ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
+            uint32_t S0, S1, q0[2], q1[2];
+            unpack<true>(r[2 * u], x);
+            divide_by_tensor_scale(x, p.gscale);
+            quantize_block(x, S0, q0);
+            unpack<true>(r[2 * u + 1], x);
+            divide_by_tensor_scale(x, p.gscale);
+            quantize_block(x, S1, q1);
+            write_nvfp4_v_pair(p.pool + rec0, tok0, blk, S0, q0, S1, q1);
+            continue;
         }
-    }
-
-    if (masked) {
-        const int q2 = 2 * static_cast<int>(lane & 3u);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int key = 8 * j + q2 + (e & 1);
-                if (key >= (e < 2 ? lim_a : lim_b))
-                    s[j][e] = -INFINITY;
-            }
+        if (ok0) {
+            unpack<true>(r[2 * u], x);
+            divide_by_tensor_scale(x, p.gscale);
+            write_nvfp4_block(p.pool + rec0, true, tok0, blk, x);
         }
-    }
-
-    // online softmax, base 2 (Q carries sm_scale * log2 e)
-    float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        mx_a = fmaxf(mx_a, fmaxf(s[j][0], s[j][1]));
-        mx_b = fmaxf(mx_b, fmaxf(s[j][2], s[j][3]));
-    }
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(kFullMask, mx_a, 1));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(kFullMask, mx_a, 2));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(kFullMask, mx_b, 1));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(kFullMask, mx_b, 2));
-    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-    // a row that has seen no key yet keeps zero weights
-    const float base_a = mn_a == -INFINITY ? 0.f : mn_a;
-    const float base_b = mn_b == -INFINITY ? 0.f : mn_b;
-    const float al_a = fast_exp2(m_a - base_a), al_b = fast_exp2(m_b - base_b);
-    m_a = mn_a;
-    m_b = mn_b;
-    float sum_a = 0.f, sum_b = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        s[j][0] = fast_exp2(s[j][0] - base_a);
-        s[j][1] = fast_exp2(s[j][1] - base_a);
-        s[j][2] = fast_exp2(s[j][2] - base_b);
-        s[j][3] = fast_exp2(s[j][3] - base_b);
-        sum_a += s[j][0] + s[j][1];
-        sum_b += s[j][2] + s[j][3];
-    }
-    l_a = l_a * al_a + sum_a;
-    l_b = l_b * al_b + sum_b;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        o[j][0] *= al_a;
-        o[j][1] *= al_a;
-        o[j][2] *= al_b;
-        o[j][3] *= al_b;
-    }
-
-    // O += P V: four k-steps of 16 keys, sixteen n-tiles of 8 channels
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t a0 = pack_f16x2(s[2 * kk][0], s[2 * kk][1]);
-        const uint32_t a1 = pack_f16x2(s[2 * kk][2], s[2 * kk][3]);
-        const uint32_t a2 = pack_f16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-        const uint32_t a3 = pack_f16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-        const uint32_t key = 16 * kk + 8 * (mi & 1u) + rr;
-#pragma unroll
-        for (int cp = 0; cp < 8; ++cp) {
-            const uint32_t chunk = 2 * cp + (mi >> 1);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_trans(vbuf + key * 256u + ((chunk ^ rr) << 4), b0, b1, b2, b3);
-            mma_f16_16816(o[2 * cp], a0, a1, a2, a3, b0, b1);
-            mma_f16_16816(o[2 * cp + 1], a0, a1, a2, a3, b2, b3);
+        if (ok1) {
+            unpack<true>(r[2 * u + 1], x);
+            divide_by_tensor_scale(x, p.gscale);
+            write_nvfp4_block(p.pool + rec1, true, tok1, blk, x);
         }
     }
 }
 
 template <bool kAppend>
-__global__ void __launch_bounds__(kExtThreads, 1) extend_kernel(const ExtendParams p)
+__global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const ExtendParams p)
 {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int b = blockIdx.z;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw_addr);
+    volatile int *fail = reinterpret_cast<volatile int *>(gbase + kOffFail);
+    const uint32_t bar = base + kOffBar;
+
+    const int b_seq = blockIdx.z;
     const int h = blockIdx.y;
     const int tile = static_cast<int>(gridDim.x - 1 - blockIdx.x);  // later rows see more keys: start them first
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
 
-    ExtCta c;
-    c.c0 = p.q_indptr[b];
-    const int c1 = p.q_indptr[b + 1];
-    c.P = p.prefix_lens[b];
-    const int kv0 = p.kv_indptr[b];
+    TcCta c;
+    c.c0 = p.q_indptr[b_seq];
+    const int c1 = p.q_indptr[b_seq + 1];
+    c.P = p.prefix_lens[b_seq];
+    const int kv0 = p.kv_indptr[b_seq];
     if (c.c0 < 0 || c1 < c.c0 || c1 > p.q_rows || c1 - c.c0 > p.max_q_len || c.P < 0 || kv0 < 0 ||
         static_cast<int64_t>(kv0) + c.P > p.prefix_rows) {
-        if (threadIdx.x == 0)
+        if (tid == 0)
             report(p.dev_status, NVFP4KV_DEV_BAD_LEN);
         return;
     }
     c.C = c1 - c.c0;
     c.p0 = kv0;
     const int g = p.group;
-    const int R = c.C * g;                 // rows of this sequence and kv head
-    const int row0 = tile * kExtRows;
+    const int R = c.C * g;
+    const int row0 = tile * kTcRows;
     if (row0 >= R)
         return;
-    const int row_end = min(row0 + kExtRows, R);
-    c.t_min = row0 / g;
-    const int t_max = (row_end - 1) / g;
-    c.n_pre = (c.P + kExtKeys - 1) / kExtKeys;
-    c.n_tiles = c.n_pre + t_max / kExtKeys + 1;
-    // chunk key tiles this CTA appends: those whose first key's first row
-    // (64 kt g) falls in its row range
-    const int own_lo = (row0 + kExtKeys * g - 1) / (kExtKeys * g);
-    const int own_hi = (row0 + kExtRows + kExtKeys * g - 1) / (kExtKeys * g);
+    const int t_max = (min(row0 + kTcRows, R) - 1) / g;
+    c.n_pre = (c.P + kTcKeys - 1) / kTcKeys;
+    c.n_tiles = c.n_pre + t_max / kTcKeys + 1;
 
-    // this lane's two rows; rows past the end repeat the last row and are not stored
-    const int r_a = row0 + 16 * warp + (lane >> 2);
-    const int r_b = r_a + 8;
-    const bool warp_live = row0 + 16 * warp < R;
-    const int t_a = min(r_a, R - 1) / g, t_b = min(r_b, R - 1) / g;
-    const int hq_a = h * g + (min(r_a, R - 1) - t_a * g);
-    const int hq_b = h * g + (min(r_b, R - 1) - t_b * g);
-    const int t_warp_max = min(row0 + 16 * warp + 15, R - 1) / g;
-
-    // Q fragments, scaled by sm_scale * log2 e and rounded to f16
-    uint32_t qa[8][4];
-    {
-        const int q2 = 2 * (lane & 3);
-        const uint16_t *qa_row = p.q + (static_cast<int64_t>(c.c0 + t_a) * p.hq + hq_a) * kHeadDim + q2;
-        const uint16_t *qb_row = p.q + (static_cast<int64_t>(c.c0 + t_b) * p.hq + hq_b) * kHeadDim + q2;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t wa0 = *reinterpret_cast<const uint32_t *>(qa_row + 16 * ks);
-            const uint32_t wb0 = *reinterpret_cast<const uint32_t *>(qb_row + 16 * ks);
-            const uint32_t wa1 = *reinterpret_cast<const uint32_t *>(qa_row + 16 * ks + 8);
-            const uint32_t wb1 = *reinterpret_cast<const uint32_t *>(qb_row + 16 * ks + 8);
-            qa[ks][0] = bf16x2_scaled_f16x2(wa0, p.qscale);
-            qa[ks][1] = bf16x2_scaled_f16x2(wb0, p.qscale);
-            qa[ks][2] = bf16x2_scaled_f16x2(wa1, p.qscale);
-            qa[ks][3] = bf16x2_scaled_f16x2(wb1, p.qscale);
+    // Q tile: rows past the end are zeros; sm_scale * log2 e folded in
+    for (int idx = tid; idx < kTcRows * 16; idx += kTcThreads) {
+        const int r = idx >> 4, piece = idx & 15;
+        const int row = row0 + r;
+        uint4 f = make_uint4(0, 0, 0, 0);
+        if (row < R) {
+            const int t = row / g;
+            const uint4 w = ldg_nc(p.q + (static_cast<int64_t>(c.c0 + t) * p.hq + h * g + (row - t * g)) * kHeadDim +
+                                   8 * piece);
+            f.x = bf16x2_to_f16x2(w.x, p.qscale);
+            f.y = bf16x2_to_f16x2(w.y, p.qscale);
+            f.z = bf16x2_to_f16x2(w.z, p.qscale);
+            f.w = bf16x2_to_f16x2(w.w, p.qscale);
         }
+        sts128(base + kOffQ + sw128(kTcRows, r, piece), f);
     }
-
-    float o[16][4];
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-        o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-
-    const uint32_t sbase = smem_addr(smem);
-    const uint32_t stage = sbase + kF16Bytes;
-    if constexpr (kAppend) {
-        // the chunk key tiles this CTA owns go into the cache first, staged
-        // through the same area; the attention below reads them from L2
-        for (int kt = own_lo; kt < own_hi && kt * kExtKeys < c.C; ++kt) {
-            load_tile(p, c, h, c.n_pre + kt, stage);
-            cp_async_wait_all();
-            __syncthreads();
-            append_tile(p, c, h, kt * kExtKeys, smem + kF16Bytes);
-            __syncthreads();
+    if (tid == 0) {
+        for (int k = 0; k < kKvStages; ++k) {
+            mbar_init(bar + 8 * (kBarKvFull + k), kProducerThreads);
+            mbar_init(bar + 8 * (kBarKvEmpty + k), 1);
         }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(bar + 8 * (kBarSFull + k), 1);
+            mbar_init(bar + 8 * (kBarPFull + k), kSoftmaxThreads);
+            mbar_init(bar + 8 * (kBarPvDone + k), 1);
+        }
+        mbar_init(bar + 8 * kBarDone, 1);
+        *fail = 0;
+        fence_mbar_init();
     }
-    load_tile(p, c, h, 0, stage);
-    store_tile(c, 0, stage, sbase);
+    if (warp == kMmaWarp)
+        tmem_alloc(base + kOffTmemSlot, kTmemCols);
+    fence_async_shared();
+    tc_fence_before_sync();
     __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + kOffTmemSlot);
 
-    for (int i = 0; i < c.n_tiles; ++i) {
-        const uint32_t buf = sbase + static_cast<uint32_t>(i & 1) * 2u * kTileBytes;
-        if (i + 1 < c.n_tiles)
-            load_tile(p, c, h, i + 1, stage);
-        if (warp_live) {
-            if (i < c.n_pre) {
-                const int lim = c.P - i * kExtKeys;
-                tile_step(buf, buf + kTileBytes, qa, o, m_a, m_b, l_a, l_b, lim < kExtKeys, lim, lim);
-            } else {
-                const int k0 = (i - c.n_pre) * kExtKeys;
-                if (k0 <= t_warp_max) {
-                    const bool masked = k0 + kExtKeys - 1 > c.t_min;
-                    tile_step(buf, buf + kTileBytes, qa, o, m_a, m_b, l_a, l_b, masked, t_a + 1 - k0,
-                              t_b + 1 - k0);
+    if (warp == kMmaWarp) {
+        if ((tid & 31) == 0) {
+            constexpr uint32_t i_qk = idesc_f16(kTcRows, kTcKeys, false);
+            constexpr uint32_t i_pv = idesc_f16(kTcRows, kHeadDim, true);
+            bool ok = true;
+            auto issue_qk = [&](int i) {
+                const int b = i & 1, st = i % kKvStages;
+                if (!wait_or_fail(bar + 8 * (kBarKvFull + st), (i / kKvStages) & 1, fail, p.dev_status))
+                    return false;
+                tc_fence_after_sync();
+                const uint32_t kb = base + kOffK + st * kKVBytes;
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    umma_f16(tmem + kColS + b * kTcKeys,
+                             smem_desc(base + kOffQ + (s >> 2) * (kTcRows * 128) + (s & 3) * 32, 16, 1024),
+                             smem_desc(kb + (s >> 2) * (kTcKeys * 128) + (s & 3) * 32, 16, 1024), i_qk, s > 0);
+                umma_commit(bar + 8 * (kBarSFull + b));
+                return true;
+            };
+            ok = issue_qk(0);
+            for (int i = 0; ok && i < c.n_tiles; ++i) {
+                const int b = i & 1;
+                if (i + 1 < c.n_tiles && !(ok = issue_qk(i + 1)))
+                    break;
+                if (!(ok = wait_or_fail(bar + 8 * (kBarPFull + b), (i >> 1) & 1, fail, p.dev_status)))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t vb = base + kOffV + (i % kKvStages) * kKVBytes;
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    umma_f16_ts(tmem + kColO, tmem + kColP + b * kColPStride + s * 8,
+                                smem_desc(vb + s * 2048, kTcKeys * 128, 1024), i_pv, i > 0 || s > 0);
+                umma_commit(bar + 8 * (kBarPvDone + b));
+                umma_commit(bar + 8 * (kBarKvEmpty + i % kKvStages));
+            }
+            // nothing of this thread's may still run when tensor memory is freed
+            umma_commit(bar + 8 * kBarDone);
+            if (!mbar_wait_bounded(bar + 8 * kBarDone, 0, kWaitLimit))
+                report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp >= kSoftmaxThreads / 32) {
+        const int pt = tid - kSoftmaxThreads;
+        for (int i = 0; i < c.n_tiles; ++i)
+            if (!produce_tile(p, c, h, i, pt, base, fail))
+                break;
+        if constexpr (kAppend) {
+            // the chunk key tiles whose first key's first row (64 kt g) falls in
+            // this CTA's rows; done while the last tiles are still in the MMAs
+            const int per = kTcKeys * g;
+            for (int kt = (row0 + per - 1) / per; kt < (row0 + kTcRows + per - 1) / per && kt * kTcKeys < c.C; ++kt)
+                append_chunk_tile(p, c, h, kt * kTcKeys, pt);
+        }
+    } else {
+        // softmax: thread r owns row row0 + r, tensor-memory lane r
+        const int r = tid;
+        const int row = row0 + r;
+        const int t = min(row, R - 1) / g;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        // the warp leaves together: its tensor-memory accesses are warp-wide
+        auto wait_warp = [&](uint32_t bar_addr, uint32_t parity) {
+            return __all_sync(kFullMask, wait_or_fail(bar_addr, parity, fail, p.dev_status));
+        };
+        for (int i = 0; i < c.n_tiles; ++i) {
+            const int b = i & 1;
+            if (!(ok = wait_warp(bar + 8 * (kBarSFull + b), (i >> 1) & 1)))
+                break;
+            tc_fence_after_sync();
+            uint32_t sr0[32], sr1[32];
+            tmem_ld32(lane_base + kColS + b * kTcKeys, sr0);
+            tmem_ld32(lane_base + kColS + b * kTcKeys + 32, sr1);
+            tmem_wait_ld();
+            float s[64];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                s[j] = __uint_as_float(sr0[j]);
+                s[j + 32] = __uint_as_float(sr1[j]);
+            }
+            const int lim = i < c.n_pre ? c.P - i * kTcKeys : t + 1 - (i - c.n_pre) * kTcKeys;
+            if (lim < kTcKeys) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    if (j >= lim)
+                        s[j] = -INFINITY;
+            }
+            // eight independent partial maxima (three-input max) and packed
+            // two-lane subtractions and sums keep the chains and counts short
+            float pm[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                pm[k] = fmax3(fmax3(s[8 * k], s[8 * k + 1], s[8 * k + 2]), fmax3(s[8 * k + 3], s[8 * k + 4], s[8 * k + 5]),
+                              fmaxf(s[8 * k + 6], s[8 * k + 7]));
+            const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+            const bool need = mx > m_used + kRescaleLog2;
+            const float m_new = need ? mx : m_used;
+            const float mbase = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = need ? fast_exp2(m_used - mbase) : 1.f;
+            const uint64_t neg2 = f32x2_pack(-mbase, -mbase);
+            uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const uint64_t d = add_f32x2(f32x2_pack(s[2 * j], s[2 * j + 1]), neg2);
+                s[2 * j] = fast_exp2(f32x2_lo(d));
+                s[2 * j + 1] = fast_exp2(f32x2_hi(d));
+                acc[j & 3] = add_f32x2(acc[j & 3], f32x2_pack(s[2 * j], s[2 * j + 1]));
+            }
+            const uint64_t a01 = add_f32x2(acc[0], acc[1]), a23 = add_f32x2(acc[2], acc[3]);
+            const uint64_t a = add_f32x2(a01, a23);
+            const float sum = f32x2_lo(a) + f32x2_hi(a);
+            l = l * alpha + sum;
+            m_used = m_new;
+            // P row into tensor memory, f16 pairs, the A operand of the value
+            // product.  P[b] was last read by the value product of tile i - 2,
+            // which ran before Q K^T of tile i (in issue order): it is free.
+            {
+                uint32_t pw[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    pw[j] = pack_f16x2(s[2 * j], s[2 * j + 1]);
+                tmem_st32(lane_base + kColP + b * kColPStride, pw);
+            }
+            // a raised maximum: rescale the O rows of the warp once the value
+            // product of tile i - 1 has landed
+            if (__any_sync(kFullMask, need) && i >= 1) {
+                const int pb = (i - 1) & 1;
+                if (!(ok = wait_warp(bar + 8 * (kBarPvDone + pb), ((i - 1) >> 1) & 1)))
+                    break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + kColO + 32 * cb, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                    tmem_st32(lane_base + kColO + 32 * cb, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            mbar_arrive(bar + 8 * (kBarPFull + b));
+        }
+        if (ok) {
+            const int last = c.n_tiles - 1;
+            ok = wait_warp(bar + 8 * (kBarPvDone + (last & 1)), (last >> 1) & 1);
+        }
+        if (ok) {
+            tc_fence_after_sync();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const bool store = row < R;
+            const int64_t off = (static_cast<int64_t>(c.c0 + t) * p.hq + h * g + (min(row, R - 1) - t * g)) * kHeadDim;
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t o[32];
+                tmem_ld32(lane_base + kColO + 32 * cb, o);
+                tmem_wait_ld();
+                if (!store)
+                    continue;
+                if (p.out_f32) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off + 32 * cb);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                             __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + off + 32 * cb);
+                    auto bf2 = [&](int j) {
+                        const __nv_bfloat162 two =
+                            __floats2bfloat162_rn(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
+                        return *reinterpret_cast<const uint32_t *>(&two);
+                    };
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_uint4(bf2(8 * k), bf2(8 * k + 2), bf2(8 * k + 4), bf2(8 * k + 6));
                 }
             }
         }
-        if (i + 1 < c.n_tiles)
-            store_tile(c, i + 1, stage, sbase + static_cast<uint32_t>((i + 1) & 1) * 2u * kTileBytes);
-        __syncthreads();
     }
 
-    if (!warp_live)
-        return;
-    l_a += __shfl_xor_sync(kFullMask, l_a, 1);
-    l_a += __shfl_xor_sync(kFullMask, l_a, 2);
-    l_b += __shfl_xor_sync(kFullMask, l_b, 1);
-    l_b += __shfl_xor_sync(kFullMask, l_b, 2);
-    const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f;
-    const float inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
-    const int q2 = 2 * (lane & 3);
-    const int64_t off_a = (static_cast<int64_t>(c.c0 + t_a) * p.hq + hq_a) * kHeadDim + q2;
-    const int64_t off_b = (static_cast<int64_t>(c.c0 + t_b) * p.hq + hq_b) * kHeadDim + q2;
-    const bool st_a = r_a < R, st_b = r_b < R;
-    if (p.out_f32) {
-        float *out = static_cast<float *>(p.out);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if (st_a)
-                *reinterpret_cast<float2 *>(out + off_a + 8 * j) = make_float2(o[j][0] * inv_a, o[j][1] * inv_a);
-            if (st_b)
-                *reinterpret_cast<float2 *>(out + off_b + 8 * j) = make_float2(o[j][2] * inv_b, o[j][3] * inv_b);
-        }
-    } else {
-        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if (st_a)
-                *reinterpret_cast<__nv_bfloat162 *>(out + off_a + 8 * j) =
-                    __floats2bfloat162_rn(o[j][0] * inv_a, o[j][1] * inv_a);
-            if (st_b)
-                *reinterpret_cast<__nv_bfloat162 *>(out + off_b + 8 * j) =
-                    __floats2bfloat162_rn(o[j][2] * inv_b, o[j][3] * inv_b);
-        }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -509,16 +561,13 @@ __global__ void __launch_bounds__(kExtThreads, 1) extend_kernel(const ExtendPara
 
 cudaError_t launch_extend_attention(const ExtendParams &p, cudaStream_t s)
 {
-    static_assert(kExtSmem <= 227 * 1024, "shared memory");
-    if (p.pool == nullptr)
-        return launch_extend_attention_tc(p, s);
-    const auto kernel = extend_kernel<true>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kExtSmem);
+    const auto kernel = p.pool != nullptr ? extend_tc_kernel<true> : extend_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     if (e != cudaSuccess)
         return e;
     const int64_t rows = static_cast<int64_t>(p.max_q_len) * p.group;
-    const dim3 grid(static_cast<unsigned>((rows + kExtRows - 1) / kExtRows), p.hkv, p.batch);
-    kernel<<<grid, kExtThreads, kExtSmem, s>>>(p);
+    const dim3 grid(static_cast<unsigned>((rows + kTcRows - 1) / kTcRows), p.hkv, p.batch);
+    kernel<<<grid, kTcThreads, kTcSmem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -141,6 +141,5 @@ cudaError_t launch_decode_fp8(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_merge(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_dequant_prefix_fp8(const PrefixParams &p, cudaStream_t s);
 cudaError_t launch_extend_attention(const ExtendParams &p, cudaStream_t s);   // appends when p.pool != null
-cudaError_t launch_extend_attention_tc(const ExtendParams &p, cudaStream_t s);  // tcgen05, attention only
 
 } // namespace nvfp4kv
