@@ -577,7 +577,7 @@ def extend_rows(dev):
     tf = flops / (t / 1e3) / 1e12
     return {"us": t * 1e3, "chunk_tokens_per_s": e.q_rows / (t / 1e3), "alg_tflops": tf,
             "alg_flops": flops, "bound": "tensor", "peak_tflops": peak, "peak_source": src,
-            "frac": tf / peak, "mma": "mma.sync m16n8k16 f16 (peak: bf16 dense, same rate)",
+            "frac": tf / peak, "mma": "tcgen05.mma kind::f16 M128 (f16 operands, fp32 accumulators in tensor memory); peak: measured bf16 dense burst, the same tensor rate as f16",
             "fused_append_us": f_ms * 1e3, "attention_then_quantize_append_us": s_ms * 1e3,
             "device_status": int(status.item())}
 
