@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the quantize / prefix-dequant rows")
+    ap.add_argument("--extend-only", default=None, choices=["ext160k", "ext8k_c2k"],
+                    help="time only the extend-attention row on this workload and print it")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -109,10 +111,28 @@ def measured_peaks():
         return None
 
 
+# the sources each profiled kernel is compiled from (a summary's counters are
+# used only while the hash of these files matches the one it records)
+KERNEL_SOURCES = {
+    "decode_nvfp4": ["abi.cpp", "decode_common.cuh", "decode_nvfp4.cu", "device_common.cuh", "merge.cu",
+                     "nvfp4kv_internal.h", "record_write.cuh"],
+    "extend_attention": ["abi.cpp", "device_common.cuh", "extend_attention.cu", "nvfp4kv_internal.h",
+                         "record_write.cuh", "tcgen05.cuh"],
+}
+
+
+def kernel_sources_hash(kernel_tag: str) -> str:
+    import hashlib
+    csrc = os.path.join(ROOT, "nvfp4_quantized_paged_nvfp4kv_gb300", "csrc")
+    h = hashlib.sha256()
+    for fn in KERNEL_SOURCES[kernel_tag]:
+        h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(kernel_tag: str, workload: str):
     """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (the summary records their hash)."""
-    import hashlib
+    the current sources of that kernel (the summary records their hash)."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -121,11 +141,7 @@ def profiled_traffic(kernel_tag: str, workload: str):
         if ":" in line and line.startswith("- "):
             k, v = line[2:].split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
-    csrc = os.path.join(ROOT, "nvfp4_quantized_paged_nvfp4kv_gb300", "csrc")
-    h = hashlib.sha256()
-    for fn in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, fn), "rb").read())
-    if fields.get("kernel_sources_sha256") != h.hexdigest()[:16]:
+    if fields.get("kernel_sources_sha256") != kernel_sources_hash(kernel_tag):
         return None
     try:
         return float(fields["dram_bytes_per_launch"])
@@ -512,13 +528,14 @@ def extend_flops(e) -> float:
     return 4.0 * e.head_dim * e.num_q_heads * tot
 
 
-def extend_rows(dev):
+def extend_rows(dev, name: str = "ext160k", steps: int = 5, warmup: int = 3, compare_fused: bool = True):
     """Extend attention of the last 8,192-token chunk of a 163,840-token
     prefill (Hq 48, Hkv 8) over the 155,648-row FP8 prefix workspace (319 MB,
-    larger than L2) and the chunk, bf16 out; mean of 5 launches after 3
-    warm-ups, CUDA events on the launching stream."""
+    larger than L2) and the chunk, bf16 out; mean of `steps` launches after
+    `warmup`, CUDA events on the launching stream.  Then the same step fused
+    with the NVFP4 write of the chunk against attention + quantize_append."""
     import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
-    e = workloads.extend_make("ext160k")
+    e = workloads.extend_make(name)
     x = workloads.extend_inputs(e, device=dev)
     out = torch.empty((e.q_rows, e.num_q_heads, e.head_dim), dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -528,10 +545,10 @@ def extend_rows(dev):
         nv.nvfp4kv_extend_attention_fp8(x["q"], x["q_indptr"], x["k_prefix"], x["v_prefix"], x["kv_indptr"],
                                         x["prefix_lens"], x["k_chunk"], x["v_chunk"], out, max_q_len=mql,
                                         dev_status=status)
-    for _ in range(3):
+    for _ in range(warmup):
         call()
     ms = []
-    for _ in range(5):
+    for _ in range(steps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         call()
@@ -539,6 +556,21 @@ def extend_rows(dev):
         torch.cuda.synchronize()
         ms.append(a.elapsed_time(b))
     t = statistics.mean(ms)
+    flops = extend_flops(e)
+    peaks = measured_peaks() or {}
+    peak = peaks.get("bf16_tflops")
+    src = "measured"
+    if peak is None:
+        peak, src = 1900.0, "fallback"
+    tf = flops / (t / 1e3) / 1e12
+    row = {"workload": name, "us": t * 1e3, "chunk_tokens_per_s": e.q_rows / (t / 1e3), "alg_tflops": tf,
+           "alg_flops": flops, "bound": "tensor", "peak_tflops": peak, "peak_source": src, "frac": tf / peak,
+           "mma": "tcgen05.mma kind::f16 M128 (f16 operands, fp32 accumulators in tensor memory); peak: measured "
+                  "bf16 dense burst, the same tensor rate as f16",
+           "traffic": profiled_traffic("extend_attention", name)}
+    if not compare_fused:
+        row["device_status"] = int(status.item())
+        return row
 
     # the same step fused with the NVFP4 write of the chunk, against the
     # attention followed by a separate quantize_append
@@ -568,18 +600,9 @@ def extend_rows(dev):
             res.append(a.elapsed_time(b))
         return statistics.mean(res)
     f_ms, s_ms = mean_ms(fused), mean_ms(separate)
-    flops = extend_flops(e)
-    peaks = measured_peaks() or {}
-    peak = peaks.get("bf16_tflops")
-    src = "measured"
-    if peak is None:
-        peak, src = 1900.0, "fallback"
-    tf = flops / (t / 1e3) / 1e12
-    return {"us": t * 1e3, "chunk_tokens_per_s": e.q_rows / (t / 1e3), "alg_tflops": tf,
-            "alg_flops": flops, "bound": "tensor", "peak_tflops": peak, "peak_source": src,
-            "frac": tf / peak, "mma": "tcgen05.mma kind::f16 M128 (f16 operands, fp32 accumulators in tensor memory); peak: measured bf16 dense burst, the same tensor rate as f16",
-            "fused_append_us": f_ms * 1e3, "attention_then_quantize_append_us": s_ms * 1e3,
-            "device_status": int(status.item())}
+    row.update({"fused_append_us": f_ms * 1e3, "attention_then_quantize_append_us": s_ms * 1e3,
+                "device_status": int(status.item())})
+    return row
 
 
 def multi_query_rows(dev, timed):
@@ -701,6 +724,12 @@ def main():
         if rank != 0:
             return 0
         print(json.dumps(run_reference(args, world, rank)))
+        return 0
+    if args.extend_only:
+        import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+        nv.load()
+        print(json.dumps(extend_rows(torch.device("cuda", 0), args.extend_only, steps=args.steps,
+                                     warmup=max(args.warmup, 3), compare_fused=False)))
         return 0
     world, rank, local = dist_init(args)
     res = run_ours(args, world, rank, local)

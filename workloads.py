@@ -253,9 +253,12 @@ class ExtendWorkload:
 
 def extend_make(name: str) -> ExtendWorkload:
     """ext160k: the last 8,192-token chunk of a 163,840-token prefill (Hq=48,
-    Hkv=8), prefix 155,648.  ext_small: four ragged sequences."""
+    Hkv=8), prefix 155,648.  ext8k_c2k: a 2,048-token chunk over an 8,192-token
+    prefix (the profiling case).  ext_small: four ragged sequences."""
     if name == "ext160k":
         return ExtendWorkload(name, (163840 - 8192,), (8192,), 48, 8, seed=_seed("ext160k"))
+    if name == "ext8k_c2k":
+        return ExtendWorkload(name, (8192,), (2048,), 48, 8, seed=_seed("ext8k_c2k"))
     if name == "ext_small":
         return ExtendWorkload(name, (0, 61, 200, 1000), (130, 1, 77, 64), 48, 8, seed=_seed("ext_small"))
     raise ValueError(name)
