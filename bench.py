@@ -64,8 +64,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the quantize / prefix-dequant rows")
-    ap.add_argument("--extend-only", default=None, choices=["ext160k", "ext8k_c2k"],
-                    help="time only the extend-attention row on this workload and print it")
+    ap.add_argument("--row-only", default=None, choices=["ext160k", "ext8k_c2k", "quantize8k", "prefix160k"],
+                    help="time only this row (extend attention on a workload, quantize_append of 8,192 "
+                         "bf16 tokens, or dequant_prefix_fp8 of a 163,840-token prefix) and print it")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -449,6 +450,12 @@ def run_ours(args, world, rank, local):
     return result
 
 
+# Per-call rows time one short launch between two events.  A GPU-side spin of
+# this many cycles before the start event keeps the GPU busy while the host
+# enqueues the call, so the interval holds the kernel, not the host's launch.
+HOST_COVER_CYCLES = 400_000
+
+
 def other_rows(dev):
     """The write side and the extend path on the long-context workload: quantize_append
     of one 8192-token bf16 prefill chunk (Hkv=8) and dequant_prefix_fp8 of a
@@ -480,6 +487,7 @@ def other_rows(dev):
         ms = []
         for _ in range(20):
             flush.fill_(1)                                   # evict the inputs from L2
+            torch.cuda._sleep(HOST_COVER_CYCLES)             # the GPU waits here, not on the host launch
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -515,8 +523,57 @@ def other_rows(dev):
                               "quantize_append_8k_bf16_us": qg_ms * 1e3},
         "multi_query": multi,
         "extend_160k_chunk8k": extend,
-        "timing": "CUDA events per call, 256 MB buffer written before each call to evict L2",
+        "timing": "CUDA events per call, 256 MB buffer written and a GPU spin before each call (L2 evicted, "
+                  "host launch hidden)",
     }
+
+
+def write_side_row(dev, name: str, steps: int, warmup: int):
+    """One write-side row alone: quantize_append of 8,192 bf16 tokens (Hkv 8)
+    into a 163,840-token cache, or dequant_prefix_fp8 of that 163,840-token
+    prefix; CUDA events per call, a 256 MB buffer written before each call."""
+    import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+    w = workloads.make("ctx160k", batch=1)
+    bt, num_pages = workloads.block_table(w)
+    cache = nv.NVFP4Cache.allocate(num_pages, w.num_kv_heads, device=dev, zero=False)
+    L = w.seq_lens[0]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    if name == "quantize8k":
+        T = 8192
+        k = workloads.kv_rows(w, "k", 0, 0, T, device=dev).to(torch.bfloat16)
+        v = workloads.kv_rows(w, "v", 0, 0, T, device=dev).to(torch.bfloat16)
+        sm = torch.from_numpy(workloads.slot_mapping(w, bt, 0, 0, T)).to(dev)
+        fn = lambda: nv.nvfp4kv_quantize_append(cache, k, v, sm)  # noqa: E731
+        alg, units = T * w.num_kv_heads * (2 * 128 * 2 + NVFP4_BYTES_PER_TOKEN_HEAD) + T * 4, T
+    else:
+        for t0 in range(0, L, workloads.CHUNK):
+            t1 = min(L, t0 + workloads.CHUNK)
+            sm = torch.from_numpy(workloads.slot_mapping(w, bt, 0, t0, t1)).to(dev)
+            nv.nvfp4kv_quantize_append(cache, workloads.kv_rows(w, "k", 0, t0, t1, device=dev),
+                                       workloads.kv_rows(w, "v", 0, t0, t1, device=dev), sm)
+        bt_d = torch.from_numpy(bt).to(dev)
+        kf = torch.empty((L, w.num_kv_heads, 128), dtype=torch.uint8, device=dev)
+        vf = torch.empty_like(kf)
+        pl = torch.tensor([L], dtype=torch.int32, device=dev)
+        ip = torch.zeros(1, dtype=torch.int32, device=dev)
+        fn = lambda: nv.nvfp4kv_dequant_prefix_fp8(cache, bt_d, pl, ip, kf, vf)  # noqa: E731
+        alg, units = L * w.num_kv_heads * (NVFP4_BYTES_PER_TOKEN_HEAD + 2 * 128), L
+    for _ in range(warmup):
+        fn()
+    ms = []
+    for _ in range(steps):
+        flush.fill_(1)
+        torch.cuda._sleep(HOST_COVER_CYCLES)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    t = statistics.mean(ms)
+    hbm = (measured_peaks() or {}).get("hbm_gbs", 6800.0)
+    return {"row": name, "us": t * 1e3, "tokens_per_s": units / (t / 1e3), "alg_bytes": alg,
+            "alg_gbs": alg / (t / 1e3) / 1e9, "frac": alg / (t / 1e3) / 1e9 / hbm, "peak_gbs": hbm}
 
 
 def extend_flops(e) -> float:
@@ -725,11 +782,16 @@ def main():
             return 0
         print(json.dumps(run_reference(args, world, rank)))
         return 0
-    if args.extend_only:
+    if args.row_only:
         import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
         nv.load()
-        print(json.dumps(extend_rows(torch.device("cuda", 0), args.extend_only, steps=args.steps,
-                                     warmup=max(args.warmup, 3), compare_fused=False)))
+        dev = torch.device("cuda", 0)
+        warm = max(args.warmup, 3)
+        if args.row_only.startswith("ext"):
+            row = extend_rows(dev, args.row_only, steps=args.steps, warmup=warm, compare_fused=False)
+        else:
+            row = write_side_row(dev, args.row_only, args.steps, warm)
+        print(json.dumps(row))
         return 0
     world, rank, local = dist_init(args)
     res = run_ours(args, world, rank, local)

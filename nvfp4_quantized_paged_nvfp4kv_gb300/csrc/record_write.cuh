@@ -65,7 +65,8 @@ __device__ __forceinline__ void divide_by_tensor_scale(float (&x)[16], float G)
 
 // amax -> E4M3 block scale -> 16 E2M1 codes (code i in bits 4i .. 4i+3).
 //
-// Each code is decided on the IEEE quotient fl32(x / s).  It is computed
+// The scale is decided on fl32(amax / 6) and each code on the IEEE quotient
+// fl32(x / s).  Both are computed
 // without a division per element: with r = RN(1/s), q0 = RN(x r) is within an
 // ulp of x / s, the remainder x - q0 s is exact through one FMA, and
 // RN(q0 + (x - q0 s) r) is the correctly rounded quotient (Markstein's
@@ -74,11 +75,21 @@ __device__ __forceinline__ void divide_by_tensor_scale(float (&x)[16], float G)
 // compared against an IEEE division for all eight in the GPU tests.
 __device__ __forceinline__ void quantize_block(const float (&x)[16], uint32_t &scale_byte, uint32_t (&packed)[2])
 {
-    float amax = 0.f;
+    // amax with three-input maxima (a NaN element is ignored, as by fmaxf);
+    // capped at the largest finite float so the quotient below stays finite
+    // (any amax above 6 * 448 saturates the scale the same way)
+    float a[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-        amax = fmaxf(amax, fabsf(x[i]));
-    const float s32 = __fdiv_rn(amax, 6.0f);
+        a[i] = fabsf(x[i]);
+    const float m = fmaxf(fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmax3(a[6], a[7], a[8])),
+                          fmax3(fmax3(a[9], a[10], a[11]), fmax3(a[12], a[13], a[14]), a[15]));
+    const float amax = fminf(fmaxf(m, 0.f), 3.40282347e+38f);   // an all-NaN block has amax 0
+    // fl32(amax / 6) by the same correction step as the elements below, with
+    // RN(1/6) = 0x3E2AAAAB
+    const float sixth = __uint_as_float(0x3E2AAAABu);
+    const float d0 = __fmul_rn(amax, sixth);
+    const float s32 = __fmaf_rn(__fmaf_rn(-d0, 6.0f, amax), sixth, d0);
     scale_byte = f32x2_to_e4m3x2(s32, 0.f) & 0xffu;
     const float sc = e4m3_to_f32(scale_byte);
     packed[0] = packed[1] = 0u;
