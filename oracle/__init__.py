@@ -63,14 +63,14 @@ def _load():
         lib.oracle_e4m3_encode_array.argtypes = [_f32p, _u8p, ctypes.c_int64]
         lib.oracle_quantize_block16.argtypes = [_f32p, _u8p, _u8p, ctypes.c_float]
         lib.oracle_quantize_append.argtypes = [
-            _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _u8p, _u8p, ctypes.c_float]
+            _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _u8p, _u8p, _f32p]
         lib.oracle_dequant_rows.argtypes = [_u8p, _u8p, ctypes.c_int64, ctypes.c_int, _f32p, ctypes.c_float]
         lib.oracle_paged_decode.argtypes = [
             _u8p, _u8p, _u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p,
-            ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_double, _f64p, ctypes.c_float]
+            ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_double, _f64p, _f32p, _f32p]
         lib.oracle_dequant_prefix_fp8.argtypes = [
             _u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int,
-            _i32p, _i32p, ctypes.c_int, _u8p, ctypes.c_float]
+            _i32p, _i32p, ctypes.c_int, _u8p, _f32p]
         lib.oracle_fp8_quantize_append.argtypes = [
             _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _u8p]
         lib.oracle_fp8_paged_decode.argtypes = [
@@ -138,20 +138,41 @@ def quantize_block16(x, global_scale: float = 1.0) -> tuple[np.ndarray, int]:
     return packed, int(scale[0])
 
 
-def quantize_append(x, slot_mapping, data, scale, page_size: int = 16, global_scale: float = 1.0) -> None:
-    """Quantise rows x[T][Hkv][d] into the NVFP4 pools (in place); values are
-    stored as global_scale * E4M3 scale * E2M1."""
+def head_tensor_scales(global_scale: float, head_scales, Hkv: int) -> np.ndarray:
+    """Tensor scale of each kv head: fl32(global_scale * head_scales[h]) (one
+    fp32 rounding), or global_scale for every head without per-head factors."""
+    g = np.float32(global_scale)
+    if head_scales is None:
+        return np.full(Hkv, g, np.float32)
+    f = np.asarray(head_scales, np.float32).reshape(Hkv)
+    return (g * f).astype(np.float32)
+
+
+def quantize_append(x, slot_mapping, data, scale, page_size: int = 16, global_scale: float = 1.0,
+                    head_scales=None) -> None:
+    """Quantise rows x[T][Hkv][d] into the NVFP4 pools (in place); a value of
+    kv head h is stored as G_h * E4M3 scale * E2M1 with G_h =
+    fl32(global_scale * head_scales[h]) (global_scale when head_scales is
+    None)."""
     x = _c(x, np.float32)
     T, Hkv, d = x.shape
     sm = _c(slot_mapping, np.int32)
     assert data.flags.c_contiguous and scale.flags.c_contiguous
     assert data.dtype == np.uint8 and scale.dtype == np.uint8
+    hs = head_tensor_scales(global_scale, head_scales, Hkv)
     _load().oracle_quantize_append(_p(x, _f32p), T, Hkv, d, _p(sm, _i32p), page_size,
-                                   _p(data, _u8p), _p(scale, _u8p), float(global_scale))
+                                   _p(data, _u8p), _p(scale, _u8p), _p(hs, _f32p))
 
 
-def dequant_rows(data, scale, global_scale: float = 1.0) -> np.ndarray:
-    """Dequantise NVFP4 rows (data[..., d/2], scale[..., d/16]) to fp32."""
+def dequant_rows(data, scale, global_scale: float = 1.0, head_scales=None) -> np.ndarray:
+    """Dequantise NVFP4 rows (data[..., d/2], scale[..., d/16]) to fp32.  With
+    head_scales, data is a pool [pages][Hkv][P][d/2] and head h's rows use
+    fl32(global_scale * head_scales[h])."""
+    if head_scales is not None:
+        Hkv = data.shape[1]
+        hs = head_tensor_scales(global_scale, head_scales, Hkv)
+        return np.stack([dequant_rows(np.ascontiguousarray(data[:, h]), np.ascontiguousarray(scale[:, h]),
+                                      float(hs[h])) for h in range(Hkv)], 1)
     data = _c(data, np.uint8)
     scale = _c(scale, np.uint8)
     d = data.shape[-1] * 2
@@ -162,8 +183,9 @@ def dequant_rows(data, scale, global_scale: float = 1.0) -> np.ndarray:
 
 
 def paged_decode(k_data, k_scale, v_data, v_scale, q, block_table, seq_lens,
-                 sm_scale: float | None = None, global_scale: float = 1.0) -> np.ndarray:
-    """fp64 GQA decode over the NVFP4 pools.  q: float32 [B][Hq][d]."""
+                 sm_scale: float | None = None, global_scale: float = 1.0, head_scales=None) -> np.ndarray:
+    """fp64 GQA decode over the NVFP4 pools.  q: float32 [B][Hq][d].
+    head_scales: None or per-head factors [2][Hkv] (K, then V)."""
     k_data = _c(k_data, np.uint8)
     k_scale = _c(k_scale, np.uint8)
     v_data = _c(v_data, np.uint8)
@@ -177,15 +199,19 @@ def paged_decode(k_data, k_scale, v_data, v_scale, q, block_table, seq_lens,
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(d)
     out = np.empty((B, Hq, d), np.float64)
+    hk = head_tensor_scales(global_scale, None if head_scales is None else np.asarray(head_scales)[0], Hkv)
+    hv = head_tensor_scales(global_scale, None if head_scales is None else np.asarray(head_scales)[1], Hkv)
     _load().oracle_paged_decode(_p(k_data, _u8p), _p(k_scale, _u8p), _p(v_data, _u8p),
                                 _p(v_scale, _u8p), Hkv, P, d, _p(q, _f32p), B, Hq,
                                 _p(bt, _i32p), bt.shape[1], _p(sl, _i32p),
-                                float(sm_scale), _p(out, _f64p), float(global_scale))
+                                float(sm_scale), _p(out, _f64p), _p(hk, _f32p), _p(hv, _f32p))
     return out
 
 
 def dequant_prefix_fp8(data, scale, block_table, prefix_lens, kv_indptr,
-                       out_rows: int | None = None, global_scale: float = 1.0) -> np.ndarray:
+                       out_rows: int | None = None, global_scale: float = 1.0, head_scales=None) -> np.ndarray:
+    """FP8 workspace rows of one tensor (K or V) of the cache; head_scales:
+    None or this tensor's per-head factors [Hkv]."""
     data = _c(data, np.uint8)
     scale = _c(scale, np.uint8)
     _, Hkv, P, half = data.shape
@@ -198,7 +224,8 @@ def dequant_prefix_fp8(data, scale, block_table, prefix_lens, kv_indptr,
     out = np.zeros((out_rows, Hkv, d), np.uint8)
     _load().oracle_dequant_prefix_fp8(_p(data, _u8p), _p(scale, _u8p), Hkv, P, d,
                                       _p(bt, _i32p), bt.shape[1], _p(pl, _i32p),
-                                      _p(ip, _i32p), len(pl), _p(out, _u8p), float(global_scale))
+                                      _p(ip, _i32p), len(pl), _p(out, _u8p),
+                                      _p(head_tensor_scales(global_scale, head_scales, Hkv), _f32p))
     return out
 
 

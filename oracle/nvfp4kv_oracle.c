@@ -194,10 +194,13 @@ static size_t row_index(int64_t page, int h, int off, int Hkv, int P)
 
 /* Write side: quantise new K or V rows [T][Hkv][d] (fp32) into the slots
  * slot_mapping[t] (negative = skip).  [LMSYS-summary] Interpretation ¶2: the
- * prefill quantises the same data it attends on into the NVFP4 cache.        */
+ * prefill quantises the same data it attends on into the NVFP4 cache.
+ * head_scale[h] is the tensor scale of kv head h (reading for per-head
+ * scales: the tensor scale G times a per-head factor, rounded to fp32 once;
+ * equal to G for every head without per-head factors).                        */
 void oracle_quantize_append(const float *x, int T, int Hkv, int d,
                             const int32_t *slot_mapping, int P,
-                            uint8_t *data, uint8_t *scale, float global_scale)
+                            uint8_t *data, uint8_t *scale, const float *head_scale)
 {
     int nb = d / 16;
 #pragma omp parallel for schedule(static)
@@ -213,7 +216,7 @@ void oracle_quantize_append(const float *x, int T, int Hkv, int d,
             for (int blk = 0; blk < nb; ++blk)
                 oracle_quantize_block16(src + 16 * blk,
                                         data + r * (size_t)(d / 2) + 8 * blk,
-                                        scale + r * (size_t)nb + blk, global_scale);
+                                        scale + r * (size_t)nb + blk, head_scale[h]);
         }
     }
 }
@@ -266,12 +269,13 @@ static void paged_decode_generic(int kind,
                                  const float *q, int B, int Hq,
                                  const int32_t *block_table, int max_pages,
                                  const int32_t *seq_lens, double sm_scale,
-                                 double *out, float global_scale)
+                                 double *out, const float *k_head_scale, const float *v_head_scale)
 {
     int g = Hq / Hkv;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int bi = 0; bi < B * Hq; ++bi) {
         int b = bi / Hq, i = bi % Hq, h = i / g;
+        float gk = k_head_scale ? k_head_scale[h] : 1.0f, gv = v_head_scale ? v_head_scale[h] : 1.0f;
         int L = seq_lens[b];
         const float *qv = q + ((size_t)b * Hq + i) * d;
         double *o = out + ((size_t)b * Hq + i) * d;
@@ -287,7 +291,7 @@ static void paged_decode_generic(int kind,
             size_t r = row_index(page, h, j % P, Hkv, P);
             double dot = 0.0;
             for (int c = 0; c < d; ++c)
-                dot += (double)qv[c] * cache_value(kind, k_data, k_scale, r, d, c, global_scale);
+                dot += (double)qv[c] * cache_value(kind, k_data, k_scale, r, d, c, gk);
             double sj = dot * sm_scale;
             if (sj > smax)
                 smax = sj;
@@ -300,11 +304,11 @@ static void paged_decode_generic(int kind,
             size_t r = row_index(page, h, j % P, Hkv, P);
             double dot = 0.0;
             for (int c = 0; c < d; ++c)
-                dot += (double)qv[c] * cache_value(kind, k_data, k_scale, r, d, c, global_scale);
+                dot += (double)qv[c] * cache_value(kind, k_data, k_scale, r, d, c, gk);
             double p = exp(dot * sm_scale - m);
             denom += p;
             for (int c = 0; c < d; ++c)
-                o[c] += p * cache_value(kind, v_data, v_scale, r, d, c, global_scale);
+                o[c] += p * cache_value(kind, v_data, v_scale, r, d, c, gv);
         }
         for (int c = 0; c < d; ++c)
             o[c] /= denom;
@@ -315,23 +319,25 @@ void oracle_paged_decode(const uint8_t *k_data, const uint8_t *k_scale,
                          const uint8_t *v_data, const uint8_t *v_scale,
                          int Hkv, int P, int d, const float *q, int B, int Hq,
                          const int32_t *block_table, int max_pages,
-                         const int32_t *seq_lens, double sm_scale, double *out, float global_scale)
+                         const int32_t *seq_lens, double sm_scale, double *out,
+                         const float *k_head_scale, const float *v_head_scale)
 {
     paged_decode_generic(0, k_data, k_scale, v_data, v_scale, Hkv, P, d, q, B, Hq,
-                         block_table, max_pages, seq_lens, sm_scale, out, global_scale);
+                         block_table, max_pages, seq_lens, sm_scale, out, k_head_scale, v_head_scale);
 }
 
 /* ------------------------------------------------------------------------ */
 /* Extend path: dequantise the cached prefix of each sequence into one
  * contiguous FP8 workspace ([LMSYS-summary] Interpretation ¶2).  Reading:
- * each value is E4M3_RNE_sat(fl32(E2M1 x scale x G)) at workspace scale 1.0
- * (the fp32 rounding only acts when G != 1); rows of sequence b go to
+ * each value is E4M3_RNE_sat(fl32(E2M1 x scale x G_h)) at workspace scale 1.0,
+ * G_h the tensor scale of kv head h (the fp32 rounding only acts when
+ * G_h != 1); rows of sequence b go to
  * workspace rows kv_indptr[b] + j, laid out [row][Hkv][d].                   */
 void oracle_dequant_prefix_fp8(const uint8_t *data, const uint8_t *scale,
                                int Hkv, int P, int d,
                                const int32_t *block_table, int max_pages,
                                const int32_t *prefix_lens, const int32_t *kv_indptr,
-                               int B, uint8_t *out, float global_scale)
+                               int B, uint8_t *out, const float *head_scale)
 {
     for (int b = 0; b < B; ++b) {
         int L = prefix_lens[b];
@@ -343,7 +349,7 @@ void oracle_dequant_prefix_fp8(const uint8_t *data, const uint8_t *scale,
                 uint8_t *dst = out + (((size_t)kv_indptr[b] + j) * Hkv + h) * d;
                 for (int c = 0; c < d; ++c) {
                     float v = (float)nvfp4_row_value(data + r * (size_t)(d / 2),
-                                                     scale + r * (size_t)(d / 16), c, global_scale);
+                                                     scale + r * (size_t)(d / 16), c, head_scale[h]);
                     dst[c] = oracle_e4m3_encode(v);
                 }
             }
@@ -380,7 +386,7 @@ void oracle_fp8_paged_decode(const uint8_t *k, const uint8_t *v, int Hkv, int P,
                              const int32_t *seq_lens, double sm_scale, double *out)
 {
     paged_decode_generic(1, k, NULL, v, NULL, Hkv, P, d, q, B, Hq, block_table,
-                         max_pages, seq_lens, sm_scale, out, 1.0f);
+                         max_pages, seq_lens, sm_scale, out, NULL, NULL);
 }
 
 /* ------------------------------------------------------------------------ */
