@@ -510,6 +510,11 @@ def other_rows(dev):
     d1_ms = timed(lambda: nv.nvfp4kv_paged_decode(cache, q, bt_d, sl, out, ws))
     dg_ms = timed(lambda: nv.nvfp4kv_paged_decode(cache_g, q, bt_d, sl, out, ws))
     qg_ms = timed(lambda: nv.nvfp4kv_quantize_append(cache_g, k, v, sm))
+    # and with per-head factors on top (K and V of each kv head their own scale)
+    factors = [[0.5 + 0.25 * h for h in range(w.num_kv_heads)], [2.0 - 0.2 * h for h in range(w.num_kv_heads)]]
+    cache_h = nv.NVFP4Cache(cache.pool, global_scale=0.37, head_scales=factors)
+    dh_ms = timed(lambda: nv.nvfp4kv_paged_decode(cache_h, q, bt_d, sl, out, ws))
+    qh_ms = timed(lambda: nv.nvfp4kv_quantize_append(cache_h, k, v, sm))
     d_bytes = L * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
     multi = multi_query_rows(dev, timed)
     extend = extend_rows(dev)
@@ -520,7 +525,9 @@ def other_rows(dev):
                                     "alg_gbs": p_bytes / (p_ms / 1e3) / 1e9, "alg_bytes": p_bytes},
         "tensor_scale_0.37": {"decode_160k_b1_us": dg_ms * 1e3, "decode_160k_b1_unit_scale_us": d1_ms * 1e3,
                               "decode_alg_gbs": d_bytes / (dg_ms / 1e3) / 1e9,
-                              "quantize_append_8k_bf16_us": qg_ms * 1e3},
+                              "quantize_append_8k_bf16_us": qg_ms * 1e3,
+                              "per_head_factors": {"decode_160k_b1_us": dh_ms * 1e3,
+                                                   "quantize_append_8k_bf16_us": qh_ms * 1e3}},
         "multi_query": multi,
         "extend_160k_chunk8k": extend,
         "timing": "CUDA events per call, 256 MB buffer written and a GPU spin before each call (L2 evicted, "

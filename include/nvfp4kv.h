@@ -111,7 +111,17 @@ typedef enum { NVFP4KV_F32 = 0, NVFP4KV_BF16 = 1 } nvfp4kv_dtype;
 #define FP8KV_RECORD_BYTES 4096
 
 /* NVFP4 cache: pool of num_pages * num_kv_heads records laid out as above,
- * 16-byte aligned; global_scale is the tensor scale G described above. */
+ * 16-byte aligned; global_scale is the tensor scale G described above.
+ * head_scales (optional, may be NULL): a HOST array of 2 * num_kv_heads
+ * per-head factors, K then V.  With it, kv head h of K uses the tensor scale
+ * G_h = fl32(global_scale * head_scales[h]) and of V fl32(global_scale *
+ * head_scales[num_kv_heads + h]) wherever G appears above (a refinement of the
+ * pages' single tensor scale; this library's).  Each factor and each product
+ * must be a positive normal finite float, and num_kv_heads at most
+ * NVFP4KV_MAX_SCALED_KV_HEADS, else calls return NVFP4KV_ERR_UNSUPPORTED.  The
+ * values are read on the host during each call. */
+#define NVFP4KV_MAX_SCALED_KV_HEADS 128
+
 typedef struct {
     void *pool;
     int32_t num_pages;
@@ -119,6 +129,7 @@ typedef struct {
     int32_t page_size;
     int32_t head_dim;
     float global_scale;
+    const float *head_scales;
 } nvfp4kv_cache;
 
 /* FP8-E4M3 comparison cache (scale 1.0): pool of records as above, 16-byte

@@ -52,7 +52,7 @@ class _Nvfp4Cache(ctypes.Structure):
     _fields_ = [("pool", ctypes.c_void_p),
                 ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("global_scale", ctypes.c_float)]
+                ("global_scale", ctypes.c_float), ("head_scales", ctypes.c_void_p)]
 
 
 class _Fp8Cache(ctypes.Structure):
@@ -155,18 +155,26 @@ def _dtype_code(t) -> int:
 class NVFP4Cache:
     """An NVFP4 pool: uint8 [num_pages][num_kv_heads][NVFP4_RECORD_BYTES] page-head
     records (layout in include/nvfp4kv.h).  global_scale is the FP32 tensor
-    scale G: a cached value is G * E4M3 block scale * E2M1 code."""
+    scale G: a cached value is G * E4M3 block scale * E2M1 code.  head_scales
+    (optional): per-head factors [2][num_kv_heads] (K, then V); kv head h then
+    uses fl32(G * factor) as its tensor scale."""
 
     record_bytes = NVFP4_RECORD_BYTES
 
-    def __init__(self, pool, global_scale: float = 1.0):
+    def __init__(self, pool, global_scale: float = 1.0, head_scales=None):
         self.pool = pool
         self.num_pages, self.num_kv_heads, rb = pool.shape
         assert rb == self.record_bytes
         self.page_size, self.head_dim = PAGE_SIZE, HEAD_DIM
         self.global_scale = float(global_scale)
+        self._hs = None
+        if head_scales is not None:
+            vals = [float(v) for row in head_scales for v in row]
+            assert len(vals) == 2 * self.num_kv_heads, "head_scales: [2][num_kv_heads]"
+            self._hs = (ctypes.c_float * len(vals))(*vals)     # host array the library reads per call
+        self.head_scales = head_scales
         self._c = _Nvfp4Cache(pool.data_ptr(), self.num_pages, self.num_kv_heads, PAGE_SIZE, HEAD_DIM,
-                              self.global_scale)
+                              self.global_scale, None if self._hs is None else ctypes.addressof(self._hs))
 
     @classmethod
     def allocate(cls, num_pages, num_kv_heads, device="cuda", zero=True, **kw):

@@ -27,6 +27,26 @@ nvfp4kv_status from_cuda(cudaError_t e)
     return e == cudaSuccess ? NVFP4KV_OK : NVFP4KV_ERR_CUDA;
 }
 
+bool normal_positive(float x)
+{
+    return x >= 1.17549435e-38f && x <= 3.40282347e+38f;
+}
+
+// Per-head tensor scales of a (checked) NVFP4 cache: fl32(G * factor) per kv
+// head of K and V, or per_head = 0 without factors.
+HeadScales head_scales_of(const nvfp4kv_cache *c)
+{
+    HeadScales hs{};
+    if (c->head_scales == nullptr)
+        return hs;
+    hs.per_head = 1;
+    for (int h = 0; h < c->num_kv_heads; ++h) {
+        hs.k[h] = c->global_scale * c->head_scales[h];
+        hs.v[h] = c->global_scale * c->head_scales[c->num_kv_heads + h];
+    }
+    return hs;
+}
+
 // Shared geometry checks for both cache kinds.
 nvfp4kv_status check_geometry(int32_t num_pages, int32_t hkv, int32_t page_size, int32_t head_dim)
 {
@@ -47,8 +67,18 @@ nvfp4kv_status check_nvfp4(const nvfp4kv_cache *c)
     if (st != NVFP4KV_OK)
         return st;
     // a positive, normal, finite tensor scale
-    if (!(c->global_scale >= 1.17549435e-38f && c->global_scale <= 3.40282347e+38f))
+    if (!normal_positive(c->global_scale))
         return NVFP4KV_ERR_UNSUPPORTED;
+    // optional per-head factors: each, and its product with G, positive normal
+    if (c->head_scales != nullptr) {
+        if (c->num_kv_heads > kMaxScaledHeads)
+            return NVFP4KV_ERR_UNSUPPORTED;
+        for (int i = 0; i < 2 * c->num_kv_heads; ++i) {
+            const float f = c->head_scales[i];
+            if (!normal_positive(f) || !normal_positive(c->global_scale * f))
+                return NVFP4KV_ERR_UNSUPPORTED;
+        }
+    }
     if (c->pool == nullptr || !aligned16(c->pool))
         return NVFP4KV_ERR_INVALID_ARG;
     return NVFP4KV_OK;
@@ -156,12 +186,19 @@ nvfp4kv_status check_decode(int32_t hkv, int32_t num_pages, const void *q, int32
 }
 
 // The NVFP4 tensor scale G: scores see G * k, so G joins the query scale;
-// outputs see G * v, so the normaliser carries it.
-void apply_tensor_scale(DecodeParams &p, float sm_scale, float G)
+// outputs see G * v, so the normaliser carries it.  With per-head factors each
+// kv head has its own query scale, append divisors and output scale.
+void apply_tensor_scale(DecodeParams &p, float sm_scale, const nvfp4kv_cache *c)
 {
+    const float G = c->global_scale;
     p.qscale = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634 * static_cast<double>(G));
     p.out_scale = G;
     p.gscale = G;
+    p.hs = head_scales_of(c);
+    if (p.hs.per_head)
+        for (int h = 0; h < c->num_kv_heads; ++h)
+            p.qs[h] = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634 *
+                                         static_cast<double>(p.hs.k[h]));
 }
 
 // Extend arguments common to both entry points.  Fills p (attention part)
@@ -250,6 +287,7 @@ nvfp4kv_status nvfp4kv_quantize_append(const nvfp4kv_cache *cache, const void *k
     p.num_pages = cache->num_pages;
     p.in_bf16 = in_dtype == NVFP4KV_BF16;
     p.gscale = cache->global_scale;
+    p.hs = head_scales_of(cache);
     return from_cuda(launch_quantize_append_nvfp4(p, to_cuda(stream)));
 }
 
@@ -274,7 +312,7 @@ nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q, i
     if (st != NVFP4KV_OK || batch == 0)
         return st;
     p.pool = static_cast<const uint8_t *>(cache->pool);
-    apply_tensor_scale(p, sm_scale, cache->global_scale);
+    apply_tensor_scale(p, sm_scale, cache);
     cudaError_t e = launch_decode_nvfp4(p, to_cuda(stream));
     if (e == cudaSuccess)
         e = launch_merge(p, to_cuda(stream));
@@ -306,7 +344,7 @@ nvfp4kv_status nvfp4kv_paged_decode_multi(const nvfp4kv_cache *cache, const void
         (int64_t{1} << 31) - 1)
         return NVFP4KV_ERR_UNSUPPORTED;
     p.pool = static_cast<const uint8_t *>(cache->pool);
-    apply_tensor_scale(p, sm_scale, cache->global_scale);
+    apply_tensor_scale(p, sm_scale, cache);
     cudaError_t e = launch_decode_nvfp4_multi(p, to_cuda(stream));
     if (e == cudaSuccess)
         e = launch_merge(p, to_cuda(stream));
@@ -346,6 +384,7 @@ nvfp4kv_status nvfp4kv_dequant_prefix_fp8(const nvfp4kv_cache *cache, const int3
     p.max_pages = max_pages_per_seq;
     p.num_pages = cache->num_pages;
     p.gscale = cache->global_scale;
+    p.hs = head_scales_of(cache);
     return from_cuda(launch_dequant_prefix_fp8(p, to_cuda(stream)));
 }
 
@@ -390,6 +429,7 @@ nvfp4kv_status nvfp4kv_extend_attention_fp8_append(const nvfp4kv_cache *cache, c
     p.slot_mapping = slot_mapping;
     p.num_pages = cache->num_pages;
     p.gscale = cache->global_scale;
+    p.hs = head_scales_of(cache);
     return from_cuda(launch_extend_attention(p, to_cuda(stream)));
 }
 
@@ -459,7 +499,7 @@ nvfp4kv_status nvfp4kv_append_paged_decode(const nvfp4kv_cache *cache, const voi
     if (st != NVFP4KV_OK || batch == 0)
         return st;
     p.pool = static_cast<const uint8_t *>(cache->pool);
-    apply_tensor_scale(p, sm_scale, cache->global_scale);
+    apply_tensor_scale(p, sm_scale, cache);
     p.k_new = k_new;
     p.v_new = v_new;
     p.append = 1;

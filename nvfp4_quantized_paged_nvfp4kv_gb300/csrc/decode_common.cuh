@@ -348,7 +348,7 @@ __device__ __forceinline__ size_t out_row(const DecodeParams &p, int b, int hp, 
 // with the row group innermost so that the row groups of a kv head read the
 // same pages close together in time.
 template <class Fmt, bool kMulti = false>
-__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_kernel(const __grid_constant__ DecodeParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
                         load16<true>(is_v ? p.v_new : p.k_new, src, x);
                     else
                         load16<false>(is_v ? p.v_new : p.k_new, src, x);
-                    divide_by_tensor_scale(x, p.gscale);
+                    divide_by_tensor_scale(x, head_tensor_scale(p.hs, is_v, hh, p.gscale));
                     Fmt::write_block(const_cast<uint8_t *>(p.pool) + (static_cast<size_t>(phys) * p.hkv + hh) * R,
                                      is_v, tok, blk, x);
                     fence_proxy_async_global();
@@ -521,6 +521,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
             limB = rB < p.rows ? L - p.q_len + rB / g + 1 : 0;
         }
         if (has_row) {
+            const float qsc = p.hs.per_head ? p.qs[kMulti ? hp : h] : p.qscale;
             const uint4 *qrow = reinterpret_cast<const uint4 *>(qsrc + 32 * tig);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -528,8 +529,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
                 const uint32_t ww[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float lo_f = __uint_as_float(ww[k] << 16) * p.qscale;
-                    const float hi_f = __uint_as_float(ww[k] & 0xffff0000u) * p.qscale;
+                    const float lo_f = __uint_as_float(ww[k] << 16) * qsc;
+                    const float hi_f = __uint_as_float(ww[k] & 0xffff0000u) * qsc;
                     qf[4 * i + k] = pack_f16x2(lo_f, hi_f);
                 }
             }
@@ -559,7 +560,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         if (owned) {
             // (a row that saw no key at all -- a multi-query row before its
             // first visible key -- has l = 0 and gets zeros)
-            const float r0 = L0 > 0.f ? p.out_scale / L0 : 0.f, r1 = L1 > 0.f ? p.out_scale / L1 : 0.f;
+            const float osc = head_tensor_scale(p.hs, true, kMulti ? hp : h, p.out_scale);
+            const float r0 = L0 > 0.f ? osc / L0 : 0.f, r1 = L1 > 0.f ? osc / L1 : 0.f;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 const int head = which ? hB : hA;
@@ -800,6 +802,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
 // group).  Segments that one worker covered were written by the decode kernel;
 // empty sequences get zeros here.
 constexpr int kMergeThreads = 256;
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p);
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams p);
 
 } // namespace nvfp4kv

@@ -63,7 +63,7 @@ __device__ __forceinline__ uint32_t e4m3_pair(uint32_t h2a, uint32_t h2b, float 
 
 } // namespace
 
-__global__ void __launch_bounds__(kPrefixThreads) dequant_prefix_kernel(const PrefixParams p)
+__global__ void __launch_bounds__(kPrefixThreads) dequant_prefix_kernel(const __grid_constant__ PrefixParams p)
 {
     __shared__ __align__(128) uint8_t buf[2][kNvfp4Record];
     __shared__ __align__(8) uint64_t bars[2];
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kPrefixThreads) dequant_prefix_kernel(const Pr
                     e2m1x8_to_f16x2x4(packed.x, f[0], f[1], f[2], f[3]);
                     e2m1x8_to_f16x2x4(packed.y, f[4], f[5], f[6], f[7]);
                     const size_t o = ((rows + tok) * p.hkv + cur.h) * kHeadDim + blk * 16;
-                    const float G = p.gscale;
+                    const float G = head_tensor_scale(p.hs, false, cur.h, p.gscale);
                     *reinterpret_cast<uint4 *>(p.k_out + o) = make_uint4(
                         e4m3_pair(hmul2(f[0], s2), hmul2(f[1], s2), G), e4m3_pair(hmul2(f[2], s2), hmul2(f[3], s2), G),
                         e4m3_pair(hmul2(f[4], s2), hmul2(f[5], s2), G), e4m3_pair(hmul2(f[6], s2), hmul2(f[7], s2), G));
@@ -171,14 +171,15 @@ __global__ void __launch_bounds__(kPrefixThreads) dequant_prefix_kernel(const Pr
                 const uint32_t s2 = e4m3x2_to_f16x2(lds_u16(rec + 2176 + row * 16 + blk * 2));   // (s_t0, s_t1)
                 // e8[r]: E4M3 bytes of channel 16*blk + r, low byte token t0, high byte t0 + 1
                 uint32_t e8[16];
+                const float Gv = head_tensor_scale(p.hs, true, cur.h, p.gscale);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t f0, f1, f2, f3;   // channels g, g + 8, g + 1, g + 9 (g = 2q), tokens (t0, t0 + 1)
                     e2m1x8_to_f16x2x4(unitw[q], f0, f1, f2, f3);
-                    e8[2 * q] = to_e4m3x2(hmul2(f0, s2), p.gscale);
-                    e8[2 * q + 8] = to_e4m3x2(hmul2(f1, s2), p.gscale);
-                    e8[2 * q + 1] = to_e4m3x2(hmul2(f2, s2), p.gscale);
-                    e8[2 * q + 9] = to_e4m3x2(hmul2(f3, s2), p.gscale);
+                    e8[2 * q] = to_e4m3x2(hmul2(f0, s2), Gv);
+                    e8[2 * q + 8] = to_e4m3x2(hmul2(f1, s2), Gv);
+                    e8[2 * q + 1] = to_e4m3x2(hmul2(f2, s2), Gv);
+                    e8[2 * q + 9] = to_e4m3x2(hmul2(f3, s2), Gv);
                 }
                 uint32_t w0[4], w1[4];
 #pragma unroll

@@ -283,6 +283,13 @@ __device__ __forceinline__ void pdl_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Tensor scale of kv head h of K or V: its per-head scale when the cache has
+// per-head factors, else the uniform one.
+__device__ __forceinline__ float head_tensor_scale(const HeadScales &hs, bool is_v, int h, float uniform)
+{
+    return hs.per_head ? (is_v ? hs.v[h] : hs.k[h]) : uniform;
+}
+
 __device__ __forceinline__ void report(int32_t *dev_status, int32_t bits)
 {
     if (dev_status != nullptr)

@@ -225,6 +225,7 @@ __device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const T
     auto offset = [&](int key, int blk) {
         return (static_cast<size_t>(c.c0 + key) * p.hkv + h) * kHeadDim + blk * 16;
     };
+    const float Gk = head_tensor_scale(p.hs, false, h, p.gscale), Gv = head_tensor_scale(p.hs, true, h, p.gscale);
     RawBlock<true> r[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -243,7 +244,7 @@ __device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const T
             continue;
         float x[16];
         unpack<true>(r[u], x);
-        divide_by_tensor_scale(x, p.gscale);
+        divide_by_tensor_scale(x, Gk);
         write_nvfp4_block(p.pool + rec, false, tok, blk, x);
     }
 #pragma unroll
@@ -270,29 +271,29 @@ __device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const T
         if (ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
             uint32_t S0, S1, q0[2], q1[2];
             unpack<true>(r[2 * u], x);
-            divide_by_tensor_scale(x, p.gscale);
+            divide_by_tensor_scale(x, Gv);
             quantize_block(x, S0, q0);
             unpack<true>(r[2 * u + 1], x);
-            divide_by_tensor_scale(x, p.gscale);
+            divide_by_tensor_scale(x, Gv);
             quantize_block(x, S1, q1);
             write_nvfp4_v_pair(p.pool + rec0, tok0, blk, S0, q0, S1, q1);
             continue;
         }
         if (ok0) {
             unpack<true>(r[2 * u], x);
-            divide_by_tensor_scale(x, p.gscale);
+            divide_by_tensor_scale(x, Gv);
             write_nvfp4_block(p.pool + rec0, true, tok0, blk, x);
         }
         if (ok1) {
             unpack<true>(r[2 * u + 1], x);
-            divide_by_tensor_scale(x, p.gscale);
+            divide_by_tensor_scale(x, Gv);
             write_nvfp4_block(p.pool + rec1, true, tok1, blk, x);
         }
     }
 }
 
 template <bool kAppend>
-__global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const ExtendParams p)
+__global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_constant__ ExtendParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);

@@ -12,7 +12,7 @@ namespace nvfp4kv {
 // its own running maximum (one pass over the partials), and the groups are
 // combined in shared memory at the end.  The segment's contributor range is
 // worked out once per CTA, before the wait for the decode kernel.
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams p)
 {
     constexpr int kGroups = kMergeThreads / 32;
     constexpr int kUnroll = 8;                   // contributors a thread loads before using any
@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
             sum.w += e * v.w;
             dsum += e * part_l[k];
         }
-        const float r = dsum > 0.f ? p.out_scale / dsum : 0.f;   // a row that saw no key: zeros
+        const float osc = head_tensor_scale(p.hs, true, hp, p.out_scale);
+        const float r = dsum > 0.f ? osc / dsum : 0.f;           // a row that saw no key: zeros
         res = make_float4(sum.x * r, sum.y * r, sum.z * r, sum.w * r);
     } else if (grp != 0) {
         return;                                  // empty sequence: zeros

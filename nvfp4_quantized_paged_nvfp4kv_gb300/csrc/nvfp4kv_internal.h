@@ -18,6 +18,16 @@ constexpr int kPartialFloats = kMaxGroup * kHeadDim + 2 * kMaxGroup;  // O[8][12
 constexpr int kNvfp4Record = 2304;           // bytes of an NVFP4 page-head record
 constexpr int kFp8Record = 4096;             // bytes of an FP8 page-head record
 constexpr int kMaxBatch = NVFP4KV_MAX_BATCH; // prefix table lives in shared memory
+constexpr int kMaxScaledHeads = NVFP4KV_MAX_SCALED_KV_HEADS;
+
+// Per-kv-head tensor scales of K and V, fl32(G * factor), used when per_head
+// is set (kernels take these parameters as __grid_constant__, so a head index
+// reads them in place); otherwise every head uses the uniform scale.
+struct HeadScales {
+    int per_head;
+    float k[kMaxScaledHeads];
+    float v[kMaxScaledHeads];
+};
 
 // Split-KV decode over either cache format.
 struct DecodeParams {
@@ -51,6 +61,10 @@ struct DecodeParams {
     int q_len;
     int rows;
     int row_groups;
+    // per-head tensor scales (NVFP4): append divisors and V output scales,
+    // and the query scale sm_scale * log2(e) * G_k,h of each kv head
+    HeadScales hs;
+    float qs[kMaxScaledHeads];
 };
 
 struct QuantParams {
@@ -64,6 +78,7 @@ struct QuantParams {
     int num_pages;
     int in_bf16;
     float gscale;                // tensor scale: blocks are taken of x / gscale
+    HeadScales hs;
 };
 
 struct PrefixParams {
@@ -79,6 +94,7 @@ struct PrefixParams {
     int max_pages;
     int num_pages;
     float gscale;                // tensor scale multiplying every value
+    HeadScales hs;
 };
 
 struct ExtendParams {
@@ -106,6 +122,7 @@ struct ExtendParams {
     const int32_t *slot_mapping; // [q rows]
     int num_pages;
     float gscale;                // tensor scale: blocks are taken of x / gscale
+    HeadScales hs;
 };
 
 // Launch with programmatic stream serialisation allowed, so the kernel's

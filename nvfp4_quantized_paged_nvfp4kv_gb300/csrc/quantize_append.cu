@@ -46,7 +46,7 @@ __device__ __forceinline__ bool site_of(const QuantParams &p, int slot, int h, i
 // the atomic nibble merge.  Data loads are issued together with the slot
 // loads (the source offset does not depend on the slot).
 template <bool kBf16>
-__global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const QuantParams p)
+__global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const __grid_constant__ QuantParams p)
 {
     pdl_wait();                  // the records may still be read by the previous kernel
     pdl_launch_dependents();
@@ -77,25 +77,26 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const QuantParams p
     const bool ok0 = has0 && site_of(p, s0, h, kNvfp4Record, rec0, tok0, rep);
     const bool ok1 = has1 && site_of(p, s1, h, kNvfp4Record, rec1, tok1, rep);
     float x[16];
+    const float G = head_tensor_scale(p.hs, is_v, h, p.gscale);
     if (is_v && ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
         uint32_t S0, S1, c0[2], c1[2];
         unpack<kBf16>(r0, x);
-        divide_by_tensor_scale(x, p.gscale);
+        divide_by_tensor_scale(x, G);
         quantize_block(x, S0, c0);
         unpack<kBf16>(r1, x);
-        divide_by_tensor_scale(x, p.gscale);
+        divide_by_tensor_scale(x, G);
         quantize_block(x, S1, c1);
         write_nvfp4_v_pair(p.pool + rec0, tok0, blk, S0, c0, S1, c1);
         return;
     }
     if (ok0) {
         unpack<kBf16>(r0, x);
-        divide_by_tensor_scale(x, p.gscale);
+        divide_by_tensor_scale(x, G);
         write_nvfp4_block(p.pool + rec0, is_v, tok0, blk, x);
     }
     if (ok1) {
         unpack<kBf16>(r1, x);
-        divide_by_tensor_scale(x, p.gscale);
+        divide_by_tensor_scale(x, G);
         write_nvfp4_block(p.pool + rec1, is_v, tok1, blk, x);
     }
 }

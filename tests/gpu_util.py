@@ -34,12 +34,13 @@ class Built:
     """GPU caches (NVFP4 and optionally FP8) for a workload plus its tables."""
 
     def __init__(self, w, spare_pages=3, fp8=True, in_dtype=torch.float32, garbage=False,
-                 keep_rows=False, global_scale=1.0):
+                 keep_rows=False, global_scale=1.0, head_scales=None):
         self.w = w
         self.global_scale = global_scale
+        self.head_scales = head_scales
         self.bt, self.num_pages = workloads.block_table(w, spare_pages=spare_pages)
         self.cache = nv.NVFP4Cache.allocate(self.num_pages, w.num_kv_heads, device=DEV,
-                                            global_scale=global_scale)
+                                            global_scale=global_scale, head_scales=head_scales)
         self.fp8 = nv.FP8Cache.allocate(self.num_pages, w.num_kv_heads, device=DEV) if fp8 else None
         if garbage:                   # unused slots hold bytes that decode to NaN scales
             self.cache.pool.fill_(0xFF)
@@ -137,10 +138,13 @@ def oracle_full(built: Built, fp8=False):
             oracle.fp8_quantize_append(k, sm, kc)
             oracle.fp8_quantize_append(v, sm, vc)
         else:
-            oracle.quantize_append(k, sm, pools[0], pools[1], global_scale=built.global_scale)
-            oracle.quantize_append(v, sm, pools[2], pools[3], global_scale=built.global_scale)
+            hs = built.head_scales
+            oracle.quantize_append(k, sm, pools[0], pools[1], global_scale=built.global_scale,
+                                   head_scales=None if hs is None else hs[0])
+            oracle.quantize_append(v, sm, pools[2], pools[3], global_scale=built.global_scale,
+                                   head_scales=None if hs is None else hs[1])
     q = built.q.float().cpu().numpy()
     if fp8:
         return oracle.fp8_paged_decode(kc, vc, q, built.bt, np.int32(w.seq_lens)), (kc, vc)
     return oracle.paged_decode(*pools, q, built.bt, np.int32(w.seq_lens),
-                               global_scale=built.global_scale), pools
+                               global_scale=built.global_scale, head_scales=built.head_scales), pools

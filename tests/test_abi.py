@@ -93,6 +93,23 @@ def test_cache_validation(kw, want):
     assert decode(cache(**kw)) == want
 
 
+def test_head_scale_validation():
+    """Per-head factors are checked on the host: each factor and its product
+    with G must be positive normal finite, num_kv_heads at most 128."""
+    def with_scales(vals, **kw):
+        arr = (ctypes.c_float * len(vals))(*vals)
+        c = cache(head_scales=ctypes.addressof(arr), **kw)
+        return append(c, k=FAKE + 4)          # passes the cache checks, then fails on k's alignment
+    assert with_scales([1.0, 2.0, 0.5, 4.0]) == nv.ERR_INVALID_ARG            # accepted
+    assert with_scales([1.0, 0.0, 0.5, 4.0]) == nv.ERR_UNSUPPORTED
+    assert with_scales([1.0, float("nan"), 0.5, 4.0]) == nv.ERR_UNSUPPORTED
+    assert with_scales([1.0, -2.0, 0.5, 4.0]) == nv.ERR_UNSUPPORTED
+    assert with_scales([1.0, 1e-40, 0.5, 4.0]) == nv.ERR_UNSUPPORTED          # subnormal factor
+    assert with_scales([1.0, 1e30, 0.5, 4.0], global_scale=1e10) == nv.ERR_UNSUPPORTED   # product overflows
+    many = [1.0] * 400
+    assert with_scales(many, num_kv_heads=200) == nv.ERR_UNSUPPORTED           # over 128 kv heads
+
+
 def test_append_validation():
     assert append(None) == nv.ERR_INVALID_ARG
     assert append(cache(), n=-1) == nv.ERR_INVALID_ARG

@@ -72,6 +72,21 @@ def test_tensor_scale(g):
     assert int(b.status.item()) == 0
 
 
+PER_HEAD = [[0.5, 3.0, 1.0 / 7.0, 1.0], [2.0, 0.3, 1.0, 9.5]]     # [K, V][kv head]
+
+
+def test_per_head_scales():
+    """Decode over a cache whose kv heads carry their own K and V tensor
+    scales: each head's query scale and normaliser carry them (owned and split
+    segments, several worker counts)."""
+    w = workloads.custom(3, 16, 4, (300, 17, 1000), seed=27)
+    b = Built(w, fp8=False, global_scale=0.37, head_scales=PER_HEAD, garbage=True)
+    want, _ = oracle_full(b)
+    for nw in (0, 7, 333):
+        assert_close(b.decode(torch.float32, num_workers=nw), want, f"per-head scales, {nw} workers")
+    assert int(b.status.item()) == 0
+
+
 def test_more_workers_than_page_heads():
     """One long sequence among many short ones: the automatic worker count,
     bounded by the largest batch the block table allows, and an explicit one
@@ -139,13 +154,13 @@ def test_long_context_sampled(name, batch):
 
 @pytest.mark.parametrize("fp8", [False, True])
 @pytest.mark.parametrize("lens", [(37, 16, 1, 300, 0), (8192, 8191, 8177)])
-def test_append_decode_equals_append_then_decode(fp8, lens, g=1.0):
+def test_append_decode_equals_append_then_decode(fp8, lens, g=1.0, hs=None):
     """The fused step writes exactly the bytes quantize_append would and then
     decodes exactly as paged_decode does."""
     w = workloads.custom(len(lens), 32, 4, lens, seed=21)
-    full = Built(w, global_scale=g)                     # all tokens appended by quantize_append
+    full = Built(w, global_scale=g, head_scales=hs)     # all tokens appended by quantize_append
     cache = (nv.FP8Cache.allocate(full.num_pages, w.num_kv_heads, device="cuda") if fp8 else
-             nv.NVFP4Cache.allocate(full.num_pages, w.num_kv_heads, device="cuda", global_scale=g))
+             nv.NVFP4Cache.allocate(full.num_pages, w.num_kv_heads, device="cuda", global_scale=g, head_scales=hs))
     app = nv.fp8kv_quantize_append if fp8 else nv.nvfp4kv_quantize_append
     k_new = torch.zeros((w.batch, w.num_kv_heads, 128), dtype=torch.float32, device="cuda")
     v_new = torch.zeros_like(k_new)
@@ -174,6 +189,31 @@ def test_append_decode_equals_append_then_decode(fp8, lens, g=1.0):
 
 def test_append_decode_with_tensor_scale():
     test_append_decode_equals_append_then_decode(False, (40, 1, 300), g=0.37)
+
+
+def test_append_decode_with_per_head_scales():
+    test_append_decode_equals_append_then_decode(False, (40, 1, 300), g=0.37, hs=PER_HEAD)
+
+
+def test_multi_query_per_head_scales():
+    """Multi-query decode (q_len 3, group 4) with per-head K and V scales."""
+    w = workloads.custom(2, 16, 4, (129, 700), seed=41)
+    b = Built(w, fp8=False, global_scale=1.5, head_scales=PER_HEAD)
+    q_len = 3
+    rng = np.random.default_rng(8)
+    q = torch.from_numpy(rng.standard_normal((w.batch, q_len, 16, 128)).astype(np.float32)).to(torch.bfloat16)
+    _, pools = oracle_full(b)
+    ref = np.zeros((w.batch, q_len, 16, 128))
+    for t in range(q_len):
+        lt = np.maximum(np.int32(w.seq_lens) - q_len + t + 1, 0).astype(np.int32)
+        ref[:, t] = oracle.paged_decode(*pools, q[:, t].float().numpy(), b.bt, lt, global_scale=1.5,
+                                        head_scales=PER_HEAD)
+    out = torch.full((w.batch, q_len, 16, 128), float("nan"), dtype=torch.float32, device="cuda")
+    ws = nv.new_workspace(device="cuda")
+    nv.nvfp4kv_paged_decode_multi(b.cache, q.cuda(), b.bt_d, b.sl_d, out, ws, dev_status=b.status)
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy(), ref, "multi-query, per-head scales")
+    assert int(b.status.item()) == 0
 
 
 @pytest.mark.parametrize("hq,hkv,q_len,lens", [

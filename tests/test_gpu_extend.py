@@ -172,9 +172,10 @@ def chunk_slots(e, seed, odd_shift=False):
     return np.concatenate(slots).astype(np.int32), len(perm)
 
 
-def run_fused(e, x, slots, num_pages, global_scale=1.0, status=None):
+def run_fused(e, x, slots, num_pages, global_scale=1.0, status=None, head_scales=None):
     xd = to_dev(x)
-    cache = nv.NVFP4Cache.allocate(num_pages, e.num_kv_heads, device=DEV, global_scale=global_scale)
+    cache = nv.NVFP4Cache.allocate(num_pages, e.num_kv_heads, device=DEV, global_scale=global_scale,
+                                   head_scales=head_scales)
     out = torch.full((e.q_rows, e.num_q_heads, 128), float("nan"), device=DEV)
     nv.nvfp4kv_extend_attention_fp8_append(cache, torch.from_numpy(slots).to(DEV), xd["q"], xd["q_indptr"],
                                            xd["k_prefix"], xd["v_prefix"], xd["kv_indptr"], xd["prefix_lens"],
@@ -184,10 +185,14 @@ def run_fused(e, x, slots, num_pages, global_scale=1.0, status=None):
     return out.cpu().numpy(), list(nvfp4_planes(cache.pool.cpu().numpy()))
 
 
-def oracle_planes(e, x, slots, num_pages, global_scale=1.0):
+def oracle_planes(e, x, slots, num_pages, global_scale=1.0, head_scales=None):
     pools = [np.zeros((num_pages, e.num_kv_heads, 16, n), np.uint8) for n in (64, 8, 64, 8)]
-    oracle.quantize_append(x["k_chunk"].float().numpy(), slots, pools[0], pools[1], global_scale=global_scale)
-    oracle.quantize_append(x["v_chunk"].float().numpy(), slots, pools[2], pools[3], global_scale=global_scale)
+    hk = None if head_scales is None else head_scales[0]
+    hv = None if head_scales is None else head_scales[1]
+    oracle.quantize_append(x["k_chunk"].float().numpy(), slots, pools[0], pools[1], global_scale=global_scale,
+                           head_scales=hk)
+    oracle.quantize_append(x["v_chunk"].float().numpy(), slots, pools[2], pools[3], global_scale=global_scale,
+                           head_scales=hv)
     return pools
 
 
@@ -226,4 +231,19 @@ def test_fused_append_tensor_scale_and_skipped_slots():
     slots[50] = -1
     assert_close(got, oracle_out(e, x), "fused extend out, G = 0.37")
     for g_, w_ in zip(planes, oracle_planes(e, x, slots, num_pages, global_scale=0.37)):
+        np.testing.assert_array_equal(g_, w_)
+
+
+def test_fused_append_per_head_scales():
+    """The chunk written at per-head tensor scales fl32(G * factor): bit-exact
+    with the oracle's quantize_append at the same scales."""
+    e = workloads.extend_custom((33, 70), (90, 41), 16, 4, seed=78)
+    x = workloads.extend_inputs(e)
+    slots, num_pages = chunk_slots(e, seed=6)
+    hs = [[0.5, 3.0, 1.0 / 7.0, 1.0], [2.0, 0.3, 1.0, 9.5]]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got, planes = run_fused(e, x, slots, num_pages, global_scale=0.37, status=status, head_scales=hs)
+    assert status.item() == 0
+    assert_close(got, oracle_out(e, x), "fused extend out, per-head scales")
+    for g_, w_ in zip(planes, oracle_planes(e, x, slots, num_pages, global_scale=0.37, head_scales=hs)):
         np.testing.assert_array_equal(g_, w_)

@@ -26,18 +26,20 @@ def run(b: Built, prefix_lens, indptr, rows):
 def expected(b: Built, prefix_lens, indptr, rows):
     _, pools = oracle_full(b)
     g = b.global_scale
+    hs = b.head_scales
     k = oracle.dequant_prefix_fp8(pools[0], pools[1], b.bt, np.int32(prefix_lens), np.int32(indptr), rows,
-                                  global_scale=g)
+                                  global_scale=g, head_scales=None if hs is None else hs[0])
     v = oracle.dequant_prefix_fp8(pools[2], pools[3], b.bt, np.int32(prefix_lens), np.int32(indptr), rows,
-                                  global_scale=g)
+                                  global_scale=g, head_scales=None if hs is None else hs[1])
     return k, v
 
 
-@pytest.mark.parametrize("g", [0.37, 3.1])
-def test_prefix_with_tensor_scale(g):
-    """Workspace values E4M3(fl32(G s e)) for a tensor scale G != 1."""
+@pytest.mark.parametrize("g,hs", [(0.37, None), (3.1, None), (0.37, [[0.5, 3.0], [2.0, 0.125]])])
+def test_prefix_with_tensor_scale(g, hs):
+    """Workspace values E4M3(fl32(G_h s e)) for a tensor scale G != 1, and with
+    per-head factors (G_h = fl32(G * factor) per kv head of K and V)."""
     w = workloads.custom(2, 8, 2, (301, 40), seed=29)
-    b = Built(w, fp8=False, global_scale=g)
+    b = Built(w, fp8=False, global_scale=g, head_scales=hs)
     lens = list(w.seq_lens)
     indptr = [3, 3 + lens[0]]
     rows = 3 + sum(lens) + 2

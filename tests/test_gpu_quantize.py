@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def run_gpu(x_k, x_v, slots, num_pages, hkv, fp8=False, global_scale=1.0):
+def run_gpu(x_k, x_v, slots, num_pages, hkv, fp8=False, global_scale=1.0, head_scales=None):
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     sm = torch.from_numpy(np.asarray(slots, np.int32)).to(DEV)
     if fp8:
@@ -22,13 +22,13 @@ def run_gpu(x_k, x_v, slots, num_pages, hkv, fp8=False, global_scale=1.0):
         nv.fp8kv_quantize_append(c, x_k.to(DEV), x_v.to(DEV), sm, status)
         torch.cuda.synchronize()
         return list(fp8_planes(c.pool.cpu().numpy())), int(status.item())
-    c = nv.NVFP4Cache.allocate(num_pages, hkv, device=DEV, global_scale=global_scale)
+    c = nv.NVFP4Cache.allocate(num_pages, hkv, device=DEV, global_scale=global_scale, head_scales=head_scales)
     nv.nvfp4kv_quantize_append(c, x_k.to(DEV), x_v.to(DEV), sm, status)
     torch.cuda.synchronize()
     return list(nvfp4_planes(c.pool.cpu().numpy())), int(status.item())
 
 
-def run_oracle(x_k, x_v, slots, num_pages, hkv, fp8=False, global_scale=1.0):
+def run_oracle(x_k, x_v, slots, num_pages, hkv, fp8=False, global_scale=1.0, head_scales=None):
     kf = x_k.float().numpy()
     vf = x_v.float().numpy()
     slots = np.asarray(slots, np.int32)
@@ -39,8 +39,10 @@ def run_oracle(x_k, x_v, slots, num_pages, hkv, fp8=False, global_scale=1.0):
         oracle.fp8_quantize_append(vf, slots, vc)
         return [kc, vc]
     pools = [np.zeros((num_pages, hkv, 16, s), np.uint8) for s in (64, 8, 64, 8)]
-    oracle.quantize_append(kf, slots, pools[0], pools[1], global_scale=global_scale)
-    oracle.quantize_append(vf, slots, pools[2], pools[3], global_scale=global_scale)
+    hk = None if head_scales is None else head_scales[0]
+    hv = None if head_scales is None else head_scales[1]
+    oracle.quantize_append(kf, slots, pools[0], pools[1], global_scale=global_scale, head_scales=hk)
+    oracle.quantize_append(vf, slots, pools[2], pools[3], global_scale=global_scale, head_scales=hv)
     return pools
 
 
@@ -134,6 +136,25 @@ def test_tensor_scale_bit_exact(g, dtype):
     slots = list(rng.permutation(pages * 16)[:T])
     got, st = run_gpu(k, v, slots, pages, hkv, global_scale=g)
     want = run_oracle(k, v, slots, pages, hkv, global_scale=g)
+    assert st == 0
+    for g_, w_ in zip(got, want):
+        np.testing.assert_array_equal(g_, w_)
+
+
+HEAD_FACTORS = [[0.5, 3.0, 1.0 / 7.0, 1.0], [2.0, 0.3, 1.0, 9.5]]     # [K, V][kv head]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_per_head_scales_bit_exact(dtype):
+    """Kv head h of K (V) quantised at fl32(G * factor): codes and scales equal
+    the oracle's."""
+    rng = np.random.default_rng(19)
+    T, hkv, pages = 90, 4, 8
+    k = torch.from_numpy((rng.standard_t(3, (T, hkv, 128)) * 3).astype(np.float32)).to(dtype)
+    v = torch.from_numpy(rng.standard_normal((T, hkv, 128)).astype(np.float32)).to(dtype)
+    slots = list(rng.permutation(pages * 16)[:T])
+    got, st = run_gpu(k, v, slots, pages, hkv, global_scale=0.37, head_scales=HEAD_FACTORS)
+    want = run_oracle(k, v, slots, pages, hkv, global_scale=0.37, head_scales=HEAD_FACTORS)
     assert st == 0
     for g_, w_ in zip(got, want):
         np.testing.assert_array_equal(g_, w_)
