@@ -181,6 +181,37 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b)
     return r;
 }
 
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// Eight fp32 -> one word of four E2M1 code pairs (round to nearest even,
+// saturating): byte j holds e[j] in its low nibble and o[j] in its high one.
+__device__ __forceinline__ uint32_t f32x8_to_e2m1x8(float e0, float o0, float e1, float o1, float e2, float o2,
+                                                    float e3, float o3)
+{
+    uint32_t w;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(w)
+        : "f"(e0), "f"(o0), "f"(e1), "f"(o1), "f"(e2), "f"(o2), "f"(e3), "f"(o3));
+    return w;
+}
+
 __device__ __forceinline__ float f32x2_lo(uint64_t v)
 {
     return __uint_as_float(static_cast<uint32_t>(v));

@@ -94,17 +94,21 @@ __device__ __forceinline__ void quantize_block(const float (&x)[16], uint32_t &s
     const float sc = e4m3_to_f32(scale_byte);
     packed[0] = packed[1] = 0u;
     if (sc != 0.f) {
+        // the quotient step two lanes at a time (packed fp32, each lane IEEE)
         const float r = __frcp_rn(sc);
-        auto quotient = [&](float v) {
-            const float q0 = __fmul_rn(v, r);
-            // the correction step turns a -0 quotient into +0: restore the sign
-            return copysignf(__fmaf_rn(__fmaf_rn(-q0, sc, v), r, q0), v);
-        };
+        const uint64_t r2 = f32x2_pack(r, r), nsc2 = f32x2_pack(-sc, -sc);
+        float q[16];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const uint32_t byte = f32x2_to_e2m1x2(quotient(x[2 * j]), quotient(x[2 * j + 1]));
-            packed[j >> 2] |= byte << (8 * (j & 3));
+            const uint64_t v2 = f32x2_pack(x[2 * j], x[2 * j + 1]);
+            const uint64_t q0 = mul_f32x2(v2, r2);
+            const uint64_t qq = fma_f32x2(fma_f32x2(q0, nsc2, v2), r2, q0);
+            // the correction step turns a -0 quotient into +0: restore the sign
+            q[2 * j] = copysignf(f32x2_lo(qq), x[2 * j]);
+            q[2 * j + 1] = copysignf(f32x2_hi(qq), x[2 * j + 1]);
         }
+        packed[0] = f32x8_to_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
+        packed[1] = f32x8_to_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
     }
 }
 
