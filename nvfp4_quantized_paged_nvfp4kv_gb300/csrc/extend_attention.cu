@@ -115,14 +115,33 @@ struct TcCta {
 // convert it to f16 in the 128-byte-swizzled layout and signal the MMA warp.
 // FP8 prefix tiles: 64 keys x 8 pieces of 16 bytes per K and per V, four
 // pieces a thread each, loaded together.  bf16 chunk tiles: 64 keys x 16
-// pieces per K and per V, eight a thread each, K then V (eight loads in
-// flight a thread keep the register count low).  Keys past the end are zeros.
+// pieces per K and per V; thread pt owns piece pt mod 16 of keys pt / 16 + 8 j
+// (j = 0..7), K then V (eight loads in flight a thread keep the register count
+// low); its offsets repeat from tile to tile and are taken once.  Keys past
+// the end are zeros.
+struct ChunkLanes {
+    int key;                         // first key of the thread's bf16 pieces
+    uint32_t src;                    // its element offset inside a chunk tile's first row
+    uint32_t dst;                    // swizzled f16 offset of its piece of key `key`
+};
+
+__device__ __forceinline__ ChunkLanes chunk_lanes(const ExtendParams &p, int pt)
+{
+    ChunkLanes l;
+    const uint32_t piece = pt & 15;
+    l.key = pt >> 4;
+    l.src = static_cast<uint32_t>(l.key * p.hkv * kHeadDim) + 8 * piece;
+    l.dst = sw128(kTcKeys, l.key, piece);
+    return l;
+}
+
 __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta &c, int h, int i, int pt,
-                                             uint32_t base, volatile int *fail)
+                                             const ChunkLanes &l, uint32_t base, volatile int *fail)
 {
     const int st = i % kKvStages;
     const uint32_t kdst = base + kOffK + st * kKVBytes, vdst = base + kOffV + st * kKVBytes;
     const uint4 zero = make_uint4(0, 0, 0, 0);
+    const size_t row_elems = static_cast<size_t>(p.hkv) * kHeadDim;   // one key's bf16 row
     uint4 raw[8];
     const bool pre = i < c.n_pre;
     const int k0 = (pre ? i : i - c.n_pre) * kTcKeys;
@@ -136,14 +155,10 @@ __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta 
             raw[u] = k0 + key < c.P ? ldg_nc(src) : zero;
         }
     } else {
+        const size_t tile = (static_cast<size_t>(c.c0 + k0) * p.hkv + h) * kHeadDim + l.src;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int idx = pt + kProducerThreads * u;
-            const int key = idx >> 4, piece = idx & 15;
-            raw[u] = k0 + key < c.C ? ldg_nc(p.k_chunk + (static_cast<int64_t>(c.c0 + k0 + key) * p.hkv + h) *
-                                                              kHeadDim + 8 * piece)
-                                    : zero;
-        }
+        for (int u = 0; u < 8; ++u)
+            raw[u] = k0 + l.key + 8 * u < c.C ? ldg_nc(p.k_chunk + tile + u * 8 * row_elems) : zero;
     }
     // stage st was last read by the MMAs of tile i - kKvStages
     if (i >= kKvStages && !wait_or_fail(base + kOffBar + 8 * (kBarKvEmpty + st), ((i / kKvStages) - 1) & 1, fail,
@@ -166,28 +181,23 @@ __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta 
             sts128(dst + sw128(kTcKeys, key, 2 * piece + 1 - first), first ? lo : hi);
         }
     } else {
+        const size_t tile = (static_cast<size_t>(c.c0 + k0) * p.hkv + h) * kHeadDim + l.src;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             if (half == 1) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int idx = pt + kProducerThreads * u;
-                    const int key = idx >> 4, piece = idx & 15;
-                    raw[u] = k0 + key < c.C ? ldg_nc(p.v_chunk + (static_cast<int64_t>(c.c0 + k0 + key) * p.hkv + h) *
-                                                                      kHeadDim + 8 * piece)
-                                            : zero;
-                }
+                for (int u = 0; u < 8; ++u)
+                    raw[u] = k0 + l.key + 8 * u < c.C ? ldg_nc(p.v_chunk + tile + u * 8 * row_elems) : zero;
             }
+            const uint32_t dst = (half ? vdst : kdst) + l.dst;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int idx = pt + kProducerThreads * u;
-                const uint32_t key = idx >> 4, piece = idx & 15;
                 uint4 f;
                 f.x = bf16x2_to_f16x2(raw[u].x, 1.f);
                 f.y = bf16x2_to_f16x2(raw[u].y, 1.f);
                 f.z = bf16x2_to_f16x2(raw[u].z, 1.f);
                 f.w = bf16x2_to_f16x2(raw[u].w, 1.f);
-                sts128((half ? vdst : kdst) + sw128(kTcKeys, key, piece), f);
+                sts128(dst + 1024u * u, f);     // keys chunk_key + 8 u: 8 u rows below, same swizzle
             }
         }
     }
@@ -411,8 +421,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
         __syncwarp();
     } else if (warp >= kSoftmaxThreads / 32) {
         const int pt = tid - kSoftmaxThreads;
+        const ChunkLanes lanes = chunk_lanes(p, pt);
         for (int i = 0; i < c.n_tiles; ++i)
-            if (!produce_tile(p, c, h, i, pt, base, fail))
+            if (!produce_tile(p, c, h, i, pt, lanes, base, fail))
                 break;
         if constexpr (kAppend) {
             // the chunk key tiles whose first key's first row (64 kt g) falls in
