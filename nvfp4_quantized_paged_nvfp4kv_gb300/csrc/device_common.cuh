@@ -122,19 +122,6 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &r0, uint
         : "r"(w));
 }
 
-// Two fp32 -> one byte of two E2M1 codes, round to nearest even, saturating;
-// `even` goes to the low nibble.
-__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float even, float odd)
-{
-    uint32_t r;
-    asm("{\n\t.reg .b8 t;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
-        "cvt.u32.u8 %0, t;\n\t}"
-        : "=r"(r)
-        : "f"(odd), "f"(even));
-    return r;
-}
-
 // Two fp32 -> two E4M3 bytes (round to nearest even, saturating); `lo` goes to
 // the low byte.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
