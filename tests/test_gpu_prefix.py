@@ -70,6 +70,23 @@ def test_prefix_bit_exact(name):
     assert int(b.status.item()) == 0
 
 
+def test_prefix_many_units_per_cta():
+    """More (sequence, page, kv head) units than CTAs, ragged lengths: each CTA
+    steps through several units whose page and sequence digits carry."""
+    lens = (3000, 17, 2999, 0, 1600)
+    w = workloads.custom(len(lens), 16, 8, lens, seed=33)
+    b = Built(w, fp8=False)
+    plens = [max(0, L - 5) for L in lens]
+    indptr = list(np.concatenate([[2], 2 + np.cumsum(plens)[:-1]]))
+    rows = 2 + sum(plens) + 1
+    got = run(b, plens, indptr, rows)
+    want = expected(b, plens, indptr, rows)
+    for g_, w_ in zip(got, want):
+        for s, L in zip(indptr, plens):
+            np.testing.assert_array_equal(g_[s:s + L], w_[s:s + L])
+    assert int(b.status.item()) == 0
+
+
 def test_prefix_160k_sampled():
     """One 160K-token prefix (the long-context extend workload) checked on
     sampled token ranges."""
