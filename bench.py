@@ -777,7 +777,11 @@ def run_reference(args, world, rank):
             "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "batch": w.batch, "num_q_heads": w.num_q_heads,
-                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim},
+                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+                       "seq_len": (w.seq_lens[0] if len(set(w.seq_lens)) == 1 else "ragged"),
+                       "kv_tokens_per_step": w.total_tokens,
+                       "step": "a bounded sample of the workload per step (see cpu_baseline.sample), "
+                               "the rate scaled to KV-tokens/s"},
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": sample},
