@@ -383,10 +383,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
             constexpr uint32_t i_qk = idesc_f16(kTcRows, kTcKeys, false);
             constexpr uint32_t i_pv = idesc_f16(kTcRows, kHeadDim, true);
             bool ok = true;
-            auto issue_qk = [&](int i) {
+            auto qk = [&](int i) {
                 const int b = i & 1, st = i % kKvStages;
-                if (!wait_or_fail(bar + 8 * (kBarKvFull + st), (i / kKvStages) & 1, fail, p.dev_status))
-                    return false;
                 tc_fence_after_sync();
                 const uint32_t kb = base + kOffK + st * kKVBytes;
 #pragma unroll
@@ -395,15 +393,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
                              smem_desc(base + kOffQ + (s >> 2) * (kTcRows * 128) + (s & 3) * 32, 16, 1024),
                              smem_desc(kb + (s >> 2) * (kTcKeys * 128) + (s & 3) * 32, 16, 1024), i_qk, s > 0);
                 umma_commit(bar + 8 * (kBarSFull + b));
-                return true;
             };
-            ok = issue_qk(0);
-            for (int i = 0; ok && i < c.n_tiles; ++i) {
+            auto pv = [&](int i) {
                 const int b = i & 1;
-                if (i + 1 < c.n_tiles && !(ok = issue_qk(i + 1)))
-                    break;
-                if (!(ok = wait_or_fail(bar + 8 * (kBarPFull + b), (i >> 1) & 1, fail, p.dev_status)))
-                    break;
                 tc_fence_after_sync();
                 const uint32_t vb = base + kOffV + (i % kKvStages) * kKVBytes;
 #pragma unroll
@@ -412,6 +404,38 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
                                 smem_desc(vb + s * 2048, kTcKeys * 128, 1024), i_pv, i > 0 || s > 0);
                 umma_commit(bar + 8 * (kBarPvDone + b));
                 umma_commit(bar + 8 * (kBarKvEmpty + i % kKvStages));
+            };
+            // Q K^T of tile j may be issued once its keys are in and S buffer
+            // j mod 2 is free (tile j - 2's P V issued), P V of tile i once its
+            // P is in.  Whichever is ready first goes first, so a value product
+            // never waits behind the conversion of the next key tile.  P V of
+            // tile i always precedes Q K^T of tile i + 2 (the P aliasing).
+            int next_qk = 0;
+            for (int i = 0; ok && i < c.n_tiles; ++i) {
+                const int b = i & 1;
+                bool pv_done = false;
+                for (uint32_t polls = 0; !pv_done;) {
+                    bool progress = false;
+                    if (next_qk <= i + 1 && next_qk < c.n_tiles &&
+                        mbar_test_wait(bar + 8 * (kBarKvFull + next_qk % kKvStages), (next_qk / kKvStages) & 1)) {
+                        qk(next_qk++);
+                        progress = true;
+                    }
+                    if (next_qk > i && mbar_test_wait(bar + 8 * (kBarPFull + b), (i >> 1) & 1)) {
+                        pv(i);
+                        pv_done = progress = true;
+                    }
+                    if (progress)
+                        continue;
+                    if (++polls > 64 * kWaitLimit || *fail) {
+                        if (!*fail) {
+                            *fail = 1;
+                            report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
+                        }
+                        ok = false;
+                        break;
+                    }
+                }
             }
             // nothing of this thread's may still run when tensor memory is freed
             umma_commit(bar + 8 * kBarDone);
