@@ -137,10 +137,14 @@ def test_llama70b_layer_sampled(name, batch):
     assert int(b.status.item()) == 0
 
 
-@pytest.mark.parametrize("name,batch", [("ctx32k", 44), ("ctx160k", 10), ("ctx1m", 1)])
-def test_long_context_sampled(name, batch):
+@pytest.mark.parametrize("name,batch,fp8", [("ctx32k", 44, True), ("ctx160k", 10, False), ("ctx1m", 1, True),
+                                            ("ctx32k", 70, False), ("ctx160k", 15, False), ("ctx1m", 2, False)])
+def test_long_context_sampled(name, batch, fp8):
+    """Each long-context workload at both batch sizes the bench reports (the
+    FP8-capacity and the NVFP4-capacity batch), as the bench launches it;
+    oracle on sampled (sequence, kv head) pairs."""
     w = workloads.make(name, batch=batch)
-    b = Built(w, spare_pages=0, fp8=(name != "ctx160k"))
+    b = Built(w, spare_pages=0, fp8=fp8)
     got = b.decode(torch.bfloat16)
     got8 = b.decode(torch.bfloat16, fp8=True) if b.fp8 is not None else None
     for seq, h in [(0, 3), (batch - 1, 6)]:
