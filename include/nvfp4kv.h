@@ -96,7 +96,8 @@ typedef enum {
     NVFP4KV_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size ... */
     NVFP4KV_ERR_UNSUPPORTED = 2,  /* valid but outside the supported geometry   */
     NVFP4KV_ERR_WORKSPACE = 3,    /* decode workspace smaller than required     */
-    NVFP4KV_ERR_CUDA = 4          /* a CUDA runtime call or launch failed       */
+    NVFP4KV_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed       */
+    NVFP4KV_ERR_DEVICE_CHECK = 5  /* a kernel set bits in the device status word */
 } nvfp4kv_status;
 
 /* Bits ORed into *dev_status by the kernels. */
@@ -388,6 +389,14 @@ int64_t nvfp4kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t pag
 /* Bytes of an FP8 pool: num_pages * num_kv_heads * page_size * 2 * head_dim. */
 int64_t fp8kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
                           int32_t head_dim);
+
+/* Read a device status word once the work on `stream` has finished:
+ * synchronises the stream, copies *dev_status (device int32) into *bits
+ * (host) and returns NVFP4KV_ERR_DEVICE_CHECK when any bit is set, NVFP4KV_OK
+ * when none is (NVFP4KV_ERR_CUDA if the synchronisation or copy fails).  The
+ * word is not reset.  Null pointers return NVFP4KV_ERR_INVALID_ARG. */
+nvfp4kv_status nvfp4kv_read_device_status(const int32_t *dev_status, nvfp4kv_stream_t stream,
+                                          int32_t *bits);
 
 /* Static description of a status code. */
 const char *nvfp4kv_status_string(nvfp4kv_status status);

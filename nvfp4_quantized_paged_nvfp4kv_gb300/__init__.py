@@ -30,7 +30,7 @@ from . import _build
 PAGE_SIZE = 16
 HEAD_DIM = 128
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = 0, 1, 2, 3, 4
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK = 0, 1, 2, 3, 4, 5
 DEV_BAD_PAGE, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 F32, BF16 = 0, 1
 
@@ -115,6 +115,7 @@ def load(build_if_missing: bool = True):
             "nvfp4kv_cache_bytes": (ctypes.c_int64, [_i32, _i32, _i32, _i32]),
             "fp8kv_cache_bytes": (ctypes.c_int64, [_i32, _i32, _i32, _i32]),
             "nvfp4kv_status_string": (ctypes.c_char_p, [_st]),
+            "nvfp4kv_read_device_status": (_st, [_vp, _vp, ctypes.POINTER(_i32)]),
             "nvfp4kv_version": (_i32, []),
         }
         for name, (res, args) in sig.items():
@@ -364,6 +365,19 @@ def nvfp4kv_cache_bytes(num_pages, num_kv_heads, page_size=PAGE_SIZE, head_dim=H
 
 def fp8kv_cache_bytes(num_pages, num_kv_heads, page_size=PAGE_SIZE, head_dim=HEAD_DIM) -> int:
     return int(load().fp8kv_cache_bytes(num_pages, num_kv_heads, page_size, head_dim))
+
+
+def read_device_status(dev_status, stream=None) -> int:
+    """Synchronise `stream` and return the bits of the device status word
+    (int32 tensor of one element); 0 when no kernel reported anything."""
+    bits = _i32(0)
+    st = load().nvfp4kv_read_device_status(_ptr(dev_status), _stream(stream), ctypes.byref(bits))
+    if st not in (OK, ERR_DEVICE_CHECK):
+        _check(st, "nvfp4kv_read_device_status")
+    return int(bits.value)
+
+
+nvfp4kv_read_device_status = read_device_status
 
 
 def status_string(status: int) -> str:

@@ -556,6 +556,19 @@ int64_t fp8kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_
     return 2 * static_cast<int64_t>(num_pages) * num_kv_heads * page_size * head_dim;
 }
 
+nvfp4kv_status nvfp4kv_read_device_status(const int32_t *dev_status, nvfp4kv_stream_t stream, int32_t *bits)
+{
+    if (dev_status == nullptr || bits == nullptr)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(to_cuda(stream)) != cudaSuccess)
+        return NVFP4KV_ERR_CUDA;
+    int32_t v = 0;
+    if (cudaMemcpy(&v, dev_status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return NVFP4KV_ERR_CUDA;
+    *bits = v;
+    return v != 0 ? NVFP4KV_ERR_DEVICE_CHECK : NVFP4KV_OK;
+}
+
 const char *nvfp4kv_status_string(nvfp4kv_status status)
 {
     switch (status) {
@@ -569,6 +582,8 @@ const char *nvfp4kv_status_string(nvfp4kv_status status)
         return "decode workspace missing, misaligned or too small";
     case NVFP4KV_ERR_CUDA:
         return "CUDA runtime error";
+    case NVFP4KV_ERR_DEVICE_CHECK:
+        return "a kernel reported bad device data (see the status bits)";
     }
     return "unknown status";
 }

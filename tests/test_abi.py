@@ -34,7 +34,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("nvfp4kv_quantize_append", "nvfp4kv_paged_decode", "nvfp4kv_dequant_prefix_fp8",
-              "fp8kv_paged_decode", "fp8kv_quantize_append", "nvfp4kv_decode_workspace_size"):
+              "fp8kv_paged_decode", "fp8kv_quantize_append", "nvfp4kv_decode_workspace_size",
+              "nvfp4kv_extend_attention_fp8", "nvfp4kv_read_device_status"):
         assert n in names
 
 
@@ -191,8 +192,14 @@ def test_extend_append_validation():
     assert call(cache(), batch=0, slots=None) == nv.OK
 
 
+def test_read_device_status_validation():
+    bits = ctypes.c_int32(0)
+    assert nv.load().nvfp4kv_read_device_status(None, None, ctypes.byref(bits)) == nv.ERR_INVALID_ARG
+    assert nv.load().nvfp4kv_read_device_status(FAKE, None, None) == nv.ERR_INVALID_ARG
+
+
 def test_status_strings_and_version():
-    for s in range(5):
+    for s in range(6):
         assert nv.status_string(s)
     assert nv.status_string(99) == "unknown status"
     assert nv.nvfp4kv_version() >= 100

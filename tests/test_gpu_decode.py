@@ -117,6 +117,10 @@ def test_bad_page_and_length_are_reported_not_faulted():
     b.sl_d = torch.tensor([40, 10 ** 6], dtype=torch.int32, device="cuda")
     b.decode(torch.float32)
     assert int(b.status.item()) & nv.DEV_BAD_LEN
+    # the same word through the C call that reads it
+    assert nv.read_device_status(b.status) == int(b.status.item())
+    b.status.zero_()
+    assert nv.read_device_status(b.status) == 0
 
 
 @pytest.mark.parametrize("name,batch", [("llama70b", 12), ("llama70b", 21)])
