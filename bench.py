@@ -119,6 +119,9 @@ KERNEL_SOURCES = {
                      "nvfp4kv_internal.h", "record_write.cuh"],
     "extend_attention": ["abi.cpp", "device_common.cuh", "extend_attention.cu", "nvfp4kv_internal.h",
                          "record_write.cuh", "tcgen05.cuh"],
+    "quantize_append": ["abi.cpp", "device_common.cuh", "nvfp4kv_internal.h", "quantize_append.cu",
+                        "record_write.cuh"],
+    "dequant_prefix": ["abi.cpp", "dequant_prefix.cu", "device_common.cuh", "nvfp4kv_internal.h"],
 }
 
 
