@@ -165,7 +165,9 @@ nvfp4kv_status nvfp4kv_quantize_append(const nvfp4kv_cache *cache, const void *k
 /* Bytes of decode workspace needed by nvfp4kv_paged_decode / fp8kv_paged_decode
  * when called with the same num_workers on the current device (num_workers 0 =
  * the automatic choice, whose need is bounded by this value).  Host only; the
- * result depends on the current device's SM count. */
+ * result depends on the current device's SM count.  A library utility: the
+ * pages describe no workspace (the split-KV scratch is this library's
+ * design). */
 size_t nvfp4kv_decode_workspace_size(int32_t num_workers);
 
 /* Decode attention over the NVFP4 cache ("SGLang stores KV cache in 4 bits",
@@ -208,7 +210,10 @@ nvfp4kv_status nvfp4kv_paged_decode(const nvfp4kv_cache *cache, const void *q,
                                     size_t workspace_bytes, int32_t num_workers,
                                     int32_t *dev_status, nvfp4kv_stream_t stream);
 
-/* One decode step: append each sequence's newest token, then attend.
+/* One decode step: append each sequence's newest token, then attend
+ * ("SGLang stores KV cache in 4 bits", Interpretation: new K/V are written to
+ * the cache in NVFP4 and the decode path dequantises inside attention; doing
+ * both in one launch is this library's fusion, not described on the pages).
  * For every sequence b with seq_lens[b] > 0, the K and V rows k_new[b],
  * v_new[b] ([batch][num_kv_heads][128], fp32 or bf16 per in_dtype, 16-byte
  * aligned) are quantised into the cache at position seq_lens[b] - 1 (page
@@ -228,7 +233,9 @@ nvfp4kv_status nvfp4kv_append_paged_decode(const nvfp4kv_cache *cache, const voi
                                            nvfp4kv_stream_t stream);
 
 /* Multi-query decode (several new tokens per sequence at once, as in
- * multi-token prediction or speculative decoding): q_len query tokens per
+ * multi-token prediction or speculative decoding; "NVFP4-KV-Cache auf der
+ * ...", "Unterstuetzung in den Engines": the engines' NVFP4 decode paths are
+ * judged on speculative decoding with multi-token prediction): q_len query tokens per
  * sequence sit at the last q_len positions and attend causally, token t
  * (0-based) over the seq_lens[b] - q_len + t + 1 first cached tokens (the
  * new tokens must already be in the cache, e.g. by nvfp4kv_quantize_append).
@@ -368,7 +375,9 @@ nvfp4kv_status fp8kv_paged_decode(const fp8kv_cache *cache, const void *q, int32
                                   int32_t num_workers, int32_t *dev_status,
                                   nvfp4kv_stream_t stream);
 
-/* The same fused step over the FP8 comparison cache. */
+/* The same fused step over the FP8 comparison cache (the FP8 baseline of
+ * "NVFP4-KV-Cache auf der ...", "Unterstuetzung in den Engines", run through
+ * the same append-then-decode step for a like-for-like comparison). */
 nvfp4kv_status fp8kv_append_paged_decode(const fp8kv_cache *cache, const void *k_new, const void *v_new,
                                          nvfp4kv_dtype in_dtype, const void *q, int32_t batch,
                                          int32_t num_q_heads, const int32_t *block_table,
@@ -386,11 +395,15 @@ nvfp4kv_status fp8kv_append_paged_decode(const fp8kv_cache *cache, const void *k
 int64_t nvfp4kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
                             int32_t head_dim);
 
-/* Bytes of an FP8 pool: num_pages * num_kv_heads * page_size * 2 * head_dim. */
+/* Bytes of an FP8 pool: num_pages * num_kv_heads * page_size * 2 * head_dim,
+ * one byte per value ("NVFP4-KV-Cache auf der ...", "Bytes pro Token: FP8
+ * gegenueber NVFP4": 16 bytes per 16 values in FP8).  Returns -1 for invalid
+ * arguments.  Host only. */
 int64_t fp8kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
                           int32_t head_dim);
 
-/* Read a device status word once the work on `stream` has finished:
+/* A library utility with no counterpart on the pages: read a device status
+ * word once the work on `stream` has finished:
  * synchronises the stream, copies *dev_status (device int32) into *bits
  * (host) and returns NVFP4KV_ERR_DEVICE_CHECK when any bit is set, NVFP4KV_OK
  * when none is (NVFP4KV_ERR_CUDA if the synchronisation or copy fails).  The
@@ -398,10 +411,10 @@ int64_t fp8kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_
 nvfp4kv_status nvfp4kv_read_device_status(const int32_t *dev_status, nvfp4kv_stream_t stream,
                                           int32_t *bits);
 
-/* Static description of a status code. */
+/* Static description of a status code (library utility). */
 const char *nvfp4kv_status_string(nvfp4kv_status status);
 
-/* Library version: major * 10000 + minor * 100 + patch. */
+/* Library version: major * 10000 + minor * 100 + patch (library utility). */
 int32_t nvfp4kv_version(void);
 
 #ifdef __cplusplus
