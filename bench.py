@@ -408,7 +408,9 @@ def run_ours(args, world, rank, local):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "nvfp4 (e2m1 + e4m3 scales) cache; f16 mma, f32 accumulate",
+        "vs_baseline": None, "dtype": "f16",
+        "dtype_detail": "NVFP4 cache (E2M1 codes, E4M3 block scales) dequantised to f16 MMA operands, "
+                        "f32 accumulation and softmax",
         "data": "synthetic (seeded generators; shapes and distributions of the workload, no real weights)",
         "config": {"workload": args.workload, "batch": w.batch, "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
