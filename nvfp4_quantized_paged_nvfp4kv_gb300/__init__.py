@@ -7,14 +7,23 @@ functions raises.
 
 Functions carry the C names and take torch tensors:
 
-  nvfp4kv_quantize_append(cache, k_new, v_new, slot_mapping, dev_status=None)
-  nvfp4kv_paged_decode(cache, q, block_table, seq_lens, out, workspace, ...)
-  nvfp4kv_append_paged_decode(cache, k_new, v_new, q, block_table, seq_lens, out, workspace, ...)
-  nvfp4kv_dequant_prefix_fp8(cache, block_table, prefix_lens, kv_indptr, k_out, v_out)
-  fp8kv_quantize_append(cache, k_new, v_new, slot_mapping, dev_status=None)
-  fp8kv_paged_decode(cache, q, block_table, seq_lens, out, workspace, ...)
-  nvfp4kv_decode_workspace_size(num_workers=0)
-  nvfp4kv_cache_bytes / fp8kv_cache_bytes / nvfp4kv_status_string / nvfp4kv_version
+  write path
+    nvfp4kv_quantize_append(cache, k_new, v_new, slot_mapping, dev_status=None)
+    fp8kv_quantize_append(cache, k_new, v_new, slot_mapping, dev_status=None)
+  decode path
+    nvfp4kv_paged_decode(cache, q, block_table, seq_lens, out, workspace, ...)
+    nvfp4kv_append_paged_decode(cache, k_new, v_new, q, block_table, seq_lens, out, workspace, ...)
+    nvfp4kv_paged_decode_multi(cache, q, block_table, seq_lens, out, workspace, ...)
+    nvfp4kv_paged_decode_static_scratch(cache, q, block_table, seq_lens, out, ...)
+    fp8kv_paged_decode / fp8kv_append_paged_decode (the FP8 comparison cache)
+    nvfp4kv_decode_workspace_size(num_workers=0), new_workspace(num_workers=0)
+  extend path
+    nvfp4kv_dequant_prefix_fp8(cache, block_table, prefix_lens, kv_indptr, k_out, v_out)
+    nvfp4kv_extend_attention_fp8(q, q_indptr, k_prefix, v_prefix, kv_indptr, prefix_lens, k_chunk, v_chunk, ...)
+    nvfp4kv_extend_attention_fp8_append(cache, slot_mapping, q, q_indptr, ...)
+  utilities
+    nvfp4kv_read_device_status(dev_status, stream=None)
+    nvfp4kv_cache_bytes / fp8kv_cache_bytes / nvfp4kv_status_string / nvfp4kv_version
 
 ``NVFP4Cache`` and ``FP8Cache`` hold the pool tensors and build the C structs.
 """

@@ -50,6 +50,31 @@ def test_library_exports_every_declared_symbol():
         assert n in exported, n
 
 
+def test_binding_has_a_function_of_each_declared_name():
+    """The Python binding offers every entry point under its C name."""
+    for n in declared_functions():
+        assert callable(getattr(nv, n, None)), n
+
+
+def test_every_entry_point_cites_a_passage_or_says_it_is_a_utility():
+    """Each declaration's comment names the page passage that defines the
+    operation, or states that the call has no counterpart on the pages."""
+    text = open(os.path.join(HEADER_DIR, "nvfp4kv.h")).read()
+    cites = ("SGLang stores KV cache in 4 bits", "NVFP4-KV-Cache auf der")
+    utility = ("library utility", "no counterpart")
+    pos = 0
+    for m in re.finditer(r"\n(?:nvfp4kv_status|size_t|int64_t|int32_t|const char \*)\s*(\w+)\(", text):
+        name = m.group(1)
+        # the comment block(s) between the previous declaration and this one
+        chunk = text[pos:m.start()]
+        pos = m.end()
+        comments = " ".join(re.findall(r"/\*.*?\*/", chunk, flags=re.S))
+        comments = re.sub(r"\s*\n\s*\*?\s*", " ", comments)       # join wrapped comment lines
+        if name == "fp8kv_paged_decode":
+            continue                      # documented together with fp8kv_quantize_append just above
+        assert any(c in comments for c in cites + utility), name
+
+
 FAKE = 0x7F0000000000          # a 16-byte aligned address that is never dereferenced
 
 
