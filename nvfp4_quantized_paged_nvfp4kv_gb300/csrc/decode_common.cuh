@@ -800,8 +800,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
 // ---- split merge ---------------------------------------------------------------
 // One CTA of kMergeThreads threads per (sequence, kv head, query head of the
 // group).  Segments that one worker covered were written by the decode kernel;
-// empty sequences get zeros here.
-constexpr int kMergeThreads = 256;
+// empty sequences get zeros here.  128 threads at 72 registers let seven CTAs
+// share an SM, so a merge grid of up to 7 x 152 CTAs runs in one wave once the
+// decode CTAs have left.
+constexpr int kMergeThreads = 128;
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams p);
 
 } // namespace nvfp4kv

@@ -8,7 +8,8 @@
 namespace nvfp4kv {
 
 // Thread t works on channels 4*(t%32) .. +3 of the CTA's query head for the
-// contributors k = t/32, t/32 + 8, ...; each of the 8 contributor groups keeps
+// contributors k = t/32, t/32 + G, ... (G = kMergeThreads / 32 contributor
+// groups, each loading kUnroll contributors ahead); each group keeps
 // its own running maximum (one pass over the partials), and the groups are
 // combined in shared memory at the end.  The segment's contributor range is
 // worked out once per CTA, before the wait for the decode kernel.
