@@ -22,6 +22,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "nvfp4kv_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+# A prebuilt copy of the same source to load instead (the sanitizer test builds
+# one with AddressSanitizer and UBSan); unset in normal use.
+_LIB_OVERRIDE = os.environ.get("NVFP4KV_ORACLE_LIB")
+CFLAGS = ["-std=c11", "-O2", "-fopenmp", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
 _lock = threading.Lock()
 _lib = None
 
@@ -33,13 +37,14 @@ _f64p = ctypes.POINTER(ctypes.c_double)
 
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (-O2, OpenMP, no fast-math, no FP contraction)."""
+    if _LIB_OVERRIDE:
+        return _LIB_OVERRIDE
     os.makedirs(_BUILD, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-std=c11", "-O2", "-fopenmp", "-fPIC", "-shared",
-           "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    cmd = ["gcc"] + CFLAGS + [_SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH

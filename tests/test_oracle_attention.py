@@ -159,6 +159,32 @@ def test_empty_sequence_gives_zeros():
     assert (got[0] == 0).all() and np.abs(got[1]).sum() > 0
 
 
+def test_table_entries_past_a_sequence_are_never_read():
+    """Only the first ceil(L_b / 16) block-table entries of a sequence take part:
+    rewriting the rest (padding -1 or any page id) changes neither the decode
+    nor the prefix dequant."""
+    w = workloads.custom(5, 16, 4, (0, 1, 15, 17, 1000), seed=4)
+    pools, bt = build_cache(w)
+    q = workloads.query(w).float().numpy()
+    bt_pad = bt.copy()
+    for b, n in enumerate(w.pages_per_seq):
+        bt_pad[b, n:] = -1
+    bt_other = bt.copy()
+    for b, n in enumerate(w.pages_per_seq):
+        bt_other[b, n:] = (np.arange(bt.shape[1] - n) * 7 + b) % bt.max()
+    a = run_oracle(pools, bt_pad, w, q)
+    c = run_oracle(pools, bt_other, w, q)
+    assert np.array_equal(a, c) and (a[0] == 0).all() and np.isfinite(a).all()
+    lens = np.int32(w.seq_lens)
+    ip = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int32)
+    for n in ("k", "v"):
+        x = oracle.dequant_prefix_fp8(pools[n + "_data"], pools[n + "_scale"], bt_pad, lens, ip,
+                                      out_rows=int(lens.sum()))
+        y = oracle.dequant_prefix_fp8(pools[n + "_data"], pools[n + "_scale"], bt_other, lens, ip,
+                                      out_rows=int(lens.sum()))
+        assert np.array_equal(x, y)
+
+
 # --- extend path: prefix -> FP8 workspace ------------------------------------
 
 def test_prefix_value_map_exhaustive():
