@@ -76,7 +76,10 @@ _st = ctypes.c_int
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The library that load() opens: libnvfp4kv.so built in-tree, or a prebuilt
+    copy of the same sources named by NVFP4KV_LIBRARY (for example a build with
+    host-side sanitizers)."""
+    return os.environ.get("NVFP4KV_LIBRARY") or _build.LIB
 
 
 def load(build_if_missing: bool = True):
@@ -85,15 +88,16 @@ def load(build_if_missing: bool = True):
     with _lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(_build.LIB):
+        path = library_path()
+        if path == _build.LIB and not os.path.exists(path):
             if not build_if_missing:
-                raise OSError(f"libnvfp4kv.so not built at {_build.LIB}")
+                raise OSError(f"libnvfp4kv.so not built at {path}")
             _build.build()
         try:
             import torch  # noqa: F401  (loads the CUDA runtime torch uses first)
         except ImportError:
             pass
-        lib = ctypes.CDLL(_build.LIB)
+        lib = ctypes.CDLL(path)
         sig = {
             "nvfp4kv_quantize_append": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _vp, _st, _i32, _vp, _vp, _vp]),
             "nvfp4kv_decode_workspace_size": (ctypes.c_size_t, [_i32]),
