@@ -18,21 +18,23 @@ def _runtime(name):
     return path if os.path.isabs(path) and os.path.exists(path) else None
 
 
-def test_abi_checks_run_clean_under_asan_and_ubsan(tmp_path):
+def test_abi_checks_run_clean_under_asan_and_ubsan():
     asan, ubsan = _runtime("libasan.so"), _runtime("libubsan.so")
     if asan is None or ubsan is None:
         pytest.skip("gcc sanitizer runtimes not installed")
+    out = os.path.join(_build.BUILD, "sanitized")          # in-tree, git-ignored
+    os.makedirs(out, exist_ok=True)
     nvcc = _build._nvcc()
     san = "-fsanitize=address,-fsanitize=undefined,-fno-sanitize-recover=undefined"
     common = ["-std=c++17", "-O1", "-g", "-Xcompiler", f"-fPIC,-fno-omit-frame-pointer,{san}",
               "-I", _build.INCLUDE, "-I", _build.CSRC] + _build.ARCH
     procs, objs = [], []
     for src in _build._sources():
-        obj = str(tmp_path / (os.path.basename(src) + ".o"))
+        obj = os.path.join(out, os.path.basename(src) + ".o")
         objs.append(obj)
         procs.append(subprocess.Popen([nvcc] + common + ["-c", src, "-o", obj]))
     assert all(p.wait() == 0 for p in procs)
-    lib = str(tmp_path / "libnvfp4kv_sanitized.so")
+    lib = os.path.join(out, "libnvfp4kv_sanitized.so")
     subprocess.run([nvcc, "-shared", "-o", lib] + objs + _build.ARCH +
                    ["-cudart", "shared", "-Xcompiler", san.replace(",-fno-sanitize-recover=undefined", "")],
                    check=True)

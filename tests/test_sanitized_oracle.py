@@ -21,11 +21,13 @@ def _runtime(name):
     return path if os.path.isabs(path) and os.path.exists(path) else None
 
 
-def test_oracle_runs_clean_under_asan_and_ubsan(tmp_path):
+def test_oracle_runs_clean_under_asan_and_ubsan():
     asan, ubsan = _runtime("libasan.so"), _runtime("libubsan.so")
     if asan is None or ubsan is None:
         pytest.skip("gcc sanitizer runtimes not installed")
-    lib = str(tmp_path / "liboracle_sanitized.so")
+    out = os.path.join(ROOT, "oracle", "_build")            # in-tree, git-ignored
+    os.makedirs(out, exist_ok=True)
+    lib = os.path.join(out, "liboracle_sanitized.so")
     flags = [f for f in oracle.CFLAGS if f != "-O2"] + ["-O1", "-g", "-fno-omit-frame-pointer",
                                                         "-fsanitize=address,undefined",
                                                         "-fno-sanitize-recover=undefined"]
