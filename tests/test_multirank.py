@@ -55,3 +55,15 @@ def test_reference_arm_under_torchrun_prints_once():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["value"] > 0 and rec["n_gpus"] == 2
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
+    # the line carries the bench contract's keys, for the same metric and workload as the GPU arm
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in rec, key
+    sys.path.insert(0, ROOT)
+    import bench
+    assert rec["metric"] == bench.METRIC and rec["unit"] == bench.UNIT and rec["higher_is_better"] is True
+    assert rec["config"]["workload"] == "llama70b_b12"
+    assert (rec["steps"], rec["warmup"]) == (1, 3)            # at least three warm-up steps, always
+    cb = rec["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == rec["value"]
+    assert rec["e2e"]["value"] == rec["value"] and rec["e2e"]["unit"] == rec["unit"]
