@@ -163,6 +163,7 @@ def test_decode_validation():
     assert decode(c, wsb=16) == nv.ERR_WORKSPACE
     assert decode(c, batch=0, q=None, out=None, bt=None, sl=None, ws=None) == nv.OK
     assert decode(c, batch=20000) == nv.ERR_UNSUPPORTED
+    assert decode(c, batch=8193) == nv.ERR_UNSUPPORTED         # NVFP4KV_MAX_BATCH + 1
 
 
 def test_prefix_validation():
