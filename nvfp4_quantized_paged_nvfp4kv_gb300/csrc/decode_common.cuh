@@ -39,8 +39,14 @@ __device__ __forceinline__ int clamp_len(int L, int max_len)
     return L < 0 ? 0 : (L > max_len ? max_len : L);
 }
 
+// Slots of the warp-sum scratch that build_prefix needs: one per warp of the
+// CTA, for any CTA of up to 32 warps.
+constexpr int kPrefixScratch = 32;
+static_assert(kDecodeWarps <= kPrefixScratch, "build_prefix takes one scratch slot per warp");
+
 // prefix[b] = sum over b' < b of hkv * ceil(len_b' / 16), for b in [0, batch].
-// Whole CTA; blockDim.x a multiple of 32, at most 32 warps.
+// Whole CTA; blockDim.x a multiple of 32, at most 32 warps; scratch holds
+// kPrefixScratch slots and must not overlap prefix.
 __device__ __forceinline__ void build_prefix(const int32_t *seq_lens, int batch, int hkv, int max_len,
                                              int32_t *prefix, int32_t *scratch, int32_t *dev_status)
 {
@@ -318,7 +324,7 @@ template <class Fmt>
 __host__ __device__ constexpr size_t decode_smem_fixed()
 {
     return 128 /* alignment slack */ + static_cast<size_t>(kDecodeWarps) * Fmt::kStages * (Fmt::kRecord + 8) +
-           8 * sizeof(int32_t);
+           kPrefixScratch * sizeof(int32_t);
 }
 
 template <class Fmt>
@@ -358,7 +364,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
     uint8_t *data_base = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(data_base + kDecodeWarps * S * R);
     int32_t *scratch = reinterpret_cast<int32_t *>(bars + kDecodeWarps * S);
-    int32_t *prefix = scratch + 8;
+    int32_t *prefix = scratch + kPrefixScratch;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;

@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     __shared__ float part_m[kGroups], part_l[kGroups];
     __shared__ int seg[3];                       // first contributor, count (-1: empty sequence), its slot
     int32_t *scratch = msmem;
-    int32_t *prefix = msmem + 32;
+    int32_t *prefix = msmem + kPrefixScratch;
     pdl_launch_dependents();                     // the next kernel may start its prologue
     const int nseg = p.hkv * p.row_groups;       // segments per sequence (row groups of kv heads)
     build_prefix(p.seq_lens, p.batch, nseg, p.max_pages * kPageSize, prefix, scratch, nullptr);
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
 
 cudaError_t launch_merge(const DecodeParams &p, cudaStream_t s)
 {
-    const size_t smem = (32 + static_cast<size_t>(p.batch) + 1) * sizeof(int32_t);
+    const size_t smem = (kPrefixScratch + static_cast<size_t>(p.batch) + 1) * sizeof(int32_t);
     if (smem > 40 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
