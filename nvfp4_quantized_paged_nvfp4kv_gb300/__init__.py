@@ -42,6 +42,7 @@ HEAD_DIM = 128
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK = 0, 1, 2, 3, 4, 5
 DEV_BAD_PAGE, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 F32, BF16 = 0, 1
+STATIC_SCRATCH_MAX_WORKERS = 3024   # NVFP4KV_STATIC_SCRATCH_MAX_WORKERS
 
 _lock = threading.Lock()
 _lib = None

@@ -73,8 +73,9 @@ extern "C" nvfp4kv_status nvfp4kv_paged_decode_static_scratch(
         return NVFP4KV_ERR_INVALID_ARG;
     if (num_workers > NVFP4KV_STATIC_SCRATCH_MAX_WORKERS)
         return NVFP4KV_ERR_WORKSPACE;
-    if (batch == 0)
-        return NVFP4KV_OK;
+    if (batch == 0)   // nothing to launch: the ordinary call checks the other arguments
+        return nvfp4kv_paged_decode(cache, q, batch, num_q_heads, block_table, max_pages_per_seq, seq_lens,
+                                    sm_scale, out, out_dtype, nullptr, 0, num_workers, dev_status, stream);
     int nw = num_workers;
     if (nw == 0) {
         // the automatic choice of nvfp4kv_paged_decode, capped by the array

@@ -166,6 +166,24 @@ def test_decode_validation():
     assert decode(c, batch=8193) == nv.ERR_UNSUPPORTED         # NVFP4KV_MAX_BATCH + 1
 
 
+def static_decode(c, hq=4, batch=0, nw=0, scale=0.088, dtype=nv.BF16):
+    return nv.load().nvfp4kv_paged_decode_static_scratch(ctypes.byref(c), None, batch, hq, None, 4, None, scale,
+                                                         None, dtype, nw, None, None)
+
+
+def test_static_scratch_decode_batch_zero_checks_arguments():
+    """At batch 0 the static-scratch call launches nothing, but it rejects the
+    same bad arguments as nvfp4kv_paged_decode does (no device is touched)."""
+    c = cache()
+    assert static_decode(c) == nv.OK
+    for kw in (dict(hq=5), dict(hq=18), dict(dtype=9), dict(scale=float("nan"))):
+        want = decode(c, batch=0, q=None, out=None, bt=None, sl=None, ws=None, **kw)
+        assert want != nv.OK
+        assert static_decode(c, **kw) == want, kw
+    assert static_decode(c, nw=nv.STATIC_SCRATCH_MAX_WORKERS + 1) == nv.ERR_WORKSPACE
+    assert static_decode(cache(head_dim=64)) == nv.ERR_UNSUPPORTED
+
+
 def test_prefix_validation():
     lib = nv.load()
     c = cache()

@@ -15,7 +15,7 @@ import torch
 
 import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
 import workloads
-from gpu_util import Built, assert_close
+from gpu_util import Built, assert_close, oracle_full
 
 pytestmark = pytest.mark.gpu
 
@@ -33,17 +33,28 @@ def test_static_scratch_decode_matches_workspace_decode(name, batch, seq_len):
     w = workloads.make(name, batch=batch, seq_len=seq_len)
     b = Built(w, fp8=False)
     ref = b.decode(torch.float32)                       # ordinary entry point, own workspace
+    want, _ = oracle_full(b)                            # and the oracle
     for call in range(2):                               # two calls in a row share the array
         out = torch.full_like(torch.from_numpy(ref), float("nan")).cuda()
         assert static_decode(b, out) == nv.OK
         torch.cuda.synchronize()
         assert_close(out.cpu().numpy(), ref, f"static-scratch decode, call {call}")
+        assert_close(out.cpu().numpy(), want, f"static-scratch decode against the oracle, call {call}")
     assert int(b.status.item()) == 0
 
 
-def test_static_scratch_rejects_too_many_workers():
-    b = Built(workloads.make("tiny"), fp8=False)
-    out = torch.empty((2, 8, 128), dtype=torch.float32, device="cuda")
+def test_static_scratch_worker_limit():
+    """The largest worker count fills the array to its end; one more is
+    refused before anything is launched."""
+    w = workloads.custom(5, 16, 4, (8000, 17, 7900, 1, 640), seed=9)   # 4,148 page-heads
+    b = Built(w, fp8=False)
+    want, _ = oracle_full(b)
+    out = torch.full((w.batch, 16, 128), float("nan"), dtype=torch.float32, device="cuda")
+    assert static_decode(b, out, num_workers=nv.STATIC_SCRATCH_MAX_WORKERS + 1) == nv.ERR_WORKSPACE
     assert static_decode(b, out, num_workers=100000) == nv.ERR_WORKSPACE
-    assert static_decode(b, out, num_workers=3024) == nv.OK
-    torch.cuda.synchronize()
+    for call in range(2):
+        out.fill_(float("nan"))
+        assert static_decode(b, out, num_workers=nv.STATIC_SCRATCH_MAX_WORKERS) == nv.OK
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy(), want, f"static scratch at its worker limit, call {call}")
+    assert int(b.status.item()) == 0
