@@ -89,6 +89,7 @@ def _load():
         lib.oracle_fp8_bytes.restype = ctypes.c_int64
         lib.oracle_fp8_bytes.argtypes = [ctypes.c_int64]
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
         return lib
 
@@ -300,3 +301,9 @@ def fp8_bytes(num_values: int) -> int:
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's parallel loops use from now on (timing only; the
+    results do not depend on it)."""
+    _load().oracle_set_num_threads(int(n))

@@ -468,3 +468,16 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Threads the parallel loops use from now on (n >= 1); for timing the oracle
+ * on one core and on all of them.  Changes no result: every parallel loop
+ * writes disjoint outputs, each computed in a fixed order. */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
