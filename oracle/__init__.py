@@ -84,6 +84,9 @@ def _load():
         lib.oracle_extend_attention.argtypes = [
             _f32p, _i32p, _u8p, _u8p, _i32p, _i32p, _f32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, ctypes.c_double, _f64p]
+        lib.oracle_extend_attention_e4m3_chunk.argtypes = [
+            _f32p, _i32p, _u8p, _u8p, _i32p, _i32p, _u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_double, _f64p]
         lib.oracle_nvfp4_bytes.restype = ctypes.c_int64
         lib.oracle_nvfp4_bytes.argtypes = [ctypes.c_int64]
         lib.oracle_fp8_bytes.restype = ctypes.c_int64
@@ -268,12 +271,16 @@ def fp8_paged_decode(k, v, q, block_table, seq_lens, sm_scale: float | None = No
 def extend_attention(q, q_indptr, k_prefix, v_prefix, kv_indptr, prefix_lens, k_chunk, v_chunk,
                      sm_scale: float | None = None) -> np.ndarray:
     """fp64 attention of each chunk token over its sequence's FP8 prefix rows
-    and the chunk's keys up to itself.  q, k_chunk, v_chunk: float32
-    [rows][H][d]; k_prefix, v_prefix: E4M3 bytes [rows][Hkv][d]."""
+    and the chunk's keys up to itself.  q: float32 [rows][Hq][d]; k_chunk,
+    v_chunk: float32 [rows][Hkv][d], or uint8 E4M3 bytes (the chunk in FP8, as
+    initial prefill receives it); k_prefix, v_prefix: E4M3 bytes
+    [rows][Hkv][d]."""
     q = _c(q, np.float32)
     rows, Hq, d = q.shape
-    kc = _c(k_chunk, np.float32)
-    vc = _c(v_chunk, np.float32)
+    e4m3 = np.asarray(k_chunk).dtype == np.uint8
+    assert (np.asarray(v_chunk).dtype == np.uint8) == e4m3, "k_chunk and v_chunk: same kind"
+    kc = _c(k_chunk, np.uint8 if e4m3 else np.float32)
+    vc = _c(v_chunk, np.uint8 if e4m3 else np.float32)
     Hkv = kc.shape[1]
     kp = _c(k_prefix, np.uint8)
     vp = _c(v_prefix, np.uint8)
@@ -283,9 +290,10 @@ def extend_attention(q, q_indptr, k_prefix, v_prefix, kv_indptr, prefix_lens, k_
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(d)
     out = np.zeros((rows, Hq, d), np.float64)
-    _load().oracle_extend_attention(_p(q, _f32p), _p(qi, _i32p), _p(kp, _u8p), _p(vp, _u8p), _p(ki, _i32p),
-                                    _p(pl, _i32p), _p(kc, _f32p), _p(vc, _f32p), len(pl), Hq, Hkv, d,
-                                    float(sm_scale), _p(out, _f64p))
+    fn = _load().oracle_extend_attention_e4m3_chunk if e4m3 else _load().oracle_extend_attention
+    cp = _u8p if e4m3 else _f32p
+    fn(_p(q, _f32p), _p(qi, _i32p), _p(kp, _u8p), _p(vp, _u8p), _p(ki, _i32p), _p(pl, _i32p), _p(kc, cp),
+       _p(vc, cp), len(pl), Hq, Hkv, d, float(sm_scale), _p(out, _f64p))
     return out
 
 

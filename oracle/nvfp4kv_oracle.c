@@ -394,15 +394,25 @@ void oracle_fp8_paged_decode(const uint8_t *k, const uint8_t *v, int Hkv, int P,
  * over the cached prefix, dequantised into the FP8 workspace, plus the new
  * chunk).  For sequence b with prefix length P_b (workspace rows kv_indptr[b]
  * .. + P_b, E4M3 at scale 1.0) and chunk rows q_indptr[b] .. q_indptr[b+1]
- * (queries and the chunk's own K/V, given as floats), chunk token i and query
- * head hq (kv head hq / g) attend over the P_b prefix keys and chunk keys
- * 0 .. i (causal within the chunk):
- *   s_j = sm_scale * q . k_j,   o = sum_j softmax(s)_j v_j   (all in double)  */
-void oracle_extend_attention(const float *q, const int32_t *q_indptr,
-                             const uint8_t *k_prefix, const uint8_t *v_prefix,
-                             const int32_t *kv_indptr, const int32_t *prefix_lens,
-                             const float *k_chunk, const float *v_chunk,
-                             int B, int Hq, int Hkv, int d, double sm_scale, double *out)
+ * (queries as floats; the chunk's own K/V as floats, or as E4M3 bytes at
+ * scale 1.0), chunk token i and query head hq (kv head hq / g) attend over the
+ * P_b prefix keys and chunk keys 0 .. i (causal within the chunk):
+ *   s_j = sm_scale * q . k_j,   o = sum_j softmax(s)_j v_j   (all in double)
+ * The E4M3 chunk is initial prefill as the same paragraph describes it: the
+ * prompt's keys and values arrive in FP8 and attention reads them as they
+ * are (prefix length 0 there; any prefix is allowed).                       */
+static double chunk_value(int chunk_e4m3, const void *chunk, size_t idx)
+{
+    if (chunk_e4m3)
+        return oracle_e4m3_value(((const uint8_t *)chunk)[idx]);
+    return (double)((const float *)chunk)[idx];
+}
+
+static void extend_generic(const float *q, const int32_t *q_indptr,
+                           const uint8_t *k_prefix, const uint8_t *v_prefix,
+                           const int32_t *kv_indptr, const int32_t *prefix_lens,
+                           const void *k_chunk, const void *v_chunk, int chunk_e4m3,
+                           int B, int Hq, int Hkv, int d, double sm_scale, double *out)
 {
     int g = Hq / Hkv;
     for (int b = 0; b < B; ++b) {
@@ -421,7 +431,7 @@ void oracle_extend_attention(const float *q, const int32_t *q_indptr,
                 double dot = 0.0;
                 for (int c = 0; c < d; ++c) {
                     double kv = j < P ? oracle_e4m3_value(k_prefix[((p0 + j) * Hkv + h) * d + c])
-                                      : (double)k_chunk[((size_t)(c0 + j - P) * Hkv + h) * d + c];
+                                      : chunk_value(chunk_e4m3, k_chunk, ((size_t)(c0 + j - P) * Hkv + h) * d + c);
                     dot += (double)qv[c] * kv;
                 }
                 sc[j] = dot * sm_scale;
@@ -436,7 +446,7 @@ void oracle_extend_attention(const float *q, const int32_t *q_indptr,
                 denom += pj;
                 for (int c = 0; c < d; ++c) {
                     double vv = j < P ? oracle_e4m3_value(v_prefix[((p0 + j) * Hkv + h) * d + c])
-                                      : (double)v_chunk[((size_t)(c0 + j - P) * Hkv + h) * d + c];
+                                      : chunk_value(chunk_e4m3, v_chunk, ((size_t)(c0 + j - P) * Hkv + h) * d + c);
                     o[c] += pj * vv;
                 }
             }
@@ -445,6 +455,27 @@ void oracle_extend_attention(const float *q, const int32_t *q_indptr,
             free(sc);
         }
     }
+}
+
+void oracle_extend_attention(const float *q, const int32_t *q_indptr,
+                             const uint8_t *k_prefix, const uint8_t *v_prefix,
+                             const int32_t *kv_indptr, const int32_t *prefix_lens,
+                             const float *k_chunk, const float *v_chunk,
+                             int B, int Hq, int Hkv, int d, double sm_scale, double *out)
+{
+    extend_generic(q, q_indptr, k_prefix, v_prefix, kv_indptr, prefix_lens, k_chunk, v_chunk, 0,
+                   B, Hq, Hkv, d, sm_scale, out);
+}
+
+/* The same with the chunk's K/V as E4M3 bytes [rows][Hkv][d] (scale 1.0). */
+void oracle_extend_attention_e4m3_chunk(const float *q, const int32_t *q_indptr,
+                                        const uint8_t *k_prefix, const uint8_t *v_prefix,
+                                        const int32_t *kv_indptr, const int32_t *prefix_lens,
+                                        const uint8_t *k_chunk, const uint8_t *v_chunk,
+                                        int B, int Hq, int Hkv, int d, double sm_scale, double *out)
+{
+    extend_generic(q, q_indptr, k_prefix, v_prefix, kv_indptr, prefix_lens, k_chunk, v_chunk, 1,
+                   B, Hq, Hkv, d, sm_scale, out);
 }
 
 /* ------------------------------------------------------------------------ */

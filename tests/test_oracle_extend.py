@@ -87,3 +87,54 @@ def test_equal_keys_give_mean_of_visible_values():
     for i in range(6):
         vis = np.concatenate([Vp, vc[:i + 1, 0].astype(np.float64)])
         np.testing.assert_allclose(got[i, 0], vis.mean(0), rtol=1e-12, atol=1e-12)
+
+
+# --- the chunk in FP8 ---------------------------------------------------------
+# "SGLang stores KV cache in 4 bits" (LMSYS summary), Interpretation: initial
+# prefill attends on the prompt's FP8 keys and values.  The oracle takes the
+# chunk as E4M3 bytes and decodes them itself; the pins decode them with torch's
+# float8_e4m3fn instead.
+
+def e4m3_chunk(kc, vc, scale=1.5):
+    to8 = lambda x: torch.from_numpy(x * scale).to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()  # noqa: E731
+    return to8(kc), to8(vc)
+
+
+def decoded(codes):
+    return torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+
+
+@pytest.mark.parametrize("prefix_lens,chunk_lens,hq,hkv", [
+    ((0, 0), (40, 7), 8, 2),          # initial prefill: no prefix at all
+    ((37, 0, 100), (5, 9, 1), 4, 2),
+    ((1, 300), (17, 40), 6, 1),
+])
+def test_e4m3_chunk_matches_torch(prefix_lens, chunk_lens, hq, hkv):
+    q, qi, kp, vp, ki, pl, kc, vc = make_case(prefix_lens, chunk_lens, hq, hkv, seed=hq + 17)
+    kc8, vc8 = e4m3_chunk(kc, vc)
+    got = oracle.extend_attention(q, qi, kp, vp, ki, pl, kc8, vc8)
+    want = torch_reference(q, qi, kp, vp, ki, pl, decoded(kc8), decoded(vc8), hq, hkv)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_e4m3_chunk_initial_prefill_is_causal_sdpa():
+    """No prefix, chunk in FP8: torch's causal scaled-dot-product attention in
+    float64 over the torch-decoded E4M3 keys and values."""
+    q, qi, kp, vp, ki, pl, kc, vc = make_case((0,), (50,), 4, 2, seed=8)
+    kc8, vc8 = e4m3_chunk(kc, vc, scale=3.0)
+    got = oracle.extend_attention(q, qi, kp, vp, ki, pl, kc8, vc8)
+    Q = torch.from_numpy(q).double().permute(1, 0, 2)
+    K = torch.from_numpy(decoded(kc8)).double().repeat_interleave(2, 1).permute(1, 0, 2)
+    V = torch.from_numpy(decoded(vc8)).double().repeat_interleave(2, 1).permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, is_causal=True).permute(1, 0, 2)
+    np.testing.assert_allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_e4m3_chunk_byte_order_matters():
+    """A transposed channel order in the chunk's bytes changes the result (the
+    pins above would notice a decode that reads the wrong byte)."""
+    q, qi, kp, vp, ki, pl, kc, vc = make_case((0,), (9,), 2, 2, seed=12)
+    kc8, vc8 = e4m3_chunk(kc, vc)
+    a = oracle.extend_attention(q, qi, kp, vp, ki, pl, kc8, vc8)
+    b = oracle.extend_attention(q, qi, kp, vp, ki, pl, kc8[:, :, ::-1].copy(), vc8)
+    assert np.abs(a - b).max() > 1e-3
