@@ -70,9 +70,11 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the quantize / prefix-dequant rows")
     ap.add_argument("--no-decode-rows", action="store_true",
                     help="skip the decode rows of the other workloads")
-    ap.add_argument("--row-only", default=None, choices=["ext160k", "ext8k_c2k", "quantize8k", "prefix160k"],
+    ap.add_argument("--row-only", default=None,
+                    choices=["ext160k", "ext8k_c2k", "quantize8k", "prefix160k", "prefill8k"],
                     help="time only this row (extend attention on a workload, quantize_append of 8,192 "
-                         "bf16 tokens, or dequant_prefix_fp8 of a 163,840-token prefix) and print it")
+                         "bf16 tokens, dequant_prefix_fp8 of a 163,840-token prefix, or FP8 initial prefill "
+                         "of 8,192 tokens) and print it")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -601,6 +603,7 @@ def other_rows(dev):
     d_bytes = L * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
     multi = multi_query_rows(dev, timed)
     extend = extend_rows(dev)
+    prefill = prefill_rows(dev)
     return {
         "quantize_append_8k_bf16": {"us": q_ms * 1e3, "tokens_per_s": T / (q_ms / 1e3),
                                     "alg_gbs": q_bytes / (q_ms / 1e3) / 1e9, "alg_bytes": q_bytes},
@@ -613,6 +616,7 @@ def other_rows(dev):
                                                    "quantize_append_8k_bf16_us": qh_ms * 1e3}},
         "multi_query": multi,
         "extend_160k_chunk8k": extend,
+        "prefill_fp8_8k": prefill,
         "timing": "CUDA events per call, 256 MB buffer written and a GPU spin before each call (L2 evicted, "
                   "host launch hidden)",
     }
@@ -749,6 +753,49 @@ def extend_rows(dev, name: str = "ext160k", steps: int = 5, warmup: int = 3, com
     f_ms, s_ms = mean_ms(fused), mean_ms(separate)
     row.update({"fused_append_us": f_ms * 1e3, "attention_then_quantize_append_us": s_ms * 1e3,
                 "device_status": int(status.item())})
+    return row
+
+
+def prefill_rows(dev, steps: int = 10, warmup: int = 3):
+    """Initial prefill of one 8,192-token prompt (Hq 48, Hkv 8, no prefix) on
+    the prompt's FP8 keys and values, attention alone and fused with the NVFP4
+    write of the same values, and the same fused step with the K/V in bf16;
+    mean of `steps` launches after `warmup`, CUDA events on the launching
+    stream."""
+    import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
+    e = workloads.extend_make("prefill8k")
+    C = e.chunk_lens[0]
+    out = torch.empty((C, e.num_q_heads, e.head_dim), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    cache = nv.NVFP4Cache.allocate(C // 16 + 1, e.num_kv_heads, device=dev, zero=False)
+    slots = torch.arange(C, dtype=torch.int32, device=dev)
+    flops = extend_flops(e)
+    peak = (measured_peaks() or {}).get("bf16_tflops", 1900.0)
+    row = {"workload": "prefill8k", "alg_flops": flops, "peak_tflops": peak}
+    for chunk in ("e4m3", "bf16"):
+        x = workloads.extend_inputs(e, device=dev, chunk=chunk)
+        args = (x["q"], x["q_indptr"], x["k_prefix"], x["v_prefix"], x["kv_indptr"], x["prefix_lens"],
+                x["k_chunk"], x["v_chunk"], out)
+        calls = {"fused_append": lambda: nv.nvfp4kv_extend_attention_fp8_append(cache, slots, *args, max_q_len=C,
+                                                                                  dev_status=status)}
+        if chunk == "e4m3":
+            calls["attention"] = lambda: nv.nvfp4kv_extend_attention_fp8(*args, max_q_len=C, dev_status=status)
+        for what, fn in calls.items():
+            for _ in range(warmup):
+                fn()
+            ms = []
+            for _ in range(steps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                torch.cuda.synchronize()
+                ms.append(a.elapsed_time(b))
+            t = statistics.mean(ms)
+            tf = flops / (t / 1e3) / 1e12
+            row[f"{chunk}_{what}"] = {"us": t * 1e3, "tokens_per_s": C / (t / 1e3), "alg_tflops": tf,
+                                      "frac": tf / peak}
+    row["device_status"] = int(status.item())
     return row
 
 
@@ -908,7 +955,9 @@ def main():
         nv.load()
         dev = torch.device("cuda", 0)
         warm = max(args.warmup, 3)
-        if args.row_only.startswith("ext"):
+        if args.row_only == "prefill8k":
+            row = prefill_rows(dev, steps=args.steps, warmup=warm)
+        elif args.row_only.startswith("ext"):
             row = extend_rows(dev, args.row_only, steps=args.steps, warmup=warm, compare_fused=False)
         else:
             row = write_side_row(dev, args.row_only, args.steps, warm)

@@ -106,7 +106,10 @@ typedef enum {
 #define NVFP4KV_DEV_BAD_LEN 0x4   /* length < 0 or > max_pages_per_seq*page_size  */
 #define NVFP4KV_DEV_TIMEOUT 0x8   /* a bounded wait for staged data gave up        */
 
-typedef enum { NVFP4KV_F32 = 0, NVFP4KV_BF16 = 1 } nvfp4kv_dtype;
+/* Element types of caller buffers.  NVFP4KV_E4M3 (OCP FP8 E4M3FN bytes at
+ * scale 1.0) is accepted only where a call says so: the chunk K/V of the
+ * extend calls. */
+typedef enum { NVFP4KV_F32 = 0, NVFP4KV_BF16 = 1, NVFP4KV_E4M3 = 2 } nvfp4kv_dtype;
 
 #define NVFP4KV_RECORD_BYTES 2304
 #define FP8KV_RECORD_BYTES 4096
@@ -304,10 +307,15 @@ nvfp4kv_status nvfp4kv_dequant_prefix_fp8(const nvfp4kv_cache *cache,
  *   values = the same rows of v_prefix / v_chunk
  *   out[q_indptr[b] + t][i] = softmax_j(sm_scale * q . key_j) . value_j
  * Prefix keys and values are E4M3 bytes (the workspace written by
- * nvfp4kv_dequant_prefix_fp8, with the same kv_indptr and prefix_lens);
- * chunk keys and values and q are bf16.
+ * nvfp4kv_dequant_prefix_fp8, with the same kv_indptr and prefix_lens); q is
+ * bf16; chunk keys and values are bf16 or E4M3 (chunk_dtype).  E4M3 chunk K/V
+ * are initial prefill as "SGLang stores KV cache in 4 bits", Interpretation
+ * ¶2 describes it: attention reads the current prompt's FP8 keys and values
+ * directly (prefix length 0 there; a prefix is allowed too).
  *   q        bf16 [q_rows][num_q_heads][128]
- *   k_chunk, v_chunk  bf16 [q_rows][num_kv_heads][128]
+ *   k_chunk, v_chunk  [q_rows][num_kv_heads][128], chunk_dtype NVFP4KV_BF16
+ *            (bf16) or NVFP4KV_E4M3 (uint8 E4M3 codes at scale 1.0); anything
+ *            else returns NVFP4KV_ERR_INVALID_ARG
  *   out      [q_rows][num_q_heads][128], out_dtype bf16 or fp32; rows outside
  *            every [q_indptr[b], q_indptr[b+1]) are not written
  *   k_prefix, v_prefix  uint8 E4M3 [prefix_rows][num_kv_heads][128]
@@ -315,7 +323,7 @@ nvfp4kv_status nvfp4kv_dequant_prefix_fp8(const nvfp4kv_cache *cache,
  *            [batch] (device)
  *   max_q_len  host bound on every q_indptr[b+1] - q_indptr[b]; it sizes the
  *            launch
- * Arithmetic: q * sm_scale * log2(e) and the chunk's keys and values are
+ * Arithmetic: q * sm_scale * log2(e) and bf16 chunk keys and values are
  * rounded to fp16 (exact for bf16 values of magnitude 2^-14 .. 65504; the
  * caller keeps |q * sm_scale| and the chunk's values below 65504), E4M3 to
  * fp16 is exact, scores and outputs accumulate in fp32, softmax weights are
@@ -331,7 +339,8 @@ nvfp4kv_status nvfp4kv_extend_attention_fp8(const void *q, const int32_t *q_indp
                                             int32_t max_q_len, const void *k_prefix,
                                             const void *v_prefix, const int32_t *kv_indptr,
                                             const int32_t *prefix_lens, int64_t prefix_rows,
-                                            const void *k_chunk, const void *v_chunk, int32_t batch,
+                                            const void *k_chunk, const void *v_chunk,
+                                            nvfp4kv_dtype chunk_dtype, int32_t batch,
                                             int32_t num_q_heads, int32_t num_kv_heads, float sm_scale,
                                             void *out, nvfp4kv_dtype out_dtype, int32_t *dev_status,
                                             nvfp4kv_stream_t stream);
@@ -341,9 +350,11 @@ nvfp4kv_status nvfp4kv_extend_attention_fp8(const void *q, const int32_t *q_indp
  * cache; the fusion removes the separate read of the chunk).  Computes out
  * exactly as nvfp4kv_extend_attention_fp8 (num_kv_heads taken from the cache)
  * and writes chunk row r's K and V into slot slot_mapping[r] of the cache, as
- * nvfp4kv_quantize_append would with in_dtype bf16 (same blocks, same bytes,
- * same tensor scale; slot < 0 skips the token, a slot >= num_pages *
- * page_size is skipped and sets NVFP4KV_DEV_BAD_SLOT).  slot_mapping: int32
+ * nvfp4kv_quantize_append would given the chunk's values (bf16 as they are;
+ * E4M3 codes as the fp32 values they stand for: the same data the attention
+ * reads, as initial prefill does) -- same blocks, same bytes, same tensor
+ * scale; slot < 0 skips the token, a slot >= num_pages * page_size is skipped
+ * and sets NVFP4KV_DEV_BAD_SLOT.  slot_mapping: int32
  * [q_rows] (device, 4-byte aligned), read only for rows inside a sequence's
  * q_indptr range; slots must be distinct.  The prefix workspace must not
  * overlap the cache. */
@@ -354,6 +365,7 @@ nvfp4kv_status nvfp4kv_extend_attention_fp8_append(const nvfp4kv_cache *cache,
                                                    const void *v_prefix, const int32_t *kv_indptr,
                                                    const int32_t *prefix_lens, int64_t prefix_rows,
                                                    const void *k_chunk, const void *v_chunk,
+                                                   nvfp4kv_dtype chunk_dtype,
                                                    int32_t batch, int32_t num_q_heads, float sm_scale,
                                                    void *out, nvfp4kv_dtype out_dtype,
                                                    int32_t *dev_status, nvfp4kv_stream_t stream);
@@ -410,6 +422,19 @@ int64_t fp8kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t page_
  * word is not reset.  Null pointers return NVFP4KV_ERR_INVALID_ARG. */
 nvfp4kv_status nvfp4kv_read_device_status(const int32_t *dev_status, nvfp4kv_stream_t stream,
                                           int32_t *bits);
+
+/* Failure detection (a library utility with no counterpart on the pages).
+ * Every kernel wait for staged data, or for another part of the same CTA,
+ * gives up after a number of polls, sets NVFP4KV_DEV_TIMEOUT in *dev_status,
+ * lets whatever it already started (bulk copies, tensor-core operations)
+ * finish and returns, so a wait that can never be satisfied costs a short
+ * delay and a status bit, not a hung GPU.  This sets that number for the
+ * calls made from now on in this process (0 = give up without polling;
+ * NVFP4KV_WAIT_LIMIT_DEFAULT is the default) and returns the previous value.
+ * The waits for work already in flight always use the default.  Host only,
+ * thread-safe; a small limit makes ordinary calls report timeouts. */
+#define NVFP4KV_WAIT_LIMIT_DEFAULT 4194304u
+uint32_t nvfp4kv_set_wait_limit(uint32_t polls);
 
 /* Static description of a status code (library utility). */
 const char *nvfp4kv_status_string(nvfp4kv_status status);

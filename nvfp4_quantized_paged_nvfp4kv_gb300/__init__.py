@@ -23,6 +23,7 @@ Functions carry the C names and take torch tensors:
     nvfp4kv_extend_attention_fp8_append(cache, slot_mapping, q, q_indptr, ...)
   utilities
     nvfp4kv_read_device_status(dev_status, stream=None)
+    nvfp4kv_set_wait_limit(polls) (failure detection: when bounded waits give up)
     nvfp4kv_cache_bytes / fp8kv_cache_bytes / nvfp4kv_status_string / nvfp4kv_version
 
 ``NVFP4Cache`` and ``FP8Cache`` hold the pool tensors and build the C structs.
@@ -41,7 +42,7 @@ HEAD_DIM = 128
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK = 0, 1, 2, 3, 4, 5
 DEV_BAD_PAGE, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
-F32, BF16 = 0, 1
+F32, BF16, E4M3 = 0, 1, 2
 STATIC_SCRATCH_MAX_WORKERS = 3024   # NVFP4KV_STATIC_SCRATCH_MAX_WORKERS
 
 _lock = threading.Lock()
@@ -119,10 +120,11 @@ def load(build_if_missing: bool = True):
             "nvfp4kv_dequant_prefix_fp8": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _i32, _vp, _vp, _i32,
                                                  _vp, _vp, _vp, _vp]),
             "nvfp4kv_extend_attention_fp8": (_st, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, ctypes.c_int64, _vp,
-                                                   _vp, _i32, _i32, _i32, ctypes.c_float, _vp, _st, _vp, _vp]),
+                                                   _vp, _st, _i32, _i32, _i32, ctypes.c_float, _vp, _st, _vp,
+                                                   _vp]),
             "nvfp4kv_extend_attention_fp8_append": (_st, [ctypes.POINTER(_Nvfp4Cache), _vp, _vp, _vp, _i32, _i32,
-                                                          _vp, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp, _i32,
-                                                          _i32, ctypes.c_float, _vp, _st, _vp, _vp]),
+                                                          _vp, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp, _st,
+                                                          _i32, _i32, ctypes.c_float, _vp, _st, _vp, _vp]),
             "fp8kv_quantize_append": (_st, [ctypes.POINTER(_Fp8Cache), _vp, _vp, _st, _i32, _vp, _vp, _vp]),
             "fp8kv_paged_decode": (_st, [ctypes.POINTER(_Fp8Cache), _vp, _i32, _i32, _vp, _i32, _vp,
                                          ctypes.c_float, _vp, _st, _vp, ctypes.c_size_t, _i32, _vp, _vp]),
@@ -131,6 +133,7 @@ def load(build_if_missing: bool = True):
             "nvfp4kv_status_string": (ctypes.c_char_p, [_st]),
             "nvfp4kv_read_device_status": (_st, [_vp, _vp, ctypes.POINTER(_i32)]),
             "nvfp4kv_version": (_i32, []),
+            "nvfp4kv_set_wait_limit": (ctypes.c_uint32, [ctypes.c_uint32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -332,15 +335,25 @@ def nvfp4kv_dequant_prefix_fp8(cache: NVFP4Cache, block_table, prefix_lens, kv_i
     _check(st, "nvfp4kv_dequant_prefix_fp8")
 
 
+def _chunk_dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return E4M3
+    raise TypeError(f"unsupported chunk dtype {t.dtype}")
+
+
 def nvfp4kv_extend_attention_fp8(q, q_indptr, k_prefix, v_prefix, kv_indptr, prefix_lens, k_chunk, v_chunk,
                                  out, max_q_len=None, sm_scale=None, dev_status=None, stream=None) -> None:
     """Extend attention: each chunk token attends over its sequence's FP8 prefix
     rows and the chunk up to itself.  q: bf16 [rows][Hq][128]; k_chunk, v_chunk:
-    bf16 [rows][Hkv][128]; k_prefix, v_prefix: E4M3 bytes [prefix rows][Hkv][128]
-    (uint8 or float8_e4m3fn); q_indptr int32 [B+1], kv_indptr and prefix_lens
-    int32 [B], all on the device; out: bf16 or fp32 [rows][Hq][128].
-    max_q_len bounds every chunk length (read from q_indptr when None, which
-    synchronises)."""
+    [rows][Hkv][128], bf16 or E4M3 bytes (uint8 or float8_e4m3fn: initial
+    prefill on the prompt's FP8 K/V); k_prefix, v_prefix: E4M3 bytes
+    [prefix rows][Hkv][128] (uint8 or float8_e4m3fn); q_indptr int32 [B+1],
+    kv_indptr and prefix_lens int32 [B], all on the device; out: bf16 or fp32
+    [rows][Hq][128].  max_q_len bounds every chunk length (read from q_indptr
+    when None, which synchronises)."""
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(HEAD_DIM)
     rows, Hq, _ = q.shape
@@ -350,16 +363,17 @@ def nvfp4kv_extend_attention_fp8(q, q_indptr, k_prefix, v_prefix, kv_indptr, pre
         max_q_len = int((q_indptr[1:] - q_indptr[:-1]).max().item()) if B > 0 else 0
     st = load().nvfp4kv_extend_attention_fp8(
         _ptr(q), _ptr(q_indptr), rows, int(max_q_len), _ptr(k_prefix), _ptr(v_prefix), _ptr(kv_indptr),
-        _ptr(prefix_lens), k_prefix.shape[0], _ptr(k_chunk), _ptr(v_chunk), B, Hq, Hkv, float(sm_scale),
-        _ptr(out), _dtype_code(out), _ptr(dev_status), _stream(stream))
+        _ptr(prefix_lens), k_prefix.shape[0], _ptr(k_chunk), _ptr(v_chunk), _chunk_dtype_code(k_chunk), B, Hq,
+        Hkv, float(sm_scale), _ptr(out), _dtype_code(out), _ptr(dev_status), _stream(stream))
     _check(st, "nvfp4kv_extend_attention_fp8")
 
 
 def nvfp4kv_extend_attention_fp8_append(cache: NVFP4Cache, slot_mapping, q, q_indptr, k_prefix, v_prefix,
                                         kv_indptr, prefix_lens, k_chunk, v_chunk, out, max_q_len=None,
                                         sm_scale=None, dev_status=None, stream=None) -> None:
-    """nvfp4kv_extend_attention_fp8 that also writes the chunk's K/V (bf16) into
-    the NVFP4 cache at slot_mapping (int32 [rows], device)."""
+    """nvfp4kv_extend_attention_fp8 that also writes the chunk's K/V (bf16 or
+    E4M3, the values the attention reads) into the NVFP4 cache at slot_mapping
+    (int32 [rows], device)."""
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(HEAD_DIM)
     rows, Hq, _ = q.shape
@@ -368,8 +382,9 @@ def nvfp4kv_extend_attention_fp8_append(cache: NVFP4Cache, slot_mapping, q, q_in
         max_q_len = int((q_indptr[1:] - q_indptr[:-1]).max().item()) if B > 0 else 0
     st = load().nvfp4kv_extend_attention_fp8_append(
         cache.c, _ptr(slot_mapping), _ptr(q), _ptr(q_indptr), rows, int(max_q_len), _ptr(k_prefix),
-        _ptr(v_prefix), _ptr(kv_indptr), _ptr(prefix_lens), k_prefix.shape[0], _ptr(k_chunk), _ptr(v_chunk), B,
-        Hq, float(sm_scale), _ptr(out), _dtype_code(out), _ptr(dev_status), _stream(stream))
+        _ptr(v_prefix), _ptr(kv_indptr), _ptr(prefix_lens), k_prefix.shape[0], _ptr(k_chunk), _ptr(v_chunk),
+        _chunk_dtype_code(k_chunk), B, Hq, float(sm_scale), _ptr(out), _dtype_code(out), _ptr(dev_status),
+        _stream(stream))
     _check(st, "nvfp4kv_extend_attention_fp8_append")
 
 
@@ -403,6 +418,15 @@ nvfp4kv_status_string = status_string
 
 def nvfp4kv_version() -> int:
     return int(load().nvfp4kv_version())
+
+
+WAIT_LIMIT_DEFAULT = 4194304        # NVFP4KV_WAIT_LIMIT_DEFAULT
+
+
+def nvfp4kv_set_wait_limit(polls: int) -> int:
+    """Polls after which a kernel's bounded waits give up (and report
+    DEV_TIMEOUT), for the calls made from now on; returns the previous value."""
+    return int(load().nvfp4kv_set_wait_limit(int(polls)))
 
 
 def new_workspace(num_workers: int = 0, device="cuda"):

@@ -2,6 +2,7 @@
 // The contract of every entry point is documented in include/nvfp4kv.h.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -11,6 +12,13 @@
 using namespace nvfp4kv;
 
 namespace {
+
+std::atomic<uint32_t> g_wait_limit{kWaitLimit};
+
+uint32_t wait_limit()
+{
+    return g_wait_limit.load(std::memory_order_relaxed);
+}
 
 bool aligned16(const void *p)
 {
@@ -182,6 +190,7 @@ nvfp4kv_status check_decode(int32_t hkv, int32_t num_pages, const void *q, int32
     p.q_len = 1;
     p.rows = group;
     p.row_groups = 1;
+    p.wait_limit = wait_limit();
     return NVFP4KV_OK;
 }
 
@@ -206,13 +215,15 @@ void apply_tensor_scale(DecodeParams &p, float sm_scale, const nvfp4kv_cache *c)
 nvfp4kv_status check_extend(const void *q, const int32_t *q_indptr, int32_t q_rows, int32_t max_q_len,
                             const void *k_prefix, const void *v_prefix, const int32_t *kv_indptr,
                             const int32_t *prefix_lens, int64_t prefix_rows, const void *k_chunk,
-                            const void *v_chunk, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                            float sm_scale, void *out, nvfp4kv_dtype out_dtype, int32_t *dev_status,
-                            ExtendParams &p)
+                            const void *v_chunk, nvfp4kv_dtype chunk_dtype, int32_t batch, int32_t num_q_heads,
+                            int32_t num_kv_heads, float sm_scale, void *out, nvfp4kv_dtype out_dtype,
+                            int32_t *dev_status, ExtendParams &p)
 {
     if (batch < 0 || q_rows < 0 || max_q_len < 0 || prefix_rows < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
         return NVFP4KV_ERR_INVALID_ARG;
     if (out_dtype != NVFP4KV_F32 && out_dtype != NVFP4KV_BF16)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (chunk_dtype != NVFP4KV_BF16 && chunk_dtype != NVFP4KV_E4M3)
         return NVFP4KV_ERR_INVALID_ARG;
     if (!std::isfinite(sm_scale))
         return NVFP4KV_ERR_INVALID_ARG;
@@ -245,8 +256,9 @@ nvfp4kv_status check_extend(const void *q, const int32_t *q_indptr, int32_t q_ro
     p.v_prefix = static_cast<const uint8_t *>(v_prefix);
     p.kv_indptr = kv_indptr;
     p.prefix_lens = prefix_lens;
-    p.k_chunk = static_cast<const uint16_t *>(k_chunk);
-    p.v_chunk = static_cast<const uint16_t *>(v_chunk);
+    p.k_chunk = k_chunk;
+    p.v_chunk = v_chunk;
+    p.chunk_e4m3 = chunk_dtype == NVFP4KV_E4M3;
     p.out = out;
     p.dev_status = dev_status;
     p.batch = batch;
@@ -259,6 +271,7 @@ nvfp4kv_status check_extend(const void *q, const int32_t *q_indptr, int32_t q_ro
     p.qscale = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
     p.out_f32 = out_dtype == NVFP4KV_F32;
     p.gscale = 1.f;
+    p.wait_limit = wait_limit();
     return NVFP4KV_OK;
 }
 
@@ -385,6 +398,7 @@ nvfp4kv_status nvfp4kv_dequant_prefix_fp8(const nvfp4kv_cache *cache, const int3
     p.num_pages = cache->num_pages;
     p.gscale = cache->global_scale;
     p.hs = head_scales_of(cache);
+    p.wait_limit = wait_limit();
     return from_cuda(launch_dequant_prefix_fp8(p, to_cuda(stream)));
 }
 
@@ -392,14 +406,15 @@ nvfp4kv_status nvfp4kv_extend_attention_fp8(const void *q, const int32_t *q_indp
                                             int32_t max_q_len, const void *k_prefix, const void *v_prefix,
                                             const int32_t *kv_indptr, const int32_t *prefix_lens,
                                             int64_t prefix_rows, const void *k_chunk, const void *v_chunk,
-                                            int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                                            float sm_scale, void *out, nvfp4kv_dtype out_dtype,
-                                            int32_t *dev_status, nvfp4kv_stream_t stream)
+                                            nvfp4kv_dtype chunk_dtype, int32_t batch, int32_t num_q_heads,
+                                            int32_t num_kv_heads, float sm_scale, void *out,
+                                            nvfp4kv_dtype out_dtype, int32_t *dev_status, nvfp4kv_stream_t stream)
 {
     ExtendParams p{};
     const nvfp4kv_status st =
         check_extend(q, q_indptr, q_rows, max_q_len, k_prefix, v_prefix, kv_indptr, prefix_lens, prefix_rows,
-                     k_chunk, v_chunk, batch, num_q_heads, num_kv_heads, sm_scale, out, out_dtype, dev_status, p);
+                     k_chunk, v_chunk, chunk_dtype, batch, num_q_heads, num_kv_heads, sm_scale, out, out_dtype,
+                     dev_status, p);
     if (st != NVFP4KV_OK || batch == 0 || max_q_len == 0)
         return st;
     return from_cuda(launch_extend_attention(p, to_cuda(stream)));
@@ -410,17 +425,17 @@ nvfp4kv_status nvfp4kv_extend_attention_fp8_append(const nvfp4kv_cache *cache, c
                                                    int32_t max_q_len, const void *k_prefix, const void *v_prefix,
                                                    const int32_t *kv_indptr, const int32_t *prefix_lens,
                                                    int64_t prefix_rows, const void *k_chunk, const void *v_chunk,
-                                                   int32_t batch, int32_t num_q_heads, float sm_scale, void *out,
-                                                   nvfp4kv_dtype out_dtype, int32_t *dev_status,
-                                                   nvfp4kv_stream_t stream)
+                                                   nvfp4kv_dtype chunk_dtype, int32_t batch, int32_t num_q_heads,
+                                                   float sm_scale, void *out, nvfp4kv_dtype out_dtype,
+                                                   int32_t *dev_status, nvfp4kv_stream_t stream)
 {
     nvfp4kv_status st = check_nvfp4(cache);
     if (st != NVFP4KV_OK)
         return st;
     ExtendParams p{};
     st = check_extend(q, q_indptr, q_rows, max_q_len, k_prefix, v_prefix, kv_indptr, prefix_lens, prefix_rows,
-                      k_chunk, v_chunk, batch, num_q_heads, cache->num_kv_heads, sm_scale, out, out_dtype,
-                      dev_status, p);
+                      k_chunk, v_chunk, chunk_dtype, batch, num_q_heads, cache->num_kv_heads, sm_scale, out,
+                      out_dtype, dev_status, p);
     if (st != NVFP4KV_OK || batch == 0 || max_q_len == 0)
         return st;
     if (slot_mapping == nullptr || (reinterpret_cast<uintptr_t>(slot_mapping) & 3u))
@@ -567,6 +582,11 @@ nvfp4kv_status nvfp4kv_read_device_status(const int32_t *dev_status, nvfp4kv_str
         return NVFP4KV_ERR_CUDA;
     *bits = v;
     return v != 0 ? NVFP4KV_ERR_DEVICE_CHECK : NVFP4KV_OK;
+}
+
+uint32_t nvfp4kv_set_wait_limit(uint32_t polls)
+{
+    return g_wait_limit.exchange(polls, std::memory_order_relaxed);
 }
 
 const char *nvfp4kv_status_string(nvfp4kv_status status)

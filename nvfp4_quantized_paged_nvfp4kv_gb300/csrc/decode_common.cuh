@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
     start_segment();
     if (npro > 2) {
         // (a wait that gives up here gives up again, reported, in the loop)
-        mbar_wait_bounded(wbar, 0, kWaitLimit);
+        mbar_wait_bounded(wbar, 0, p.wait_limit);
         __syncwarp();
         for (int x = lo + 2; x < lo + npro; ++x)
             issue(x, x - lo);
@@ -743,10 +743,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         // Lanes poll independently and may leave the loop at different polls;
         // the vote reconverges the warp before the warp-wide MMAs below and
         // makes the give-up decision uniform.
-        const bool arrived = np == 2 ? mbar_wait2_bounded(wbar + 8 * st, ph, wbar + 8 * st1, ph1, kWaitLimit)
-                                     : mbar_wait_bounded(wbar + 8 * st, ph, kWaitLimit);
+        const bool arrived = np == 2 ? mbar_wait2_bounded(wbar + 8 * st, ph, wbar + 8 * st1, ph1, p.wait_limit)
+                                     : mbar_wait_bounded(wbar + 8 * st, ph, p.wait_limit);
         if (!__all_sync(kFullMask, arrived)) {
-            // staged data never arrived: report, let the copies in flight land, stop
+            // staged data never arrived: report, let the copies in flight land
+            // (at the default limit, whatever p.wait_limit is), stop
             if (lane == 0)
                 report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
             const int pending = min(S, hi - j);

@@ -124,16 +124,18 @@ __global__ void __launch_bounds__(kPrefixThreads) dequant_prefix_kernel(const __
             staged_n = stage(nxt, k ^ 1, Ln);
         }
         if (staged) {
-            const bool arrived = mbar_wait_bounded(bar0 + 8 * k, (parity >> k) & 1u, kWaitLimit);
-            parity ^= 1u << k;
+            const bool arrived = mbar_wait_bounded(bar0 + 8 * k, (parity >> k) & 1u, p.wait_limit);
             if (!__syncthreads_and(arrived)) {
-                // staged data never arrived: report, let the other copy land, stop
+                // staged data never arrived: report, let both copies in flight
+                // (this unit's and the next one's) land at the default limit, stop
                 if (t == 0)
                     report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
+                mbar_wait_bounded(bar0 + 8 * k, (parity >> k) & 1u, kWaitLimit);
                 if (staged_n)
                     mbar_wait_bounded(bar0 + 8 * (k ^ 1), (parity >> (k ^ 1)) & 1u, kWaitLimit);
                 return;
             }
+            parity ^= 1u << k;
             const uint32_t rec = smem_addr(buf[k]);
             const int j0 = cur.pg * kPageSize;
             const size_t rows = static_cast<size_t>(cur.base) + j0;     // output row of token 0

@@ -49,9 +49,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for phase `parity` of a barrier, giving up after `limit` polls.
-constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a staged-data wait gives up
-
+// Wait for phase `parity` of a barrier, giving up after `limit` polls (none
+// when limit is 0).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit)
 {
     for (uint32_t i = 0; i < limit; ++i)
@@ -60,9 +59,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
-// ---- asynchronous copies global -> shared ---------------------------------
-
-// Untiled bulk copy; both addresses 16-byte aligned, bytes a multiple of 16.
 // Waits (bounded) until the phases with parity pa of barrier a and pb of
 // barrier b have completed, polling both in one loop.
 __device__ __forceinline__ bool mbar_wait2_bounded(uint32_t a, uint32_t pa, uint32_t b, uint32_t pb, uint32_t limit)
@@ -77,6 +73,9 @@ __device__ __forceinline__ bool mbar_wait2_bounded(uint32_t a, uint32_t pa, uint
     return false;
 }
 
+// ---- asynchronous copies global -> shared ---------------------------------
+
+// Untiled bulk copy; both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
     asm volatile(

@@ -17,9 +17,11 @@
 //                 memory
 //   O += P V      tcgen05.mma M128 N128 K16 x 4 with P read from tensor
 //                 memory, O resident in tensor memory
-// Warps 0-3 run the softmax, warps 4-7 convert key tiles (E4M3 prefix rows or
-// bf16 chunk rows) to f16 in the 128-byte-swizzled operand layout, warp 8
-// allocates tensor memory and issues the MMAs.  mbarriers order the roles;
+// Warps 0-3 run the softmax, warps 4-7 convert key tiles (E4M3 prefix rows,
+// and bf16 or E4M3 chunk rows) to f16 in the 128-byte-swizzled operand
+// layout, warp 8 allocates tensor memory and issues the MMAs.  E4M3 chunk
+// rows are initial prefill as the same paragraph describes it: attention on
+// the current prompt's FP8 keys and values.  mbarriers order the roles;
 // every wait is bounded and a timeout is reported.
 //
 // The appending variant also writes the chunk's K/V into the NVFP4 cache
@@ -94,11 +96,12 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float s)
     return pack_f16x2(__uint_as_float(w << 16) * s, __uint_as_float(w & 0xffff0000u) * s);
 }
 
-__device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, volatile int *fail, int32_t *dev_status)
+__device__ __forceinline__ bool wait_or_fail(uint32_t bar, uint32_t parity, volatile int *fail, int32_t *dev_status,
+                                             uint32_t limit)
 {
     if (*fail)
         return false;
-    if (mbar_wait_bounded(bar, parity, kWaitLimit))
+    if (mbar_wait_bounded(bar, parity, limit))
         return true;
     *fail = 1;
     report(dev_status, NVFP4KV_DEV_TIMEOUT);
@@ -113,8 +116,8 @@ struct TcCta {
 
 // Producer thread pt (0..127): load key tile i, wait until its stage is free,
 // convert it to f16 in the 128-byte-swizzled layout and signal the MMA warp.
-// FP8 prefix tiles: 64 keys x 8 pieces of 16 bytes per K and per V, four
-// pieces a thread each, loaded together.  bf16 chunk tiles: 64 keys x 16
+// FP8 tiles (every prefix tile; chunk tiles when kChunk8): 64 keys x 8 pieces
+// of 16 bytes per K and per V, four pieces a thread each, loaded together.  bf16 chunk tiles: 64 keys x 16
 // pieces per K and per V; thread pt owns piece pt mod 16 of keys pt / 16 + 8 j
 // (j = 0..7), K then V (eight loads in flight a thread keep the register count
 // low); its offsets repeat from tile to tile and are taken once.  Keys past
@@ -135,6 +138,7 @@ __device__ __forceinline__ ChunkLanes chunk_lanes(const ExtendParams &p, int pt)
     return l;
 }
 
+template <bool kChunk8>
 __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta &c, int h, int i, int pt,
                                              const ChunkLanes &l, uint32_t base, volatile int *fail)
 {
@@ -142,29 +146,35 @@ __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta 
     const uint32_t kdst = base + kOffK + st * kKVBytes, vdst = base + kOffV + st * kKVBytes;
     const uint4 zero = make_uint4(0, 0, 0, 0);
     const size_t row_elems = static_cast<size_t>(p.hkv) * kHeadDim;   // one key's bf16 row
+    const uint16_t *k_chunk = static_cast<const uint16_t *>(p.k_chunk);
+    const uint16_t *v_chunk = static_cast<const uint16_t *>(p.v_chunk);
     uint4 raw[8];
     const bool pre = i < c.n_pre;
+    const bool e4m3 = kChunk8 || pre;
     const int k0 = (pre ? i : i - c.n_pre) * kTcKeys;
-    if (pre) {
+    if (e4m3) {
+        const uint8_t *kb = pre ? p.k_prefix : static_cast<const uint8_t *>(p.k_chunk);
+        const uint8_t *vb = pre ? p.v_prefix : static_cast<const uint8_t *>(p.v_chunk);
+        const int64_t r0 = pre ? c.p0 + k0 : static_cast<int64_t>(c.c0) + k0;
+        const int lim = pre ? c.P : c.C;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int idx = pt + kProducerThreads * (u & 3);
             const int key = idx >> 3, piece = idx & 7;
-            const uint8_t *src = (u < 4 ? p.k_prefix : p.v_prefix) + ((c.p0 + k0 + key) * p.hkv + h) * kHeadDim +
-                                 16 * piece;
-            raw[u] = k0 + key < c.P ? ldg_nc(src) : zero;
+            const uint8_t *src = (u < 4 ? kb : vb) + ((r0 + key) * p.hkv + h) * kHeadDim + 16 * piece;
+            raw[u] = k0 + key < lim ? ldg_nc(src) : zero;
         }
     } else {
         const size_t tile = (static_cast<size_t>(c.c0 + k0) * p.hkv + h) * kHeadDim + l.src;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-            raw[u] = k0 + l.key + 8 * u < c.C ? ldg_nc(p.k_chunk + tile + u * 8 * row_elems) : zero;
+            raw[u] = k0 + l.key + 8 * u < c.C ? ldg_nc(k_chunk + tile + u * 8 * row_elems) : zero;
     }
     // stage st was last read by the MMAs of tile i - kKvStages
     if (i >= kKvStages && !wait_or_fail(base + kOffBar + 8 * (kBarKvEmpty + st), ((i / kKvStages) - 1) & 1, fail,
-                                        p.dev_status))
+                                        p.dev_status, p.wait_limit))
         return false;
-    if (pre) {
+    if (e4m3) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int idx = pt + kProducerThreads * (u & 3);
@@ -187,7 +197,7 @@ __device__ __forceinline__ bool produce_tile(const ExtendParams &p, const TcCta 
             if (half == 1) {
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    raw[u] = k0 + l.key + 8 * u < c.C ? ldg_nc(p.v_chunk + tile + u * 8 * row_elems) : zero;
+                    raw[u] = k0 + l.key + 8 * u < c.C ? ldg_nc(v_chunk + tile + u * 8 * row_elems) : zero;
             }
             const uint32_t dst = (half ? vdst : kdst) + l.dst;
 #pragma unroll
@@ -225,24 +235,72 @@ __device__ __forceinline__ bool append_site(const ExtendParams &p, int slot, int
     return true;
 }
 
+// One 16-value block of a chunk row as loaded: two 16-byte pieces of bf16, or
+// one of E4M3 codes (kChunk8).
+template <bool kChunk8>
+struct ChunkBlock {
+    uint4 v[kChunk8 ? 1 : 2];
+};
+
+template <bool kChunk8>
+__device__ __forceinline__ void load_raw(const void *src, size_t elem_off, ChunkBlock<kChunk8> &r)
+{
+    if constexpr (kChunk8) {
+        r.v[0] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(src) + elem_off));
+    } else {
+        RawBlock<true> b;
+        load_raw<true>(src, elem_off, b);
+        r.v[0] = b.v[0];
+        r.v[1] = b.v[1];
+    }
+}
+
+// The block's values as fp32, exactly (bf16 widened; E4M3 through f16, which
+// holds every E4M3 value).
+template <bool kChunk8>
+__device__ __forceinline__ void unpack(const ChunkBlock<kChunk8> &r, float (&x)[16])
+{
+    if constexpr (kChunk8) {
+        const uint32_t w[4] = {r.v[0].x, r.v[0].y, r.v[0].z, r.v[0].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t lo, hi;
+            e4m3x4_to_f16x2x2(w[k], lo, hi);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+            x[4 * k] = a.x;
+            x[4 * k + 1] = a.y;
+            x[4 * k + 2] = b.x;
+            x[4 * k + 3] = b.y;
+        }
+    } else {
+        RawBlock<true> b;
+        b.v[0] = r.v[0];
+        b.v[1] = r.v[1];
+        unpack<true>(b, x);
+    }
+}
+
 // Producer thread pt quantises chunk keys k0 .. k0 + 63 of kv head h into the
-// cache, reading the bf16 rows from global memory (each group of loads issued
-// together).  K: 64 keys x 8 blocks, four a thread.  V: 32 key pairs x 8
-// blocks, two a thread; a pair on an even slot and its successor is written
-// whole, any other token through the atomic nibble merge.
+// cache, reading the chunk rows (bf16, or E4M3 when kChunk8) from global
+// memory (each group of loads issued together).  K: 64 keys x 8 blocks, four a
+// thread.  V: 32 key pairs x 8 blocks, two a thread; a pair on an even slot
+// and its successor is written whole, any other token through the atomic
+// nibble merge.
+template <bool kChunk8>
 __device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const TcCta &c, int h, int k0, int pt)
 {
     auto offset = [&](int key, int blk) {
         return (static_cast<size_t>(c.c0 + key) * p.hkv + h) * kHeadDim + blk * 16;
     };
     const float Gk = head_tensor_scale(p.hs, false, h, p.gscale), Gv = head_tensor_scale(p.hs, true, h, p.gscale);
-    RawBlock<true> r[4];
+    ChunkBlock<kChunk8> r[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int item = pt + kProducerThreads * u;
         const int key = k0 + (item >> 3), blk = item & 7;
         if (key < c.C)
-            load_raw<true>(p.k_chunk, offset(key, blk), r[u]);
+            load_raw<kChunk8>(p.k_chunk, offset(key, blk), r[u]);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -253,7 +311,7 @@ __device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const T
         if (key >= c.C || !append_site(p, p.slot_mapping[c.c0 + key], h, rec, tok, blk == 0))
             continue;
         float x[16];
-        unpack<true>(r[u], x);
+        unpack<kChunk8>(r[u], x);
         divide_by_tensor_scale(x, Gk);
         write_nvfp4_block(p.pool + rec, false, tok, blk, x);
     }
@@ -262,9 +320,9 @@ __device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const T
         const int item = pt + kProducerThreads * u;
         const int key0 = k0 + 2 * (item >> 3), blk = item & 7;
         if (key0 < c.C)
-            load_raw<true>(p.v_chunk, offset(key0, blk), r[2 * u]);
+            load_raw<kChunk8>(p.v_chunk, offset(key0, blk), r[2 * u]);
         if (key0 + 1 < c.C)
-            load_raw<true>(p.v_chunk, offset(key0 + 1, blk), r[2 * u + 1]);
+            load_raw<kChunk8>(p.v_chunk, offset(key0 + 1, blk), r[2 * u + 1]);
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -280,29 +338,29 @@ __device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const T
         float x[16];
         if (ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
             uint32_t S0, S1, q0[2], q1[2];
-            unpack<true>(r[2 * u], x);
+            unpack<kChunk8>(r[2 * u], x);
             divide_by_tensor_scale(x, Gv);
             quantize_block(x, S0, q0);
-            unpack<true>(r[2 * u + 1], x);
+            unpack<kChunk8>(r[2 * u + 1], x);
             divide_by_tensor_scale(x, Gv);
             quantize_block(x, S1, q1);
             write_nvfp4_v_pair(p.pool + rec0, tok0, blk, S0, q0, S1, q1);
             continue;
         }
         if (ok0) {
-            unpack<true>(r[2 * u], x);
+            unpack<kChunk8>(r[2 * u], x);
             divide_by_tensor_scale(x, Gv);
             write_nvfp4_block(p.pool + rec0, true, tok0, blk, x);
         }
         if (ok1) {
-            unpack<true>(r[2 * u + 1], x);
+            unpack<kChunk8>(r[2 * u + 1], x);
             divide_by_tensor_scale(x, Gv);
             write_nvfp4_block(p.pool + rec1, true, tok1, blk, x);
         }
     }
 }
 
-template <bool kAppend>
+template <bool kAppend, bool kChunk8>
 __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_constant__ ExtendParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -414,7 +472,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
             for (int i = 0; ok && i < c.n_tiles; ++i) {
                 const int b = i & 1;
                 bool pv_done = false;
-                for (uint32_t polls = 0; !pv_done;) {
+                for (uint64_t polls = 0; !pv_done;) {
                     bool progress = false;
                     if (next_qk <= i + 1 && next_qk < c.n_tiles &&
                         mbar_test_wait(bar + 8 * (kBarKvFull + next_qk % kKvStages), (next_qk / kKvStages) & 1)) {
@@ -427,7 +485,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
                     }
                     if (progress)
                         continue;
-                    if (++polls > 64 * kWaitLimit || *fail) {
+                    if (++polls > 64ull * p.wait_limit || *fail) {
                         if (!*fail) {
                             *fail = 1;
                             report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
@@ -438,6 +496,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
                 }
             }
             // nothing of this thread's may still run when tensor memory is freed
+            // (waited for at the default limit, whatever p.wait_limit is)
             umma_commit(bar + 8 * kBarDone);
             if (!mbar_wait_bounded(bar + 8 * kBarDone, 0, kWaitLimit))
                 report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
@@ -447,14 +506,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
         const int pt = tid - kSoftmaxThreads;
         const ChunkLanes lanes = chunk_lanes(p, pt);
         for (int i = 0; i < c.n_tiles; ++i)
-            if (!produce_tile(p, c, h, i, pt, lanes, base, fail))
+            if (!produce_tile<kChunk8>(p, c, h, i, pt, lanes, base, fail))
                 break;
         if constexpr (kAppend) {
             // the chunk key tiles whose first key's first row (64 kt g) falls in
             // this CTA's rows; done while the last tiles are still in the MMAs
             const int per = kTcKeys * g;
             for (int kt = (row0 + per - 1) / per; kt < (row0 + kTcRows + per - 1) / per && kt * kTcKeys < c.C; ++kt)
-                append_chunk_tile(p, c, h, kt * kTcKeys, pt);
+                append_chunk_tile<kChunk8>(p, c, h, kt * kTcKeys, pt);
         }
     } else {
         // softmax: thread r owns row row0 + r, tensor-memory lane r
@@ -466,7 +525,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
         bool ok = true;
         // the warp leaves together: its tensor-memory accesses are warp-wide
         auto wait_warp = [&](uint32_t bar_addr, uint32_t parity) {
-            return __all_sync(kFullMask, wait_or_fail(bar_addr, parity, fail, p.dev_status));
+            return __all_sync(kFullMask, wait_or_fail(bar_addr, parity, fail, p.dev_status, p.wait_limit));
         };
         for (int i = 0; i < c.n_tiles; ++i) {
             const int b = i & 1;
@@ -597,7 +656,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
 
 cudaError_t launch_extend_attention(const ExtendParams &p, cudaStream_t s)
 {
-    const auto kernel = p.pool != nullptr ? extend_tc_kernel<true> : extend_tc_kernel<false>;
+    const auto kernel = p.chunk_e4m3 ? (p.pool != nullptr ? extend_tc_kernel<true, true> : extend_tc_kernel<false, true>)
+                                     : (p.pool != nullptr ? extend_tc_kernel<true, false> : extend_tc_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     if (e != cudaSuccess)
         return e;

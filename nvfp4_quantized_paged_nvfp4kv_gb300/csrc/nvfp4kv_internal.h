@@ -19,6 +19,12 @@ constexpr int kNvfp4Record = 2304;           // bytes of an NVFP4 page-head reco
 constexpr int kFp8Record = 4096;             // bytes of an FP8 page-head record
 constexpr int kMaxBatch = NVFP4KV_MAX_BATCH; // prefix table lives in shared memory
 constexpr int kMaxScaledHeads = NVFP4KV_MAX_SCALED_KV_HEADS;
+// Polls before a wait for staged data (or for another role of the CTA) gives
+// up and reports NVFP4KV_DEV_TIMEOUT; the launching calls pass the current
+// process-wide limit (nvfp4kv_set_wait_limit) in the kernels' parameters.  A
+// wait that only lets work already in flight land before the CTA exits always
+// uses this default, whatever the setting.
+constexpr uint32_t kWaitLimit = NVFP4KV_WAIT_LIMIT_DEFAULT;
 
 // Per-kv-head tensor scales of K and V, fl32(G * factor), used when per_head
 // is set (kernels take these parameters as __grid_constant__, so a head index
@@ -65,6 +71,7 @@ struct DecodeParams {
     // and the query scale sm_scale * log2(e) * G_k,h of each kv head
     HeadScales hs;
     float qs[kMaxScaledHeads];
+    uint32_t wait_limit;         // polls before a wait gives up (kWaitLimit by default)
 };
 
 struct QuantParams {
@@ -95,6 +102,7 @@ struct PrefixParams {
     int num_pages;
     float gscale;                // tensor scale multiplying every value
     HeadScales hs;
+    uint32_t wait_limit;         // polls before a wait gives up (kWaitLimit by default)
 };
 
 struct ExtendParams {
@@ -104,8 +112,8 @@ struct ExtendParams {
     const uint8_t *v_prefix;
     const int32_t *kv_indptr;    // [batch] first prefix row of each sequence
     const int32_t *prefix_lens;  // [batch]
-    const uint16_t *k_chunk;     // bf16 [q rows][hkv][128]
-    const uint16_t *v_chunk;
+    const void *k_chunk;         // [q rows][hkv][128]: bf16, or E4M3 bytes when chunk_e4m3
+    const void *v_chunk;
     void *out;                   // [q rows][hq][128], bf16 or fp32
     int32_t *dev_status;
     int batch;
@@ -117,12 +125,14 @@ struct ExtendParams {
     int64_t prefix_rows;         // rows of the prefix workspace
     float qscale;                // sm_scale * log2(e)
     int out_f32;
+    int chunk_e4m3;              // chunk K/V are E4M3 bytes (initial prefill on FP8 K/V)
     // fused NVFP4 append of the chunk (null pool: attention only)
     uint8_t *pool;               // page-head records [num_pages][hkv][record]
     const int32_t *slot_mapping; // [q rows]
     int num_pages;
     float gscale;                // tensor scale: blocks are taken of x / gscale
     HeadScales hs;
+    uint32_t wait_limit;         // polls before a wait gives up (kWaitLimit by default)
 };
 
 // Launch with programmatic stream serialisation allowed, so the kernel's

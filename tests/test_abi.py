@@ -196,9 +196,9 @@ def test_prefix_validation():
 
 
 def extend(q=FAKE, qi=FAKE, rows=100, mql=50, kp=FAKE, vp=FAKE, ki=FAKE, pl=FAKE, prows=1000, kc=FAKE, vc=FAKE,
-           batch=2, hq=16, hkv=2, scale=0.088, out=FAKE, dtype=nv.BF16):
-    return nv.load().nvfp4kv_extend_attention_fp8(q, qi, rows, mql, kp, vp, ki, pl, prows, kc, vc, batch, hq,
-                                                  hkv, scale, out, dtype, None, None)
+           batch=2, hq=16, hkv=2, scale=0.088, out=FAKE, dtype=nv.BF16, cdtype=nv.BF16):
+    return nv.load().nvfp4kv_extend_attention_fp8(q, qi, rows, mql, kp, vp, ki, pl, prows, kc, vc, cdtype, batch,
+                                                  hq, hkv, scale, out, dtype, None, None)
 
 
 def test_extend_validation():
@@ -219,14 +219,21 @@ def test_extend_validation():
     assert extend(qi=FAKE + 2) == nv.ERR_INVALID_ARG
     assert extend(batch=0, q=None, qi=None, ki=None, pl=None, kc=None, vc=None, out=None) == nv.OK
     assert extend(mql=0, q=None, out=None) == nv.OK
+    # chunk K/V: bf16 or E4M3 only
+    assert extend(cdtype=nv.F32, kp=None) == nv.ERR_INVALID_ARG
+    assert extend(cdtype=7, kp=None) == nv.ERR_INVALID_ARG
+    assert extend(cdtype=nv.F32, hq=18) == nv.ERR_INVALID_ARG       # the dtype is checked first
+    assert extend(cdtype=nv.E4M3, hq=18) == nv.ERR_UNSUPPORTED      # accepted, then the group is too large
+    assert extend(cdtype=nv.E4M3, batch=0, q=None, qi=None, ki=None, pl=None, kc=None, vc=None, out=None) == nv.OK
+    assert extend(cdtype=nv.E4M3, kc=FAKE + 8) == nv.ERR_INVALID_ARG
 
 
 def test_extend_append_validation():
     f = nv.load().nvfp4kv_extend_attention_fp8_append
 
-    def call(c, slots=FAKE, hq=4, batch=2, mql=50):
-        return f(ctypes.byref(c), slots, FAKE, FAKE, 100, mql, FAKE, FAKE, FAKE, FAKE, 1000, FAKE, FAKE, batch,
-                 hq, 0.088, FAKE, nv.BF16, None, None)
+    def call(c, slots=FAKE, hq=4, batch=2, mql=50, cdtype=nv.BF16):
+        return f(ctypes.byref(c), slots, FAKE, FAKE, 100, mql, FAKE, FAKE, FAKE, FAKE, 1000, FAKE, FAKE, cdtype,
+                 batch, hq, 0.088, FAKE, nv.BF16, None, None)
     assert call(cache(global_scale=0.0)) == nv.ERR_UNSUPPORTED
     assert call(cache(pool=None)) == nv.ERR_INVALID_ARG
     assert call(cache(), slots=None) == nv.ERR_INVALID_ARG
@@ -234,6 +241,9 @@ def test_extend_append_validation():
     assert call(cache(), hq=5) == nv.ERR_INVALID_ARG          # Hq % Hkv (2 in the cache) != 0
     assert call(cache(), hq=18) == nv.ERR_UNSUPPORTED
     assert call(cache(), batch=0, slots=None) == nv.OK
+    assert call(cache(), cdtype=nv.F32) == nv.ERR_INVALID_ARG
+    assert call(cache(), cdtype=nv.F32, hq=18) == nv.ERR_INVALID_ARG
+    assert call(cache(), cdtype=nv.E4M3, hq=18) == nv.ERR_UNSUPPORTED
 
 
 def test_read_device_status_validation():
@@ -264,3 +274,15 @@ def test_cache_bytes_match_the_printed_figures():
     assert nv.fp8kv_cache_bytes(1, 1) == nv.FP8_RECORD_BYTES
     assert 80 * nv.nvfp4kv_cache_bytes(131072 // 16, 8) == 11.25 * 2 ** 30
     assert nv.nvfp4kv_cache_bytes(1, 1, 16, 100) == -1
+
+
+def test_set_wait_limit_returns_the_previous_value():
+    """The process-wide poll limit of the kernels' bounded waits (host only)."""
+    lib = nv.load()
+    first = lib.nvfp4kv_set_wait_limit(7)
+    try:
+        assert first == nv.WAIT_LIMIT_DEFAULT
+        assert lib.nvfp4kv_set_wait_limit(0) == 7
+        assert lib.nvfp4kv_set_wait_limit(0xFFFFFFFF) == 0
+    finally:
+        assert lib.nvfp4kv_set_wait_limit(first) == 0xFFFFFFFF

@@ -254,7 +254,11 @@ class ExtendWorkload:
 def extend_make(name: str) -> ExtendWorkload:
     """ext160k: the last 8,192-token chunk of a 163,840-token prefill (Hq=48,
     Hkv=8), prefix 155,648.  ext8k_c2k: a 2,048-token chunk over an 8,192-token
-    prefix (the profiling case).  ext_small: four ragged sequences."""
+    prefix (the profiling case).  ext_small: four ragged sequences.
+    prefill8k: initial prefill of one 8,192-token prompt (no prefix; Hq=48,
+    Hkv=8), the chunk the 160K workload quantises."""
+    if name == "prefill8k":
+        return ExtendWorkload(name, (0,), (8192,), 48, 8, seed=_seed("prefill8k"))
     if name == "ext160k":
         return ExtendWorkload(name, (163840 - 8192,), (8192,), 48, 8, seed=_seed("ext160k"))
     if name == "ext8k_c2k":
@@ -279,17 +283,27 @@ def e4m3_codes(shape, gen, device="cpu") -> torch.Tensor:
     return torch.where(z, torch.zeros_like(code), code).to(torch.uint8)
 
 
-def extend_inputs(e: ExtendWorkload, device="cpu") -> dict:
-    """q (bf16 [rows][Hq][d]), k_chunk / v_chunk (bf16 [rows][Hkv][d]),
+def extend_inputs(e: ExtendWorkload, device="cpu", chunk: str = "bf16") -> dict:
+    """q (bf16 [rows][Hq][d]), k_chunk / v_chunk ([rows][Hkv][d]: bf16 ~ N(0,1),
+    or with chunk="e4m3" random E4M3 codes as uint8, the prompt's K/V as FP8),
     k_prefix / v_prefix (uint8 E4M3 [prefix rows][Hkv][d]) and the int32 index
     arrays q_indptr, kv_indptr, prefix_lens."""
     gen = torch.Generator(device=device)
     gen.manual_seed(_seed(e.seed, "extend"))
     rows, d = e.q_rows, e.head_dim
+    q = torch.randn((rows, e.num_q_heads, d), generator=gen, device=device).to(torch.bfloat16)
+    if chunk == "bf16":
+        kc = torch.randn((rows, e.num_kv_heads, d), generator=gen, device=device).to(torch.bfloat16)
+        vc = torch.randn((rows, e.num_kv_heads, d), generator=gen, device=device).to(torch.bfloat16)
+    elif chunk == "e4m3":
+        kc = e4m3_codes((rows, e.num_kv_heads, d), gen, device)
+        vc = e4m3_codes((rows, e.num_kv_heads, d), gen, device)
+    else:
+        raise ValueError(chunk)
     out = {
-        "q": torch.randn((rows, e.num_q_heads, d), generator=gen, device=device).to(torch.bfloat16),
-        "k_chunk": torch.randn((rows, e.num_kv_heads, d), generator=gen, device=device).to(torch.bfloat16),
-        "v_chunk": torch.randn((rows, e.num_kv_heads, d), generator=gen, device=device).to(torch.bfloat16),
+        "q": q,
+        "k_chunk": kc,
+        "v_chunk": vc,
         "k_prefix": e4m3_codes((e.prefix_rows, e.num_kv_heads, d), gen, device),
         "v_prefix": e4m3_codes((e.prefix_rows, e.num_kv_heads, d), gen, device),
     }
