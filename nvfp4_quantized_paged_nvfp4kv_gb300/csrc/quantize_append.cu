@@ -44,10 +44,13 @@ __device__ __forceinline__ bool site_of(const QuantParams &p, int slot, int h, i
 // slot is odd, so that consecutive slots (the usual prefill order) form the
 // record's token pairs; such a pair is written whole, any other token through
 // the atomic nibble merge.  Data loads are issued together with the slot
-// loads (the source offset does not depend on the slot).
+// loads (the source offset does not depend on the slot).  The value and
+// reciprocal of each block-scale byte come from a table in shared memory,
+// filled once per CTA while the loads are in flight.
 template <bool kBf16>
 __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const __grid_constant__ QuantParams p)
 {
+    __shared__ float2 scale_tab[128];
     pdl_wait();                  // the records may still be read by the previous kernel
     pdl_launch_dependents();
     const unsigned idx = blockIdx.x * blockDim.x + threadIdx.x;
@@ -59,10 +62,9 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const __grid_consta
     const int first = __ldg(p.slot_mapping);
     const int o = (is_v && first >= 0) ? (first & 1) : 0;
     const unsigned pairs = (static_cast<unsigned>(p.num_tokens) + o + 1) / 2;
-    if (pr >= pairs)
-        return;
     const int t0 = static_cast<int>(2 * pr) - o, t1 = t0 + 1;
-    const bool has0 = t0 >= 0, has1 = t1 < p.num_tokens;
+    const bool live = pr < pairs;
+    const bool has0 = live && t0 >= 0, has1 = live && t1 < p.num_tokens;
     const void *src = is_v ? p.v_new : p.k_new;
     RawBlock<kBf16> r0, r1;
     if (has0)
@@ -71,6 +73,11 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const __grid_consta
         load_raw<kBf16>(src, (static_cast<size_t>(t1) * p.hkv + h) * kHeadDim + blk * 16, r1);
     const int s0 = has0 ? __ldg(p.slot_mapping + t0) : -1;
     const int s1 = has1 ? __ldg(p.slot_mapping + t1) : -1;
+    fill_scale_table(scale_tab);
+    __syncthreads();
+    if (!live)
+        return;
+    const ScaleTable tab{scale_tab};
     size_t rec0 = 0, rec1 = 0;
     int tok0 = 0, tok1 = 0;
     const bool rep = !is_v && blk == 0 && h == 0;
@@ -82,22 +89,22 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const __grid_consta
         uint32_t S0, S1, c0[2], c1[2];
         unpack<kBf16>(r0, x);
         divide_by_tensor_scale(x, G);
-        quantize_block(x, S0, c0);
+        quantize_block(x, S0, c0, tab);
         unpack<kBf16>(r1, x);
         divide_by_tensor_scale(x, G);
-        quantize_block(x, S1, c1);
+        quantize_block(x, S1, c1, tab);
         write_nvfp4_v_pair(p.pool + rec0, tok0, blk, S0, c0, S1, c1);
         return;
     }
     if (ok0) {
         unpack<kBf16>(r0, x);
         divide_by_tensor_scale(x, G);
-        write_nvfp4_block(p.pool + rec0, is_v, tok0, blk, x);
+        write_nvfp4_block(p.pool + rec0, is_v, tok0, blk, x, tab);
     }
     if (ok1) {
         unpack<kBf16>(r1, x);
         divide_by_tensor_scale(x, G);
-        write_nvfp4_block(p.pool + rec1, is_v, tok1, blk, x);
+        write_nvfp4_block(p.pool + rec1, is_v, tok1, blk, x, tab);
     }
 }
 

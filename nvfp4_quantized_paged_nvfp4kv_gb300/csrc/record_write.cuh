@@ -63,17 +63,48 @@ __device__ __forceinline__ void divide_by_tensor_scale(float (&x)[16], float G)
     }
 }
 
+// The value s of an E4M3 block-scale byte S (0 .. 126) and RN(1/s) (0 for
+// s = 0), computed on the spot ...
+struct ScaleOfByte {
+    __device__ __forceinline__ float2 operator()(uint32_t S) const
+    {
+        const float sc = e4m3_to_f32(S);
+        return make_float2(sc, sc != 0.f ? __frcp_rn(sc) : 0.f);
+    }
+};
+
+// ... or read from a table of all 128 bytes in shared memory, filled by
+// fill_scale_table (the same values, computed once per CTA).
+struct ScaleTable {
+    const float2 *t;
+    __device__ __forceinline__ float2 operator()(uint32_t S) const { return t[S]; }
+};
+
+// Whole CTA (at least 128 threads' worth of entries are filled in a loop);
+// the caller synchronises the CTA before the first read.
+__device__ __forceinline__ void fill_scale_table(float2 *t)
+{
+    for (uint32_t i = threadIdx.x; i < 128u; i += blockDim.x)
+        t[i] = i < 127u ? ScaleOfByte()(i) : make_float2(0.f, 0.f);
+}
+
 // amax -> E4M3 block scale -> 16 E2M1 codes (code i in bits 4i .. 4i+3).
 //
 // The scale is decided on fl32(amax / 6) and each code on the IEEE quotient
-// fl32(x / s).  Both are computed
-// without a division per element: with r = RN(1/s), q0 = RN(x r) is within an
-// ulp of x / s, the remainder x - q0 s is exact through one FMA, and
-// RN(q0 + (x - q0 s) r) is the correctly rounded quotient (Markstein's
-// correction step).  s has at most four significant bits, so only eight
-// mantissas occur; every fp32 quotient in the range that decides a code is
-// compared against an IEEE division for all eight in the GPU tests.
-__device__ __forceinline__ void quantize_block(const float (&x)[16], uint32_t &scale_byte, uint32_t (&packed)[2])
+// fl32(x / s).  Both are computed without a division per element: with
+// r = RN(1/s), q0 = RN(x r) is within an ulp of x / s, the remainder x - q0 s
+// is exact through one FMA, and RN(q0 + (x - q0 s) r) is the correctly
+// rounded quotient (Markstein's correction step).  s has at most four
+// significant bits, so only eight mantissas occur; every fp32 quotient in the
+// range that decides a code is compared against an IEEE division for all eight
+// in the GPU tests.  The step runs on the negated terms -- q0' = RN(x (-r)),
+// e = RN(x + q0' s), q' = RN(q0' + e (-r)) = -RN(x / s) exactly -- because then
+// a zero quotient keeps the sign of x (a remainder that cancels to zero is +0,
+// and -0 + -0 is -0 where +0 + -0 would lose it); E2M1 rounding is symmetric,
+// so the codes of -q' are those of q' with each sign bit flipped.
+template <class ScaleFn = ScaleOfByte>
+__device__ __forceinline__ void quantize_block(const float (&x)[16], uint32_t &scale_byte, uint32_t (&packed)[2],
+                                               ScaleFn scale_of = ScaleFn())
 {
     // amax with three-input maxima (a NaN element is ignored, as by fmaxf);
     // capped at the largest finite float so the quotient below stays finite
@@ -91,34 +122,35 @@ __device__ __forceinline__ void quantize_block(const float (&x)[16], uint32_t &s
     const float d0 = __fmul_rn(amax, sixth);
     const float s32 = __fmaf_rn(__fmaf_rn(-d0, 6.0f, amax), sixth, d0);
     scale_byte = f32x2_to_e4m3x2(s32, 0.f) & 0xffu;
-    const float sc = e4m3_to_f32(scale_byte);
+    const float2 sr = scale_of(scale_byte);
+    const float sc = sr.x;
     packed[0] = packed[1] = 0u;
     if (sc != 0.f) {
         // the quotient step two lanes at a time (packed fp32, each lane IEEE)
-        const float r = __frcp_rn(sc);
-        const uint64_t r2 = f32x2_pack(r, r), nsc2 = f32x2_pack(-sc, -sc);
+        const uint64_t nr2 = f32x2_pack(-sr.y, -sr.y), sc2 = f32x2_pack(sc, sc);
         float q[16];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint64_t v2 = f32x2_pack(x[2 * j], x[2 * j + 1]);
-            const uint64_t q0 = mul_f32x2(v2, r2);
-            const uint64_t qq = fma_f32x2(fma_f32x2(q0, nsc2, v2), r2, q0);
-            // the correction step turns a -0 quotient into +0: restore the sign
-            q[2 * j] = copysignf(f32x2_lo(qq), x[2 * j]);
-            q[2 * j + 1] = copysignf(f32x2_hi(qq), x[2 * j + 1]);
+            const uint64_t q0 = mul_f32x2(v2, nr2);
+            const uint64_t qq = fma_f32x2(fma_f32x2(q0, sc2, v2), nr2, q0);
+            q[2 * j] = f32x2_lo(qq);
+            q[2 * j + 1] = f32x2_hi(qq);
         }
-        packed[0] = f32x8_to_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
-        packed[1] = f32x8_to_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
+        packed[0] = f32x8_to_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]) ^ 0x88888888u;
+        packed[1] = f32x8_to_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]) ^ 0x88888888u;
     }
 }
 
 // NVFP4: quantise x (block blk of token tok of the record) and write it.  K
 // rows are natural (one 8-byte store); a V block is merged into the 8 words
 // that hold its token pair with atomic AND/OR on the thread's own nibbles.
-__device__ __forceinline__ void write_nvfp4_block(uint8_t *rec, bool is_v, int tok, int blk, const float (&x)[16])
+template <class ScaleFn = ScaleOfByte>
+__device__ __forceinline__ void write_nvfp4_block(uint8_t *rec, bool is_v, int tok, int blk, const float (&x)[16],
+                                                  ScaleFn scale_of = ScaleFn())
 {
     uint32_t S, packed[2];
-    quantize_block(x, S, packed);
+    quantize_block(x, S, packed, scale_of);
     if (!is_v) {
         *reinterpret_cast<uint2 *>(rec + tok * 64 + blk * 8) = make_uint2(packed[0], packed[1]);
         rec[2048 + tok * 8 + blk] = static_cast<uint8_t>(S);
