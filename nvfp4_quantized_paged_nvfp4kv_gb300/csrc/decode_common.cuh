@@ -805,12 +805,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
 }
 
 // ---- split merge ---------------------------------------------------------------
-// One CTA of kMergeThreads threads per (sequence, kv head, query head of the
-// group).  Segments that one worker covered were written by the decode kernel;
-// empty sequences get zeros here.  128 threads at 72 registers let seven CTAs
-// share an SM, so a merge grid of up to 7 x 152 CTAs runs in one wave once the
-// decode CTAs have left.
-constexpr int kMergeThreads = 128;
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams p);
+// One CTA per (sequence, kv head, query head of the group), of kThreads
+// threads: 32 per contributor group.  Segments that one worker covered were
+// written by the decode kernel; empty sequences get zeros here.  The launch
+// picks the CTA width from the contributors a segment has on average: 128
+// threads (72 registers, seven CTAs to an SM, so a grid of up to 7 x 152 CTAs
+// runs in one wave once the decode CTAs have left) while four groups take a
+// segment's contributors in about one round of loads, wider CTAs for the few
+// long segments of a small batch at a long context.
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__ DecodeParams p);
 
 } // namespace nvfp4kv

@@ -8,14 +8,15 @@
 namespace nvfp4kv {
 
 // Thread t works on channels 4*(t%32) .. +3 of the CTA's query head for the
-// contributors k = t/32, t/32 + G, ... (G = kMergeThreads / 32 contributor
+// contributors k = t/32, t/32 + G, ... (G = kThreads / 32 contributor
 // groups, each loading kUnroll contributors ahead); each group keeps
 // its own running maximum (one pass over the partials), and the groups are
 // combined in shared memory at the end.  The segment's contributor range is
 // worked out once per CTA, before the wait for the decode kernel.
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams p)
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__ DecodeParams p)
 {
-    constexpr int kGroups = kMergeThreads / 32;
+    constexpr int kGroups = kThreads / 32;
     constexpr int kUnroll = 8;                   // contributors a thread loads before using any
     extern __shared__ int32_t msmem[];
     __shared__ float4 part[kGroups][32];
@@ -137,17 +138,36 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     }
 }
 
-cudaError_t launch_merge(const DecodeParams &p, cudaStream_t s)
+template <int kThreads>
+static cudaError_t launch_merge_width(const DecodeParams &p, cudaStream_t s)
 {
     const size_t smem = (kPrefixScratch + static_cast<size_t>(p.batch) + 1) * sizeof(int32_t);
     if (smem > 40 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(merge_kernel<kThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess)
             return e;
     }
-    return launch_pdl(merge_kernel, dim3(p.batch * p.hkv * p.row_groups, p.rows < kMaxGroup ? p.rows : kMaxGroup),
-                      dim3(kMergeThreads), smem, s, p);
+    return launch_pdl(merge_kernel<kThreads>,
+                      dim3(p.batch * p.hkv * p.row_groups, p.rows < kMaxGroup ? p.rows : kMaxGroup),
+                      dim3(kThreads), smem, s, p);
+}
+
+// Contributors per segment on average: the workers over the segments (a
+// segment's page-heads are its sequence's pages; lengths are on the device,
+// so equal lengths are assumed).  Each group of 32 threads loads eight
+// contributors per round; the width gives about one round.
+cudaError_t launch_merge(const DecodeParams &p, cudaStream_t s)
+{
+    const long long segments = static_cast<long long>(p.batch) * p.hkv * p.row_groups;
+    const long long per_segment = segments > 0 ? (p.num_workers + segments - 1) / segments : 1;
+    if (per_segment > 8 * 16)
+        return launch_merge_width<1024>(p, s);
+    if (per_segment > 8 * 8)
+        return launch_merge_width<512>(p, s);
+    if (per_segment > 8 * 4)
+        return launch_merge_width<256>(p, s);
+    return launch_merge_width<128>(p, s);
 }
 
 int sm_count()
