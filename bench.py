@@ -541,6 +541,21 @@ def run_ours(args, world, rank, local):
 HOST_COVER_CYCLES = 400_000
 
 
+class L2Flush:
+    """Evicts the timed call's inputs from L2 before each timed call: a
+    256 MB buffer is written (twice the L2), then a second one is read, so
+    that the dirty lines of the write are written back before the timed call
+    rather than inside it."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(32 << 20, dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        self.w.fill_(1)
+        self.r.sum()
+
+
 def other_rows(dev):
     """The write side and the extend path on the long-context workload: quantize_append
     of one 8192-token bf16 prefill chunk (Hkv=8) and dequant_prefix_fp8 of a
@@ -564,14 +579,14 @@ def other_rows(dev):
     vf = torch.empty_like(kf)
     pl = torch.tensor([L], dtype=torch.int32, device=dev)
     ip = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def timed(fn):
         for _ in range(3):
             fn()
         ms = []
         for _ in range(20):
-            flush.fill_(1)                                   # evict the inputs from L2
+            flush()                                          # evict the inputs from L2
             torch.cuda._sleep(HOST_COVER_CYCLES)             # the GPU waits here, not on the host launch
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
@@ -581,9 +596,32 @@ def other_rows(dev):
             ms.append(a.elapsed_time(b))
         return statistics.mean(ms)
 
-    q_ms = timed(lambda: nv.nvfp4kv_quantize_append(cache, k, v, sm))
+    # Back to back, as in a prefill loop: the mean of n calls between two
+    # events (a single short call's event interval is quantised to ~2 us on
+    # this GPU).  Each quantize call reads its own copy of the 8K-token rows,
+    # rotated among enough copies that none is still in L2 when it comes round.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(2, math.ceil(3 * l2 / (2 * k.numel() * k.element_size())) + 1)
+    kv_copies = [(k.clone(), v.clone()) for _ in range(copies)]
+
+    def back_to_back(call, n=2 * copies):
+        for i in range(3):
+            call(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(n):
+            call(i)
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    def quantize_into(c):
+        return lambda i: nv.nvfp4kv_quantize_append(c, kv_copies[i % copies][0], kv_copies[i % copies][1], sm)
+
+    q_ms = back_to_back(quantize_into(cache))
     q_bytes = T * w.num_kv_heads * (2 * 128 * 2 + NVFP4_BYTES_PER_TOKEN_HEAD) + T * 4
-    p_ms = timed(lambda: nv.nvfp4kv_dequant_prefix_fp8(cache, bt_d, pl, ip, kf, vf))
+    p_ms = back_to_back(lambda i: nv.nvfp4kv_dequant_prefix_fp8(cache, bt_d, pl, ip, kf, vf), n=10)
     p_bytes = L * w.num_kv_heads * (NVFP4_BYTES_PER_TOKEN_HEAD + 2 * 128)
     # the same cache read as one with a calibrated tensor scale G = 0.37: the
     # decode of the 160K sequence and the quantise path cost what G = 1 costs
@@ -592,14 +630,15 @@ def other_rows(dev):
     sl = torch.tensor([L], dtype=torch.int32, device=dev)
     out = torch.empty((1, w.num_q_heads, 128), dtype=torch.bfloat16, device=dev)
     ws = nv.new_workspace(device=dev)
-    d1_ms = timed(lambda: nv.nvfp4kv_paged_decode(cache, q, bt_d, sl, out, ws))
-    dg_ms = timed(lambda: nv.nvfp4kv_paged_decode(cache_g, q, bt_d, sl, out, ws))
-    qg_ms = timed(lambda: nv.nvfp4kv_quantize_append(cache_g, k, v, sm))
+    d1_ms = back_to_back(lambda i: nv.nvfp4kv_paged_decode(cache, q, bt_d, sl, out, ws), n=20)
+    dg_ms = back_to_back(lambda i: nv.nvfp4kv_paged_decode(cache_g, q, bt_d, sl, out, ws), n=20)
+    qg_ms = back_to_back(quantize_into(cache_g))
     # and with per-head factors on top (K and V of each kv head their own scale)
     factors = [[0.5 + 0.25 * h for h in range(w.num_kv_heads)], [2.0 - 0.2 * h for h in range(w.num_kv_heads)]]
     cache_h = nv.NVFP4Cache(cache.pool, global_scale=0.37, head_scales=factors)
-    dh_ms = timed(lambda: nv.nvfp4kv_paged_decode(cache_h, q, bt_d, sl, out, ws))
-    qh_ms = timed(lambda: nv.nvfp4kv_quantize_append(cache_h, k, v, sm))
+    dh_ms = back_to_back(lambda i: nv.nvfp4kv_paged_decode(cache_h, q, bt_d, sl, out, ws), n=20)
+    qh_ms = back_to_back(quantize_into(cache_h))
+    del kv_copies
     d_bytes = L * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
     multi = multi_query_rows(dev, timed)
     extend = extend_rows(dev)
@@ -617,21 +656,23 @@ def other_rows(dev):
         "multi_query": multi,
         "extend_160k_chunk8k": extend,
         "prefill_fp8_8k": prefill,
-        "timing": "CUDA events per call, 256 MB buffer written and a GPU spin before each call (L2 evicted, "
-                  "host launch hidden)",
+        "timing": "quantize, prefix and 160K decode rows: calls back to back between two CUDA events, the "
+                  "quantize inputs rotated among copies totalling over 3x L2 (the other inputs exceed L2); "
+                  "multi-query rows: one call per event pair after a 256 MB write and a 256 MB read (L2 "
+                  "evicted) and a GPU spin covering the host launch",
     }
 
 
 def write_side_row(dev, name: str, steps: int, warmup: int):
     """One write-side row alone: quantize_append of 8,192 bf16 tokens (Hkv 8)
     into a 163,840-token cache, or dequant_prefix_fp8 of that 163,840-token
-    prefix; CUDA events per call, a 256 MB buffer written before each call."""
+    prefix; CUDA events per call, L2 evicted before each call (L2Flush)."""
     import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
     w = workloads.make("ctx160k", batch=1)
     bt, num_pages = workloads.block_table(w)
     cache = nv.NVFP4Cache.allocate(num_pages, w.num_kv_heads, device=dev, zero=False)
     L = w.seq_lens[0]
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     if name == "quantize8k":
         T = 8192
         k = workloads.kv_rows(w, "k", 0, 0, T, device=dev).to(torch.bfloat16)
@@ -656,7 +697,7 @@ def write_side_row(dev, name: str, steps: int, warmup: int):
         fn()
     ms = []
     for _ in range(steps):
-        flush.fill_(1)
+        flush()
         torch.cuda._sleep(HOST_COVER_CYCLES)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
