@@ -71,7 +71,8 @@ def parse():
     ap.add_argument("--no-decode-rows", action="store_true",
                     help="skip the decode rows of the other workloads")
     ap.add_argument("--row-only", default=None,
-                    choices=["ext160k", "ext8k_c2k", "quantize8k", "prefix160k", "prefill8k"],
+                    choices=["ext160k", "ext8k_c2k", "ext160k_e4m3", "ext8k_c2k_e4m3", "quantize8k", "prefix160k",
+                             "prefill8k"],
                     help="time only this row (extend attention on a workload, quantize_append of 8,192 "
                          "bf16 tokens, dequant_prefix_fp8 of a 163,840-token prefix, or FP8 initial prefill "
                          "of 8,192 tokens) and print it")
@@ -642,6 +643,7 @@ def other_rows(dev):
     d_bytes = L * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
     multi = multi_query_rows(dev, timed)
     extend = extend_rows(dev)
+    extend8 = extend_rows(dev, chunk="e4m3")
     prefill = prefill_rows(dev)
     return {
         "quantize_append_8k_bf16": {"us": q_ms * 1e3, "tokens_per_s": T / (q_ms / 1e3),
@@ -655,6 +657,7 @@ def other_rows(dev):
                                                    "quantize_append_8k_bf16_us": qh_ms * 1e3}},
         "multi_query": multi,
         "extend_160k_chunk8k": extend,
+        "extend_160k_chunk8k_e4m3": extend8,
         "prefill_fp8_8k": prefill,
         "timing": "quantize, prefix and 160K decode rows: calls back to back between two CUDA events, the "
                   "quantize inputs rotated among copies totalling over 3x L2 (the other inputs exceed L2); "
@@ -720,15 +723,17 @@ def extend_flops(e) -> float:
     return 4.0 * e.head_dim * e.num_q_heads * tot
 
 
-def extend_rows(dev, name: str = "ext160k", steps: int = 5, warmup: int = 3, compare_fused: bool = True):
+def extend_rows(dev, name: str = "ext160k", steps: int = 5, warmup: int = 3, compare_fused: bool = True,
+                chunk: str = "bf16"):
     """Extend attention of the last 8,192-token chunk of a 163,840-token
     prefill (Hq 48, Hkv 8) over the 155,648-row FP8 prefix workspace (319 MB,
-    larger than L2) and the chunk, bf16 out; mean of `steps` launches after
-    `warmup`, CUDA events on the launching stream.  Then the same step fused
-    with the NVFP4 write of the chunk against attention + quantize_append."""
+    larger than L2) and the chunk (bf16, or E4M3 as the pages' FP8 prefill
+    has it), bf16 out; mean of `steps` launches after `warmup`, CUDA events on
+    the launching stream.  Then the same step fused with the NVFP4 write of
+    the chunk against attention + quantize_append."""
     import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
     e = workloads.extend_make(name)
-    x = workloads.extend_inputs(e, device=dev)
+    x = workloads.extend_inputs(e, device=dev, chunk=chunk)
     out = torch.empty((e.q_rows, e.num_q_heads, e.head_dim), dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     mql = max(e.chunk_lens)
@@ -755,11 +760,13 @@ def extend_rows(dev, name: str = "ext160k", steps: int = 5, warmup: int = 3, com
     if peak is None:
         peak, src = 1900.0, "fallback"
     tf = flops / (t / 1e3) / 1e12
-    row = {"workload": name, "us": t * 1e3, "chunk_tokens_per_s": e.q_rows / (t / 1e3), "alg_tflops": tf,
-           "alg_flops": flops, "bound": "tensor", "peak_tflops": peak, "peak_source": src, "frac": tf / peak,
-           "mma": "tcgen05.mma kind::f16 M128 (f16 operands, fp32 accumulators in tensor memory); peak: measured "
-                  "bf16 dense burst, the same tensor rate as f16",
-           "traffic": profiled_traffic("extend_attention", name)}
+    mma = ("tcgen05.mma kind::f16 M128 (f16 operands, fp32 accumulators in tensor memory)" if chunk == "bf16" else
+           "tcgen05.mma M128: Q K^T kind::f8f6f4 (E4M3 key tiles by TMA, Q as three E4M3 terms), P V kind::f16; "
+           "fp32 accumulators in tensor memory")
+    row = {"workload": name, "chunk": chunk, "us": t * 1e3, "chunk_tokens_per_s": e.q_rows / (t / 1e3),
+           "alg_tflops": tf, "alg_flops": flops, "bound": "tensor", "peak_tflops": peak, "peak_source": src,
+           "frac": tf / peak, "mma": mma + "; peak: measured bf16 dense burst",
+           "traffic": profiled_traffic("extend_attention", name) if chunk == "bf16" else None}
     if not compare_fused:
         row["device_status"] = int(status.item())
         return row
@@ -775,9 +782,14 @@ def extend_rows(dev, name: str = "ext160k", steps: int = 5, warmup: int = 3, com
     def fused():
         nv.nvfp4kv_extend_attention_fp8_append(cache, slots, *args, max_q_len=mql, dev_status=status)
 
+    # the separate write quantises the same values (E4M3 codes held exactly in bf16)
+    kq, vq = ((x["k_chunk"].view(torch.float8_e4m3fn).to(torch.bfloat16),
+               x["v_chunk"].view(torch.float8_e4m3fn).to(torch.bfloat16)) if chunk == "e4m3" else
+              (x["k_chunk"], x["v_chunk"]))
+
     def separate():
         nv.nvfp4kv_extend_attention_fp8(*args, max_q_len=mql, dev_status=status)
-        nv.nvfp4kv_quantize_append(cache, x["k_chunk"], x["v_chunk"], slots, status)
+        nv.nvfp4kv_quantize_append(cache, kq, vq, slots, status)
 
     def mean_ms(fn):
         for _ in range(2):
@@ -999,7 +1011,8 @@ def main():
         if args.row_only == "prefill8k":
             row = prefill_rows(dev, steps=args.steps, warmup=warm)
         elif args.row_only.startswith("ext"):
-            row = extend_rows(dev, args.row_only, steps=args.steps, warmup=warm, compare_fused=False)
+            row = extend_rows(dev, args.row_only.replace("_e4m3", ""), steps=args.steps, warmup=warm,
+                              compare_fused=False, chunk="e4m3" if args.row_only.endswith("_e4m3") else "bf16")
         else:
             row = write_side_row(dev, args.row_only, args.steps, warm)
         print(json.dumps(row))

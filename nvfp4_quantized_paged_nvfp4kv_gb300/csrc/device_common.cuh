@@ -250,34 +250,41 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
 }
 
 // ---- shared loads ----------------------------------------------------------
+//
+// Each carries a "memory" clobber: the data they read is written by bulk
+// copies, TMA loads or other threads, and the loads must stay between the
+// barrier wait that makes it valid and the arrive that releases the buffer
+// (the compiler does not know what an asm reads and may otherwise move it
+// across either).
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
+                 : "r"(addr)
+                 : "memory");
     return v;
 }
 
 __device__ __forceinline__ uint2 lds64(uint32_t addr)
 {
     uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
     return v;
 }
 
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr)
 {
     uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
     return v;
 }
 
 __device__ __forceinline__ uint32_t lds_u8(uint32_t addr)
 {
     uint32_t v;
-    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 

@@ -28,6 +28,10 @@
 // ("SGLang stores KV cache in 4 bits", Interpretation: prefill quantises the
 // new K/V into the cache): each chunk key tile has one owning CTA, whose
 // converter warps quantise it after their last key tile.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "record_write.cuh"
 #include "tcgen05.cuh"
 
@@ -360,6 +364,43 @@ __device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const T
     }
 }
 
+// Softmax thread of row `row` (tensor-memory lane base lane_base): O / l to
+// the output row, once the last value product has landed (the warp together:
+// tensor-memory loads are warp-wide).
+__device__ __forceinline__ void store_out_row(const ExtendParams &p, const TcCta &c, int h, int row, int R, int g,
+                                              int t, uint32_t lane_base, float l)
+{
+    tc_fence_after_sync();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const bool store = row < R;
+    const int64_t off = (static_cast<int64_t>(c.c0 + t) * p.hq + h * g + (min(row, R - 1) - t * g)) * kHeadDim;
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + kColO + 32 * cb, o);
+        tmem_wait_ld();
+        if (!store)
+            continue;
+        if (p.out_f32) {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off + 32 * cb);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                     __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+        } else {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + off + 32 * cb);
+            auto bf2 = [&](int j) {
+                const __nv_bfloat162 two =
+                    __floats2bfloat162_rn(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
+                return *reinterpret_cast<const uint32_t *>(&two);
+            };
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                dst[k] = make_uint4(bf2(8 * k), bf2(8 * k + 2), bf2(8 * k + 4), bf2(8 * k + 6));
+        }
+    }
+}
+
 template <bool kAppend, bool kChunk8>
 __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_constant__ ExtendParams p)
 {
@@ -611,37 +652,424 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
             const int last = c.n_tiles - 1;
             ok = wait_warp(bar + 8 * (kBarPvDone + (last & 1)), (last >> 1) & 1);
         }
-        if (ok) {
-            tc_fence_after_sync();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const bool store = row < R;
-            const int64_t off = (static_cast<int64_t>(c.c0 + t) * p.hq + h * g + (min(row, R - 1) - t * g)) * kHeadDim;
+        if (ok)
+            store_out_row(p, c, h, row, R, g, t, lane_base, l);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---- all keys in E4M3: Q K^T on kind::f8f6f4 with the key tiles from TMA ----
+//
+// When the chunk's keys and values are E4M3 too (initial prefill and extends
+// on FP8 K/V), every key tile is E4M3 bytes, one 128-byte row per key: the
+// TMA unit loads a 64-key tile of one kv head straight into the 128-byte
+// swizzle the MMA reads, and S = Q K^T runs as tcgen05.mma kind::f8f6f4 with
+// Q split into three E4M3 terms (hi, mid, lo), all accumulated into S.  Each
+// row of Q is first multiplied by a power of two 2^e_r that puts its largest
+// element in [128, 256); the softmax takes S * 2^-e_r.  The three terms carry
+// about twelve significant bits of q (each term rounds the remainder of the
+// ones before it to E4M3), against f16's eleven.  Values stay on the f16
+// path: the TMA unit loads the E4M3 value tile into a staging buffer, the
+// converter warps turn it into the f16 operand of P V (rows past the
+// sequence's keys become zeros), and P V runs on kind::f16 as in the kernel
+// above.  Warp 9 issues the TMA loads.
+constexpr int kF8Threads = kTcThreads + 32;                 // + the TMA warp
+constexpr int kF8TmaWarp = 9;
+constexpr uint32_t kF8QTerm = kTcRows * kHeadDim;           // 16 KB per E4M3 term
+constexpr uint32_t kF8KBytes = kTcKeys * kHeadDim;          // 8 KB per E4M3 key tile
+constexpr uint32_t kF8OffQ = 0;                             // three terms
+constexpr uint32_t kF8OffK = kF8OffQ + 3 * kF8QTerm;        // two stages
+constexpr uint32_t kF8OffV = kF8OffK + 2 * kF8KBytes;       // two f16 stages (kKVBytes each)
+constexpr uint32_t kF8OffVraw = kF8OffV + 2 * kKVBytes;     // one E4M3 staging tile
+constexpr uint32_t kF8OffBar = kF8OffVraw + kF8KBytes;
+enum {
+    kF8KFull = 0, kF8KvEmpty = 2, kF8VrawFull = 4, kF8VrawEmpty = 5, kF8VFull = 6, kF8SFull = 8, kF8PFull = 10,
+    kF8PvDone = 12, kF8Done = 14, kF8NumBars = 15
+};
+constexpr uint32_t kF8OffRowInv = kF8OffBar + 8 * kF8NumBars + 8;     // 16-byte aligned
+constexpr uint32_t kF8OffTmemSlot = kF8OffRowInv + 4 * kTcRows;
+constexpr uint32_t kF8OffFail = kF8OffTmemSlot + 4;
+constexpr uint32_t kF8Smem = kF8OffFail + 4 + 1024;
+static_assert(kF8OffRowInv % 16 == 0, "row scale table alignment");
+static_assert(kF8OffK % 1024 == 0 && kF8OffV % 1024 == 0 && kF8OffVraw % 1024 == 0, "swizzle atoms");
+static_assert(2 * (kF8Smem + 1024) <= 228 * 1024, "two CTAs per SM");
+
+// Two fp32 -> E4M3 bytes and back to fp32, exactly (the decode is exact).
+__device__ __forceinline__ float2 e4m3x2_value(uint32_t two)
+{
+    const uint32_t h = e4m3x2_to_f16x2(two);
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+
+template <bool kAppend>
+__global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_constant__ ExtendParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw_addr);
+    volatile int *fail = reinterpret_cast<volatile int *>(gbase + kF8OffFail);
+    float *rowinv = reinterpret_cast<float *>(gbase + kF8OffRowInv);
+    const uint32_t bar = base + kF8OffBar;
+    auto B = [&](int k) { return bar + 8 * k; };
+
+    const int b_seq = blockIdx.z;
+    const int h = blockIdx.y;
+    const int tile = static_cast<int>(gridDim.x - 1 - blockIdx.x);  // later rows see more keys: start them first
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+
+    TcCta c;
+    c.c0 = p.q_indptr[b_seq];
+    const int c1 = p.q_indptr[b_seq + 1];
+    c.P = p.prefix_lens[b_seq];
+    const int kv0 = p.kv_indptr[b_seq];
+    if (c.c0 < 0 || c1 < c.c0 || c1 > p.q_rows || c1 - c.c0 > p.max_q_len || c.P < 0 || kv0 < 0 ||
+        static_cast<int64_t>(kv0) + c.P > p.prefix_rows) {
+        if (tid == 0)
+            report(p.dev_status, NVFP4KV_DEV_BAD_LEN);
+        return;
+    }
+    c.C = c1 - c.c0;
+    c.p0 = kv0;
+    const int g = p.group;
+    const int R = c.C * g;
+    const int row0 = tile * kTcRows;
+    if (row0 >= R)
+        return;
+    const int t_max = (min(row0 + kTcRows, R) - 1) / g;
+    c.n_pre = (c.P + kTcKeys - 1) / kTcKeys;
+    c.n_tiles = c.n_pre + t_max / kTcKeys + 1;
+
+    // Q as three E4M3 terms, each row scaled by a power of two first.  Sixteen
+    // consecutive lanes hold one row (eight channels each): the CTA's threads
+    // cover the 2,048 pieces in whole warps, so the row maximum is a shuffle
+    // over those lanes.
+    for (int idx0 = warp * 32; idx0 < kTcRows * 16; idx0 += kF8Threads) {
+        const int idx = idx0 + lane;
+        const int r = idx >> 4, piece = idx & 15;
+        const int row = row0 + r;
+        float x[8];
+        if (row < R) {
+            const int t = row / g;
+            const uint4 w = ldg_nc(p.q + (static_cast<int64_t>(c.c0 + t) * p.hq + h * g + (row - t * g)) * kHeadDim +
+                                   8 * piece);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t o[32];
-                tmem_ld32(lane_base + kColO + 32 * cb, o);
-                tmem_wait_ld();
-                if (!store)
-                    continue;
-                if (p.out_f32) {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off + 32 * cb);
+            for (int k = 0; k < 4; ++k) {
+                x[2 * k] = __uint_as_float(ww[k] << 16) * p.qscale;
+                x[2 * k + 1] = __uint_as_float(ww[k] & 0xffff0000u) * p.qscale;
+            }
+        } else {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                             __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
-                } else {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + off + 32 * cb);
-                    auto bf2 = [&](int j) {
-                        const __nv_bfloat162 two =
-                            __floats2bfloat162_rn(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
-                        return *reinterpret_cast<const uint32_t *>(&two);
-                    };
+            for (int k = 0; k < 8; ++k)
+                x[k] = 0.f;
+        }
+        float am = 0.f;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_uint4(bf2(8 * k), bf2(8 * k + 2), bf2(8 * k + 4), bf2(8 * k + 6));
-                }
+        for (int k = 0; k < 8; ++k)
+            am = fmaxf(am, fabsf(x[k]));
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1)
+            am = fmaxf(am, __shfl_xor_sync(kFullMask, am, o));
+        // 2^e with amax * 2^e in [128, 256); rows of (almost) zeros keep scale 1
+        int e = 0;
+        if (am >= 1e-30f)
+            e = 7 - (static_cast<int>((__float_as_uint(am) >> 23) & 0xffu) - 127);
+        const float sc = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+        if (piece == 0)
+            rowinv[r] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+        uint32_t term[3][2];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float a = x[2 * k] * sc, b = x[2 * k + 1] * sc;
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+                const uint32_t two = f32x2_to_e4m3x2(a, b);
+                const float2 v = e4m3x2_value(two);
+                a -= v.x;                         // exact: the remainder of an E4M3 rounding
+                b -= v.y;
+                if (k & 1)
+                    term[t][k >> 1] |= two << 16;
+                else
+                    term[t][k >> 1] = two;
             }
         }
+        const uint32_t off = r * 128u + ((static_cast<uint32_t>(piece >> 1) ^ (r & 7u)) << 4) + (piece & 1) * 8u;
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(base + kF8OffQ + t * kF8QTerm + off),
+                         "r"(term[t][0]), "r"(term[t][1])
+                         : "memory");
+    }
+    if (tid == 0) {
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(B(kF8KFull + k), 1);
+            mbar_init(B(kF8KvEmpty + k), 1);
+            mbar_init(B(kF8VFull + k), kProducerThreads);
+            mbar_init(B(kF8SFull + k), 1);
+            mbar_init(B(kF8PFull + k), kSoftmaxThreads);
+            mbar_init(B(kF8PvDone + k), 1);
+        }
+        mbar_init(B(kF8VrawFull), 1);
+        mbar_init(B(kF8VrawEmpty), kProducerThreads);
+        mbar_init(B(kF8Done), 1);
+        *fail = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp)
+        tmem_alloc(base + kF8OffTmemSlot, kTmemCols);
+    fence_async_shared();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + kF8OffTmemSlot);
+
+    if (warp == kF8TmaWarp) {
+        if (lane == 0) {
+            // key tile i: K into stage i % 2, V into the staging tile
+            int issued = 0;
+            for (int i = 0; i < c.n_tiles; ++i) {
+                const int st = i & 1;
+                const bool pre = i < c.n_pre;
+                const int rowc = pre ? static_cast<int>(c.p0) + i * kTcKeys : c.c0 + (i - c.n_pre) * kTcKeys;
+                // the stage was last read by the MMAs of tile i - 2
+                if (i >= 2 && !wait_or_fail(B(kF8KvEmpty + st), ((i >> 1) - 1) & 1, fail, p.dev_status, p.wait_limit))
+                    break;
+                mbar_arrive_expect_tx(B(kF8KFull + st), kF8KBytes);
+                tma_load_3d(base + kF8OffK + st * kF8KBytes, pre ? &p.tm_k_prefix : &p.tm_k_chunk, 0, h, rowc,
+                            B(kF8KFull + st));
+                // the staging tile was last read by the converters for tile i - 1
+                if (i >= 1 && !wait_or_fail(B(kF8VrawEmpty), (i - 1) & 1, fail, p.dev_status, p.wait_limit)) {
+                    issued = 2 * i + 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(B(kF8VrawFull), kF8KBytes);
+                tma_load_3d(base + kF8OffVraw, pre ? &p.tm_v_prefix : &p.tm_v_chunk, 0, h, rowc, B(kF8VrawFull));
+                issued = 2 * i + 2;
+            }
+            // nothing issued may still be in flight when the CTA exits: the
+            // last two K tiles and the last staging tile (earlier ones were
+            // waited for before their buffers were reused)
+            const int nk = (issued + 1) >> 1, nv = issued >> 1;
+            for (int i = max(0, nk - 2); i < nk; ++i)
+                if (!mbar_wait_bounded(B(kF8KFull + (i & 1)), (i >> 1) & 1, kWaitLimit))
+                    report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
+            if (nv > 0 && !mbar_wait_bounded(B(kF8VrawFull), (nv - 1) & 1, kWaitLimit))
+                report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            constexpr uint32_t i_qk = idesc_f16(kTcRows, kTcKeys, false);   // E4M3 x E4M3 -> f32 (same bits)
+            constexpr uint32_t i_pv = idesc_f16(kTcRows, kHeadDim, true);
+            bool ok = true;
+            auto qk = [&](int i) {
+                const int b = i & 1, st = i & 1;
+                tc_fence_after_sync();
+                const uint32_t kb = base + kF8OffK + st * kF8KBytes;
+#pragma unroll
+                for (int t = 0; t < 3; ++t)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_f8(tmem + kColS + b * kTcKeys,
+                                smem_desc(base + kF8OffQ + t * kF8QTerm + ks * 32, 16, 1024),
+                                smem_desc(kb + ks * 32, 16, 1024), i_qk, t > 0 || ks > 0);
+                umma_commit(B(kF8SFull + b));
+            };
+            auto pv = [&](int i) {
+                const int b = i & 1, st = i & 1;
+                tc_fence_after_sync();
+                const uint32_t vb = base + kF8OffV + st * kKVBytes;
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    umma_f16_ts(tmem + kColO, tmem + kColP + b * kColPStride + s * 8,
+                                smem_desc(vb + s * 2048, kTcKeys * 128, 1024), i_pv, i > 0 || s > 0);
+                umma_commit(B(kF8PvDone + b));
+                umma_commit(B(kF8KvEmpty + st));
+            };
+            // Q K^T of tile j once its keys are in and tile j - 2's P V is
+            // issued; P V of tile i once its P and its converted values are
+            // in; whichever is ready first goes first.
+            int next_qk = 0;
+            for (int i = 0; ok && i < c.n_tiles; ++i) {
+                const int b = i & 1;
+                bool pv_done = false;
+                for (uint64_t polls = 0; !pv_done;) {
+                    bool progress = false;
+                    if (next_qk <= i + 1 && next_qk < c.n_tiles &&
+                        mbar_test_wait(B(kF8KFull + (next_qk & 1)), (next_qk >> 1) & 1)) {
+                        qk(next_qk++);
+                        progress = true;
+                    }
+                    if (next_qk > i && mbar_test_wait(B(kF8PFull + b), (i >> 1) & 1) &&
+                        mbar_test_wait(B(kF8VFull + b), (i >> 1) & 1)) {
+                        pv(i);
+                        pv_done = progress = true;
+                    }
+                    if (progress)
+                        continue;
+                    if (++polls > 64ull * p.wait_limit || *fail) {
+                        if (!*fail) {
+                            *fail = 1;
+                            report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
+                        }
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            // nothing of this thread's may still run when tensor memory is freed
+            // (waited for at the default limit, whatever p.wait_limit is)
+            umma_commit(B(kF8Done));
+            if (!mbar_wait_bounded(B(kF8Done), 0, kWaitLimit))
+                report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp >= kSoftmaxThreads / 32) {
+        // converters: thread pt turns half a row of the staged E4M3 value tile
+        // (key pt / 2, channels 64 (pt % 2) .. + 63) into f16
+        const int pt = tid - kSoftmaxThreads;
+        const int key = pt >> 1, half = pt & 1;
+        for (int i = 0; i < c.n_tiles; ++i) {
+            const int st = i & 1;
+            const int lim = i < c.n_pre ? c.P - i * kTcKeys : c.C - (i - c.n_pre) * kTcKeys;
+            if (!wait_or_fail(B(kF8VrawFull), i & 1, fail, p.dev_status, p.wait_limit))
+                break;
+            uint4 raw[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+                raw[jj] = lds128(base + kF8OffVraw + key * 128u +
+                                 ((static_cast<uint32_t>(4 * half + jj) ^ (key & 7u)) << 4));
+            // the next TMA load (async proxy) overwrites the staging tile these
+            // generic-proxy reads come from: a proxy fence orders the reads
+            // before the release, as a plain arrive does not across proxies
+            fence_async_shared();
+            mbar_arrive(B(kF8VrawEmpty));
+            // the f16 stage was last read by the MMAs of tile i - 2
+            if (i >= 2 && !wait_or_fail(B(kF8KvEmpty + st), ((i >> 1) - 1) & 1, fail, p.dev_status, p.wait_limit))
+                break;
+            const uint32_t dst = base + kF8OffV + st * kKVBytes;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+                if (key < lim) {
+                    e4m3x4_to_f16x2x2(raw[jj].x, lo.x, lo.y);
+                    e4m3x4_to_f16x2x2(raw[jj].y, lo.z, lo.w);
+                    e4m3x4_to_f16x2x2(raw[jj].z, hi.x, hi.y);
+                    e4m3x4_to_f16x2x2(raw[jj].w, hi.z, hi.w);
+                }
+                const int cch = 8 * half + 2 * jj;       // 16-byte f16 chunk index over the 128 channels
+                sts128(dst + sw128(kTcKeys, key, cch), lo);
+                sts128(dst + sw128(kTcKeys, key, cch + 1), hi);
+            }
+            fence_async_shared();
+            mbar_arrive(B(kF8VFull + st));
+        }
+        if constexpr (kAppend) {
+            const int per = kTcKeys * g;
+            for (int kt = (row0 + per - 1) / per; kt < (row0 + kTcRows + per - 1) / per && kt * kTcKeys < c.C; ++kt)
+                append_chunk_tile<true>(p, c, h, kt * kTcKeys, pt);
+        }
+    } else {
+        // softmax: thread r owns row row0 + r, tensor-memory lane r; scores are
+        // S * 2^-e_r
+        const int r = tid;
+        const int row = row0 + r;
+        const int t = min(row, R - 1) / g;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const float inv = rowinv[r];
+        const uint64_t inv2 = f32x2_pack(inv, inv);
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        auto wait_warp = [&](uint32_t bar_addr, uint32_t parity) {
+            return __all_sync(kFullMask, wait_or_fail(bar_addr, parity, fail, p.dev_status, p.wait_limit));
+        };
+        for (int i = 0; i < c.n_tiles; ++i) {
+            const int b = i & 1;
+            if (!(ok = wait_warp(B(kF8SFull + b), (i >> 1) & 1)))
+                break;
+            tc_fence_after_sync();
+            uint32_t sr0[32], sr1[32];
+            tmem_ld32(lane_base + kColS + b * kTcKeys, sr0);
+            tmem_ld32(lane_base + kColS + b * kTcKeys + 32, sr1);
+            tmem_wait_ld();
+            float s[64];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                s[j] = __uint_as_float(sr0[j]);
+                s[j + 32] = __uint_as_float(sr1[j]);
+            }
+            const int lim = i < c.n_pre ? c.P - i * kTcKeys : t + 1 - (i - c.n_pre) * kTcKeys;
+            if (lim < kTcKeys) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    if (j >= lim)
+                        s[j] = -INFINITY;
+            }
+            float pm[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                pm[k] = fmax3(fmax3(s[8 * k], s[8 * k + 1], s[8 * k + 2]), fmax3(s[8 * k + 3], s[8 * k + 4], s[8 * k + 5]),
+                              fmaxf(s[8 * k + 6], s[8 * k + 7]));
+            const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7])) * inv;
+            const bool need = mx > m_used + kRescaleLog2;
+            const float m_new = need ? mx : m_used;
+            const float mbase = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = need ? fast_exp2(m_used - mbase) : 1.f;
+            const uint64_t neg2 = f32x2_pack(-mbase, -mbase);
+            uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const uint64_t d = fma_f32x2(f32x2_pack(s[2 * j], s[2 * j + 1]), inv2, neg2);
+                s[2 * j] = fast_exp2(f32x2_lo(d));
+                s[2 * j + 1] = fast_exp2(f32x2_hi(d));
+                acc[j & 3] = add_f32x2(acc[j & 3], f32x2_pack(s[2 * j], s[2 * j + 1]));
+            }
+            const uint64_t a01 = add_f32x2(acc[0], acc[1]), a23 = add_f32x2(acc[2], acc[3]);
+            const uint64_t a = add_f32x2(a01, a23);
+            const float sum = f32x2_lo(a) + f32x2_hi(a);
+            l = l * alpha + sum;
+            m_used = m_new;
+            {
+                uint32_t pw[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    pw[j] = pack_f16x2(s[2 * j], s[2 * j + 1]);
+                tmem_st32(lane_base + kColP + b * kColPStride, pw);
+            }
+            if (__any_sync(kFullMask, need) && i >= 1) {
+                const int pb = (i - 1) & 1;
+                if (!(ok = wait_warp(B(kF8PvDone + pb), ((i - 1) >> 1) & 1)))
+                    break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + kColO + 32 * cb, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                    tmem_st32(lane_base + kColO + 32 * cb, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            mbar_arrive(B(kF8PFull + b));
+        }
+        if (ok) {
+            const int last = c.n_tiles - 1;
+            ok = wait_warp(B(kF8PvDone + (last & 1)), (last >> 1) & 1);
+        }
+        if (ok)
+            store_out_row(p, c, h, row, R, g, t, lane_base, l);
     }
 
     tc_fence_before_sync();
@@ -654,15 +1082,82 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
 
 } // namespace
 
+namespace {
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// E4M3 rows [rows][hkv][128] as a 3-D tensor (bytes, head, row), read in
+// boxes of 64 rows of one head in the 128-byte swizzle; rows outside read as
+// zeros.
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, const void *base, int64_t rows, int hkv)
+{
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(hkv),
+                                static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(hkv) * kHeadDim};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1u, static_cast<cuuint32_t>(kTcKeys)};
+    const cuuint32_t elem[3] = {1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, elem,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor maps of the all-E4M3 kernel, or false when that kernel cannot
+// run (no encoder, or row coordinates beyond 32 bits).
+bool fill_tensor_maps(ExtendParams &q)
+{
+    constexpr int64_t kMaxRows = (int64_t{1} << 31) - 2 * kTcKeys;
+    if (q.prefix_rows >= kMaxRows || q.q_rows >= kMaxRows || q.q_rows < 1)
+        return false;
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr)
+        return false;
+    // with no prefix rows no prefix tile is ever loaded: the chunk rows stand in
+    const bool has_prefix = q.prefix_rows > 0;
+    const void *kp = has_prefix ? static_cast<const void *>(q.k_prefix) : q.k_chunk;
+    const void *vp = has_prefix ? static_cast<const void *>(q.v_prefix) : q.v_chunk;
+    const int64_t prows = has_prefix ? q.prefix_rows : q.q_rows;
+    return encode_rows(enc, &q.tm_k_prefix, kp, prows, q.hkv) && encode_rows(enc, &q.tm_v_prefix, vp, prows, q.hkv) &&
+           encode_rows(enc, &q.tm_k_chunk, q.k_chunk, q.q_rows, q.hkv) &&
+           encode_rows(enc, &q.tm_v_chunk, q.v_chunk, q.q_rows, q.hkv);
+}
+
+} // namespace
+
 cudaError_t launch_extend_attention(const ExtendParams &p, cudaStream_t s)
 {
+    const int64_t rows = static_cast<int64_t>(p.max_q_len) * p.group;
+    const dim3 grid(static_cast<unsigned>((rows + kTcRows - 1) / kTcRows), p.hkv, p.batch);
+    if (p.chunk_e4m3) {
+        // every key tile E4M3: the TMA + kind::f8f6f4 kernel
+        ExtendParams q = p;
+        if (fill_tensor_maps(q)) {
+            const auto kernel = q.pool != nullptr ? extend_f8_kernel<true> : extend_f8_kernel<false>;
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8Smem);
+            if (e != cudaSuccess)
+                return e;
+            kernel<<<grid, kF8Threads, kF8Smem, s>>>(q);
+            return cudaGetLastError();
+        }
+    }
     const auto kernel = p.chunk_e4m3 ? (p.pool != nullptr ? extend_tc_kernel<true, true> : extend_tc_kernel<false, true>)
                                      : (p.pool != nullptr ? extend_tc_kernel<true, false> : extend_tc_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     if (e != cudaSuccess)
         return e;
-    const int64_t rows = static_cast<int64_t>(p.max_q_len) * p.group;
-    const dim3 grid(static_cast<unsigned>((rows + kTcRows - 1) / kTcRows), p.hkv, p.batch);
     kernel<<<grid, kTcThreads, kTcSmem, s>>>(p);
     return cudaGetLastError();
 }

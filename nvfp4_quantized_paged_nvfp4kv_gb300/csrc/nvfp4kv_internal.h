@@ -1,6 +1,7 @@
 // Internal interface between the C ABI (abi.cpp) and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -133,6 +134,13 @@ struct ExtendParams {
     float gscale;                // tensor scale: blocks are taken of x / gscale
     HeadScales hs;
     uint32_t wait_limit;         // polls before a wait gives up (kWaitLimit by default)
+    // E4M3 chunks: tensor maps of the four E4M3 row sets as [rows][hkv][128]
+    // bytes, 64-row boxes of one kv head in the 128-byte swizzle, for the
+    // kernel that reads every key tile by TMA (filled by the launcher)
+    CUtensorMap tm_k_prefix;
+    CUtensorMap tm_v_prefix;
+    CUtensorMap tm_k_chunk;
+    CUtensorMap tm_v_chunk;
 };
 
 // Launch with programmatic stream serialisation allowed, so the kernel's

@@ -67,6 +67,20 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// D (tensor memory) = A * B (+ D), kind::f8f6f4 with both operands E4M3 in
+// shared memory (an instruction descriptor with A and B format 0 = E4M3 and
+// an f32 D has the same bits as idesc_f16's); K = 32 per instruction.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
 // Arrive once on an mbarrier when every earlier tcgen05 operation of this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
@@ -162,6 +176,27 @@ __device__ __forceinline__ void tmem_wait_ld()
 __device__ __forceinline__ void tmem_wait_st()
 {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- tensor memory access by the TMA unit ----------------------------------
+
+// Tiled copy of a three-dimensional box from global memory (described by a
+// tensor map in kernel-parameter space) to shared memory; completes
+// `bytes` of the barrier's transaction count.  The innermost coordinate must
+// be 16-byte aligned (here always 0); rows outside the tensor read as zeros.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int c0, int c1, int c2, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 } // namespace nvfp4kv

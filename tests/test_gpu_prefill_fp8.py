@@ -146,9 +146,11 @@ def test_fp8_chunk_fused_write_scales_and_skipped_slots():
 
 
 def test_fp8_chunk_equals_bf16_chunk_of_the_same_values():
-    """E4M3 values held exactly in bf16 give the same attention and the same
-    cache bytes through the bf16 path: the two chunk modes read one set of
-    values."""
+    """E4M3 values held exactly in bf16 give the same cache bytes through the
+    bf16 path: the two chunk modes read one set of values.  The attention runs
+    on different kernels (E4M3 keys on kind::f8f6f4 with Q in three E4M3
+    terms; bf16 keys on kind::f16 with Q in f16), so both outputs are held to
+    the oracle's rather than to each other bit for bit."""
     e = workloads.extend_custom((0, 33), (100, 45), 24, 8, seed=3)
     x = inputs(e)
     slots, num_pages = slots_for(e, seed=3)
@@ -157,7 +159,9 @@ def test_fp8_chunk_equals_bf16_chunk_of_the_same_values():
     xb["k_chunk"] = x["k_chunk"].view(torch.float8_e4m3fn).to(torch.bfloat16)
     xb["v_chunk"] = x["v_chunk"].view(torch.float8_e4m3fn).to(torch.bfloat16)
     gotb, planesb = run_fused(e, xb, slots, num_pages)
-    np.testing.assert_array_equal(got8, gotb)
+    want = oracle_out(x)
+    assert_close(got8, want, "E4M3 chunk")
+    assert_close(gotb, want, "the same values as a bf16 chunk")
     for a, b in zip(planes8, planesb):
         np.testing.assert_array_equal(a, b)
 

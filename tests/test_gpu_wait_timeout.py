@@ -75,12 +75,14 @@ def test_prefix_dequant_wait_runs_out_then_recovers(no_waiting):
     np.testing.assert_array_equal(k.cpu().numpy(), want_k)
 
 
+@pytest.mark.parametrize("chunk", ["bf16", "e4m3"])
 @pytest.mark.parametrize("fused", [False, True])
-def test_extend_wait_runs_out_then_recovers(no_waiting, fused):
-    """The tensor-core extend kernel: its roles give up, the MMAs already
-    issued are waited for before tensor memory is freed."""
+def test_extend_wait_runs_out_then_recovers(no_waiting, fused, chunk):
+    """The tensor-core extend kernels (bf16 chunks; E4M3 chunks, whose key
+    tiles come by TMA): their roles give up, the MMAs and TMA loads already
+    issued are waited for before the CTA frees tensor memory and exits."""
     e = workloads.extend_custom((70, 300), (100, 129), 16, 2, seed=63)
-    x = workloads.extend_inputs(e)
+    x = workloads.extend_inputs(e, chunk=chunk)
     xd = {k: t.to(DEV) for k, t in x.items()}
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     cache = nv.NVFP4Cache.allocate(64, e.num_kv_heads, device=DEV)
@@ -102,5 +104,6 @@ def test_extend_wait_runs_out_then_recovers(no_waiting, fused):
     assert nv.read_device_status(status) == 0
     want = oracle.extend_attention(x["q"].float().numpy(), x["q_indptr"].numpy(), x["k_prefix"].numpy(),
                                    x["v_prefix"].numpy(), x["kv_indptr"].numpy(), x["prefix_lens"].numpy(),
-                                   x["k_chunk"].float().numpy(), x["v_chunk"].float().numpy())
-    assert_close(out.cpu().numpy(), want, "extend after a timeout")
+                                   x["k_chunk"].numpy() if chunk == "e4m3" else x["k_chunk"].float().numpy(),
+                                   x["v_chunk"].numpy() if chunk == "e4m3" else x["v_chunk"].float().numpy())
+    assert_close(out.cpu().numpy(), want, f"extend ({chunk} chunk) after a timeout")
