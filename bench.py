@@ -597,13 +597,15 @@ def other_rows(dev):
             ms.append(a.elapsed_time(b))
         return statistics.mean(ms)
 
-    # Back to back, as in a prefill loop: the mean of n calls between two
-    # events (a single short call's event interval is quantised to ~2 us on
-    # this GPU).  Each quantize call reads its own copy of the 8K-token rows,
+    # Back to back, as in a prefill loop over layers: the mean of n calls
+    # between two events (a single short call's event interval is quantised
+    # to ~2 us on this GPU).  Each quantize call reads its own copy of the
+    # 8K-token rows and writes its own cache (as each layer has its own),
     # rotated among enough copies that none is still in L2 when it comes round.
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     copies = max(2, math.ceil(3 * l2 / (2 * k.numel() * k.element_size())) + 1)
     kv_copies = [(k.clone(), v.clone()) for _ in range(copies)]
+    pools = [nv.NVFP4Cache.allocate(num_pages, w.num_kv_heads, device=dev, zero=False) for _ in range(copies)]
 
     def back_to_back(call, n=2 * copies):
         for i in range(3):
@@ -617,10 +619,12 @@ def other_rows(dev):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / n
 
-    def quantize_into(c):
-        return lambda i: nv.nvfp4kv_quantize_append(c, kv_copies[i % copies][0], kv_copies[i % copies][1], sm)
+    def quantize_into(g=1.0, factors=None):
+        cs = [nv.NVFP4Cache(c.pool, global_scale=g, head_scales=factors) for c in pools]
+        return lambda i: nv.nvfp4kv_quantize_append(cs[i % copies], kv_copies[i % copies][0],
+                                                    kv_copies[i % copies][1], sm)
 
-    q_ms = back_to_back(quantize_into(cache))
+    q_ms = back_to_back(quantize_into())
     q_bytes = T * w.num_kv_heads * (2 * 128 * 2 + NVFP4_BYTES_PER_TOKEN_HEAD) + T * 4
     p_ms = back_to_back(lambda i: nv.nvfp4kv_dequant_prefix_fp8(cache, bt_d, pl, ip, kf, vf), n=10)
     p_bytes = L * w.num_kv_heads * (NVFP4_BYTES_PER_TOKEN_HEAD + 2 * 128)
@@ -633,13 +637,13 @@ def other_rows(dev):
     ws = nv.new_workspace(device=dev)
     d1_ms = back_to_back(lambda i: nv.nvfp4kv_paged_decode(cache, q, bt_d, sl, out, ws), n=20)
     dg_ms = back_to_back(lambda i: nv.nvfp4kv_paged_decode(cache_g, q, bt_d, sl, out, ws), n=20)
-    qg_ms = back_to_back(quantize_into(cache_g))
+    qg_ms = back_to_back(quantize_into(0.37))
     # and with per-head factors on top (K and V of each kv head their own scale)
     factors = [[0.5 + 0.25 * h for h in range(w.num_kv_heads)], [2.0 - 0.2 * h for h in range(w.num_kv_heads)]]
     cache_h = nv.NVFP4Cache(cache.pool, global_scale=0.37, head_scales=factors)
     dh_ms = back_to_back(lambda i: nv.nvfp4kv_paged_decode(cache_h, q, bt_d, sl, out, ws), n=20)
-    qh_ms = back_to_back(quantize_into(cache_h))
-    del kv_copies
+    qh_ms = back_to_back(quantize_into(0.37, factors))
+    del kv_copies, pools
     d_bytes = L * w.num_kv_heads * NVFP4_BYTES_PER_TOKEN_HEAD
     multi = multi_query_rows(dev, timed)
     extend = extend_rows(dev)
@@ -659,8 +663,9 @@ def other_rows(dev):
         "extend_160k_chunk8k": extend,
         "extend_160k_chunk8k_e4m3": extend8,
         "prefill_fp8_8k": prefill,
-        "timing": "quantize, prefix and 160K decode rows: calls back to back between two CUDA events, the "
-                  "quantize inputs rotated among copies totalling over 3x L2 (the other inputs exceed L2); "
+        "timing": "quantize, prefix and 160K decode rows: calls back to back between two CUDA events, each "
+                  "quantize call with its own copy of the inputs and its own cache, rotated among copies "
+                  "totalling over 3x L2 (the other inputs exceed L2); "
                   "multi-query rows: one call per event pair after a 256 MB write and a 256 MB read (L2 "
                   "evicted) and a GPU spin covering the host launch",
     }

@@ -688,9 +688,11 @@ constexpr uint32_t kF8OffK = kF8OffQ + 3 * kF8QTerm;        // two stages
 constexpr uint32_t kF8OffV = kF8OffK + 2 * kF8KBytes;       // two f16 stages (kKVBytes each)
 constexpr uint32_t kF8OffVraw = kF8OffV + 2 * kKVBytes;     // one E4M3 staging tile
 constexpr uint32_t kF8OffBar = kF8OffVraw + kF8KBytes;
+// K stages are released after their Q K^T (kF8KEmpty), V stages after their
+// P V (kF8VEmpty)
 enum {
-    kF8KFull = 0, kF8KvEmpty = 2, kF8VrawFull = 4, kF8VrawEmpty = 5, kF8VFull = 6, kF8SFull = 8, kF8PFull = 10,
-    kF8PvDone = 12, kF8Done = 14, kF8NumBars = 15
+    kF8KFull = 0, kF8VEmpty = 2, kF8VrawFull = 4, kF8VrawEmpty = 5, kF8VFull = 6, kF8SFull = 8, kF8PFull = 10,
+    kF8PvDone = 12, kF8Done = 14, kF8KEmpty = 15, kF8NumBars = 17
 };
 constexpr uint32_t kF8OffRowInv = kF8OffBar + 8 * kF8NumBars + 8;     // 16-byte aligned
 constexpr uint32_t kF8OffTmemSlot = kF8OffRowInv + 4 * kTcRows;
@@ -811,7 +813,8 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
     if (tid == 0) {
         for (int k = 0; k < 2; ++k) {
             mbar_init(B(kF8KFull + k), 1);
-            mbar_init(B(kF8KvEmpty + k), 1);
+            mbar_init(B(kF8VEmpty + k), 1);
+            mbar_init(B(kF8KEmpty + k), 1);
             mbar_init(B(kF8VFull + k), kProducerThreads);
             mbar_init(B(kF8SFull + k), 1);
             mbar_init(B(kF8PFull + k), kSoftmaxThreads);
@@ -839,8 +842,8 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
                 const int st = i & 1;
                 const bool pre = i < c.n_pre;
                 const int rowc = pre ? static_cast<int>(c.p0) + i * kTcKeys : c.c0 + (i - c.n_pre) * kTcKeys;
-                // the stage was last read by the MMAs of tile i - 2
-                if (i >= 2 && !wait_or_fail(B(kF8KvEmpty + st), ((i >> 1) - 1) & 1, fail, p.dev_status, p.wait_limit))
+                // the K stage was last read by Q K^T of tile i - 2
+                if (i >= 2 && !wait_or_fail(B(kF8KEmpty + st), ((i >> 1) - 1) & 1, fail, p.dev_status, p.wait_limit))
                     break;
                 mbar_arrive_expect_tx(B(kF8KFull + st), kF8KBytes);
                 tma_load_3d(base + kF8OffK + st * kF8KBytes, pre ? &p.tm_k_prefix : &p.tm_k_chunk, 0, h, rowc,
@@ -882,6 +885,7 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
                                 smem_desc(base + kF8OffQ + t * kF8QTerm + ks * 32, 16, 1024),
                                 smem_desc(kb + ks * 32, 16, 1024), i_qk, t > 0 || ks > 0);
                 umma_commit(B(kF8SFull + b));
+                umma_commit(B(kF8KEmpty + st));
             };
             auto pv = [&](int i) {
                 const int b = i & 1, st = i & 1;
@@ -892,7 +896,7 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
                     umma_f16_ts(tmem + kColO, tmem + kColP + b * kColPStride + s * 8,
                                 smem_desc(vb + s * 2048, kTcKeys * 128, 1024), i_pv, i > 0 || s > 0);
                 umma_commit(B(kF8PvDone + b));
-                umma_commit(B(kF8KvEmpty + st));
+                umma_commit(B(kF8VEmpty + st));
             };
             // Q K^T of tile j once its keys are in and tile j - 2's P V is
             // issued; P V of tile i once its P and its converted values are
@@ -952,8 +956,8 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
             // before the release, as a plain arrive does not across proxies
             fence_async_shared();
             mbar_arrive(B(kF8VrawEmpty));
-            // the f16 stage was last read by the MMAs of tile i - 2
-            if (i >= 2 && !wait_or_fail(B(kF8KvEmpty + st), ((i >> 1) - 1) & 1, fail, p.dev_status, p.wait_limit))
+            // the f16 stage was last read by P V of tile i - 2
+            if (i >= 2 && !wait_or_fail(B(kF8VEmpty + st), ((i >> 1) - 1) & 1, fail, p.dev_status, p.wait_limit))
                 break;
             const uint32_t dst = base + kF8OffV + st * kKVBytes;
 #pragma unroll
