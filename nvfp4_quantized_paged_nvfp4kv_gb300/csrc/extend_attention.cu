@@ -297,7 +297,8 @@ __device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const T
     auto offset = [&](int key, int blk) {
         return (static_cast<size_t>(c.c0 + key) * p.hkv + h) * kHeadDim + blk * 16;
     };
-    const float Gk = head_tensor_scale(p.hs, false, h, p.gscale), Gv = head_tensor_scale(p.hs, true, h, p.gscale);
+    const TensorScale Gk = tensor_scale(head_tensor_scale(p.hs, false, h, p.gscale));
+    const TensorScale Gv = tensor_scale(head_tensor_scale(p.hs, true, h, p.gscale));
     ChunkBlock<kChunk8> r[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {

@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const __grid_consta
     const bool ok0 = has0 && site_of(p, s0, h, kNvfp4Record, rec0, tok0, rep);
     const bool ok1 = has1 && site_of(p, s1, h, kNvfp4Record, rec1, tok1, rep);
     float x[16];
-    const float G = head_tensor_scale(p.hs, is_v, h, p.gscale);
+    const TensorScale G = tensor_scale(head_tensor_scale(p.hs, is_v, h, p.gscale));
     if (is_v && ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
         uint32_t S0, S1, c0[2], c1[2];
         unpack<kBf16>(r0, x);

@@ -52,15 +52,65 @@ __device__ __forceinline__ void load16(const void *src, size_t elem_off, float (
     unpack<kBf16>(r, x);
 }
 
-// Values relative to the tensor scale G (the block procedure runs on
-// fl32(x / G); nothing to do at G = 1).
-__device__ __forceinline__ void divide_by_tensor_scale(float (&x)[16], float G)
+// A tensor scale G and r = RN(1/G); r = 0 where G lies outside [2^-32, 2^32]
+// (every quotient then takes the IEEE division).
+struct TensorScale {
+    float G, r;
+};
+
+__device__ __forceinline__ TensorScale tensor_scale(float G)
 {
-    if (G != 1.f) {
+    return {G, (G >= 0x1p-32f && G <= 0x1p32f) ? __frcp_rn(G) : 0.f};
+}
+
+// Values relative to the tensor scale G: the block procedure runs on the
+// correctly rounded quotients fl32(x / G) (nothing to do at G = 1).
+//
+// No division per element.  With r = RN(1/G), q0 = RN(x r) is within two ulps
+// of x / G; one correction step, q1 = RN(q0 + (x - q0 G) r) with the
+// remainder through an FMA, brings it within one ulp, and a second gives
+// RN(x / G) exactly (Markstein's theorem: a quotient within one ulp, corrected
+// once with the correctly rounded reciprocal, is the correctly rounded
+// quotient when nothing underflows or overflows).  G in [2^-32, 2^32] and
+// |x| < 2^64 keep every step finite and r normal.  The remainder can lose
+// bits only for |x| < 2^-80, and there |x / G| < 2^-48: no such value decides
+// a code or a scale (a block of them has scale 0; beside a larger value,
+// whose scale is at least 2^-9, they give a zero code), and the steps keep
+// its sign.  A block with a larger value takes the IEEE division.  The steps
+// are written on q G - x (the addend -x), so that a zero quotient keeps the
+// sign of x: q0 = -0 for x = -0, q0 G - x = +0, and -0 - (+0) r = -0.
+__device__ __forceinline__ void divide_by_tensor_scale(float (&x)[16], TensorScale ts)
+{
+    if (ts.G == 1.f)
+        return;
+    const float m = fmaxf(fmax3(fmax3(fabsf(x[0]), fabsf(x[1]), fabsf(x[2])),
+                                fmax3(fabsf(x[3]), fabsf(x[4]), fabsf(x[5])),
+                                fmax3(fabsf(x[6]), fabsf(x[7]), fabsf(x[8]))),
+                          fmax3(fmax3(fabsf(x[9]), fabsf(x[10]), fabsf(x[11])),
+                                fmax3(fabsf(x[12]), fabsf(x[13]), fabsf(x[14])), fabsf(x[15])));
+    if (ts.r != 0.f && m < 0x1p64f) {
+        const uint64_t r2 = f32x2_pack(ts.r, ts.r), nr2 = f32x2_pack(-ts.r, -ts.r), g2 = f32x2_pack(ts.G, ts.G);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint64_t v2 = f32x2_pack(x[2 * j], x[2 * j + 1]);
+            const uint64_t nv2 = v2 ^ 0x8000000080000000ull;
+            uint64_t q = mul_f32x2(v2, r2);
+            q = fma_f32x2(fma_f32x2(q, g2, nv2), nr2, q);
+            q = fma_f32x2(fma_f32x2(q, g2, nv2), nr2, q);
+            x[2 * j] = f32x2_lo(q);
+            x[2 * j + 1] = f32x2_hi(q);
+        }
+    } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            x[i] = __fdiv_rn(x[i], G);
+            x[i] = __fdiv_rn(x[i], ts.G);
     }
+}
+
+__device__ __forceinline__ void divide_by_tensor_scale(float (&x)[16], float G)
+{
+    if (G != 1.f)
+        divide_by_tensor_scale(x, tensor_scale(G));
 }
 
 // The value s of an E4M3 block-scale byte S (0 .. 126) and RN(1/s) (0 for

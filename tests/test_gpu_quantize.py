@@ -178,14 +178,14 @@ def test_skipped_and_out_of_range_slots():
         np.testing.assert_array_equal(g_, w_)
 
 
-def _blocks_to_gpu_codes(blocks):
+def _blocks_to_gpu_codes(blocks, global_scale=1.0):
     """Quantise float32 blocks [N][16] (N multiple of 8) as rows of one kv head;
     returns the K codes and scales (K rows of a record are in natural order)."""
     n = blocks.shape[0]
     T = n // 8
     pages = (T + 15) // 16
     x = torch.from_numpy(blocks.reshape(T, 1, 128)).to(DEV)
-    c = nv.NVFP4Cache.allocate(pages, 1, device=DEV)
+    c = nv.NVFP4Cache.allocate(pages, 1, device=DEV, global_scale=global_scale)
     sm = torch.arange(T, dtype=torch.int32, device=DEV)
     nv.nvfp4kv_quantize_append(c, x, x, sm)
     rec = c.pool.reshape(-1, nv.NVFP4_RECORD_BYTES)                   # one kv head: page = record
@@ -281,3 +281,74 @@ def test_block_scale_sweep():
         np.testing.assert_array_equal(scale.cpu().numpy(), sc.reshape(-1))
         want = np.stack([data & 15, data >> 4], -1).reshape(hi - lo, 16)
         np.testing.assert_array_equal(codes.cpu().numpy(), want)
+
+
+def _offsets(x0: np.ndarray, k: int) -> np.ndarray:
+    """x0 moved by k units in the last place (away from zero for k > 0)."""
+    bits = x0.astype(np.float32).view(np.int32)
+    return (bits + np.int32(k)).view(np.float32)
+
+
+def _oracle_codes(blocks, global_scale):
+    T = blocks.shape[0] // 8
+    data = np.zeros((T, 1, 1, 64), np.uint8)
+    sc = np.zeros((T, 1, 1, 8), np.uint8)
+    oracle.quantize_append(blocks.reshape(T, 1, 128), np.arange(T, dtype=np.int32), data, sc, page_size=1,
+                           global_scale=global_scale)
+    return np.stack([data & 15, data >> 4], -1).reshape(-1, 16), sc.reshape(-1)
+
+
+TENSOR_SCALES = ([0.37, 3.1, 2.0 ** -7, 1.5, 3.0, 6.0, 448.0, 1.0 / 3.0,
+                  float(np.uint32(0x3F800001).view(np.float32)),      # 1 + 2^-23
+                  float(np.uint32(0x3F7FFFFF).view(np.float32)),      # 1 - 2^-24
+                  float(np.uint32(0x3FFFFFFF).view(np.float32)),      # 2 - 2^-23
+                  float(np.uint32(0x3FAAAAAB).view(np.float32)),      # RN(4/3)
+                  1.3 * 2.0 ** -31, 1.7 * 2.0 ** 31,                  # near the ends of [2^-32, 2^32]
+                  1.37 * 2.0 ** -33, 1.37 * 2.0 ** 33]                # outside it: the IEEE division
+                 + [float(np.float32(g)) for g in np.exp2(np.random.default_rng(23).uniform(-30, 30, 24))])
+
+
+@pytest.mark.parametrize("g", TENSOR_SCALES)
+def test_tensor_scale_quotients_at_decision_boundaries(g):
+    """The block procedure runs on fl32(x / G), which the kernel forms from
+    RN(1/G) and correction steps rather than a division.  Values are placed
+    within three ulps of x / G = b for every E2M1 rounding boundary b (block
+    scale 1 from a sixth value 6 G), and block maxima within three ulps of
+    x / G = 6 m for E4M3 midpoints m (the scale byte decided by one ulp),
+    plus random full-mantissa values, values below 2^-80 next to larger ones
+    and alone, and values of 2^64 and more: every scale byte and code equals
+    the oracle's, which divides in IEEE fp32."""
+    g32 = np.float32(g)
+    rng = np.random.default_rng(int(g32.view(np.uint32)))
+    blocks = []
+    # element boundaries at block scale 1
+    bounds = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float64)
+    base = np.concatenate([bounds, -bounds]) * np.float64(g32)
+    vals = np.concatenate([_offsets(base.astype(np.float32), k) for k in range(-3, 4)])
+    vals = np.concatenate([vals, np.zeros((-len(vals)) % 15, np.float32)])
+    b = np.empty((len(vals) // 15, 16), np.float32)
+    b[:, :15] = vals.reshape(-1, 15)
+    b[:, 15] = np.float32(6.0 * np.float64(g32))
+    blocks.append(b)
+    # block maxima next to E4M3 midpoints (scale mantissas 1 + (2j+1)/16, three binades)
+    mids = np.array([(1 + (2 * j + 1) / 16) * 2.0 ** e for e in (-3, 0, 3) for j in range(8)])
+    amax = np.concatenate([_offsets((6 * mids * np.float64(g32)).astype(np.float32), k) for k in range(-3, 4)])
+    b = (rng.uniform(-1, 1, (len(amax), 16)) * amax[:, None]).astype(np.float32)
+    b[:, 0] = amax
+    blocks.append(b)
+    # random values with full mantissas, from 2^-12 G to 2^9 G
+    b = (np.exp2(rng.uniform(-12, 9, (4096, 16))) * rng.choice([-1.0, 1.0], (4096, 16)) *
+         np.float64(g32)).astype(np.float32)
+    blocks.append(b)
+    # tiny values (|x| < 2^-80), beside a value of 4 G and alone; huge values
+    tiny = (rng.uniform(0.5, 1, (64, 16)) * 2.0 ** -90 * rng.choice([-1.0, 1.0], (64, 16))).astype(np.float32)
+    mixed = tiny.copy()
+    mixed[:, 7] = np.float32(4.0 * np.float64(g32))
+    huge = (rng.uniform(-1, 1, (64, 16)) * 2.0 ** 70).astype(np.float32)
+    blocks += [tiny, mixed, huge]
+    blocks = np.concatenate(blocks)
+    blocks = np.concatenate([blocks, np.zeros(((-len(blocks)) % 8, 16), np.float32)])
+    codes, scale = _blocks_to_gpu_codes(blocks, global_scale=float(g32))
+    want_codes, want_scale = _oracle_codes(blocks, float(g32))
+    np.testing.assert_array_equal(scale.cpu().numpy(), want_scale)
+    np.testing.assert_array_equal(codes.cpu().numpy(), want_codes)
