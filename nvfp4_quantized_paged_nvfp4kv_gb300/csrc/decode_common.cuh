@@ -461,6 +461,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
     int seg_begin = prefix[b] + h * n;
 
     pdl_wait();
+    // The first two records go out at once, the rest of the ring once the
+    // first has landed: when every warp asks for its whole ring together,
+    // each warp's first record would arrive late in that burst.  With the
+    // fused append, the records before the first page that receives a new
+    // token (the last page-head of the first segment, if the warp reaches
+    // it) go out before the append, so the warps that append do not start
+    // streaming later than the others.
+    const int npro = min(S, hi - lo);
+    const int app_first = (!kMulti && p.append && seg_begin + n - 1 < hi) ? seg_begin + n - 1 : hi;
+    const int npre = min(min(2, npro), app_first - lo);
+    for (int x = lo; x < lo + npre; ++x)
+        issue(x, x - lo);
     if (!kMulti && p.append) {
         // Fused append: the warp that streams the last page-head of a segment
         // first writes that sequence's new token (position seq_len - 1) into
@@ -495,12 +507,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
         }
         __syncwarp();
     }
-
-    // The first two records go out at once, the rest of the ring once the
-    // first has landed: when every warp asks for its whole ring together,
-    // each warp's first record would arrive late in that burst.
-    const int npro = min(S, hi - lo);
-    for (int x = lo; x < lo + min(2, npro); ++x)
+    for (int x = lo + npre; x < lo + min(2, npro); ++x)
         issue(x, x - lo);
 
     uint32_t qf[16];

@@ -295,6 +295,14 @@ __device__ __forceinline__ void fence_proxy_async_global()
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Orders this thread's shared-memory accesses through the generic proxy with
+// the asynchronous proxy's (bulk copies, TMA, the tensor core): writes become
+// visible to its reads, reads complete before its later writes.
+__device__ __forceinline__ void fence_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding kernel in the stream
 // (no-op when the launch did not allow overlap) / let the next one start.
 __device__ __forceinline__ void pdl_wait()

@@ -671,31 +671,42 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
 // on FP8 K/V), every key tile is E4M3 bytes, one 128-byte row per key: the
 // TMA unit loads a 64-key tile of one kv head straight into the 128-byte
 // swizzle the MMA reads, and S = Q K^T runs as tcgen05.mma kind::f8f6f4 with
-// Q split into three E4M3 terms (hi, mid, lo), all accumulated into S.  Each
-// row of Q is first multiplied by a power of two 2^e_r that puts its largest
-// element in [128, 256); the softmax takes S * 2^-e_r.  The three terms carry
-// about twelve significant bits of q (each term rounds the remainder of the
-// ones before it to E4M3), against f16's eleven.  Values stay on the f16
-// path: the TMA unit loads the E4M3 value tile into a staging buffer, the
-// converter warps turn it into the f16 operand of P V (rows past the
-// sequence's keys become zeros), and P V runs on kind::f16 as in the kernel
-// above.  Warp 9 issues the TMA loads.
+// Q split into two E4M3 terms (hi, lo), both accumulated into S.  Each row of
+// the bf16 Q is first multiplied by a power of two 2^e_r that puts its largest
+// element in [128, 256); the softmax takes S * 2^-e_r * sm_scale.  A bf16
+// value has eight significant bits: hi = E4M3(x) keeps the first four, and the
+// remainder x - hi is a multiple of x's last place no larger than hi's half
+// place, so lo = E4M3(x - hi) holds it exactly wherever it is not below
+// E4M3's subnormal step 2^-9 (scaled elements of at least 1/4); smaller
+// elements keep an error of at most 2^-10, under 2^-17 of the row's largest.
+// Values stay on the f16 path: the TMA unit loads the E4M3 value tile into a
+// staging ring, the converter warps turn it into the f16 operand of P V (rows
+// past the sequence's keys become zeros), and P V runs on kind::f16 as in the
+// kernel above.  Warp 9 issues the TMA loads: key tiles into a ring of three
+// stages, value tiles into a ring of two, so that a tile's load latency is
+// covered by the work on the tiles before it.
 constexpr int kF8Threads = kTcThreads + 32;                 // + the TMA warp
 constexpr int kF8TmaWarp = 9;
+constexpr int kF8QTerms = 2;
+constexpr int kF8KStages = 3;                               // E4M3 key tiles
+constexpr int kF8VrawStages = 2;                            // E4M3 value tiles
 constexpr uint32_t kF8QTerm = kTcRows * kHeadDim;           // 16 KB per E4M3 term
-constexpr uint32_t kF8KBytes = kTcKeys * kHeadDim;          // 8 KB per E4M3 key tile
-constexpr uint32_t kF8OffQ = 0;                             // three terms
-constexpr uint32_t kF8OffK = kF8OffQ + 3 * kF8QTerm;        // two stages
-constexpr uint32_t kF8OffV = kF8OffK + 2 * kF8KBytes;       // two f16 stages (kKVBytes each)
-constexpr uint32_t kF8OffVraw = kF8OffV + 2 * kKVBytes;     // one E4M3 staging tile
-constexpr uint32_t kF8OffBar = kF8OffVraw + kF8KBytes;
-// K stages are released after their Q K^T (kF8KEmpty), V stages after their
-// P V (kF8VEmpty)
+constexpr uint32_t kF8KBytes = kTcKeys * kHeadDim;          // 8 KB per E4M3 key or value tile
+constexpr uint32_t kF8OffQ = 0;
+constexpr uint32_t kF8OffK = kF8OffQ + kF8QTerms * kF8QTerm;
+constexpr uint32_t kF8OffV = kF8OffK + kF8KStages * kF8KBytes;     // two f16 stages (kKVBytes each)
+constexpr uint32_t kF8OffVraw = kF8OffV + 2 * kKVBytes;
+constexpr uint32_t kF8OffBar = kF8OffVraw + kF8VrawStages * kF8KBytes;
+// K stages are released after their Q K^T (kF8KEmpty), staged value tiles
+// after their conversion (kF8VrawEmpty), f16 V stages after their P V
+// (kF8VEmpty)
 enum {
-    kF8KFull = 0, kF8VEmpty = 2, kF8VrawFull = 4, kF8VrawEmpty = 5, kF8VFull = 6, kF8SFull = 8, kF8PFull = 10,
-    kF8PvDone = 12, kF8Done = 14, kF8KEmpty = 15, kF8NumBars = 17
+    kF8KFull = 0, kF8KEmpty = kF8KFull + kF8KStages, kF8VrawFull = kF8KEmpty + kF8KStages,
+    kF8VrawEmpty = kF8VrawFull + kF8VrawStages, kF8VFull = kF8VrawEmpty + kF8VrawStages, kF8VEmpty = kF8VFull + 2,
+    kF8SFull = kF8VEmpty + 2, kF8PFull = kF8SFull + 2, kF8PvDone = kF8PFull + 2, kF8Done = kF8PvDone + 2,
+    kF8NumBars = kF8Done + 1
 };
-constexpr uint32_t kF8OffRowInv = kF8OffBar + 8 * kF8NumBars + 8;     // 16-byte aligned
+constexpr uint32_t kF8OffRowInv = (kF8OffBar + 8 * kF8NumBars + 15) / 16 * 16;
 constexpr uint32_t kF8OffTmemSlot = kF8OffRowInv + 4 * kTcRows;
 constexpr uint32_t kF8OffFail = kF8OffTmemSlot + 4;
 constexpr uint32_t kF8Smem = kF8OffFail + 4 + 1024;
@@ -750,10 +761,10 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
     c.n_pre = (c.P + kTcKeys - 1) / kTcKeys;
     c.n_tiles = c.n_pre + t_max / kTcKeys + 1;
 
-    // Q as three E4M3 terms, each row scaled by a power of two first.  Sixteen
-    // consecutive lanes hold one row (eight channels each): the CTA's threads
-    // cover the 2,048 pieces in whole warps, so the row maximum is a shuffle
-    // over those lanes.
+    // Q as two E4M3 terms, each row scaled by a power of two first (the
+    // softmax scale is applied to S).  Sixteen consecutive lanes hold one row
+    // (eight channels each): the CTA's threads cover the 2,048 pieces in whole
+    // warps, so the row maximum is a shuffle over those lanes.
     for (int idx0 = warp * 32; idx0 < kTcRows * 16; idx0 += kF8Threads) {
         const int idx = idx0 + lane;
         const int r = idx >> 4, piece = idx & 15;
@@ -766,8 +777,8 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                x[2 * k] = __uint_as_float(ww[k] << 16) * p.qscale;
-                x[2 * k + 1] = __uint_as_float(ww[k] & 0xffff0000u) * p.qscale;
+                x[2 * k] = __uint_as_float(ww[k] << 16);
+                x[2 * k + 1] = __uint_as_float(ww[k] & 0xffff0000u);
             }
         } else {
 #pragma unroll
@@ -787,13 +798,13 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
             e = 7 - (static_cast<int>((__float_as_uint(am) >> 23) & 0xffu) - 127);
         const float sc = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
         if (piece == 0)
-            rowinv[r] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-        uint32_t term[3][2];
+            rowinv[r] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23) * p.qscale;
+        uint32_t term[kF8QTerms][2];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             float a = x[2 * k] * sc, b = x[2 * k + 1] * sc;
 #pragma unroll
-            for (int t = 0; t < 3; ++t) {
+            for (int t = 0; t < kF8QTerms; ++t) {
                 const uint32_t two = f32x2_to_e4m3x2(a, b);
                 const float2 v = e4m3x2_value(two);
                 a -= v.x;                         // exact: the remainder of an E4M3 rounding
@@ -806,23 +817,27 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
         }
         const uint32_t off = r * 128u + ((static_cast<uint32_t>(piece >> 1) ^ (r & 7u)) << 4) + (piece & 1) * 8u;
 #pragma unroll
-        for (int t = 0; t < 3; ++t)
+        for (int t = 0; t < kF8QTerms; ++t)
             asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(base + kF8OffQ + t * kF8QTerm + off),
                          "r"(term[t][0]), "r"(term[t][1])
                          : "memory");
     }
     if (tid == 0) {
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < kF8KStages; ++k) {
             mbar_init(B(kF8KFull + k), 1);
-            mbar_init(B(kF8VEmpty + k), 1);
             mbar_init(B(kF8KEmpty + k), 1);
+        }
+        for (int k = 0; k < kF8VrawStages; ++k) {
+            mbar_init(B(kF8VrawFull + k), 1);
+            mbar_init(B(kF8VrawEmpty + k), kProducerThreads);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(B(kF8VEmpty + k), 1);
             mbar_init(B(kF8VFull + k), kProducerThreads);
             mbar_init(B(kF8SFull + k), 1);
             mbar_init(B(kF8PFull + k), kSoftmaxThreads);
             mbar_init(B(kF8PvDone + k), 1);
         }
-        mbar_init(B(kF8VrawFull), 1);
-        mbar_init(B(kF8VrawEmpty), kProducerThreads);
         mbar_init(B(kF8Done), 1);
         *fail = 0;
         fence_mbar_init();
@@ -837,36 +852,40 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
 
     if (warp == kF8TmaWarp) {
         if (lane == 0) {
-            // key tile i: K into stage i % 2, V into the staging tile
-            int issued = 0;
+            // key tile i: K into stage i % kF8KStages, V into staging stage
+            // i % kF8VrawStages
+            int nk = 0, nv = 0;                  // loads issued
             for (int i = 0; i < c.n_tiles; ++i) {
-                const int st = i & 1;
+                const int sk = i % kF8KStages, sv = i % kF8VrawStages;
                 const bool pre = i < c.n_pre;
                 const int rowc = pre ? static_cast<int>(c.p0) + i * kTcKeys : c.c0 + (i - c.n_pre) * kTcKeys;
-                // the K stage was last read by Q K^T of tile i - 2
-                if (i >= 2 && !wait_or_fail(B(kF8KEmpty + st), ((i >> 1) - 1) & 1, fail, p.dev_status, p.wait_limit))
+                // the K stage was last read by Q K^T of tile i - kF8KStages
+                if (i >= kF8KStages &&
+                    !wait_or_fail(B(kF8KEmpty + sk), (i / kF8KStages - 1) & 1, fail, p.dev_status, p.wait_limit))
                     break;
-                mbar_arrive_expect_tx(B(kF8KFull + st), kF8KBytes);
-                tma_load_3d(base + kF8OffK + st * kF8KBytes, pre ? &p.tm_k_prefix : &p.tm_k_chunk, 0, h, rowc,
-                            B(kF8KFull + st));
-                // the staging tile was last read by the converters for tile i - 1
-                if (i >= 1 && !wait_or_fail(B(kF8VrawEmpty), (i - 1) & 1, fail, p.dev_status, p.wait_limit)) {
-                    issued = 2 * i + 1;
+                mbar_arrive_expect_tx(B(kF8KFull + sk), kF8KBytes);
+                tma_load_3d(base + kF8OffK + sk * kF8KBytes, pre ? &p.tm_k_prefix : &p.tm_k_chunk, 0, h, rowc,
+                            B(kF8KFull + sk));
+                ++nk;
+                // the staging stage was last read by the converters for tile
+                // i - kF8VrawStages
+                if (i >= kF8VrawStages && !wait_or_fail(B(kF8VrawEmpty + sv), (i / kF8VrawStages - 1) & 1, fail,
+                                                        p.dev_status, p.wait_limit))
                     break;
-                }
-                mbar_arrive_expect_tx(B(kF8VrawFull), kF8KBytes);
-                tma_load_3d(base + kF8OffVraw, pre ? &p.tm_v_prefix : &p.tm_v_chunk, 0, h, rowc, B(kF8VrawFull));
-                issued = 2 * i + 2;
+                mbar_arrive_expect_tx(B(kF8VrawFull + sv), kF8KBytes);
+                tma_load_3d(base + kF8OffVraw + sv * kF8KBytes, pre ? &p.tm_v_prefix : &p.tm_v_chunk, 0, h, rowc,
+                            B(kF8VrawFull + sv));
+                ++nv;
             }
             // nothing issued may still be in flight when the CTA exits: the
-            // last two K tiles and the last staging tile (earlier ones were
-            // waited for before their buffers were reused)
-            const int nk = (issued + 1) >> 1, nv = issued >> 1;
-            for (int i = max(0, nk - 2); i < nk; ++i)
-                if (!mbar_wait_bounded(B(kF8KFull + (i & 1)), (i >> 1) & 1, kWaitLimit))
+            // last loads of each ring (earlier ones were waited for before
+            // their stage was reused)
+            for (int i = max(0, nk - kF8KStages); i < nk; ++i)
+                if (!mbar_wait_bounded(B(kF8KFull + i % kF8KStages), (i / kF8KStages) & 1, kWaitLimit))
                     report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
-            if (nv > 0 && !mbar_wait_bounded(B(kF8VrawFull), (nv - 1) & 1, kWaitLimit))
-                report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
+            for (int i = max(0, nv - kF8VrawStages); i < nv; ++i)
+                if (!mbar_wait_bounded(B(kF8VrawFull + i % kF8VrawStages), (i / kF8VrawStages) & 1, kWaitLimit))
+                    report(p.dev_status, NVFP4KV_DEV_TIMEOUT);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -875,11 +894,11 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
             constexpr uint32_t i_pv = idesc_f16(kTcRows, kHeadDim, true);
             bool ok = true;
             auto qk = [&](int i) {
-                const int b = i & 1, st = i & 1;
+                const int b = i & 1, st = i % kF8KStages;
                 tc_fence_after_sync();
                 const uint32_t kb = base + kF8OffK + st * kF8KBytes;
 #pragma unroll
-                for (int t = 0; t < 3; ++t)
+                for (int t = 0; t < kF8QTerms; ++t)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         umma_f8(tmem + kColS + b * kTcKeys,
@@ -909,7 +928,7 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
                 for (uint64_t polls = 0; !pv_done;) {
                     bool progress = false;
                     if (next_qk <= i + 1 && next_qk < c.n_tiles &&
-                        mbar_test_wait(B(kF8KFull + (next_qk & 1)), (next_qk >> 1) & 1)) {
+                        mbar_test_wait(B(kF8KFull + next_qk % kF8KStages), (next_qk / kF8KStages) & 1)) {
                         qk(next_qk++);
                         progress = true;
                     }
@@ -939,24 +958,27 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
         __syncwarp();
     } else if (warp >= kSoftmaxThreads / 32) {
         // converters: thread pt turns half a row of the staged E4M3 value tile
-        // (key pt / 2, channels 64 (pt % 2) .. + 63) into f16
+        // (key pt % 64, channels 64 (pt / 64) .. + 63) into f16.  A warp takes
+        // 32 consecutive keys of one half, so each eight lanes of a 16-byte
+        // load or store meet eight different bank groups (the chunk index is
+        // xored with the key's low three bits).
         const int pt = tid - kSoftmaxThreads;
-        const int key = pt >> 1, half = pt & 1;
+        const int key = pt & 63, half = pt >> 6;
         for (int i = 0; i < c.n_tiles; ++i) {
-            const int st = i & 1;
+            const int st = i & 1, sv = i % kF8VrawStages;
             const int lim = i < c.n_pre ? c.P - i * kTcKeys : c.C - (i - c.n_pre) * kTcKeys;
-            if (!wait_or_fail(B(kF8VrawFull), i & 1, fail, p.dev_status, p.wait_limit))
+            if (!wait_or_fail(B(kF8VrawFull + sv), (i / kF8VrawStages) & 1, fail, p.dev_status, p.wait_limit))
                 break;
             uint4 raw[4];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
-                raw[jj] = lds128(base + kF8OffVraw + key * 128u +
+                raw[jj] = lds128(base + kF8OffVraw + sv * kF8KBytes + key * 128u +
                                  ((static_cast<uint32_t>(4 * half + jj) ^ (key & 7u)) << 4));
-            // the next TMA load (async proxy) overwrites the staging tile these
+            // a later TMA load (async proxy) overwrites the staging tile these
             // generic-proxy reads come from: a proxy fence orders the reads
             // before the release, as a plain arrive does not across proxies
             fence_async_shared();
-            mbar_arrive(B(kF8VrawEmpty));
+            mbar_arrive(B(kF8VrawEmpty + sv));
             // the f16 stage was last read by P V of tile i - 2
             if (i >= 2 && !wait_or_fail(B(kF8VEmpty + st), ((i >> 1) - 1) & 1, fail, p.dev_status, p.wait_limit))
                 break;

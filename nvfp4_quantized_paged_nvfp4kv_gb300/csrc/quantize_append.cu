@@ -46,9 +46,11 @@ __device__ __forceinline__ bool site_of(const QuantParams &p, int slot, int h, i
 // the atomic nibble merge.  Data loads are issued together with the slot
 // loads (the source offset does not depend on the slot).  The value and
 // reciprocal of each block-scale byte come from a table in shared memory,
-// filled once per CTA while the loads are in flight.
+// filled once per CTA while the loads are in flight.  The kernel is bound by
+// its instruction issue more than by memory: bf16 rows fit five CTAs to an SM
+// (48 registers, no spills), fp32 rows four.
 template <bool kBf16>
-__global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const __grid_constant__ QuantParams p)
+__global__ void __launch_bounds__(256, kBf16 ? 5 : 4) quantize_nvfp4_kernel(const __grid_constant__ QuantParams p)
 {
     __shared__ float2 scale_tab[128];
     pdl_wait();                  // the records may still be read by the previous kernel
@@ -56,8 +58,16 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const __grid_consta
     const unsigned idx = blockIdx.x * blockDim.x + threadIdx.x;
     const int blk = static_cast<int>(idx & 7u);
     const unsigned unit = idx >> 3;                  // pair * hkv + h
-    const int h = static_cast<int>(unit % static_cast<unsigned>(p.hkv));
-    const unsigned pr = unit / static_cast<unsigned>(p.hkv);
+    const unsigned hk = static_cast<unsigned>(p.hkv);
+    unsigned hu, pr;
+    if ((hk & (hk - 1u)) == 0u) {                    // a power of two: no division
+        hu = unit & (hk - 1u);
+        pr = unit >> (__ffs(hk) - 1);
+    } else {
+        hu = unit % hk;
+        pr = unit / hk;
+    }
+    const int h = static_cast<int>(hu);
     const bool is_v = blockIdx.y == 1;
     const int first = __ldg(p.slot_mapping);
     const int o = (is_v && first >= 0) ? (first & 1) : 0;

@@ -227,22 +227,29 @@ __device__ __forceinline__ void write_nvfp4_block(uint8_t *rec, bool is_v, int t
 
 // NVFP4, V block blk of both tokens of a token pair (tok0 even, tok0 + 1), from
 // their scale bytes and codes: every byte of theirs is written whole, no atomics.
+// Byte 2*blk of chunk group g holds channel 16blk + g (low nibble token tok0,
+// high nibble tok0 + 1) and byte 2*blk + 1 channel 16blk + g + 8.  The nibble
+// pairs are formed a word at a time: from the codes a (tok0) and b (tok0 + 1)
+// of eight channels, (a & 0x0F0F0F0F) | ((b << 4) & 0xF0F0F0F0) holds the even
+// channels' bytes and ((a >> 4) & 0x0F0F0F0F) | (b & 0xF0F0F0F0) the odd ones';
+// one byte permutation then pairs the low and high channel bytes of two groups.
 __device__ __forceinline__ void write_nvfp4_v_pair(uint8_t *rec, int tok0, int blk, uint32_t S0,
                                                    const uint32_t (&p0)[2], uint32_t S1, const uint32_t (&p1)[2])
 {
     const int row = tok0 >> 1;
-    const uint64_t c0 = (static_cast<uint64_t>(p0[1]) << 32) | p0[0];
-    const uint64_t c1 = (static_cast<uint64_t>(p1[1]) << 32) | p1[0];
+    constexpr uint32_t kLo = 0x0F0F0F0Fu;
+    const uint32_t el = (p0[0] & kLo) | ((p1[0] << 4) & ~kLo);     // groups 0,2,4,6: channel 16blk + g
+    const uint32_t ol = ((p0[0] >> 4) & kLo) | (p1[0] & ~kLo);     // groups 1,3,5,7
+    const uint32_t eh = (p0[1] & kLo) | ((p1[1] << 4) & ~kLo);     // the same groups, channel 16blk + g + 8
+    const uint32_t oh = ((p0[1] >> 4) & kLo) | (p1[1] & ~kLo);
+    const uint32_t w[4] = {__byte_perm(el, eh, 0x5140), __byte_perm(ol, oh, 0x5140),   // groups {0,2}, {1,3}
+                           __byte_perm(el, eh, 0x7362), __byte_perm(ol, oh, 0x7362)};  // groups {4,6}, {5,7}
+    uint8_t *base = rec + 1024 + row * 128 + 2 * blk;
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
-        // bytes 2*blk (channel 16blk + g) and 2*blk + 1 (channel 16blk + g + 8);
-        // low nibble token tok0, high nibble token tok0 + 1
-        const uint32_t lo = (static_cast<uint32_t>(c0 >> (4 * g)) & 15u) |
-                            ((static_cast<uint32_t>(c1 >> (4 * g)) & 15u) << 4);
-        const uint32_t hi = (static_cast<uint32_t>(c0 >> (4 * (g + 8))) & 15u) |
-                            ((static_cast<uint32_t>(c1 >> (4 * (g + 8))) & 15u) << 4);
-        *reinterpret_cast<uint16_t *>(rec + 1024 + row * 128 + ((g + 2 * row) & 7) * 16 + 2 * blk) =
-            static_cast<uint16_t>(lo | (hi << 8));
+        const uint32_t word = w[(g & 1) | ((g >> 2) << 1)];
+        const uint32_t v = ((g >> 1) & 1) ? (word >> 16) : word;
+        *reinterpret_cast<uint16_t *>(base + ((g + 2 * row) & 7) * 16) = static_cast<uint16_t>(v);
     }
     *reinterpret_cast<uint16_t *>(rec + 2176 + row * 16 + blk * 2) = static_cast<uint16_t>(S0 | (S1 << 8));
 }

@@ -101,12 +101,6 @@ __device__ __forceinline__ void tc_fence_after_sync()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Thread writes to shared memory become visible to the tensor core's reads.
-__device__ __forceinline__ void fence_async_shared()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Non-blocking: has the phase with this parity completed?
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
 {

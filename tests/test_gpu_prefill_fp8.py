@@ -148,7 +148,7 @@ def test_fp8_chunk_fused_write_scales_and_skipped_slots():
 def test_fp8_chunk_equals_bf16_chunk_of_the_same_values():
     """E4M3 values held exactly in bf16 give the same cache bytes through the
     bf16 path: the two chunk modes read one set of values.  The attention runs
-    on different kernels (E4M3 keys on kind::f8f6f4 with Q in three E4M3
+    on different kernels (E4M3 keys on kind::f8f6f4 with Q in two E4M3
     terms; bf16 keys on kind::f16 with Q in f16), so both outputs are held to
     the oracle's rather than to each other bit for bit."""
     e = workloads.extend_custom((0, 33), (100, 45), 24, 8, seed=3)

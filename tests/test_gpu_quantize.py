@@ -352,3 +352,48 @@ def test_tensor_scale_quotients_at_decision_boundaries(g):
     want_codes, want_scale = _oracle_codes(blocks, float(g32))
     np.testing.assert_array_equal(scale.cpu().numpy(), want_scale)
     np.testing.assert_array_equal(codes.cpu().numpy(), want_codes)
+
+
+@pytest.mark.parametrize("hkv", [1, 3, 5, 8, 16, 17, 24, 32, 33, 40])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_kv_head_counts_and_ragged_token_counts(hkv, dtype):
+    """kv head counts from 1 to 40 (powers of two and not), token counts from
+    1 to several CTAs' worth, first slots even and odd, consecutive and
+    shuffled slots: every byte against the oracle."""
+    rng = np.random.default_rng(100 + hkv)
+    for T, odd, shuffled in ((1, False, False), (2, True, False), (15, False, True), (33, True, False),
+                             (100, False, False), (257, True, True)):
+        pages = (T + 2) // 16 + 2
+        if shuffled:
+            slots = rng.permutation(pages * 16)[:T].astype(np.int32)
+            if odd and slots[0] % 2 == 0:                  # put an odd slot first
+                j = int(np.flatnonzero(slots % 2 == 1)[0])
+                slots[[0, j]] = slots[[j, 0]]
+        else:
+            slots = np.arange(T, dtype=np.int32) + (1 if odd else 0)
+        k = torch.from_numpy((rng.standard_normal((T, hkv, 128)) * 2).astype(np.float32)).to(dtype)
+        v = torch.from_numpy(rng.standard_t(4, (T, hkv, 128)).astype(np.float32)).to(dtype)
+        got, st = run_gpu(k, v, slots, pages, hkv)
+        want = run_oracle(k, v, slots, pages, hkv)
+        assert st == 0
+        for name, g_, w_ in zip(("k data", "k scale", "v data", "v scale"), got, want):
+            np.testing.assert_array_equal(g_, w_, err_msg=f"{name}, T={T}, hkv={hkv}")
+
+
+@pytest.mark.parametrize("first", [0, 1])
+def test_prefill_chunk_8k_tokens_8_heads(first):
+    """The benchmarked size: 8,192 bf16 tokens of 8 kv heads into a cache of
+    shuffled pages (the long-context workload's block table), starting on an
+    even and on an odd slot; every byte against the oracle."""
+    w = workloads.make("ctx160k", batch=1)
+    bt, num_pages = workloads.block_table(w)
+    T = 8192
+    sm = workloads.slot_mapping(w, bt, 0, first, first + T)
+    k = workloads.kv_rows(w, "k", 0, 0, T).to(torch.bfloat16)
+    v = workloads.kv_rows(w, "v", 0, 0, T).to(torch.bfloat16)
+    used = np.unique(sm // 16)
+    got, st = run_gpu(k, v, sm, num_pages, w.num_kv_heads)
+    want = run_oracle(k, v, sm, num_pages, w.num_kv_heads)
+    assert st == 0
+    for name, g_, w_ in zip(("k data", "k scale", "v data", "v scale"), got, want):
+        np.testing.assert_array_equal(g_[used], w_[used], err_msg=name)

@@ -21,10 +21,12 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture
-def no_waiting():
-    prev = nv.nvfp4kv_set_wait_limit(0)
+def run_out():
+    """Call it once the inputs are built: from then on every wait gives up at
+    once; the previous limit comes back after the test."""
+    prev = nv.nvfp4kv_set_wait_limit(nv.WAIT_LIMIT_DEFAULT)
     try:
-        yield
+        yield lambda: nv.nvfp4kv_set_wait_limit(0)
     finally:
         nv.nvfp4kv_set_wait_limit(prev)
 
@@ -42,9 +44,10 @@ def run_decodes(b, status):
     return [o.cpu().numpy() for o in outs]
 
 
-def test_decode_wait_runs_out_then_recovers(no_waiting):
+def test_decode_wait_runs_out_then_recovers(run_out):
     w = workloads.custom(3, 16, 4, (300, 17, 1000), seed=61)
     b = Built(w)
+    run_out()
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     run_decodes(b, status)
     assert nv.read_device_status(status) == nv.DEV_TIMEOUT
@@ -56,9 +59,10 @@ def test_decode_wait_runs_out_then_recovers(no_waiting):
     assert_close(got8, oracle_full(b, fp8=True)[0], "fp8 decode after a timeout")
 
 
-def test_prefix_dequant_wait_runs_out_then_recovers(no_waiting):
+def test_prefix_dequant_wait_runs_out_then_recovers(run_out):
     w = workloads.custom(2, 8, 2, (200, 77), seed=62)
     b = Built(w, fp8=False)
+    run_out()
     indptr = torch.tensor([0, 200], dtype=torch.int32, device=DEV)
     k = torch.zeros((277, 2, 128), dtype=torch.uint8, device=DEV)
     v = torch.zeros_like(k)
@@ -77,7 +81,7 @@ def test_prefix_dequant_wait_runs_out_then_recovers(no_waiting):
 
 @pytest.mark.parametrize("chunk", ["bf16", "e4m3"])
 @pytest.mark.parametrize("fused", [False, True])
-def test_extend_wait_runs_out_then_recovers(no_waiting, fused, chunk):
+def test_extend_wait_runs_out_then_recovers(run_out, fused, chunk):
     """The tensor-core extend kernels (bf16 chunks; E4M3 chunks, whose key
     tiles come by TMA): their roles give up, the MMAs and TMA loads already
     issued are waited for before the CTA frees tensor memory and exits."""
@@ -96,6 +100,7 @@ def test_extend_wait_runs_out_then_recovers(no_waiting, fused, chunk):
             nv.nvfp4kv_extend_attention_fp8_append(cache, slots, *args, max_q_len=129, dev_status=status)
         else:
             nv.nvfp4kv_extend_attention_fp8(*args, max_q_len=129, dev_status=status)
+    run_out()
     call()
     assert nv.read_device_status(status) == nv.DEV_TIMEOUT
     nv.nvfp4kv_set_wait_limit(nv.WAIT_LIMIT_DEFAULT)
@@ -107,3 +112,4 @@ def test_extend_wait_runs_out_then_recovers(no_waiting, fused, chunk):
                                    x["k_chunk"].numpy() if chunk == "e4m3" else x["k_chunk"].float().numpy(),
                                    x["v_chunk"].numpy() if chunk == "e4m3" else x["v_chunk"].float().numpy())
     assert_close(out.cpu().numpy(), want, f"extend ({chunk} chunk) after a timeout")
+
