@@ -153,7 +153,10 @@ def profiled_traffic(kernel_tag: str, workload: str):
     for line in open(path):
         if ":" in line and line.startswith("- "):
             k, v = line[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
+            v = v.strip()
+            if v.startswith("`") and "`" in v[1:]:
+                v = v[1:v.index("`", 1)]             # the quoted value, without a trailing note
+            fields[k.strip()] = v
     if fields.get("kernel_sources_sha256") != kernel_sources_hash(kernel_tag):
         return None
     try:
@@ -651,9 +654,11 @@ def other_rows(dev):
     prefill = prefill_rows(dev)
     return {
         "quantize_append_8k_bf16": {"us": q_ms * 1e3, "tokens_per_s": T / (q_ms / 1e3),
-                                    "alg_gbs": q_bytes / (q_ms / 1e3) / 1e9, "alg_bytes": q_bytes},
+                                    "alg_gbs": q_bytes / (q_ms / 1e3) / 1e9, "alg_bytes": q_bytes,
+                                    "traffic": profiled_traffic("quantize_append", "nvfp4_8k_bf16")},
         "dequant_prefix_fp8_160k": {"us": p_ms * 1e3, "tokens_per_s": L / (p_ms / 1e3),
-                                    "alg_gbs": p_bytes / (p_ms / 1e3) / 1e9, "alg_bytes": p_bytes},
+                                    "alg_gbs": p_bytes / (p_ms / 1e3) / 1e9, "alg_bytes": p_bytes,
+                                    "traffic": profiled_traffic("dequant_prefix", "fp8_160k")},
         "tensor_scale_0.37": {"decode_160k_b1_us": dg_ms * 1e3, "decode_160k_b1_unit_scale_us": d1_ms * 1e3,
                               "decode_alg_gbs": d_bytes / (dg_ms / 1e3) / 1e9,
                               "quantize_append_8k_bf16_us": qg_ms * 1e3,
@@ -771,7 +776,7 @@ def extend_rows(dev, name: str = "ext160k", steps: int = 5, warmup: int = 3, com
     row = {"workload": name, "chunk": chunk, "us": t * 1e3, "chunk_tokens_per_s": e.q_rows / (t / 1e3),
            "alg_tflops": tf, "alg_flops": flops, "bound": "tensor", "peak_tflops": peak, "peak_source": src,
            "frac": tf / peak, "mma": mma + "; peak: measured bf16 dense burst",
-           "traffic": profiled_traffic("extend_attention", name) if chunk == "bf16" else None}
+           "traffic": profiled_traffic("extend_attention", name if chunk == "bf16" else name + "_e4m3")}
     if not compare_fused:
         row["device_status"] = int(status.item())
         return row

@@ -30,14 +30,41 @@ struct PrefixUnit {
     int len, phys, base;
 };
 
-__device__ __forceinline__ PrefixUnit prefix_unit(const PrefixParams &p, long long u)
+// Position (sequence, page, kv head) of unit u; units are numbered with the
+// kv head innermost.
+struct UnitPos {
+    int b, pg, h;
+};
+
+__device__ __forceinline__ UnitPos unit_pos(const PrefixParams &p, long long u)
+{
+    UnitPos x;
+    x.h = static_cast<int>(u % p.hkv);
+    u /= p.hkv;
+    x.pg = static_cast<int>(u % p.max_pages);
+    x.b = static_cast<int>(u / p.max_pages);
+    return x;
+}
+
+// x += d in the same mixed radix (d.h < hkv and d.pg < max_pages, so one
+// carry per digit); the grid stride costs no division after the first unit.
+__device__ __forceinline__ void advance(UnitPos &x, const UnitPos &d, const PrefixParams &p)
+{
+    x.h += d.h;
+    int c = x.h >= p.hkv;
+    x.h -= c ? p.hkv : 0;
+    x.pg += d.pg + c;
+    c = x.pg >= p.max_pages;
+    x.pg -= c ? p.max_pages : 0;
+    x.b += d.b + c;
+}
+
+__device__ __forceinline__ PrefixUnit prefix_unit(const PrefixParams &p, const UnitPos &x)
 {
     PrefixUnit t;
-    long long r = u;
-    t.h = static_cast<int>(r % p.hkv);
-    r /= p.hkv;
-    t.pg = static_cast<int>(r % p.max_pages);
-    t.b = static_cast<int>(r / p.max_pages);
+    t.h = x.h;
+    t.pg = x.pg;
+    t.b = x.b;
     t.len = __ldg(p.prefix_lens + t.b);
     t.phys = __ldg(p.block_table + static_cast<size_t>(t.b) * p.max_pages + t.pg);
     t.base = __ldg(p.kv_indptr + t.b);
@@ -109,7 +136,9 @@ __global__ void __launch_bounds__(kPrefixThreads) dequant_prefix_kernel(const __
     long long u = blockIdx.x;
     if (u >= units)
         return;
-    PrefixUnit cur = prefix_unit(p, u);
+    UnitPos pos = unit_pos(p, u);
+    const UnitPos stride = unit_pos(p, gridDim.x);
+    PrefixUnit cur = prefix_unit(p, pos);
     int L = 0;
     bool staged = stage(cur, 0, L);
     uint32_t parity = 0u;        // bit k: phase parity of buffer k's barrier
@@ -120,7 +149,8 @@ __global__ void __launch_bounds__(kPrefixThreads) dequant_prefix_kernel(const __
         int Ln = 0;
         bool staged_n = false;
         if (un < units) {
-            nxt = prefix_unit(p, un);
+            advance(pos, stride, p);
+            nxt = prefix_unit(p, pos);
             staged_n = stage(nxt, k ^ 1, Ln);
         }
         if (staged) {
