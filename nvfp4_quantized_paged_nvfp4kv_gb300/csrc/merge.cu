@@ -14,17 +14,15 @@ namespace nvfp4kv {
 // combined in shared memory at the end.  The segment's contributor range is
 // worked out once per CTA, before the wait for the decode kernel.
 template <int kThreads>
-__global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__ DecodeParams p)
+__device__ __forceinline__ void merge_segment_row(const DecodeParams &p, int32_t *msmem)
 {
     constexpr int kGroups = kThreads / 32;
     constexpr int kUnroll = 8;                   // contributors a thread loads before using any
-    extern __shared__ int32_t msmem[];
     __shared__ float4 part[kGroups][32];
     __shared__ float part_m[kGroups], part_l[kGroups];
     __shared__ int seg[3];                       // first contributor, count (-1: empty sequence), its slot
     int32_t *scratch = msmem;
     int32_t *prefix = msmem + kPrefixScratch;
-    pdl_launch_dependents();                     // the next kernel may start its prologue
     const int nseg = p.hkv * p.row_groups;       // segments per sequence (row groups of kv heads)
     build_prefix(p.seq_lens, p.batch, nseg, p.max_pages * kPageSize, prefix, scratch, nullptr);
 
@@ -136,6 +134,20 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__
     } else {
         *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o) = res;
     }
+}
+
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__ DecodeParams p)
+{
+    extern __shared__ int32_t msmem[];
+    pdl_launch_dependents();                     // the next kernel may start its prologue
+    merge_segment_row<kThreads>(p, msmem);
+    // The next kernel in the stream waits for this grid only, and the decode's
+    // own outputs (segments one worker covered) must be complete by then: one
+    // thread of the grid always waits for the decode grid, so this grid cannot
+    // complete before it, even when no segment has partials to merge.
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        pdl_wait();
 }
 
 template <int kThreads>
