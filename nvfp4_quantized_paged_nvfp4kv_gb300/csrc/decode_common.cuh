@@ -151,10 +151,11 @@ struct Nvfp4Format {
     static constexpr int kStages = 5;
     static constexpr int kRecord = 2304;
 
+    // x as left by divide_by_tensor_scale, whose code flip comes with it
     __device__ static __forceinline__ void write_block(uint8_t *rec, bool is_v, int tok, int blk,
-                                                       const float (&x)[16])
+                                                       const float (&x)[16], uint32_t flip)
     {
-        write_nvfp4_block(rec, is_v, tok, blk, x);
+        write_nvfp4_block(rec, is_v, tok, blk, x, ScaleOfByte(), flip);
     }
 
     // m-tile j, row r (0..15) is channel 16j + r: each m-tile is one scale block.
@@ -251,8 +252,9 @@ struct Fp8Format {
     static constexpr int kStages = 3;
     static constexpr int kRecord = 4096;
 
+    // (the FP8 cache has no tensor scale: x is the row itself, flip kCodeFlip)
     __device__ static __forceinline__ void write_block(uint8_t *rec, bool is_v, int tok, int blk,
-                                                       const float (&x)[16])
+                                                       const float (&x)[16], uint32_t)
     {
         write_fp8_block(rec, is_v, tok, blk, x);
     }
@@ -497,9 +499,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
                         load16<true>(is_v ? p.v_new : p.k_new, src, x);
                     else
                         load16<false>(is_v ? p.v_new : p.k_new, src, x);
-                    divide_by_tensor_scale(x, head_tensor_scale(p.hs, is_v, hh, p.gscale));
+                    const uint32_t flip = divide_by_tensor_scale(x, head_tensor_scale(p.hs, is_v, hh, p.gscale));
                     Fmt::write_block(const_cast<uint8_t *>(p.pool) + (static_cast<size_t>(phys) * p.hkv + hh) * R,
-                                     is_v, tok, blk, x);
+                                     is_v, tok, blk, x, flip);
                     fence_proxy_async_global();
                 }
             }

@@ -317,8 +317,8 @@ __device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const T
             continue;
         float x[16];
         unpack<kChunk8>(r[u], x);
-        divide_by_tensor_scale(x, Gk);
-        write_nvfp4_block(p.pool + rec, false, tok, blk, x);
+        const uint32_t flip = divide_by_tensor_scale(x, Gk);
+        write_nvfp4_block(p.pool + rec, false, tok, blk, x, ScaleOfByte(), flip);
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -344,23 +344,23 @@ __device__ __forceinline__ void append_chunk_tile(const ExtendParams &p, const T
         if (ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
             uint32_t S0, S1, q0[2], q1[2];
             unpack<kChunk8>(r[2 * u], x);
-            divide_by_tensor_scale(x, Gv);
-            quantize_block(x, S0, q0);
+            uint32_t flip = divide_by_tensor_scale(x, Gv);
+            quantize_block(x, S0, q0, ScaleOfByte(), flip);
             unpack<kChunk8>(r[2 * u + 1], x);
-            divide_by_tensor_scale(x, Gv);
-            quantize_block(x, S1, q1);
+            flip = divide_by_tensor_scale(x, Gv);
+            quantize_block(x, S1, q1, ScaleOfByte(), flip);
             write_nvfp4_v_pair(p.pool + rec0, tok0, blk, S0, q0, S1, q1);
             continue;
         }
         if (ok0) {
             unpack<kChunk8>(r[2 * u], x);
-            divide_by_tensor_scale(x, Gv);
-            write_nvfp4_block(p.pool + rec0, true, tok0, blk, x);
+            const uint32_t flip = divide_by_tensor_scale(x, Gv);
+            write_nvfp4_block(p.pool + rec0, true, tok0, blk, x, ScaleOfByte(), flip);
         }
         if (ok1) {
             unpack<kChunk8>(r[2 * u + 1], x);
-            divide_by_tensor_scale(x, Gv);
-            write_nvfp4_block(p.pool + rec1, true, tok1, blk, x);
+            const uint32_t flip = divide_by_tensor_scale(x, Gv);
+            write_nvfp4_block(p.pool + rec1, true, tok1, blk, x, ScaleOfByte(), flip);
         }
     }
 }
@@ -685,6 +685,15 @@ __global__ void __launch_bounds__(kTcThreads, 2) extend_tc_kernel(const __grid_c
 // kernel above.  Warp 9 issues the TMA loads: key tiles into a ring of three
 // stages, value tiles into a ring of two, so that a tile's load latency is
 // covered by the work on the tiles before it.
+//
+// With a bf16 chunk (kChunkBf16) the prefix tiles run as above and the chunk
+// tiles come from the converter warps: each bf16 key tile is multiplied by a
+// power of two 2^f that puts its largest element in [128, 256) and split, as
+// Q is, into hi and lo E4M3 terms (exact for bf16 under the same bound); hi
+// goes to the key stage, lo to the idle value staging stage, and Q K^T
+// accumulates the four products of the terms.  The tile's 2^-f reaches the
+// softmax through a small ring in shared memory with its own barriers.  The
+// values are converted bf16 -> f16 as in the kernel above.
 constexpr int kF8Threads = kTcThreads + 32;                 // + the TMA warp
 constexpr int kF8TmaWarp = 9;
 constexpr int kF8QTerms = 2;
@@ -704,10 +713,18 @@ enum {
     kF8KFull = 0, kF8KEmpty = kF8KFull + kF8KStages, kF8VrawFull = kF8KEmpty + kF8KStages,
     kF8VrawEmpty = kF8VrawFull + kF8VrawStages, kF8VFull = kF8VrawEmpty + kF8VrawStages, kF8VEmpty = kF8VFull + 2,
     kF8SFull = kF8VEmpty + 2, kF8PFull = kF8SFull + 2, kF8PvDone = kF8PFull + 2, kF8Done = kF8PvDone + 2,
-    kF8NumBars = kF8Done + 1
+    // bf16 chunk tiles: the low key term's stage released by Q K^T, the
+    // tile scale ring filled by the converters, and two converter-only
+    // barriers (the tile maximum exchanged; every term stored), each used by
+    // alternate chunk tiles
+    kF8KloEmpty = kF8Done + 1, kF8KScale = kF8KloEmpty + 2, kF8KRed = kF8KScale + 8, kF8KTerm = kF8KRed + 2,
+    kF8NumBars = kF8KTerm + 2
 };
+constexpr int kF8KScaleRing = 8;                            // converters run at most ~5 tiles ahead
 constexpr uint32_t kF8OffRowInv = (kF8OffBar + 8 * kF8NumBars + 15) / 16 * 16;
-constexpr uint32_t kF8OffTmemSlot = kF8OffRowInv + 4 * kTcRows;
+constexpr uint32_t kF8OffKScale = kF8OffRowInv + 4 * kTcRows;      // 2^-f of chunk tiles [ring]
+constexpr uint32_t kF8OffKRed = kF8OffKScale + 4 * kF8KScaleRing;  // converter warps' maxima [2][4]
+constexpr uint32_t kF8OffTmemSlot = kF8OffKRed + 4 * 8;
 constexpr uint32_t kF8OffFail = kF8OffTmemSlot + 4;
 constexpr uint32_t kF8Smem = kF8OffFail + 4 + 1024;
 static_assert(kF8OffRowInv % 16 == 0, "row scale table alignment");
@@ -721,7 +738,7 @@ __device__ __forceinline__ float2 e4m3x2_value(uint32_t two)
     return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
-template <bool kAppend>
+template <bool kAppend, bool kChunkBf16>
 __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_constant__ ExtendParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -839,6 +856,16 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
             mbar_init(B(kF8PvDone + k), 1);
         }
         mbar_init(B(kF8Done), 1);
+        if constexpr (kChunkBf16) {
+            for (int k = 0; k < 2; ++k)
+                mbar_init(B(kF8KloEmpty + k), 1);
+            for (int k = 0; k < kF8KScaleRing; ++k)
+                mbar_init(B(kF8KScale + k), 1);
+            for (int k = 0; k < 2; ++k) {
+                mbar_init(B(kF8KRed + k), kProducerThreads);
+                mbar_init(B(kF8KTerm + k), kProducerThreads);
+            }
+        }
         *fail = 0;
         fence_mbar_init();
     }
@@ -855,7 +882,8 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
             // key tile i: K into stage i % kF8KStages, V into staging stage
             // i % kF8VrawStages
             int nk = 0, nv = 0;                  // loads issued
-            for (int i = 0; i < c.n_tiles; ++i) {
+            const int n_tma = kChunkBf16 ? c.n_pre : c.n_tiles;     // bf16 chunk tiles come from the converters
+            for (int i = 0; i < n_tma; ++i) {
                 const int sk = i % kF8KStages, sv = i % kF8VrawStages;
                 const bool pre = i < c.n_pre;
                 const int rowc = pre ? static_cast<int>(c.p0) + i * kTcKeys : c.c0 + (i - c.n_pre) * kTcKeys;
@@ -904,6 +932,19 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
                         umma_f8(tmem + kColS + b * kTcKeys,
                                 smem_desc(base + kF8OffQ + t * kF8QTerm + ks * 32, 16, 1024),
                                 smem_desc(kb + ks * 32, 16, 1024), i_qk, t > 0 || ks > 0);
+                if (kChunkBf16 && i >= c.n_pre) {
+                    // the chunk tile's low key term, in the staging stage
+                    const int sl = (i - c.n_pre) & 1;
+                    const uint32_t klo = base + kF8OffVraw + sl * kF8KBytes;
+#pragma unroll
+                    for (int t = 0; t < kF8QTerms; ++t)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            umma_f8(tmem + kColS + b * kTcKeys,
+                                    smem_desc(base + kF8OffQ + t * kF8QTerm + ks * 32, 16, 1024),
+                                    smem_desc(klo + ks * 32, 16, 1024), i_qk, true);
+                    umma_commit(B(kF8KloEmpty + sl));
+                }
                 umma_commit(B(kF8SFull + b));
                 umma_commit(B(kF8KEmpty + st));
             };
@@ -964,7 +1005,119 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
         // xored with the key's low three bits).
         const int pt = tid - kSoftmaxThreads;
         const int key = pt & 63, half = pt >> 6;
+        // bf16 chunk tile i (kChunkBf16): thread pt takes channels 64 half ..
+        // + 63 of key pt % 64 for K, then for V.  The converters meet only on
+        // mbarriers with bounded waits (a thread that gave up elsewhere stops
+        // arriving, and the others' waits give up after it).  Returns false
+        // when a wait gave up.
+        auto chunk_tile = [&](int i) {
+            const int cc = i - c.n_pre, sk = i % kF8KStages, sl = cc & 1, st = i & 1;
+            const bool live = cc * kTcKeys + key < c.C;
+            const size_t src =
+                (static_cast<size_t>(c.c0 + cc * kTcKeys + key) * p.hkv + h) * kHeadDim + 64 * half;
+            const uint16_t *kc = static_cast<const uint16_t *>(p.k_chunk);
+            const uint16_t *vc = static_cast<const uint16_t *>(p.v_chunk);
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            uint4 kr[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                kr[j] = live ? ldg_nc(kc + src + 8 * j) : zero;
+            // the tile's largest |k| (bf16 magnitudes compare as integers)
+            uint32_t m2 = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                m2 = __vmaxu2(m2, kr[j].x & 0x7fff7fffu);
+                m2 = __vmaxu2(m2, kr[j].y & 0x7fff7fffu);
+                m2 = __vmaxu2(m2, kr[j].z & 0x7fff7fffu);
+                m2 = __vmaxu2(m2, kr[j].w & 0x7fff7fffu);
+            }
+            float am = __uint_as_float(max(m2 & 0xffffu, m2 >> 16) << 16);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                am = fmaxf(am, __shfl_xor_sync(kFullMask, am, o));
+            float *kred = reinterpret_cast<float *>(gbase + kF8OffKRed) + 4 * sl;
+            if (lane == 0)
+                kred[warp - kSoftmaxThreads / 32] = am;
+            mbar_arrive(B(kF8KRed + sl));
+            if (!wait_or_fail(B(kF8KRed + sl), (cc >> 1) & 1, fail, p.dev_status, p.wait_limit))
+                return false;
+            am = fmaxf(fmaxf(kred[0], kred[1]), fmaxf(kred[2], kred[3]));
+            int e = 0;
+            if (am >= 1e-30f)
+                e = 7 - (static_cast<int>((__float_as_uint(am) >> 23) & 0xffu) - 127);
+            const float sc = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+            // the key stage was last read by Q K^T of tile i - 3, the low-term
+            // stage by Q K^T of chunk tile cc - 2
+            if (i >= kF8KStages &&
+                !wait_or_fail(B(kF8KEmpty + sk), (i / kF8KStages - 1) & 1, fail, p.dev_status, p.wait_limit))
+                return false;
+            if (cc >= 2 &&
+                !wait_or_fail(B(kF8KloEmpty + sl), ((cc >> 1) - 1) & 1, fail, p.dev_status, p.wait_limit))
+                return false;
+            const uint32_t khi = base + kF8OffK + sk * kF8KBytes, klo = base + kF8OffVraw + sl * kF8KBytes;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t w[4] = {kr[j].x, kr[j].y, kr[j].z, kr[j].w};
+                uint32_t th[2], tl[2];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float a = __uint_as_float(w[k] << 16) * sc, bb = __uint_as_float(w[k] & 0xffff0000u) * sc;
+                    const uint32_t hi2 = f32x2_to_e4m3x2(a, bb);
+                    const float2 v = e4m3x2_value(hi2);
+                    const uint32_t lo2 = f32x2_to_e4m3x2(a - v.x, bb - v.y);   // exact remainders
+                    if (k & 1) {
+                        th[k >> 1] |= hi2 << 16;
+                        tl[k >> 1] |= lo2 << 16;
+                    } else {
+                        th[k >> 1] = hi2;
+                        tl[k >> 1] = lo2;
+                    }
+                }
+                const uint32_t off =
+                    key * 128u + ((static_cast<uint32_t>(4 * half + (j >> 1)) ^ (key & 7u)) << 4) + (j & 1) * 8u;
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(khi + off), "r"(th[0]), "r"(th[1]) : "memory");
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(klo + off), "r"(tl[0]), "r"(tl[1]) : "memory");
+            }
+            fence_async_shared();
+            mbar_arrive(B(kF8KTerm + sl));
+            if (pt == 0) {
+                // every converter's terms are stored: publish the tile
+                if (!wait_or_fail(B(kF8KTerm + sl), (cc >> 1) & 1, fail, p.dev_status, p.wait_limit))
+                    return false;
+                reinterpret_cast<float *>(gbase + kF8OffKScale)[cc % kF8KScaleRing] =
+                    __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+                mbar_arrive(B(kF8KScale + cc % kF8KScaleRing));
+                mbar_arrive(B(kF8KFull + sk));
+            }
+            // values: bf16 -> f16 into stage st (last read by P V of tile i - 2)
+            uint4 vr[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                vr[j] = live ? ldg_nc(vc + src + 8 * j) : zero;
+            if (i >= 2 && !wait_or_fail(B(kF8VEmpty + st), ((i >> 1) - 1) & 1, fail, p.dev_status, p.wait_limit))
+                return false;
+            const uint32_t dst = base + kF8OffV + st * kKVBytes;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint4 f;
+                f.x = bf16x2_to_f16x2(vr[j].x, 1.f);
+                f.y = bf16x2_to_f16x2(vr[j].y, 1.f);
+                f.z = bf16x2_to_f16x2(vr[j].z, 1.f);
+                f.w = bf16x2_to_f16x2(vr[j].w, 1.f);
+                sts128(dst + sw128(kTcKeys, key, 8 * half + j), f);
+            }
+            fence_async_shared();
+            mbar_arrive(B(kF8VFull + st));
+            return true;
+        };
         for (int i = 0; i < c.n_tiles; ++i) {
+            if constexpr (kChunkBf16) {
+                if (i >= c.n_pre) {
+                    if (!chunk_tile(i))
+                        break;
+                    continue;
+                }
+            }
             const int st = i & 1, sv = i % kF8VrawStages;
             const int lim = i < c.n_pre ? c.P - i * kTcKeys : c.C - (i - c.n_pre) * kTcKeys;
             if (!wait_or_fail(B(kF8VrawFull + sv), (i / kF8VrawStages) & 1, fail, p.dev_status, p.wait_limit))
@@ -1002,17 +1155,16 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
         if constexpr (kAppend) {
             const int per = kTcKeys * g;
             for (int kt = (row0 + per - 1) / per; kt < (row0 + kTcRows + per - 1) / per && kt * kTcKeys < c.C; ++kt)
-                append_chunk_tile<true>(p, c, h, kt * kTcKeys, pt);
+                append_chunk_tile<!kChunkBf16>(p, c, h, kt * kTcKeys, pt);
         }
     } else {
         // softmax: thread r owns row row0 + r, tensor-memory lane r; scores are
-        // S * 2^-e_r
+        // S * 2^-e_r (times 2^-f for a bf16 chunk tile)
         const int r = tid;
         const int row = row0 + r;
         const int t = min(row, R - 1) / g;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const float inv = rowinv[r];
-        const uint64_t inv2 = f32x2_pack(inv, inv);
+        const float inv_row = rowinv[r];
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         auto wait_warp = [&](uint32_t bar_addr, uint32_t parity) {
@@ -1022,6 +1174,15 @@ __global__ void __launch_bounds__(kF8Threads, 2) extend_f8_kernel(const __grid_c
             const int b = i & 1;
             if (!(ok = wait_warp(B(kF8SFull + b), (i >> 1) & 1)))
                 break;
+            float inv = inv_row;
+            if (kChunkBf16 && i >= c.n_pre) {
+                // the chunk tile's key scale 2^-f, published with its terms
+                const int cc = i - c.n_pre;
+                if (!(ok = wait_warp(B(kF8KScale + cc % kF8KScaleRing), (cc / kF8KScaleRing) & 1)))
+                    break;
+                inv *= reinterpret_cast<const volatile float *>(gbase + kF8OffKScale)[cc % kF8KScaleRing];
+            }
+            const uint64_t inv2 = f32x2_pack(inv, inv);
             tc_fence_after_sync();
             uint32_t sr0[32], sr1[32];
             tmem_ld32(lane_base + kColS + b * kTcKeys, sr0);
@@ -1164,15 +1325,24 @@ bool fill_tensor_maps(ExtendParams &q)
 
 } // namespace
 
+constexpr int64_t kMixedPrefixRatio = 8;
+
 cudaError_t launch_extend_attention(const ExtendParams &p, cudaStream_t s)
 {
     const int64_t rows = static_cast<int64_t>(p.max_q_len) * p.group;
     const dim3 grid(static_cast<unsigned>((rows + kTcRows - 1) / kTcRows), p.hkv, p.batch);
-    if (p.chunk_e4m3) {
-        // every key tile E4M3: the TMA + kind::f8f6f4 kernel
+    if (p.chunk_e4m3 || p.prefix_rows >= kMixedPrefixRatio * static_cast<int64_t>(p.q_rows)) {
+        // E4M3 prefix tiles (and chunk tiles, when E4M3 too): the TMA +
+        // kind::f8f6f4 kernel; bf16 chunk tiles go through its converters,
+        // at a higher cost per tile than on the kind::f16 kernel, so a bf16
+        // chunk takes this kernel only when the prefix rows outnumber the
+        // chunk rows by kMixedPrefixRatio.
         ExtendParams q = p;
         if (fill_tensor_maps(q)) {
-            const auto kernel = q.pool != nullptr ? extend_f8_kernel<true> : extend_f8_kernel<false>;
+            const auto kernel = p.chunk_e4m3 ? (q.pool != nullptr ? extend_f8_kernel<true, false>
+                                                                  : extend_f8_kernel<false, false>)
+                                             : (q.pool != nullptr ? extend_f8_kernel<true, true>
+                                                                  : extend_f8_kernel<false, true>);
             cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8Smem);
             if (e != cudaSuccess)
                 return e;

@@ -98,23 +98,23 @@ __global__ void __launch_bounds__(256, kBf16 ? 5 : 4) quantize_nvfp4_kernel(cons
     if (is_v && ok0 && ok1 && (s0 & 1) == 0 && s1 == s0 + 1) {
         uint32_t S0, S1, c0[2], c1[2];
         unpack<kBf16>(r0, x);
-        divide_by_tensor_scale(x, G);
-        quantize_block(x, S0, c0, tab);
+        uint32_t flip = divide_by_tensor_scale(x, G);
+        quantize_block(x, S0, c0, tab, flip);
         unpack<kBf16>(r1, x);
-        divide_by_tensor_scale(x, G);
-        quantize_block(x, S1, c1, tab);
+        flip = divide_by_tensor_scale(x, G);
+        quantize_block(x, S1, c1, tab, flip);
         write_nvfp4_v_pair(p.pool + rec0, tok0, blk, S0, c0, S1, c1);
         return;
     }
     if (ok0) {
         unpack<kBf16>(r0, x);
-        divide_by_tensor_scale(x, G);
-        write_nvfp4_block(p.pool + rec0, is_v, tok0, blk, x, tab);
+        const uint32_t flip = divide_by_tensor_scale(x, G);
+        write_nvfp4_block(p.pool + rec0, is_v, tok0, blk, x, tab, flip);
     }
     if (ok1) {
         unpack<kBf16>(r1, x);
-        divide_by_tensor_scale(x, G);
-        write_nvfp4_block(p.pool + rec1, is_v, tok1, blk, x, tab);
+        const uint32_t flip = divide_by_tensor_scale(x, G);
+        write_nvfp4_block(p.pool + rec1, is_v, tok1, blk, x, tab, flip);
     }
 }
 

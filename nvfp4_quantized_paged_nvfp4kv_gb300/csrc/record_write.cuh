@@ -64,7 +64,10 @@ __device__ __forceinline__ TensorScale tensor_scale(float G)
 }
 
 // Values relative to the tensor scale G: the block procedure runs on the
-// correctly rounded quotients fl32(x / G) (nothing to do at G = 1).
+// correctly rounded quotients y = fl32(x / G) (nothing to do at G = 1).
+// Returns the code flip quantize_block must apply: kCodeFlip when x now
+// holds y, 0 when it holds -y (the division-free path, which ends on the
+// negated quotients; quantize_block negates its input anyway).
 //
 // No division per element.  With r = RN(1/G), q0 = RN(x r) is within two ulps
 // of x / G; one correction step, q1 = RN(q0 + (x - q0 G) r) with the
@@ -77,40 +80,43 @@ __device__ __forceinline__ TensorScale tensor_scale(float G)
 // a code or a scale (a block of them has scale 0; beside a larger value,
 // whose scale is at least 2^-9, they give a zero code), and the steps keep
 // its sign.  A block with a larger value takes the IEEE division.  The steps
-// are written on q G - x (the addend -x), so that a zero quotient keeps the
-// sign of x: q0 = -0 for x = -0, q0 G - x = +0, and -0 - (+0) r = -0.
-__device__ __forceinline__ void divide_by_tensor_scale(float (&x)[16], TensorScale ts)
+// run on the negated terms -- q0' = RN(x (-r)), e = RN(x + q0' G) = x - q0 G,
+// q' = RN(q0' + e (-r)) = -q, twice -- so that a zero quotient keeps the sign
+// of x (a remainder that cancels is +0, and -0 + -0 stays -0) and x needs no
+// negation.
+constexpr uint32_t kCodeFlip = 0x88888888u;
+
+__device__ __forceinline__ uint32_t divide_by_tensor_scale(float (&x)[16], TensorScale ts)
 {
     if (ts.G == 1.f)
-        return;
+        return kCodeFlip;
     const float m = fmaxf(fmax3(fmax3(fabsf(x[0]), fabsf(x[1]), fabsf(x[2])),
                                 fmax3(fabsf(x[3]), fabsf(x[4]), fabsf(x[5])),
                                 fmax3(fabsf(x[6]), fabsf(x[7]), fabsf(x[8]))),
                           fmax3(fmax3(fabsf(x[9]), fabsf(x[10]), fabsf(x[11])),
                                 fmax3(fabsf(x[12]), fabsf(x[13]), fabsf(x[14])), fabsf(x[15])));
     if (ts.r != 0.f && m < 0x1p64f) {
-        const uint64_t r2 = f32x2_pack(ts.r, ts.r), nr2 = f32x2_pack(-ts.r, -ts.r), g2 = f32x2_pack(ts.G, ts.G);
+        const uint64_t nr2 = f32x2_pack(-ts.r, -ts.r), g2 = f32x2_pack(ts.G, ts.G);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint64_t v2 = f32x2_pack(x[2 * j], x[2 * j + 1]);
-            const uint64_t nv2 = v2 ^ 0x8000000080000000ull;
-            uint64_t q = mul_f32x2(v2, r2);
-            q = fma_f32x2(fma_f32x2(q, g2, nv2), nr2, q);
-            q = fma_f32x2(fma_f32x2(q, g2, nv2), nr2, q);
+            uint64_t q = mul_f32x2(v2, nr2);
+            q = fma_f32x2(fma_f32x2(q, g2, v2), nr2, q);
+            q = fma_f32x2(fma_f32x2(q, g2, v2), nr2, q);
             x[2 * j] = f32x2_lo(q);
             x[2 * j + 1] = f32x2_hi(q);
         }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            x[i] = __fdiv_rn(x[i], ts.G);
+        return 0u;
     }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        x[i] = __fdiv_rn(x[i], ts.G);
+    return kCodeFlip;
 }
 
-__device__ __forceinline__ void divide_by_tensor_scale(float (&x)[16], float G)
+__device__ __forceinline__ uint32_t divide_by_tensor_scale(float (&x)[16], float G)
 {
-    if (G != 1.f)
-        divide_by_tensor_scale(x, tensor_scale(G));
+    return G != 1.f ? divide_by_tensor_scale(x, tensor_scale(G)) : kCodeFlip;
 }
 
 // The value s of an E4M3 block-scale byte S (0 .. 126) and RN(1/s) (0 for
@@ -151,10 +157,12 @@ __device__ __forceinline__ void fill_scale_table(float2 *t)
 // e = RN(x + q0' s), q' = RN(q0' + e (-r)) = -RN(x / s) exactly -- because then
 // a zero quotient keeps the sign of x (a remainder that cancels to zero is +0,
 // and -0 + -0 is -0 where +0 + -0 would lose it); E2M1 rounding is symmetric,
-// so the codes of -q' are those of q' with each sign bit flipped.
+// so the codes of -q' are those of q' with each sign bit flipped (flip =
+// kCodeFlip).  Given x = -y (flip = 0), the same steps end on RN(y / s) and
+// its codes need no flip.
 template <class ScaleFn = ScaleOfByte>
 __device__ __forceinline__ void quantize_block(const float (&x)[16], uint32_t &scale_byte, uint32_t (&packed)[2],
-                                               ScaleFn scale_of = ScaleFn())
+                                               ScaleFn scale_of = ScaleFn(), uint32_t flip = kCodeFlip)
 {
     // amax with three-input maxima (a NaN element is ignored, as by fmaxf);
     // capped at the largest finite float so the quotient below stays finite
@@ -187,8 +195,8 @@ __device__ __forceinline__ void quantize_block(const float (&x)[16], uint32_t &s
             q[2 * j] = f32x2_lo(qq);
             q[2 * j + 1] = f32x2_hi(qq);
         }
-        packed[0] = f32x8_to_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]) ^ 0x88888888u;
-        packed[1] = f32x8_to_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]) ^ 0x88888888u;
+        packed[0] = f32x8_to_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]) ^ flip;
+        packed[1] = f32x8_to_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]) ^ flip;
     }
 }
 
@@ -197,10 +205,10 @@ __device__ __forceinline__ void quantize_block(const float (&x)[16], uint32_t &s
 // that hold its token pair with atomic AND/OR on the thread's own nibbles.
 template <class ScaleFn = ScaleOfByte>
 __device__ __forceinline__ void write_nvfp4_block(uint8_t *rec, bool is_v, int tok, int blk, const float (&x)[16],
-                                                  ScaleFn scale_of = ScaleFn())
+                                                  ScaleFn scale_of = ScaleFn(), uint32_t flip = kCodeFlip)
 {
     uint32_t S, packed[2];
-    quantize_block(x, S, packed, scale_of);
+    quantize_block(x, S, packed, scale_of, flip);
     if (!is_v) {
         *reinterpret_cast<uint2 *>(rec + tok * 64 + blk * 8) = make_uint2(packed[0], packed[1]);
         rec[2048 + tok * 8 + blk] = static_cast<uint8_t>(S);

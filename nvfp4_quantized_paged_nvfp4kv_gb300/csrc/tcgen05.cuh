@@ -193,4 +193,5 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+
 } // namespace nvfp4kv

@@ -247,3 +247,32 @@ def test_fused_append_per_head_scales():
     assert_close(got, oracle_out(e, x), "fused extend out, per-head scales")
     for g_, w_ in zip(planes, oracle_planes(e, x, slots, num_pages, global_scale=0.37, head_scales=hs)):
         np.testing.assert_array_equal(g_, w_)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_bf16_chunk_behind_long_prefix(fused):
+    """A bf16 chunk behind FP8 prefixes of at least eight times its rows runs
+    on the E4M3-key kernel, its key tiles split into two E4M3 terms under a
+    power-of-two scale per tile.  Keys of magnitudes 1e-3 .. 1e3 (past E4M3's
+    448 and below its normal range; q scaled down to keep the scores
+    moderate), one sequence with no prefix among long ones, chunks across
+    64-key tiles: attention against the oracle, cache bytes bit for bit."""
+    e = workloads.extend_custom((3000, 0, 2500), (130, 70, 65), 48, 8, seed=91)
+    assert e.prefix_rows >= 8 * e.q_rows
+    x = workloads.extend_inputs(e)
+    rng = np.random.default_rng(92)
+    f = torch.from_numpy(10.0 ** rng.uniform(-3, 3, (e.q_rows, e.num_kv_heads, 1))).float()
+    x["k_chunk"] = (x["k_chunk"].float() * f).to(torch.bfloat16)
+    x["q"] = (x["q"].float() * 0.01).to(torch.bfloat16)
+    want = oracle_out(e, x)
+    if not fused:
+        got = run(e, to_dev(x)).cpu().numpy()
+        assert_close(got, want, "bf16 chunk behind a long prefix")
+        return
+    slots, num_pages = chunk_slots(e, seed=93)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got, planes = run_fused(e, x, slots, num_pages, status=status)
+    assert status.item() == 0
+    assert_close(got, want, "fused bf16 chunk behind a long prefix")
+    for g_, w_ in zip(planes, oracle_planes(e, x, slots, num_pages)):
+        np.testing.assert_array_equal(g_, w_)

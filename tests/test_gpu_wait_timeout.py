@@ -79,14 +79,17 @@ def test_prefix_dequant_wait_runs_out_then_recovers(run_out):
     np.testing.assert_array_equal(k.cpu().numpy(), want_k)
 
 
-@pytest.mark.parametrize("chunk", ["bf16", "e4m3"])
+@pytest.mark.parametrize("chunk", ["bf16", "e4m3", "bf16_long_prefix"])
 @pytest.mark.parametrize("fused", [False, True])
 def test_extend_wait_runs_out_then_recovers(run_out, fused, chunk):
     """The tensor-core extend kernels (bf16 chunks; E4M3 chunks, whose key
-    tiles come by TMA): their roles give up, the MMAs and TMA loads already
-    issued are waited for before the CTA frees tensor memory and exits."""
-    e = workloads.extend_custom((70, 300), (100, 129), 16, 2, seed=63)
-    x = workloads.extend_inputs(e, chunk=chunk)
+    tiles come by TMA; bf16 chunks behind long prefixes, whose chunk tiles the
+    converters split and publish): their roles give up, the MMAs and TMA loads
+    already issued are waited for before the CTA frees tensor memory and exits."""
+    e8 = chunk == "e4m3"
+    prefix = (3000, 2500) if chunk == "bf16_long_prefix" else (70, 300)
+    e = workloads.extend_custom(prefix, (100, 129), 16, 2, seed=63)
+    x = workloads.extend_inputs(e, chunk="e4m3" if e8 else "bf16")
     xd = {k: t.to(DEV) for k, t in x.items()}
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     cache = nv.NVFP4Cache.allocate(64, e.num_kv_heads, device=DEV)
@@ -109,7 +112,7 @@ def test_extend_wait_runs_out_then_recovers(run_out, fused, chunk):
     assert nv.read_device_status(status) == 0
     want = oracle.extend_attention(x["q"].float().numpy(), x["q_indptr"].numpy(), x["k_prefix"].numpy(),
                                    x["v_prefix"].numpy(), x["kv_indptr"].numpy(), x["prefix_lens"].numpy(),
-                                   x["k_chunk"].numpy() if chunk == "e4m3" else x["k_chunk"].float().numpy(),
-                                   x["v_chunk"].numpy() if chunk == "e4m3" else x["v_chunk"].float().numpy())
+                                   x["k_chunk"].numpy() if e8 else x["k_chunk"].float().numpy(),
+                                   x["v_chunk"].numpy() if e8 else x["v_chunk"].float().numpy())
     assert_close(out.cpu().numpy(), want, f"extend ({chunk} chunk) after a timeout")
 
