@@ -770,9 +770,14 @@ def extend_rows(dev, name: str = "ext160k", steps: int = 5, warmup: int = 3, com
     if peak is None:
         peak, src = 1900.0, "fallback"
     tf = flops / (t / 1e3) / 1e12
-    mma = ("tcgen05.mma kind::f16 M128 (f16 operands, fp32 accumulators in tensor memory)" if chunk == "bf16" else
-           "tcgen05.mma M128: Q K^T kind::f8f6f4 (E4M3 key tiles by TMA, Q as two E4M3 terms), P V kind::f16; "
-           "fp32 accumulators in tensor memory")
+    f8 = ("tcgen05.mma M128: Q K^T kind::f8f6f4 (E4M3 key tiles by TMA, Q as two E4M3 terms), P V kind::f16; "
+          "fp32 accumulators in tensor memory")
+    if chunk == "e4m3":
+        mma = f8
+    elif e.prefix_rows >= 8 * e.q_rows:        # the library's dispatch: a bf16 chunk behind a long prefix
+        mma = f8 + "; the bf16 chunk tiles split into two E4M3 terms by the converter warps"
+    else:
+        mma = "tcgen05.mma kind::f16 M128 (f16 operands, fp32 accumulators in tensor memory)"
     row = {"workload": name, "chunk": chunk, "us": t * 1e3, "chunk_tokens_per_s": e.q_rows / (t / 1e3),
            "alg_tflops": tf, "alg_flops": flops, "bound": "tensor", "peak_tflops": peak, "peak_source": src,
            "frac": tf / peak, "mma": mma + "; peak: measured bf16 dense burst",
