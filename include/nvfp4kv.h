@@ -323,10 +323,16 @@ nvfp4kv_status nvfp4kv_dequant_prefix_fp8(const nvfp4kv_cache *cache,
  *            [batch] (device)
  *   max_q_len  host bound on every q_indptr[b+1] - q_indptr[b]; it sizes the
  *            launch
- * Arithmetic: q * sm_scale * log2(e) and bf16 chunk keys and values are
- * rounded to fp16 (exact for bf16 values of magnitude 2^-14 .. 65504; the
- * caller keeps |q * sm_scale| and the chunk's values below 65504), E4M3 to
- * fp16 is exact, scores and outputs accumulate in fp32, softmax weights are
+ * Arithmetic.  With E4M3 chunk K/V, or bf16 ones behind prefix_rows of at
+ * least 8 * q_rows: q meets the keys as two E4M3 terms of its bf16 values,
+ * each row multiplied by a power of two first (exact for every element but
+ * those below 2^-10 of the row's largest, whose error stays under 2^-17 of
+ * it), and sm_scale * log2(e) is applied to the fp32 scores; bf16 chunk keys
+ * are split the same way per 64-key tile.  Otherwise q * sm_scale * log2(e)
+ * and bf16 chunk keys are rounded to fp16 (exact for bf16 values of magnitude
+ * 2^-14 .. 65504; the caller keeps |q * sm_scale| below 65504).  Values: E4M3
+ * to fp16 is exact, bf16 chunk values are rounded to fp16 (kept below 65504
+ * by the caller).  Scores and outputs accumulate in fp32, softmax weights are
  * rounded to fp16 for the value product.
  * Pointers 16-byte aligned (index arrays 4-byte).  Group g = num_q_heads /
  * num_kv_heads in 1..8; batch and num_kv_heads at most 65535.  Device check:
