@@ -53,14 +53,14 @@ __device__ __forceinline__ void load16(const void *src, size_t elem_off, float (
 }
 
 // A tensor scale G and r = RN(1/G); r = 0 where G lies outside [2^-32, 2^32]
-// (every quotient then takes the IEEE division).
+// (every quotient then takes the IEEE division) and at G = 1 (no division).
 struct TensorScale {
     float G, r;
 };
 
 __device__ __forceinline__ TensorScale tensor_scale(float G)
 {
-    return {G, (G >= 0x1p-32f && G <= 0x1p32f) ? __frcp_rn(G) : 0.f};
+    return {G, (G != 1.f && G >= 0x1p-32f && G <= 0x1p32f) ? __frcp_rn(G) : 0.f};
 }
 
 // Values relative to the tensor scale G: the block procedure runs on the
