@@ -610,17 +610,21 @@ def other_rows(dev):
     kv_copies = [(k.clone(), v.clone()) for _ in range(copies)]
     pools = [nv.NVFP4Cache.allocate(num_pages, w.num_kv_heads, device=dev, zero=False) for _ in range(copies)]
 
-    def back_to_back(call, n=2 * copies):
+    def back_to_back(call, n=2 * copies, passes=5):
+        """median over `passes` passes of the mean of n calls between two events"""
         for i in range(3):
             call(i)
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for i in range(n):
-            call(i)
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / n
+        means = []
+        for _ in range(passes):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for i in range(n):
+                call(i)
+            b.record()
+            torch.cuda.synchronize()
+            means.append(a.elapsed_time(b) / n)
+        return statistics.median(means)
 
     def quantize_into(g=1.0, factors=None):
         cs = [nv.NVFP4Cache(c.pool, global_scale=g, head_scales=factors) for c in pools]
@@ -668,7 +672,8 @@ def other_rows(dev):
         "extend_160k_chunk8k": extend,
         "extend_160k_chunk8k_e4m3": extend8,
         "prefill_fp8_8k": prefill,
-        "timing": "quantize, prefix and 160K decode rows: calls back to back between two CUDA events, each "
+        "timing": "quantize, prefix and 160K decode rows: calls back to back between two CUDA events (the "
+                  "median of five such passes), each "
                   "quantize call with its own copy of the inputs and its own cache, rotated among copies "
                   "totalling over 3x L2 (the other inputs exceed L2); "
                   "multi-query rows: one call per event pair after a 256 MB write and a 256 MB read (L2 "
