@@ -817,12 +817,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_ke
 // One CTA per (sequence, kv head, query head of the group), of kThreads
 // threads: 32 per contributor group.  Segments that one worker covered were
 // written by the decode kernel; empty sequences get zeros here.  The launch
-// picks the CTA width from the contributors a segment has on average: 128
-// threads (72 registers, seven CTAs to an SM, so a grid of up to 7 x 152 CTAs
-// runs in one wave once the decode CTAs have left) while four groups take a
-// segment's contributors in about one round of loads, wider CTAs for the few
-// long segments of a small batch at a long context.
+// picks the CTA width from the contributors a segment has on average: 64
+// threads while two groups take them in one round of loads -- capped at 64
+// registers, such a CTA fits beside a decode CTA (61,440 of an SM's 65,536
+// registers), so merge CTAs become resident while the decode runs and the next
+// step's decode CTA need not wait for them to leave; 128 threads while four
+// groups do (seven CTAs to an SM once the decode CTA has left); wider CTAs for
+// the few long segments of a small batch at a long context.
 template <int kThreads>
-__global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__ DecodeParams p);
+__global__ void __launch_bounds__(kThreads, kThreads == 64 ? 16 : 1) merge_kernel(const __grid_constant__ DecodeParams p);
 
 } // namespace nvfp4kv

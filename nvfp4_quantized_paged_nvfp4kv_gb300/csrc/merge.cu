@@ -137,7 +137,7 @@ __device__ __forceinline__ void merge_segment_row(const DecodeParams &p, int32_t
 }
 
 template <int kThreads>
-__global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__ DecodeParams p)
+__global__ void __launch_bounds__(kThreads, kThreads == 64 ? 16 : 1) merge_kernel(const __grid_constant__ DecodeParams p)
 {
     extern __shared__ int32_t msmem[];
     pdl_launch_dependents();                     // the next kernel may start its prologue
@@ -179,7 +179,9 @@ cudaError_t launch_merge(const DecodeParams &p, cudaStream_t s)
         return launch_merge_width<512>(p, s);
     if (per_segment > 8 * 4)
         return launch_merge_width<256>(p, s);
-    return launch_merge_width<128>(p, s);
+    if (per_segment > 8 * 2)
+        return launch_merge_width<128>(p, s);
+    return launch_merge_width<64>(p, s);
 }
 
 int sm_count()
