@@ -10,7 +10,7 @@ import torch
 import nvfp4_quantized_paged_nvfp4kv_gb300 as nv
 import oracle
 import workloads
-from gpu_util import Built, assert_close, oracle_full, oracle_single_head
+from gpu_util import DEV, Built, assert_close, oracle_full, oracle_single_head
 
 pytestmark = pytest.mark.gpu
 
@@ -262,3 +262,67 @@ def test_multi_query_decode(hq, hkv, q_len, lens):
         torch.cuda.synchronize()
         assert_close(out.cpu().numpy(), ref, f"multi-query q_len={q_len} workers={nw}")
     assert int(b.status.item()) == 0
+
+
+@pytest.mark.parametrize("where", ["start", "middle", "end"])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_score_spread_across_a_split_segment(where, fp8):
+    """Keys whose scores stand ~370 (log2 units) above the others, in one
+    stretch of each long segment: the split-KV partials of one segment then
+    carry maxima hundreds apart, and the merge must weight them by the
+    log-sum-exp rule without overflow or loss (workers 0, 1 and 3 put the
+    stretch at the start, middle or end of a worker's range, or in a segment
+    one worker covers).  The result is the oracle's softmax, which is all but
+    entirely that stretch's mean of V."""
+    lens = (3000, 4100)
+    hq, hkv = 16, 2
+    rng = np.random.default_rng(11)
+    nb = len(lens)
+    bt = np.full((nb, max((L + 15) // 16 for L in lens)), -1, np.int32)
+    perm = rng.permutation(sum((L + 15) // 16 for L in lens)).astype(np.int32)
+    off = 0
+    for i, L in enumerate(lens):
+        n = (L + 15) // 16
+        bt[i, :n] = perm[off:off + n]
+        off += n
+    num_pages = off
+    q = torch.ones((nb, hq, 128), dtype=torch.bfloat16)
+    sm_scale = 0.5
+    if fp8:
+        cache = nv.FP8Cache.allocate(num_pages, hkv, device=DEV)
+        kc = np.zeros((num_pages, hkv, 16, 128), np.uint8)
+        vc = np.zeros_like(kc)
+    else:
+        cache = nv.NVFP4Cache.allocate(num_pages, hkv, device=DEV)
+        pools = [np.zeros((num_pages, hkv, 16, s), np.uint8) for s in (64, 8, 64, 8)]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for i, L in enumerate(lens):
+        k = rng.standard_normal((L, hkv, 128)).astype(np.float32)
+        v = rng.standard_normal((L, hkv, 128)).astype(np.float32)
+        a = {"start": 20, "middle": L // 2, "end": L - 200}[where]
+        k[a:a + 100] = 4.0
+        sm = (bt[i, np.arange(L) // 16].astype(np.int64) * 16 + np.arange(L) % 16).astype(np.int32)
+        args = (torch.from_numpy(k).to(DEV), torch.from_numpy(v).to(DEV), torch.from_numpy(sm).to(DEV), status)
+        if fp8:
+            nv.fp8kv_quantize_append(cache, *args)
+            oracle.fp8_quantize_append(k, sm, kc)
+            oracle.fp8_quantize_append(v, sm, vc)
+        else:
+            nv.nvfp4kv_quantize_append(cache, *args)
+            oracle.quantize_append(k, sm, pools[0], pools[1])
+            oracle.quantize_append(v, sm, pools[2], pools[3])
+    sl = np.int32(lens)
+    if fp8:
+        want = oracle.fp8_paged_decode(kc, vc, q.float().numpy(), bt, sl, sm_scale=sm_scale)
+    else:
+        want = oracle.paged_decode(*pools, q.float().numpy(), bt, sl, sm_scale=sm_scale)
+    fn = nv.fp8kv_paged_decode if fp8 else nv.nvfp4kv_paged_decode
+    for nw in (0, 1, 3):
+        out = torch.full((nb, hq, 128), float("nan"), dtype=torch.float32, device=DEV)
+        ws = nv.new_workspace(nw, device=DEV)
+        ws.fill_(0xFF)
+        fn(cache, q.to(DEV), torch.from_numpy(bt).to(DEV), torch.from_numpy(sl).to(DEV), out, ws,
+           sm_scale=sm_scale, num_workers=nw, dev_status=status)
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy(), want, f"score spread at the {where}, workers={nw}")
+    assert int(status.item()) == 0
