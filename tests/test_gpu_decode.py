@@ -205,6 +205,56 @@ def test_append_decode_equals_append_then_decode(fp8, lens, g=1.0, hs=None):
     assert_close(out.cpu().numpy(), want, "fused append + decode")
 
 
+@pytest.mark.parametrize("name,batch", [("llama70b", 12), ("ctx160k", 15), ("ctx1m", 2)])
+def test_fused_step_full_size_sampled(name, batch):
+    """The step the bench times -- append_paged_decode at the full workload
+    size with the automatic worker count: the cache holds seq_len - 1 tokens,
+    the call writes token seq_len - 1 of every sequence and attends over all of
+    them.  The written pool equals quantize_append's byte for byte, and sampled
+    (sequence, kv head) outputs equal the oracle's decode over all tokens."""
+    w = workloads.make(name, batch=batch)
+    full = Built(w, spare_pages=0, fp8=False)            # every token through quantize_append
+    cache = nv.NVFP4Cache.allocate(full.num_pages, w.num_kv_heads, device=DEV)
+    k_new = torch.zeros((w.batch, w.num_kv_heads, 128), dtype=torch.bfloat16, device=DEV)
+    v_new = torch.zeros_like(k_new)
+    for b_, L in enumerate(w.seq_lens):
+        for t0 in range(0, L - 1, workloads.CHUNK):
+            t1 = min(L - 1, t0 + workloads.CHUNK)
+            sm = torch.from_numpy(workloads.slot_mapping(w, full.bt, b_, t0, t1)).to(DEV)
+            nv.nvfp4kv_quantize_append(cache, workloads.kv_rows(w, "k", b_, t0, t1, device=DEV),
+                                       workloads.kv_rows(w, "v", b_, t0, t1, device=DEV), sm)
+        k_new[b_] = workloads.kv_rows(w, "k", b_, L - 1, L, device=DEV)[0].to(torch.bfloat16)
+        v_new[b_] = workloads.kv_rows(w, "v", b_, L - 1, L, device=DEV)[0].to(torch.bfloat16)
+    # the bf16 rows are what both sides quantise: rebuild the reference's last token from them
+    for b_, L in enumerate(w.seq_lens):
+        sm = torch.from_numpy(workloads.slot_mapping(w, full.bt, b_, L - 1, L)).to(DEV)
+        nv.nvfp4kv_quantize_append(full.cache, k_new[b_:b_ + 1].contiguous(), v_new[b_:b_ + 1].contiguous(), sm)
+        full.rows[(b_, "last")] = (k_new[b_:b_ + 1].float().cpu().numpy(), v_new[b_:b_ + 1].float().cpu().numpy())
+    out = torch.full((w.batch, w.num_q_heads, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = nv.new_workspace(device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nv.nvfp4kv_append_paged_decode(cache, k_new, v_new, full.q, full.bt_d, full.sl_d, out, ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(cache.pool, full.cache.pool), "fused write differs from quantize_append"
+    got = out.float().cpu().numpy()
+    g = w.group
+    rng = np.random.default_rng(batch + 5)
+    for seq, h in [(0, 0), (batch - 1, w.num_kv_heads - 1)] + [tuple(x) for x in rng.integers(
+            [0, 0], [batch, w.num_kv_heads], (2, 2))]:
+        L = w.seq_lens[seq]
+        k = np.concatenate([full.rows_of(seq, "k", h)[:L - 1], full.rows[(seq, "last")][0][:, h:h + 1]], 0)
+        v = np.concatenate([full.rows_of(seq, "v", h)[:L - 1], full.rows[(seq, "last")][1][:, h:h + 1]], 0)
+        npg = (L + 15) // 16
+        pools = [np.zeros((npg, 1, 16, s_), np.uint8) for s_ in (64, 8, 64, 8)]
+        sm = np.arange(L, dtype=np.int32)
+        oracle.quantize_append(k, sm, pools[0], pools[1])
+        oracle.quantize_append(v, sm, pools[2], pools[3])
+        q = full.q[seq:seq + 1, h * g:(h + 1) * g].float().cpu().numpy()
+        want = oracle.paged_decode(*pools, q, np.arange(npg, dtype=np.int32)[None, :], np.int32([L]))[0]
+        assert_close(got[seq, h * g:(h + 1) * g], want, f"{name} fused step seq {seq} kv head {h}")
+
+
 def test_append_decode_with_tensor_scale():
     test_append_decode_equals_append_then_decode(False, (40, 1, 300), g=0.37)
 
